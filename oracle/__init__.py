@@ -1,0 +1,30 @@
+"""Oracle: a plain, slow, float64 CPU statement of what the attention path computes.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call, link or execute
+anything under ``oracle/``; only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` do.  The oracle shares no code
+with the CUDA library (no kernels, headers, helpers or constants); both are fed from the
+seeded generators in ``workloads/``, which hold none of the method's arithmetic.
+
+Sources (web pages, cited by title and section):
+  * "Attention in Code" (sotaaz.com/post/attention-in-code): the ``attend`` / ``causal``
+    pair in "one function all designs use", grouped-query heads in section 1, the sliding
+    ring cache in section 2, the sink in section 3.
+  * "RBS-Attention review" (patty.io): block centroid scoring, mean dilution, the maximum
+    key-block radius judged against its own distribution, two thresholded branches joined
+    by a union, block-sparse FlashAttention execution.
+  * "Attention Variants" lesson (factory.pai-world.com): the causal sliding-window mask and
+    its W=4 diagram.
+  * "Attention Masking" guide (devhandbook.co.kr): per-sequence length (padding) masks.
+
+Modules:
+  attention  -- attend (dense / windowed / sink / block-masked / ragged), visibility rule
+  blocks     -- block centroids and radii, mean-score + radius-rescue block selection
+  ring       -- W-slot ring-buffer decode (the windowed cache of "Attention in Code" s.2)
+"""
+from .attention import attend, positions, visible
+from .blocks import allowed_blocks, block_stats, radius_zscores, select_blocks
+from .ring import ring_decode
+
+__all__ = ["attend", "positions", "visible", "allowed_blocks", "block_stats",
+           "radius_zscores", "select_blocks", "ring_decode"]

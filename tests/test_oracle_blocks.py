@@ -1,0 +1,199 @@
+"""Pins for the block-statistics and block-selection oracle.  CPU only."""
+import math
+
+import numpy as np
+import pytest
+from scipy.spatial.distance import cdist
+
+from oracle import allowed_blocks, attend, block_stats, radius_zscores, select_blocks
+from workloads import planted_outliers
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def test_block_stats_by_direct_distances():
+    """Centroids as explicit sums and radii as the largest pairwise distance from scipy's
+    cdist, with a ragged last block and a shorter second sequence."""
+    k = _rand((2, 3, 45, 7), 101)
+    lens = np.array([45, 30])
+    kb = 8
+    c, r = block_stats(k, lens, kb)
+    assert c.shape == (2, 3, 6, 7) and r.shape == (2, 3, 6)
+    for b in range(2):
+        for h in range(3):
+            for beta in range(6):
+                lo, hi = beta * kb, min((beta + 1) * kb, int(lens[b]))
+                if lo >= hi:
+                    assert np.all(c[b, h, beta] == 0) and r[b, h, beta] == 0
+                    continue
+                keys = k[b, h, lo:hi]
+                cen = sum(keys[j] for j in range(hi - lo)) / (hi - lo)
+                assert np.max(np.abs(c[b, h, beta] - cen)) <= 1e-14
+                far = cdist(keys, cen[None, :]).max()
+                assert abs(r[b, h, beta] - far) <= 1e-13
+
+
+def test_block_stats_degenerate_blocks():
+    """A block of identical keys has radius 0; a one-key block has centroid = that key."""
+    k = np.tile(_rand((1, 1, 1, 5), 111), (1, 1, 9, 1))
+    k[0, 0, 8] = _rand((5,), 112)
+    c, r = block_stats(k, None, 4)
+    assert r[0, 0, 0] == 0 and r[0, 0, 1] == 0
+    assert np.array_equal(c[0, 0, 2], k[0, 0, 8]) and r[0, 0, 2] == 0
+
+
+def test_radius_bounds_every_score_in_the_block():
+    """Cauchy-Schwarz: for any q, max_j q.k_j <= q.c + ||q|| r over the block's keys, with
+    equality at q = k_far - c (k_far the key farthest from the centroid)."""
+    k = _rand((1, 1, 64 * 6, 16), 121)
+    c, r = block_stats(k, None, 64)
+    rng = np.random.default_rng(122)
+    for beta in range(6):
+        keys = k[0, 0, beta * 64:(beta + 1) * 64]
+        for _ in range(20):
+            qv = rng.standard_normal(16) * rng.uniform(0.1, 5)
+            bound = qv @ c[0, 0, beta] + np.linalg.norm(qv) * r[0, 0, beta]
+            assert (keys @ qv).max() <= bound + 1e-12
+        far = keys[np.argmax(np.linalg.norm(keys - c[0, 0, beta], axis=1))]
+        qv = far - c[0, 0, beta]
+        bound = qv @ c[0, 0, beta] + np.linalg.norm(qv) * r[0, 0, beta]
+        assert abs((keys @ qv).max() - bound) <= 1e-11
+
+
+@pytest.mark.parametrize("Tq,Tk,qb,kb,W", [(40, 40, 8, 5, 0), (23, 61, 8, 4, 0), (30, 30, 7, 3, 6),
+                                           (16, 50, 4, 8, 13), (1, 33, 128, 4, 9)])
+def test_allowed_blocks_by_enumerating_pairs(Tq, Tk, qb, kb, W):
+    """Closed-form block visibility against enumerating every (row, key) pair."""
+    for alpha in range(-(-Tq // qb)):
+        brute = np.zeros(-(-Tk // kb), dtype=bool)
+        for t in range(alpha * qb, min(Tq, (alpha + 1) * qb)):
+            i = Tk - Tq + t
+            for j in range(Tk):
+                if j <= i and (W == 0 or j > i - W):
+                    brute[j // kb] = True
+        assert np.array_equal(allowed_blocks(alpha, Tq, Tk, qb, kb, True, W), brute)
+    assert np.all(allowed_blocks(0, Tq, Tk, qb, kb, causal=False))
+
+
+def _brute_select(q, c, r, Tk, qb, kb, W, tau, lam):
+    """Pure-Python selection: enumerated visibility, explicit means and z-scores."""
+    B, H, Tq, d = q.shape
+    n_kv = c.shape[1]
+    g = H // n_kv
+    nQb, nKb = -(-Tq // qb), -(-Tk // kb)
+    out = np.zeros((B, H, nQb, nKb), dtype=np.uint8)
+    for b in range(B):
+        for h in range(H):
+            kvh = h // g
+            rr = [float(r[b, kvh, x]) for x in range(nKb)]
+            mu = sum(rr) / nKb
+            sd = math.sqrt(sum((x - mu) ** 2 for x in rr) / nKb)
+            for alpha in range(nQb):
+                rows = range(alpha * qb, min(Tq, (alpha + 1) * qb))
+                vis = set()
+                own = set()
+                for t in rows:
+                    i = Tk - Tq + t
+                    own.add(i // kb)
+                    for j in range(Tk):
+                        if j <= i and (W == 0 or j > i - W):
+                            vis.add(j // kb)
+                qm = [sum(q[b, h, t, e] for t in rows) / len(rows) for e in range(d)]
+                score = {x: sum(qm[e] * c[b, kvh, x, e] for e in range(d)) / math.sqrt(d) for x in vis}
+                top = max(score.values())
+                for x in vis:
+                    keep = score[x] >= top - tau
+                    keep |= sd > 0 and (rr[x] - mu) / sd >= lam
+                    keep |= x in own
+                    out[b, h, alpha, x] = keep
+    return out
+
+
+@pytest.mark.parametrize("tau,lam,W", [(0.02, 1.5, 0), (0.0, 2.0, 0), (0.05, 1.0, 40), (math.inf, 3.0, 0)])
+def test_select_matches_brute_force(tau, lam, W):
+    """Tiny case (T = 256, query block 32, key block 16) against the pure-Python selection."""
+    B, H, n_kv, T, d, qb, kb = 1, 4, 2, 256, 8, 32, 16
+    q = _rand((B, H, T, d), 131)
+    k = _rand((B, n_kv, T, d), 132)
+    k[0, 0, 37] *= 6.0
+    k[0, 1, 200] *= 6.0
+    c, r = block_stats(k, None, kb)
+    mask, nsel = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, window=W, tau_mean=tau,
+                               lambda_radius=lam)
+    brute = _brute_select(q, c, r, T, qb, kb, W, tau, lam)
+    assert np.array_equal(mask, brute)
+    assert np.array_equal(nsel, brute.sum(axis=3))
+
+
+def test_select_dense_limit_and_chunked_queries():
+    """tau_mean = inf keeps every visible block; the block-sparse attention over that mask is
+    the dense result.  Works with Tq < Tk (a chunk at an offset) and a window."""
+    B, H, n_kv, Tq, Tk, d, qb, kb, W = 1, 4, 2, 40, 100, 8, 16, 8, 30
+    q = _rand((B, H, Tq, d), 141)
+    k = _rand((B, n_kv, Tk, d), 142)
+    v = _rand((B, n_kv, Tk, d), 143)
+    c, r = block_stats(k, None, kb)
+    mask, _ = select_blocks(q, c, r, Tk=Tk, q_block=qb, k_block=kb, window=W)
+    for alpha in range(mask.shape[2]):
+        vis = allowed_blocks(alpha, Tq, Tk, qb, kb, True, W)
+        assert np.array_equal(mask[0, :, alpha].astype(bool), np.tile(vis, (H, 1)))
+    dense, _ = attend(q, k, v, causal=True, window=W)
+    sparse, _ = attend(q, k, v, causal=True, window=W, block_mask=mask, q_block=qb, k_block=kb)
+    assert np.array_equal(sparse, dense)
+
+
+def test_select_keeps_diagonal_and_argmax():
+    """With tau_mean = 0 and no rescue, each query block keeps exactly its best-scoring
+    visible key block plus the blocks over its own positions, so no row is empty."""
+    B, H, n_kv, T, d, qb, kb = 1, 2, 1, 96, 8, 16, 8
+    q = _rand((B, H, T, d), 151)
+    k = _rand((B, n_kv, T, d), 152)
+    c, r = block_stats(k, None, kb)
+    mask, nsel, mm, zm = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=0.0,
+                                       lambda_radius=math.inf, return_margins=True)
+    for h in range(H):
+        for alpha in range(T // qb):
+            own = set(range(alpha * qb // kb, ((alpha + 1) * qb - 1) // kb + 1))
+            sel = set(np.nonzero(mask[0, h, alpha])[0])
+            assert own <= sel and len(sel - own) <= 1
+            vis = allowed_blocks(alpha, T, T, qb, kb)
+            best = np.nanargmax(np.where(vis, mm[0, h, alpha], -np.inf))
+            assert best in sel
+    # Every row keeps a key: dense attention over the mask has no empty rows.
+    v = _rand((B, n_kv, T, d), 153)
+    _, lse = attend(q, k, v, block_mask=mask, q_block=qb, k_block=kb)
+    assert np.all(np.isfinite(lse))
+
+
+def test_radius_branch_rescues_planted_outliers_that_the_mean_misses():
+    """"RBS-Attention review", mean dilution: one planted key of norm 8 sqrt(d) in a block of
+    64 ordinary keys barely moves the centroid's score, but its radius stands far out of the
+    head's radius distribution.  The radius branch finds every planted block; the mean
+    branch alone, at a budget of ~10% of blocks, finds few of them."""
+    n_kv, H, T, d, kb, qb = 2, 4, 64 * 160, 32, 64, 128
+    k = _rand((1, n_kv, T, d), 161).astype(np.float32).astype(np.float64)
+    planted = planted_outliers(162, n_kv, T, d, kb, fraction=0.05)
+    for kvh, blk, tok, vec in planted:
+        k[0, kvh, tok] = vec
+    q = _rand((1, H, T, d), 163)
+    c, r = block_stats(k, None, kb)
+    for kvh in range(n_kv):
+        z = radius_zscores(r[0, kvh])
+        hit = {blk for kh, blk, _, _ in planted if kh == kvh}
+        found = set(np.nonzero(z >= 3.0)[0])
+        assert found == hit
+    mask_r, _ = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=-math.inf,
+                              lambda_radius=3.0)
+    _, _, mm, _ = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=0.0,
+                                lambda_radius=math.inf, return_margins=True)
+    last = mask_r.shape[2] - 1  # the last query block sees every key block
+    for h in range(H):
+        hit = sorted({blk for kh, blk, _, _ in planted if kh == h // (H // n_kv)})
+        rescued = set(np.nonzero(mask_r[0, h, last])[0])
+        assert set(hit) <= rescued
+        # mean branch with the top 10% of blocks by mean score
+        s = mm[0, h, last]
+        top = set(np.argsort(-s)[:len(s) // 10])
+        assert len(top & set(hit)) <= len(hit) // 2
