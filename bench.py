@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Benchmark of the attention hot path on B300, printing ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--no-parts] [--no-cpu-baseline]
+
+Main line: bf16 dense causal GQA prefill, B2 H32 Hkv8 d128 Tq=Tk=8192, TFLOP/s counted from
+the algorithmic causal FLOPs (4 d per allowed (query, key) pair: QK^T and PV, 2 FLOP per
+multiply-add), with q/k/v resident in HBM.  A step is one ga_attend over that batch; L2 is
+flushed (a 256 MiB write) before every timed step, outside the timed events.
+
+"parts" (N = 1, rank 0 only) measures the other workloads of the path with the same timing
+rules: KV-cache decode (GB/s of K/V read), the Tq=512 chunk at absolute positions, window
+1024 + sink at d=256 and the same inputs full causal, and the 128K block-sparse prefill (block
+statistics, block selection, sparse attention at several densities).
+
+Multi-GPU (torchrun): every rank runs its own replica of the main workload (no data-path
+collective: the units are independent), timing is the max over ranks, value is the total
+over ranks ("scaling": "weak").
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same workload and
+metric (the pages give no GPU implementation to run).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOP/s & decode KV-read GB/s, as % of B300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ------------------------------------------------------------------------------ utilities
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def causal_pairs(Tq, Tk, window=0):
+    """Allowed (query, key) pairs of one head: rows at absolute positions Tk-Tq .. Tk-1."""
+    i = np.arange(Tk - Tq, Tk, dtype=np.int64)
+    n = i + 1
+    if window:
+        n = np.minimum(n, window)
+    return int(n.sum())
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("prefill_tc.cuh", "ptx.cuh", "common.cuh", "decode.cuh", "blocks.cuh", "ga.cu"):
+        with open(os.path.join(ROOT, "sparse_prefill_gqa_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    src = kernel_source_hash()
+    with open(p) as f:
+        for line in f:
+            m = re.match(r"(\S+)\s+(\S+)\s+bytes=(\d+)\s+src=(\w+)", line.strip())
+            if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:
+                return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML every ~20 ms while running."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x1: "gpu_idle", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._t = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self._nv = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM))
+                r = self._nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for bit, name in self.REASONS.items():
+                    if r & bit and name != "gpu_idle":
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(0.02)
+
+    def __enter__(self):
+        if self._nv:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------------------ inputs
+def device_bf16(torch, seed, tag, shape, lengths=None):
+    from workloads import randn_bhtd
+    bits = randn_bhtd(seed, tag, shape, "bf16", lengths=lengths)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def timed_steps(torch, fn, steps, warmup, flush=None, stream=None):
+    """Per-step CUDA-event times (ms) on the launching stream, L2 flushed before each step."""
+    for _ in range(warmup):
+        if flush is not None:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    s = stream or torch.cuda.current_stream()
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+# ------------------------------------------------------------------------------ parts
+def part_decode_and_chunk(torch, ga, steps, warmup, flush, peaks):
+    from workloads import get_config, uniform_lengths
+    c = get_config(3)
+    B, H, n_kv, d, Tk = c.batch, c.n_heads, c.n_kv, c.d, c.Tk
+    lens = uniform_lengths(c.seed, B, *c.k_len_range)
+    k = device_bf16(torch, c.seed, "k", (B, n_kv, Tk, d), lengths=lens)
+    v = device_bf16(torch, c.seed, "v", (B, n_kv, Tk, d), lengths=lens)
+    k_lens = torch.from_numpy(lens).cuda()
+    res = {}
+    # decode Tq = 1
+    q = device_bf16(torch, c.seed, "q", (B, H, 1, d))
+    out = torch.empty_like(q)
+    ws = torch.empty(max(1, ga.ga_workspace_size(B, H, n_kv, d, 1, Tk, torch.bfloat16)),
+                     dtype=torch.uint8, device="cuda")
+    t = timed_steps(torch, lambda: ga.ga_attend(q, k, v, out, k_lens=k_lens, workspace=ws),
+                    steps, warmup, flush)
+    kv_bytes = 2 * 2 * d * n_kv * int(lens.sum())
+    ms = statistics.mean(t)
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    res["decode"] = {"workload": c.name + " [Tq=1]", "ms": ms, "GB/s": gbs,
+                     "frac_hbm": gbs / peaks["hbm_gbs"], "kv_bytes": kv_bytes,
+                     "launches_per_step": 2}
+    del q, out
+    # chunk Tq = 512 at absolute positions Tk_b - 512 + t
+    Tq = c.extra["chunk_Tq"]
+    q = device_bf16(torch, c.seed, "q512", (B, H, Tq, d))
+    out = torch.empty_like(q)
+    t = timed_steps(torch, lambda: ga.ga_attend(q, k, v, out, k_lens=k_lens), steps, warmup, flush)
+    flops = 4 * d * H * sum(causal_pairs(Tq, int(n)) for n in lens)
+    ms = statistics.mean(t)
+    res["chunk"] = {"workload": c.name + " [Tq=512]", "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+                    "flops": flops, "launches_per_step": 1}
+    return res
+
+
+def part_window_sink(torch, ga, steps, warmup, flush, peaks):
+    from workloads import get_config
+    c = get_config(4)
+    B, H, n_kv, d, T, W = c.batch, c.n_heads, c.n_kv, c.d, c.Tq, c.window
+    q = device_bf16(torch, c.seed, "q", (B, H, T, d))
+    k = device_bf16(torch, c.seed, "k", (B, n_kv, T, d))
+    v = device_bf16(torch, c.seed, "v", (B, n_kv, T, d))
+    rng = np.random.Generator(np.random.PCG64(c.seed))
+    sink = torch.from_numpy(rng.standard_normal(H).astype(np.float32)).cuda()
+    out = torch.empty_like(q)
+    tw = statistics.mean(timed_steps(torch, lambda: ga.ga_attend(q, k, v, out, window=W, sink=sink),
+                                     steps, warmup, flush))
+    tf = statistics.mean(timed_steps(torch, lambda: ga.ga_attend(q, k, v, out, sink=sink),
+                                     steps, warmup, flush))
+    fw = 4 * d * H * B * causal_pairs(T, T, W)
+    ff = 4 * d * H * B * causal_pairs(T, T)
+    return {"window": {"workload": c.name + " [window]", "ms": tw, "TFLOP/s": fw / (tw * 1e-3) / 1e12,
+                       "flops": fw},
+            "full_causal": {"workload": c.name + " [full causal]", "ms": tf,
+                            "TFLOP/s": ff / (tf * 1e-3) / 1e12, "flops": ff},
+            "composite_5to1": {"TFLOP/s": (5 * fw + ff) / ((5 * tw + tf) * 1e-3) / 1e12}}
+
+
+def part_sparse(torch, ga, steps, warmup, flush, peaks):
+    from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
+    c = get_config(5)
+    B, H, n_kv, d, T, qb, kb = c.batch, c.n_heads, c.n_kv, c.d, c.Tq, c.q_block, c.k_block
+    q = device_bf16(torch, c.seed, "q", (B, H, T, d))
+    kbits = randn_bhtd(c.seed, "k", (B, n_kv, T, d), "bf16")
+    for kvh, blk, tok, vec in planted_outliers(c.seed, n_kv, T, d, kb, c.planted_fraction):
+        kbits[0, kvh, tok] = f32_to_bf16_bits(vec)
+    k = torch.from_numpy(kbits.view(np.int16)).view(torch.bfloat16).cuda()
+    del kbits
+    v = device_bf16(torch, c.seed, "v", (B, n_kv, T, d))
+    lam = c.extra["lambda_radius"]
+    nQb, nKb = T // qb, T // kb
+    # allowed (query, key) pairs inside each (query block, key block) of the causal mask
+    a = torch.arange(nQb, device="cuda", dtype=torch.int64)[:, None]
+    bidx = torch.arange(nKb, device="cuda", dtype=torch.int64)[None, :]
+    rows_i = a * qb + torch.arange(qb, device="cuda")[None, :]          # [nQb, qb] positions
+    pairs = torch.zeros(nQb, nKb, dtype=torch.int64, device="cuda")
+    for r in range(qb):
+        i = rows_i[:, r:r + 1]
+        pairs += torch.clamp(i + 1 - bidx * kb, 0, kb)
+    allowed_blocks = int((pairs > 0).sum()) * H
+
+    res = {}
+    cen = torch.empty(B, n_kv, nKb, d, dtype=torch.float32, device="cuda")
+    rad = torch.empty(B, n_kv, nKb, dtype=torch.float32, device="cuda")
+    ts = timed_steps(torch, lambda: ga.ga_block_stats(k, kb, centroid=cen, radius=rad), steps, warmup, flush)
+    stats_bytes = k.numel() * 2 + cen.numel() * 4 + rad.numel() * 4
+    res["block_stats"] = {"ms": statistics.mean(ts),
+                          "GB/s": stats_bytes / (statistics.mean(ts) * 1e-3) / 1e9,
+                          "frac_hbm": stats_bytes / (statistics.mean(ts) * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    mask = torch.empty(B, H, nQb, nKb, dtype=torch.uint8, device="cuda")
+    nsel = torch.empty(B, H, nQb, dtype=torch.int32, device="cuda")
+
+    def select(tau):
+        ga.ga_select_blocks(q, cen, rad, Tk=T, q_block=qb, k_block=kb, tau_mean=tau, lambda_radius=lam,
+                            block_mask=mask, n_selected=nsel)
+
+    def density():
+        return float(mask.sum()) / allowed_blocks
+
+    tsel = timed_steps(torch, lambda: select(0.05), steps, warmup, flush)
+    sel_bytes = q.numel() * 2 + cen.numel() * 4 + mask.numel()
+    res["block_select"] = {"ms": statistics.mean(tsel),
+                           "GB/s": sel_bytes / (statistics.mean(tsel) * 1e-3) / 1e9}
+    # tau for target densities (bisection on the measured density)
+    targets = [0.05, 0.1, 0.2, 0.4]
+    sweep = []
+    out = torch.empty_like(q)
+    for tgt in targets + [1.0]:
+        if tgt >= 1.0:
+            tau = math.inf
+        else:
+            lo, hi = 0.0, 0.2
+            for _ in range(14):
+                mid = 0.5 * (lo + hi)
+                select(mid)
+                if density() < tgt:
+                    lo = mid
+                else:
+                    hi = mid
+            tau = hi
+        select(tau)
+        dens = density()
+        sel_pairs = int((mask[0].to(torch.int64) * pairs[None]).sum())
+        flops = 4 * d * sel_pairs
+        t = statistics.mean(timed_steps(torch, lambda: ga.ga_attend(q, k, v, out, block_mask=mask,
+                                                                    q_block=qb, k_block=kb),
+                                        max(2, steps // 2), min(warmup, 2), flush))
+        sweep.append({"tau_mean": tau, "density": dens, "ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12})
+    dens = np.array([s["density"] for s in sweep])
+    tms = np.array([s["ms"] for s in sweep])
+    A = np.vstack([dens, np.ones_like(dens)]).T
+    coef, resid, *_ = np.linalg.lstsq(A, tms, rcond=None)
+    pred = A @ coef
+    r2 = 1 - ((tms - pred) ** 2).sum() / ((tms - tms.mean()) ** 2).sum()
+    res["sparse_attention"] = {"workload": c.name, "sweep": sweep, "linear_fit_ms": list(coef),
+                               "r2": float(r2), "sparse_over_dense_at_0.1": float(tms[1] / tms[-1])}
+    return res
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def cpu_oracle_timed(budget_s):
+    import oracle
+    from workloads import get_config, normal_slices, bf16_bits_to_f32, sample_rows
+    cores = len(os.sched_getaffinity(0))
+    c = get_config(2)
+    rows = sample_rows(c.Tq, 256, seed=c.seed)
+    tot_flops, tot_time, heads = 0, 0.0, 0
+    while tot_time < budget_s and heads < c.batch * c.n_heads:
+        b, h = divmod(heads, c.n_heads)
+        kvh = h // c.g
+        q = bf16_bits_to_f32(normal_slices(c.seed, "q", b, h, c.Tq, c.d))[None, None].astype(np.float64)
+        k = bf16_bits_to_f32(normal_slices(c.seed, "k", b, kvh, c.Tk, c.d))[None, None].astype(np.float64)
+        v = bf16_bits_to_f32(normal_slices(c.seed, "v", b, kvh, c.Tk, c.d))[None, None].astype(np.float64)
+        ts = time.perf_counter()
+        oracle.attend(q, k, v, rows=rows)
+        tot_time += time.perf_counter() - ts
+        tot_flops += 4 * c.d * int((rows + 1).sum())
+        heads += 1
+    sample = (f"{heads} (batch, head) pairs x {len(rows)} sampled query rows of the B2 H32 Hkv8 d128 "
+              f"T8192 causal workload through the float64 NumPy oracle (input generation excluded)")
+    return tot_flops / tot_time / 1e12, cores, sample, tot_time
+
+
+# ------------------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-parts", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from workloads import get_config
+    c = get_config(2)
+    flops_step = 4 * c.d * c.n_heads * c.batch * causal_pairs(c.Tq, c.Tk)
+    workload = {"workload": "bf16 dense causal GQA prefill B2 H32 Hkv8 d128 Tq=Tk=8192",
+                "global_batch": c.batch * world, "seq_len": c.Tq, "n_heads": c.n_heads,
+                "n_kv": c.n_kv, "head_dim": c.d, "parallelism": f"replicas x{world}",
+                "l2": "flushed before every timed step (256 MiB write, outside the timed events)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + warmup)))
+        vals = []
+        cores = 0
+        sample = ""
+        for i in range(warmup + args.steps):
+            v, cores, sample, _ = cpu_oracle_timed(budget)
+            if i >= warmup:
+                vals.append(v)
+        val = statistics.mean(vals)
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": warmup, "ms_per_step": flops_step / (val * 1e12) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded PCG64 N(0,1), cast to bf16 on the host, upcast to f64)",
+                "config": workload,
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample + f"; about {budget:.0f} s of oracle time per step"},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    import sparse_prefill_gqa_b300 as ga
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    peaks, peaks_src = load_peaks()
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.fill_(1)
+
+    B, H, n_kv, d, T = c.batch, c.n_heads, c.n_kv, c.d, c.Tq
+    q = device_bf16(torch, c.seed, "q", (B, H, T, d))
+    k = device_bf16(torch, c.seed, "k", (B, n_kv, T, d))
+    v = device_bf16(torch, c.seed, "v", (B, n_kv, T, d))
+    out = torch.empty_like(q)
+
+    def step():
+        ga.ga_attend(q, k, v, out)
+
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev = []
+        s = torch.cuda.current_stream()
+        for _ in range(args.steps):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            b_ = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            step()
+            b_.record(s)
+            ev.append((a, b_))
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    times = [a.elapsed_time(b_) for a, b_ in ev]
+    total_ms = sum(times)
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    kern_tflops = flops_step / (statistics.mean(times) * 1e-3) / 1e12
+
+    # end to end: pinned host buffers, copies inside the timed region
+    qh = q.cpu().pin_memory()
+    kh = k.cpu().pin_memory()
+    vh = v.cpu().pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        ga.ga_attend(qd, kd, vd, out)
+        oh.copy_(out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    te = timed_steps(torch, e2e_step, e2e_steps, 2)
+    e2e_val = flops_step / (statistics.mean(te) * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peak_key = "bf16_tflops"
+    roof = {"kernel": "prefill_tc_kernel<128,128>", "bound": "tensor", "achieved": kern_tflops,
+            "peak": peaks[peak_key], "unit": "TFLOP/s", "frac": kern_tflops / peaks[peak_key],
+            "peak_source": f"{peaks_src} ({peak_key})",
+            "algorithmic_flops_per_launch": flops_step,
+            "traffic": traffic_record("prefill_tc_kernel_128_128", "dense-causal-8k")}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded PCG64 N(0,1) drawn in fp32, cast to bf16 on the host)",
+            "config": workload, "roofline": roof, "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
+                    "d2h_bytes_per_step": out.numel() * 2}}
+
+    if not args.no_parts and world == 1:
+        parts = {}
+        ps, pw = max(3, args.steps // 4), 3
+        for name, fn in (("decode_chunk", part_decode_and_chunk), ("window_sink", part_window_sink),
+                         ("sparse_128k", part_sparse)):
+            try:
+                parts.update(fn(torch, ga, ps, pw, flush, peaks))
+            except Exception as e:  # report, never hide
+                parts[name] = {"error": repr(e)}
+            torch.cuda.empty_cache()
+        line["parts"] = parts
+    if not args.no_cpu_baseline:
+        val, cores, sample, _ = cpu_oracle_timed(12.0)
+        line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,183 @@
+/*
+ * ga.h -- C ABI of libga: grouped-query scaled-dot-product attention with an
+ * absolute-position causal mask, an optional sliding window, an optional per-head sink,
+ * split-K decode, and radius-bounded block-sparse prefill, for NVIDIA B300 (sm_103a).
+ *
+ * Sources (web pages, by title and section):
+ *   "Attention in Code" (sotaaz.com/post/attention-in-code):
+ *       "one function all designs use"   -- attend(q, k, v, mask, sink) and causal(Tq, Tk, window)
+ *       section 1 (MHA, MQA, GQA)          -- query head h reads kv head h / (n_heads / n_kv)
+ *       section 3 (attention sink)         -- one logit per head with no value behind it
+ *   "Express note" (tilnote.io), "causal attention is a position problem"
+ *                                          -- the causal rule uses absolute positions
+ *   "Attention Masking" guide (devhandbook.co.kr), Example 6 -- per-sequence key lengths
+ *   "RBS-Attention review" (patty.io)       -- block centroids, maximum key-block radius,
+ *                                              mean-score and radius-rescue branches, union,
+ *                                              block-sparse FlashAttention execution
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, row-major, in device memory:
+ *       q, out     [batch, n_heads, Tq, d]
+ *       k, v       [batch, n_kv, Tk_max, d]
+ *     Element type is given by `dtype` (GA_F32: float, GA_BF16: bfloat16); accumulation
+ *     is always fp32.  Every tensor pointer must be 16-byte aligned.
+ *   - Query row t of sequence b sits at absolute position i = Tk_b - Tq + t, where
+ *     Tk_b = k_lens[b] (or Tk_max).  Key j may be used by that row when
+ *       j < Tk_b  and  (!causal or j <= i)  and  (window == 0 or j > i - window)
+ *       and (block_mask == NULL or block_mask[b, h, t / q_block, j / k_block] != 0).
+ *     A chunk's own keys and values must already be written at positions
+ *     Tk_b - Tq .. Tk_b - 1 of the cache.
+ *   - Ownership: the caller owns every buffer, including workspaces.  The library never
+ *     allocates device memory and never synchronises the stream, except in
+ *     ga_read_device_status.  All launches go to `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and are asynchronous.
+ *   - Errors: argument checks run on the host before any launch and return a negative
+ *     ga_status without touching the GPU.  A failed launch returns GA_ERR_CUDA.  A device
+ *     wait that runs past its time limit records GA_ERR_DEVICE_TIMEOUT in a sticky device
+ *     status word, read (and cleared) by ga_read_device_status.
+ */
+#ifndef GA_H
+#define GA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that this header needs no CUDA headers. */
+typedef struct CUstream_st* ga_stream_t;
+
+typedef enum { GA_F32 = 0, GA_BF16 = 1 } ga_dtype;
+
+typedef enum {
+  GA_OK = 0,
+  GA_ERR_INVALID_ARG = -1,     /* a size, pointer, alignment or combination is invalid   */
+  GA_ERR_UNSUPPORTED = -2,     /* valid, but outside what the kernels implement          */
+  GA_ERR_CUDA = -3,            /* a CUDA runtime or driver call failed                   */
+  GA_ERR_DEVICE_TIMEOUT = -4,  /* a device-side wait ran past its limit (sticky status)  */
+  GA_ERR_WORKSPACE = -5        /* workspace pointer missing or smaller than required     */
+} ga_status;
+
+/*
+ * ga_attend -- out = softmax(q k^T / sqrt(d) + mask) v for every (b, h, t).
+ * ("Attention in Code", "one function all designs use"; GQA from section 1.)
+ *
+ *   q, k, v, out   device tensors as above; out has q's shape and dtype.
+ *   batch >= 1; n_heads >= 1; 1 <= n_kv <= n_heads with n_heads % n_kv == 0;
+ *   d: head dimension, 1..256 (GA_F32) or one of 16, 32, 64, 128, 256 (GA_BF16);
+ *   1 <= Tq <= Tk_max; every k_lens[b] must lie in [Tq, Tk_max] (not checked on the
+ *   host when k_lens lives on the device: out-of-range lengths give undefined rows).
+ *   k_lens       device int32 [batch], or NULL for "every sequence holds Tk_max keys".
+ *   causal       1: absolute-position causal rule; 0: no causal rule (requires window == 0).
+ *   window       0: no window; W >= 1: the W most recent positions including the query's
+ *                own ("Attention in Code" causal(); "Attention Variants" window mask).
+ *   sink         device float [n_heads] logits, or NULL.  A sink joins the softmax
+ *                normaliser of every row of its query head and carries no value
+ *                ("Attention in Code", section 3); it is not scaled by 1/sqrt(d).
+ *   block_mask   device uint8 [batch, n_heads, ceil(Tq/q_block), ceil(Tk_max/k_block)],
+ *                nonzero = the (query block, key block) pair may be used; or NULL.
+ *                Key blocks that are zero are never loaded by the tensor-core kernels.
+ *   q_block, k_block  block sizes of block_mask (ignored when it is NULL).  The tensor-core
+ *                path takes q_block % 128 == 0 and k_block % 64 == 0; other values run on the
+ *                CUDA-core path.
+ *   lse          optional device float [batch, n_heads, Tq]: natural-log normaliser
+ *                ln(sum_allowed e^s + e^sink); -inf for a row with no allowed key and no sink.
+ *   A row with no allowed key gets out = 0.
+ *   workspace    device scratch of at least ga_workspace_size(...) bytes (may be NULL when
+ *                that size is 0).  Must not be used by another call in flight.
+ */
+int ga_attend(const void* q, const void* k, const void* v, void* out,
+              int batch, int n_heads, int n_kv, int d, int Tq, int Tk_max,
+              const int32_t* k_lens, int causal, int window, const float* sink,
+              const uint8_t* block_mask, int q_block, int k_block, float* lse,
+              ga_dtype dtype, void* workspace, size_t workspace_bytes, ga_stream_t stream);
+
+/* Bytes of workspace ga_attend needs for these sizes (0 when it needs none); SIZE_MAX
+ * when the sizes are invalid.  Only the split-K decode path (Tq * n_heads / n_kv <= 16,
+ * bf16) uses workspace: per (b, h, query row, key chunk) one fp32 partial output row plus
+ * its running max and sum. */
+size_t ga_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk_max,
+                         ga_dtype dtype);
+
+/*
+ * ga_block_stats -- centroid and maximum radius of every key block.
+ * ("RBS-Attention review": blocks represented by their centroid; the maximum key-block
+ * radius is the distance from the centroid to the farthest key of the block.)
+ *
+ *   k          device [batch, n_kv, Tk_max, d], GA_BF16 or GA_F32.
+ *   k_lens     device int32 [batch] or NULL (= Tk_max for every sequence).
+ *   k_block    keys per block, 1..1024.
+ *   centroid   device float [batch, n_kv, nKb, d], nKb = ceil(Tk_max / k_block):
+ *              (1/n) sum of the n keys present in the block.
+ *   radius     device float [batch, n_kv, nKb]: max over the block's keys of the
+ *              Euclidean distance to the centroid.
+ *   Blocks with no key present (j >= k_lens[b]) get a zero centroid and zero radius.
+ *   d: 1..256.
+ */
+int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, int d,
+                   int Tk_max, int k_block, float* centroid, float* radius, ga_dtype dtype,
+                   ga_stream_t stream);
+
+/*
+ * ga_select_blocks -- block mask for radius-bounded sparse prefill.
+ * ("RBS-Attention review": mean score of a query block against key-block centroids, a
+ * radius-rescue branch judged against the head's own radius distribution, each with its
+ * own threshold, joined by a union.)
+ *
+ * For query block alpha (rows alpha*q_block .. min(Tq, (alpha+1)*q_block) - 1, absolute
+ * positions i_first .. i_last = Tk - Tq + those rows) of query head h, kv head
+ * kvh = h / (n_heads / n_kv):
+ *   visible(beta)  key block beta holds a key some row of the block may use under the
+ *                  causal rule and window (all blocks when causal == 0);
+ *   s(beta)        = mean_rows(q) . centroid[beta] / sqrt(d)             (fp32)
+ *   mean branch    s(beta) >= max_{visible} s - tau_mean                 (INFINITY = dense)
+ *   radius branch  (radius[beta] - mu) / sigma >= lambda_radius, mu and sigma (population)
+ *                  over the radii of all ceil(Tk/k_block) blocks of (b, kvh), in fp64;
+ *                  nothing is rescued when sigma == 0
+ *   diagonal       key blocks overlapping [i_first, i_last] are always kept
+ *   block_mask[b, h, alpha, beta] = visible && (mean || radius || diagonal)
+ * Key blocks beta >= ceil(Tk/k_block) of a row are written as 0 up to nKb_out.
+ *
+ *   q          device [batch, n_heads, Tq, d] (GA_BF16 or GA_F32).
+ *   centroid, radius  as produced by ga_block_stats for the same k_block (row stride nKb_out).
+ *   Tk         keys present in every sequence (Tq <= Tk); nKb_out = ceil(Tk_max/k_block) is
+ *              the row length of block_mask, centroid and radius (nKb_out >= ceil(Tk/k_block)).
+ *   block_mask device uint8 out [batch, n_heads, ceil(Tq/q_block), nKb_out].
+ *   n_selected device int32 out [batch, n_heads, ceil(Tq/q_block)], or NULL.
+ *   d: 1..256; q_block: 1..4096; ceil(Tk/k_block) <= 32768.
+ */
+int ga_select_blocks(const void* q, const float* centroid, const float* radius,
+                     int batch, int n_heads, int n_kv, int d, int Tq, int Tk, int nKb_out,
+                     int q_block, int k_block, int causal, int window,
+                     float tau_mean, float lambda_radius,
+                     uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype,
+                     ga_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the sticky device status: GA_OK, or
+ * GA_ERR_DEVICE_TIMEOUT when some kernel gave up on a wait since the last read.  Returns
+ * GA_ERR_CUDA when the synchronisation itself fails. */
+int ga_read_device_status(ga_stream_t stream);
+
+/* Time limit for every device-side wait, in nanoseconds (default 2e9; minimum 1e5).
+ * Applies to launches made after the call. */
+void ga_set_wait_timeout_ns(uint64_t ns);
+
+/* Launches one small kernel that waits on a flag nothing ever sets, with the bounded wait
+ * every kernel of the library uses, and returns the launch status.  The wait gives up
+ * after `timeout_ns` and records GA_ERR_DEVICE_TIMEOUT, which ga_read_device_status then
+ * reports.  Used to test the failure path without faulting or hanging the GPU. */
+int ga_selftest_wait_timeout(uint64_t timeout_ns, ga_stream_t stream);
+
+/* Human-readable name of a ga_status value (a static string). */
+const char* ga_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int ga_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GA_H */

@@ -1,0 +1,213 @@
+"""Python binding of libga (include/ga.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does nothing but check
+tensors, allocate outputs and workspace through PyTorch (device memory is PyTorch's job),
+and pass pointers, sizes and the current CUDA stream to the library.  All arithmetic runs in
+the library's CUDA kernels; there is no fallback of any kind: if ``libga.so`` is missing or
+fails to load, every call raises.
+
+Layouts (row-major, contiguous, on one CUDA device):
+    q, out   [batch, n_heads, Tq, d]
+    k, v     [batch, n_kv, Tk_max, d]
+    dtype    torch.float32 or torch.bfloat16 (accumulation is fp32 either way)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "GAError", "lib", "library_path", "ga_attend", "ga_workspace_size", "ga_block_stats",
+    "ga_select_blocks", "ga_read_device_status", "ga_set_wait_timeout_ns",
+    "ga_selftest_wait_timeout", "ga_status_string", "ga_version", "GA_OK", "GA_ERR_INVALID_ARG",
+    "GA_ERR_UNSUPPORTED", "GA_ERR_CUDA", "GA_ERR_DEVICE_TIMEOUT", "GA_ERR_WORKSPACE",
+]
+
+GA_OK, GA_ERR_INVALID_ARG, GA_ERR_UNSUPPORTED = 0, -1, -2
+GA_ERR_CUDA, GA_ERR_DEVICE_TIMEOUT, GA_ERR_WORKSPACE = -3, -4, -5
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+class GAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {ga_status_string(status)} ({status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libga.so")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libga.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run `python -m sparse_prefill_gqa_b300.build`")
+    L = ctypes.CDLL(path)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.ga_attend.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32, vp, vp, i32,
+                            i32, vp, i32, vp, sz, vp]
+    L.ga_attend.restype = i32
+    L.ga_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    L.ga_workspace_size.restype = sz
+    L.ga_block_stats.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp]
+    L.ga_block_stats.restype = i32
+    L.ga_select_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                   f32, f32, vp, vp, i32, vp]
+    L.ga_select_blocks.restype = i32
+    L.ga_read_device_status.argtypes = [vp]
+    L.ga_read_device_status.restype = i32
+    L.ga_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.ga_set_wait_timeout_ns.restype = None
+    L.ga_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    L.ga_selftest_wait_timeout.restype = i32
+    L.ga_status_string.argtypes = [i32]
+    L.ga_status_string.restype = ctypes.c_char_p
+    L.ga_version.argtypes = []
+    L.ga_version.restype = i32
+    _LIB = L
+    return L
+
+
+def ga_status_string(status: int) -> str:
+    return lib().ga_status_string(int(status)).decode()
+
+
+def ga_version() -> int:
+    return int(lib().ga_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != GA_OK:
+        raise GAError(status, what)
+
+
+def _need(t, name, dtype=None, dims=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimensions")
+
+
+def ga_workspace_size(batch, n_heads, n_kv, d, Tq, Tk_max, dtype) -> int:
+    return int(lib().ga_workspace_size(batch, n_heads, n_kv, d, Tq, Tk_max, _DTYPES[dtype]))
+
+
+def ga_attend(q, k, v, out=None, *, k_lens=None, causal=True, window=0, sink=None,
+              block_mask=None, q_block=128, k_block=64, lse=None, workspace=None, stream=None):
+    """softmax(q k^T / sqrt(d) + mask) v with GQA heads; returns ``out`` (allocated if None).
+
+    k_lens: int32 [batch] keys present per sequence; sink: float32 [n_heads];
+    block_mask: uint8 [batch, n_heads, ceil(Tq/q_block), ceil(Tk_max/k_block)];
+    lse: optional float32 [batch, n_heads, Tq] output; workspace: uint8 scratch of at least
+    ga_workspace_size(...) bytes (allocated here if None and needed).
+    """
+    L = lib()
+    if q.dtype not in _DTYPES:
+        raise ValueError("q must be float32 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, 4)
+    B, H, Tq, d = q.shape
+    n_kv, Tk_max = k.shape[1], k.shape[2]
+    if k.shape != (B, n_kv, Tk_max, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [batch, n_kv, Tk_max, d] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, 4)
+    if k_lens is not None:
+        _need(k_lens, "k_lens", torch.int32, 1)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, 1)
+    if block_mask is not None:
+        _need(block_mask, "block_mask", torch.uint8, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    need = ga_workspace_size(B, H, n_kv, d, Tq, Tk_max, q.dtype) if H % max(n_kv, 1) == 0 else 0
+    if need == 2 ** 64 - 1:
+        need = 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = L.ga_attend(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tq, Tk_max, _ptr(k_lens),
+                     int(bool(causal)), int(window), _ptr(sink), _ptr(block_mask), int(q_block),
+                     int(k_block), _ptr(lse), _DTYPES[q.dtype], _ptr(workspace), ws_bytes,
+                     _stream(stream))
+    _check(st, "ga_attend")
+    return out
+
+
+def ga_block_stats(k, k_block=64, *, k_lens=None, centroid=None, radius=None, stream=None):
+    """Centroid [B, n_kv, nKb, d] and maximum radius [B, n_kv, nKb] of every key block."""
+    L = lib()
+    _need(k, "k", None, 4)
+    B, n_kv, Tk_max, d = k.shape
+    nKb = -(-Tk_max // k_block)
+    if centroid is None:
+        centroid = torch.empty(B, n_kv, nKb, d, dtype=torch.float32, device=k.device)
+    if radius is None:
+        radius = torch.empty(B, n_kv, nKb, dtype=torch.float32, device=k.device)
+    _need(centroid, "centroid", torch.float32, 4)
+    _need(radius, "radius", torch.float32, 3)
+    if k_lens is not None:
+        _need(k_lens, "k_lens", torch.int32, 1)
+    st = L.ga_block_stats(_ptr(k), _ptr(k_lens), B, n_kv, d, Tk_max, int(k_block), _ptr(centroid),
+                          _ptr(radius), _DTYPES[k.dtype], _stream(stream))
+    _check(st, "ga_block_stats")
+    return centroid, radius
+
+
+def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, causal=True,
+                     window=0, tau_mean=math.inf, lambda_radius=3.0, block_mask=None,
+                     n_selected=None, n_kv=None, stream=None):
+    """Block mask (uint8 [B, H, nQb, nKb]) and per-row counts (int32 [B, H, nQb])."""
+    L = lib()
+    _need(q, "q", None, 4)
+    B, H, Tq, d = q.shape
+    n_kv = centroid.shape[1] if n_kv is None else n_kv
+    nKb_out = centroid.shape[2]
+    Tk = nKb_out * k_block if Tk is None else Tk
+    nQb = -(-Tq // q_block)
+    if block_mask is None:
+        block_mask = torch.empty(B, H, nQb, nKb_out, dtype=torch.uint8, device=q.device)
+    if n_selected is None:
+        n_selected = torch.empty(B, H, nQb, dtype=torch.int32, device=q.device)
+    st = L.ga_select_blocks(_ptr(q), _ptr(centroid), _ptr(radius), B, H, n_kv, d, Tq, int(Tk),
+                            nKb_out, int(q_block), int(k_block), int(bool(causal)), int(window),
+                            float(tau_mean), float(lambda_radius), _ptr(block_mask), _ptr(n_selected),
+                            _DTYPES[q.dtype], _stream(stream))
+    _check(st, "ga_select_blocks")
+    return block_mask, n_selected
+
+
+def ga_read_device_status(stream=None) -> int:
+    return int(lib().ga_read_device_status(_stream(stream)))
+
+
+def ga_set_wait_timeout_ns(ns: int) -> None:
+    lib().ga_set_wait_timeout_ns(int(ns))
+
+
+def ga_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
+    return int(lib().ga_selftest_wait_timeout(int(timeout_ns), _stream(stream)))

@@ -1,0 +1,26 @@
+// common.cuh -- shapes passed to every attention kernel, and shared constants.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace ga {
+
+// Everything an attention kernel needs to know about one ga_attend call.
+struct AttnShape {
+  int batch, n_heads, n_kv, d, Tq, Tk_max;
+  const int32_t* k_lens;        // device [batch] or null
+  int causal, window;
+  const float* sink;            // device [n_heads] or null
+  const uint8_t* block_mask;    // device [batch, n_heads, nQb, nKb] or null
+  int q_block, k_block, nQb, nKb;
+  uint64_t timeout_ns;          // limit for every device-side wait
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace ga

@@ -1,0 +1,326 @@
+// ga.cu -- the C ABI of libga (declared in include/ga.h): argument validation, TMA tensor
+// maps, kernel selection and launch.  Every entry point validates on the host before any
+// CUDA call and returns a ga_status; nothing here allocates device memory.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ga.h"
+#include "attend_simt.cuh"
+#include "blocks.cuh"
+#include "common.cuh"
+#include "decode.cuh"
+#include "prefill_tc.cuh"
+
+namespace ga {
+
+namespace {
+
+uint64_t g_timeout_ns = 2000000000ull;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda) --------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 map over a [planes, rows, cols] row-major tensor, boxes of box_rows x 64 columns
+// with the 128-byte swizzle; out-of-range rows read as zero.
+bool make_map_bf16(CUtensorMap* map, const void* base, int cols, long long rows, long long planes,
+                   int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K>
+int set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess
+             ? GA_OK
+             : GA_ERR_CUDA;
+}
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? GA_OK : GA_ERR_CUDA; }
+
+// ---- split-K decode geometry (shared by ga_workspace_size and ga_attend) -----------------
+bool decode_eligible(int n_heads, int n_kv, int d, int Tq, ga_dtype dtype, const void* block_mask) {
+  const int g = n_heads / n_kv;
+  return dtype == GA_BF16 && block_mask == nullptr && (d == 64 || d == 128) && (long long)g * Tq <= 16;
+}
+
+int decode_chunk_len(int batch, int n_kv, int Tk_max) {
+  const long long want = (long long)Tk_max * batch * n_kv / (148LL * 8);
+  long long c = (want + 63) / 64 * 64;
+  if (c < 512) c = 512;
+  if (c > 4096) c = 4096;
+  return (int)c;
+}
+
+int tc_eligible(int d, ga_dtype dtype, const void* q, const void* k, const void* v, const void* out,
+                const void* block_mask, int q_block, int k_block) {
+  if (dtype != GA_BF16 || !(d == 128 || d == 256)) return 0;
+  if (block_mask && (q_block % 128 != 0 || k_block % 64 != 0)) return 0;
+  return aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out);
+}
+
+}  // namespace
+
+// ---- self-test kernel for the bounded wait ------------------------------------------------
+__global__ void selftest_wait_kernel(const volatile int* flag, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer();
+  while (*flag == 0) {
+    if (globaltimer() - t0 > timeout_ns) {
+      record_status(GA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    __nanosleep(1000);
+  }
+}
+
+__device__ int g_never_set_flag = 0;
+
+}  // namespace ga
+
+using namespace ga;
+
+extern "C" {
+
+int ga_version(void) { return 100; }
+
+const char* ga_status_string(int status) {
+  switch (status) {
+    case GA_OK: return "GA_OK";
+    case GA_ERR_INVALID_ARG: return "GA_ERR_INVALID_ARG: invalid size, pointer, alignment or combination";
+    case GA_ERR_UNSUPPORTED: return "GA_ERR_UNSUPPORTED: valid but not implemented by the kernels";
+    case GA_ERR_CUDA: return "GA_ERR_CUDA: a CUDA call failed";
+    case GA_ERR_DEVICE_TIMEOUT: return "GA_ERR_DEVICE_TIMEOUT: a device-side wait ran past its limit";
+    case GA_ERR_WORKSPACE: return "GA_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown ga_status";
+  }
+}
+
+void ga_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns < 100000ull ? 100000ull : ns; }
+
+int ga_read_device_status(ga_stream_t stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GA_ERR_CUDA;
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return GA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return GA_ERR_CUDA;
+  return v;
+}
+
+int ga_selftest_wait_timeout(uint64_t timeout_ns, ga_stream_t stream) {
+  int* flag = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&flag), g_never_set_flag) != cudaSuccess)
+    return GA_ERR_CUDA;
+  selftest_wait_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(flag, timeout_ns);
+  return launch_status();
+}
+
+size_t ga_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk_max, ga_dtype dtype) {
+  if (batch < 1 || n_heads < 1 || n_kv < 1 || n_heads % n_kv != 0 || d < 1 || d > 256 || Tq < 1 ||
+      Tk_max < Tq)
+    return SIZE_MAX;
+  if (!decode_eligible(n_heads, n_kv, d, Tq, dtype, nullptr)) return 0;
+  const int chunk = decode_chunk_len(batch, n_kv, Tk_max);
+  const int n_chunks = (Tk_max + chunk - 1) / chunk;
+  if (n_chunks <= 1) return 0;
+  return (size_t)batch * n_heads * Tq * n_chunks * (size_t)(d + 2) * sizeof(float);
+}
+
+int ga_attend(const void* q, const void* k, const void* v, void* out, int batch, int n_heads,
+              int n_kv, int d, int Tq, int Tk_max, const int32_t* k_lens, int causal, int window,
+              const float* sink, const uint8_t* block_mask, int q_block, int k_block, float* lse,
+              ga_dtype dtype, void* workspace, size_t workspace_bytes, ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!q || !k || !v || !out) return GA_ERR_INVALID_ARG;
+  if (dtype != GA_F32 && dtype != GA_BF16) return GA_ERR_INVALID_ARG;
+  if (batch < 1 || n_heads < 1 || n_kv < 1 || n_kv > n_heads || n_heads % n_kv != 0)
+    return GA_ERR_INVALID_ARG;
+  if (d < 1 || d > 256 || Tq < 1 || Tk_max < Tq) return GA_ERR_INVALID_ARG;
+  if ((causal != 0 && causal != 1) || window < 0 || (window > 0 && !causal)) return GA_ERR_INVALID_ARG;
+  if (block_mask && (q_block < 1 || k_block < 1)) return GA_ERR_INVALID_ARG;
+  if (batch > 65535 || n_heads > 65535) return GA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (lse && !aligned16(lse)) || (sink && !aligned16(sink)) || (k_lens && !aligned16(k_lens)))
+    return GA_ERR_INVALID_ARG;
+
+  AttnShape sh{};
+  sh.batch = batch; sh.n_heads = n_heads; sh.n_kv = n_kv; sh.d = d; sh.Tq = Tq; sh.Tk_max = Tk_max;
+  sh.k_lens = k_lens; sh.causal = causal; sh.window = window; sh.sink = sink;
+  sh.block_mask = block_mask;
+  sh.q_block = block_mask ? q_block : 1;
+  sh.k_block = block_mask ? k_block : 1;
+  sh.nQb = block_mask ? (Tq + q_block - 1) / q_block : 0;
+  sh.nKb = block_mask ? (Tk_max + k_block - 1) / k_block : 0;
+  sh.timeout_ns = g_timeout_ns;
+
+  // ---- fp32 storage: CUDA-core kernel (fp32 arithmetic throughout) -----------------------
+  if (dtype == GA_F32) {
+    dim3 grid((Tq + kSimtWarps - 1) / kSimtWarps, n_heads, batch);
+    attend_simt_kernel<float><<<grid, 32 * kSimtWarps, 0, stream>>>(
+        (const float*)q, (const float*)k, (const float*)v, (float*)out, lse, sh);
+    return launch_status();
+  }
+
+  const __nv_bfloat16* qb = (const __nv_bfloat16*)q;
+  __nv_bfloat16* ob = (__nv_bfloat16*)out;
+
+  // ---- split-K decode ------------------------------------------------------------------
+  if (decode_eligible(n_heads, n_kv, d, Tq, dtype, block_mask)) {
+    DecodeShape ds{};
+    ds.a = sh;
+    ds.g = n_heads / n_kv;
+    ds.rows = ds.g * Tq;
+    ds.chunk_len = decode_chunk_len(batch, n_kv, Tk_max);
+    ds.n_chunks = (Tk_max + ds.chunk_len - 1) / ds.chunk_len;
+    if (ds.n_chunks == 1) ds.chunk_len = (Tk_max + 63) / 64 * 64;
+    const size_t need = ga_workspace_size(batch, n_heads, n_kv, d, Tq, Tk_max, dtype);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+      return GA_ERR_WORKSPACE;
+    float* ws_o = (float*)workspace;
+    float* ws_ml = need ? ws_o + (size_t)batch * n_heads * Tq * ds.n_chunks * d : nullptr;
+    CUtensorMap tk, tv;
+    if (!make_map_bf16(&tk, k, d, Tk_max, (long long)batch * n_kv, 64) ||
+        !make_map_bf16(&tv, v, d, Tk_max, (long long)batch * n_kv, 64))
+      return GA_ERR_CUDA;
+    dim3 grid(ds.n_chunks, n_kv, batch);
+    if (d == 128) {
+      static int ok = set_smem(decode_splitk_kernel<128>, DecodeCfg<128>::SMEM_BYTES);
+      if (ok != GA_OK) return ok;
+      decode_splitk_kernel<128><<<grid, DecodeCfg<128>::THREADS, DecodeCfg<128>::SMEM_BYTES, stream>>>(
+          tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
+    } else {
+      static int ok = set_smem(decode_splitk_kernel<64>, DecodeCfg<64>::SMEM_BYTES);
+      if (ok != GA_OK) return ok;
+      decode_splitk_kernel<64><<<grid, DecodeCfg<64>::THREADS, DecodeCfg<64>::SMEM_BYTES, stream>>>(
+          tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
+    }
+    int st = launch_status();
+    if (st != GA_OK || ds.n_chunks == 1) return st;
+    dim3 cgrid(Tq, n_heads, batch);
+    if (d == 128)
+      decode_combine_kernel<128><<<cgrid, 128, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
+    else
+      decode_combine_kernel<64><<<cgrid, 64, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
+    return launch_status();
+  }
+
+  // ---- tensor-core prefill ---------------------------------------------------------------
+  if (tc_eligible(d, dtype, q, k, v, out, block_mask, q_block, k_block)) {
+    CUtensorMap tq, tk, tv;
+    const int BN = d == 128 ? 128 : 64;
+    if (!make_map_bf16(&tq, q, d, Tq, (long long)batch * n_heads, 128) ||
+        !make_map_bf16(&tk, k, d, Tk_max, (long long)batch * n_kv, 64) ||
+        !make_map_bf16(&tv, v, d, Tk_max, (long long)batch * n_kv, 64))
+      return GA_ERR_CUDA;
+    (void)BN;
+    dim3 grid((Tq + 127) / 128, n_heads, batch);
+    if (d == 128) {
+      using C = PrefillCfg<128, 128>;
+      static int ok = set_smem(prefill_tc_kernel<128, 128>, C::SMEM_BYTES);
+      if (ok != GA_OK) return ok;
+      prefill_tc_kernel<128, 128><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, ob, lse, sh);
+    } else {
+      using C = PrefillCfg<256, 64>;
+      static int ok = set_smem(prefill_tc_kernel<256, 64>, C::SMEM_BYTES);
+      if (ok != GA_OK) return ok;
+      prefill_tc_kernel<256, 64><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, ob, lse, sh);
+    }
+    return launch_status();
+  }
+
+  // ---- everything else: CUDA-core kernel on bf16 storage --------------------------------
+  dim3 grid((Tq + kSimtWarps - 1) / kSimtWarps, n_heads, batch);
+  attend_simt_kernel<__nv_bfloat16><<<grid, 32 * kSimtWarps, 0, stream>>>(
+      qb, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, ob, lse, sh);
+  return launch_status();
+}
+
+int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, int d, int Tk_max,
+                   int k_block, float* centroid, float* radius, ga_dtype dtype, ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!k || !centroid || !radius) return GA_ERR_INVALID_ARG;
+  if (dtype != GA_F32 && dtype != GA_BF16) return GA_ERR_INVALID_ARG;
+  if (batch < 1 || n_kv < 1 || d < 1 || d > 256 || Tk_max < 1 || k_block < 1 || k_block > 1024)
+    return GA_ERR_INVALID_ARG;
+  if (batch > 65535 || n_kv > 65535) return GA_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(centroid) || !aligned16(radius) || (k_lens && !aligned16(k_lens)))
+    return GA_ERR_INVALID_ARG;
+  const int nKb = (Tk_max + k_block - 1) / k_block;
+  dim3 grid(nKb, n_kv, batch);
+  if (dtype == GA_BF16)
+    block_stats_kernel<__nv_bfloat16><<<grid, kStatsThreads, 0, stream>>>(
+        (const __nv_bfloat16*)k, k_lens, n_kv, d, Tk_max, k_block, nKb, centroid, radius);
+  else
+    block_stats_kernel<float><<<grid, kStatsThreads, 0, stream>>>((const float*)k, k_lens, n_kv, d,
+                                                                  Tk_max, k_block, nKb, centroid, radius);
+  return launch_status();
+}
+
+int ga_select_blocks(const void* q, const float* centroid, const float* radius, int batch,
+                     int n_heads, int n_kv, int d, int Tq, int Tk, int nKb_out, int q_block,
+                     int k_block, int causal, int window, float tau_mean, float lambda_radius,
+                     uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype, ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!q || !centroid || !radius || !block_mask) return GA_ERR_INVALID_ARG;
+  if (dtype != GA_F32 && dtype != GA_BF16) return GA_ERR_INVALID_ARG;
+  if (batch < 1 || n_heads < 1 || n_kv < 1 || n_kv > n_heads || n_heads % n_kv != 0)
+    return GA_ERR_INVALID_ARG;
+  if (d < 1 || d > 256 || Tq < 1 || Tk < Tq || q_block < 1 || q_block > 4096 || k_block < 1)
+    return GA_ERR_INVALID_ARG;
+  if ((causal != 0 && causal != 1) || window < 0 || (window > 0 && !causal)) return GA_ERR_INVALID_ARG;
+  if (std::isnan(tau_mean) || std::isnan(lambda_radius)) return GA_ERR_INVALID_ARG;
+  const long long nKb = ((long long)Tk + k_block - 1) / k_block;
+  if (nKb_out < nKb) return GA_ERR_INVALID_ARG;
+  if (nKb > 32768 || batch > 65535 || n_heads > 65535) return GA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(centroid) || !aligned16(radius)) return GA_ERR_INVALID_ARG;
+
+  SelectShape s{};
+  s.batch = batch; s.n_heads = n_heads; s.n_kv = n_kv; s.d = d; s.Tq = Tq; s.Tk = Tk;
+  s.nKb_out = nKb_out; s.q_block = q_block; s.k_block = k_block; s.causal = causal;
+  s.window = window; s.nQb = (Tq + q_block - 1) / q_block; s.nKb = (int)nKb;
+  s.tau_mean = tau_mean; s.lambda_radius = lambda_radius;
+  const int D4 = (d + 3) / 4 * 4 + 4;
+  const size_t smem = (size_t)(kSelQT + kSelBT) * D4 * 4 + (kSelThreads / 32) * 8 + kSelQT * 8 + nKb + 16;
+  static int ok_bf = set_smem(select_blocks_kernel<__nv_bfloat16>, 200 * 1024);
+  static int ok_f = set_smem(select_blocks_kernel<float>, 200 * 1024);
+  if (ok_bf != GA_OK || ok_f != GA_OK) return GA_ERR_CUDA;
+  dim3 grid((s.nQb + kSelQT - 1) / kSelQT, n_heads, batch);
+  if (dtype == GA_BF16)
+    select_blocks_kernel<__nv_bfloat16><<<grid, kSelThreads, smem, stream>>>(
+        (const __nv_bfloat16*)q, centroid, radius, block_mask, n_selected, s);
+  else
+    select_blocks_kernel<float><<<grid, kSelThreads, smem, stream>>>((const float*)q, centroid, radius,
+                                                                     block_mask, n_selected, s);
+  return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point include/ga.h
+declares, and rejects invalid arguments on the host before any CUDA call."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import sparse_prefill_gqa_b300 as ga
+from sparse_prefill_gqa_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return ga.lib()
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(ga_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert {"ga_attend", "ga_block_stats", "ga_select_blocks", "ga_workspace_size"} <= names
+    for n in sorted(names):
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    assert ga.ga_status_string(0) == "GA_OK"
+    for s in (-1, -2, -3, -4, -5):
+        assert ga.ga_status_string(s).startswith("GA_ERR")
+    assert ga.ga_version() >= 100
+
+
+def _attend(L, **kw):
+    p = ctypes.c_void_p(4096)        # aligned, never dereferenced: validation fails first
+    a = dict(q=p, k=p, v=p, out=p, batch=1, n_heads=8, n_kv=2, d=128, Tq=16, Tk=32, k_lens=None,
+             causal=1, window=0, sink=None, mask=None, qb=128, kb=64, lse=None, dtype=1, ws=None,
+             wsb=0, stream=None)
+    a.update(kw)
+    return L.ga_attend(a["q"], a["k"], a["v"], a["out"], a["batch"], a["n_heads"], a["n_kv"], a["d"],
+                       a["Tq"], a["Tk"], a["k_lens"], a["causal"], a["window"], a["sink"], a["mask"],
+                       a["qb"], a["kb"], a["lse"], a["dtype"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(out=None), dict(n_heads=6, n_kv=4), dict(n_kv=0), dict(n_kv=16),
+    dict(d=0), dict(d=257), dict(Tq=0), dict(Tq=33, Tk=32), dict(causal=2), dict(window=-1),
+    dict(causal=0, window=4), dict(mask=ctypes.c_void_p(4096), qb=0), dict(dtype=7),
+    dict(q=ctypes.c_void_p(4100)), dict(sink=ctypes.c_void_p(4104)), dict(batch=0),
+])
+def test_attend_rejects_invalid_arguments(L, kw):
+    assert _attend(L, **kw) == ga.GA_ERR_INVALID_ARG
+
+
+def test_decode_workspace_is_checked_before_launch(L):
+    # GQA decode (g * Tq <= 16, bf16, d = 128) over a long cache needs split-K workspace.
+    need = ga.ga_workspace_size(64, 32, 8, 128, 1, 32768, __import__("torch").bfloat16)
+    assert need > 0
+    assert _attend(L, batch=64, n_heads=32, n_kv=8, Tq=1, Tk=32768) == ga.GA_ERR_WORKSPACE
+    assert L.ga_workspace_size(1, 8, 2, 128, 512, 4096, 1) == 0          # prefill needs none
+    assert L.ga_workspace_size(1, 8, 3, 128, 1, 4096, 1) == 2 ** 64 - 1  # invalid sizes
+
+
+def test_block_calls_reject_invalid_arguments(L):
+    p = ctypes.c_void_p(4096)
+    assert L.ga_block_stats(None, None, 1, 1, 128, 64, 64, p, p, 1, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_block_stats(p, None, 1, 1, 128, 64, 0, p, p, 1, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_block_stats(p, None, 1, 1, 300, 64, 64, p, p, 1, None) == ga.GA_ERR_INVALID_ARG
+    args = [p, p, p, 1, 8, 2, 128, 256, 256, 4, 128, 64, 1, 0, math.inf, 3.0, p, None, 1, None]
+    bad = list(args)
+    bad[5] = 3                                  # n_heads % n_kv != 0
+    assert L.ga_select_blocks(*bad) == ga.GA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[9] = 3                                  # nKb_out < ceil(Tk / k_block)
+    assert L.ga_select_blocks(*bad) == ga.GA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[14] = math.nan                          # NaN threshold
+    assert L.ga_select_blocks(*bad) == ga.GA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[16] = None                              # no output
+    assert L.ga_select_blocks(*bad) == ga.GA_ERR_INVALID_ARG
