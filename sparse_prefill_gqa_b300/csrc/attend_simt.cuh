@@ -60,7 +60,7 @@ attend_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   if (t >= sh.Tq) return;
   const int d = sh.d;
   const int kvh = h / (sh.n_heads / sh.n_kv);
-  const int Tk = sh.k_lens ? sh.k_lens[b] : sh.Tk_max;
+  const int Tk = seq_keys(sh.k_lens, b, sh.Tk_max);
   const long long i = (long long)Tk - sh.Tq + t;           // absolute position of row t
   const long long hi = sh.causal ? min((long long)Tk, i + 1) : (long long)Tk;  // exclusive
   const long long lo = sh.window > 0 ? max(0LL, i - sh.window + 1) : 0LL;

@@ -29,7 +29,7 @@ block_stats_kernel(const T* __restrict__ k, const int32_t* __restrict__ k_lens, 
   __shared__ float c_s[kSimtMaxD];
   __shared__ float r2_s[kStatsThreads / 32];
   const int beta = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int Tk = k_lens ? k_lens[b] : Tk_max;
+  const int Tk = seq_keys(k_lens, b, Tk_max);
   const long long j0 = (long long)beta * k_block;
   const int n = (int)max(0LL, min((long long)k_block, (long long)Tk - j0));
   const size_t blk = ((size_t)b * n_kv + kvh) * nKb + beta;
@@ -254,7 +254,7 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
           if (pass == 0) {
             // scores are finite; order-preserving integer max on the float bits
             atomicMax(reinterpret_cast<int*>(&rowmax[ta + ia]),
-                      score >= 0.f ? __float_as_int(score) : (int)(0x80000000u ^ ~__float_as_uint(score)));
+                      __float_as_int(score) >= 0 ? __float_as_int(score) : (int)(0x80000000u ^ ~__float_as_uint(score)));
           } else {
             const bool keep = score >= rowmax[ta + ia] - s.tau_mean || rescue[beta] ||
                               block_diagonal(s, alpha, beta);

@@ -23,4 +23,10 @@ struct AttnShape {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Keys present in sequence b: k_lens[b] clamped to [0, Tk_max] (Tk_max when k_lens is null),
+// so a bad length can shrink or empty a row but never move a read past the cache.
+__device__ __forceinline__ int seq_keys(const int32_t* k_lens, int b, int Tk_max) {
+  return k_lens ? min(max(k_lens[b], 0), Tk_max) : Tk_max;
+}
+
 }  // namespace ga

@@ -73,7 +73,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int Tk = s.a.k_lens ? s.a.k_lens[b] : s.a.Tk_max;
+  const int Tk = seq_keys(s.a.k_lens, b, s.a.Tk_max);
   int kbeg, kend;
   decode_chunk_range(s, Tk, c, kbeg, kend);
   if (kbeg >= kend) return;                       // chunk holds no usable key (uniform)
@@ -341,7 +341,7 @@ decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ 
                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse, DecodeShape s) {
   const int tq = blockIdx.x, hh = blockIdx.y, b = blockIdx.z;
   const int dim = threadIdx.x;
-  const int Tk = s.a.k_lens ? s.a.k_lens[b] : s.a.Tk_max;
+  const int Tk = seq_keys(s.a.k_lens, b, s.a.Tk_max);
   const size_t qrow = ((size_t)b * s.a.n_heads + hh) * s.a.Tq + tq;
   float M = -INFINITY;
   for (int c = 0; c < s.n_chunks; ++c) {

@@ -116,7 +116,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint64_t tmo = sh.timeout_ns;
 
   TileRange r;
-  r.Tk = sh.k_lens ? sh.k_lens[b] : sh.Tk_max;
+  r.Tk = seq_keys(sh.k_lens, b, sh.Tk_max);
   r.t0 = qt * C::BM;
   r.rows = min(C::BM, sh.Tq - r.t0);
   r.i_first = (long long)r.Tk - sh.Tq + r.t0;
