@@ -2,7 +2,7 @@
 """Benchmark of the attention hot path on B300, printing ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--no-parts] [--no-cpu-baseline]
+                    [--no-parts] [--no-cpu-baseline] [--case NAME [--batch B]]
 
 Main line: bf16 dense causal GQA prefill, B2 H32 Hkv8 d128 Tq=Tk=8192, TFLOP/s counted from
 the algorithmic causal FLOPs (4 d per allowed (query, key) pair: QK^T and PV, 2 FLOP per
@@ -85,53 +85,78 @@ def traffic_record(kernel, workload):
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML every ~20 ms while running."""
+    """Samples SM clock, power and throttle reasons with nvidia-smi every 100 ms; a reader
+    thread stamps each line on arrival, and mark() / summary() keep only the samples taken
+    between the two marks (the timed region)."""
 
-    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
-               0x4: "sw_power_cap", 0x1: "gpu_idle", 0x80: "hw_power_brake_slowdown"}
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
-        self._stop = threading.Event()
-        self._t = None
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self._nv = None
+        self.device_index = device_index
+        self.proc = None
+        self.lines = []          # (host time, csv line)
+        self.t0 = self.t1 = None
+        self._reader = None
 
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM))
-                r = self._nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                for bit, name in self.REASONS.items():
-                    if r & bit and name != "gpu_idle":
-                        self.reasons.add(name)
-            except Exception:
-                pass
-            time.sleep(0.02)
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
 
     def __enter__(self):
-        if self._nv:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        import subprocess
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *a):
-        self._stop.set()
-        if self._t:
-            self._t.join()
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self._reader is not None:
+                self._reader.join(timeout=5)
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                    "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        mhz, mx, reasons, power = [], None, set(), []
+        for t, ln in self.lines:
+            if self.t0 is not None and not (self.t0 <= t <= (self.t1 or t) + 0.1):
+                continue
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                mhz.append(float(f[0]))
+                mx = float(f[1])
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz),
+                "power_w_max": max(power) if power else None,
+                "source": "nvidia-smi -lms 100, samples inside the timed region"}
 
 
 # ------------------------------------------------------------------------------ inputs
@@ -164,15 +189,17 @@ def timed_steps(torch, fn, steps, warmup, flush=None, stream=None):
 
 
 # ------------------------------------------------------------------------------ parts
-def part_decode_and_chunk(torch, ga, steps, warmup, flush, peaks):
+def part_decode_and_chunk(torch, ga, steps, warmup, flush, peaks, batch=None, which=("decode", "chunk")):
     from workloads import get_config, uniform_lengths
     c = get_config(3)
-    B, H, n_kv, d, Tk = c.batch, c.n_heads, c.n_kv, c.d, c.Tk
+    B, H, n_kv, d, Tk = batch or c.batch, c.n_heads, c.n_kv, c.d, c.Tk
     lens = uniform_lengths(c.seed, B, *c.k_len_range)
     k = device_bf16(torch, c.seed, "k", (B, n_kv, Tk, d), lengths=lens)
     v = device_bf16(torch, c.seed, "v", (B, n_kv, Tk, d), lengths=lens)
     k_lens = torch.from_numpy(lens).cuda()
     res = {}
+    if "decode" not in which:
+        return dict(res, **_chunk(torch, ga, c, B, H, n_kv, d, k, v, k_lens, lens, steps, warmup, flush))
     # decode Tq = 1
     q = device_bf16(torch, c.seed, "q", (B, H, 1, d))
     out = torch.empty_like(q)
@@ -187,16 +214,21 @@ def part_decode_and_chunk(torch, ga, steps, warmup, flush, peaks):
                      "frac_hbm": gbs / peaks["hbm_gbs"], "kv_bytes": kv_bytes,
                      "launches_per_step": 2}
     del q, out
-    # chunk Tq = 512 at absolute positions Tk_b - 512 + t
+    if "chunk" in which:
+        res.update(_chunk(torch, ga, c, B, H, n_kv, d, k, v, k_lens, lens, steps, warmup, flush))
+    return res
+
+
+def _chunk(torch, ga, c, B, H, n_kv, d, k, v, k_lens, lens, steps, warmup, flush):
+    """Tq = 512 chunk at absolute positions Tk_b - 512 + t over the decode workload's cache."""
     Tq = c.extra["chunk_Tq"]
     q = device_bf16(torch, c.seed, "q512", (B, H, Tq, d))
     out = torch.empty_like(q)
     t = timed_steps(torch, lambda: ga.ga_attend(q, k, v, out, k_lens=k_lens), steps, warmup, flush)
     flops = 4 * d * H * sum(causal_pairs(Tq, int(n)) for n in lens)
     ms = statistics.mean(t)
-    res["chunk"] = {"workload": c.name + " [Tq=512]", "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
-                    "flops": flops, "launches_per_step": 1}
-    return res
+    return {"chunk": {"workload": c.name + " [Tq=512]", "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+                      "flops": flops, "launches_per_step": 1}}
 
 
 def part_window_sink(torch, ga, steps, warmup, flush, peaks):
@@ -327,15 +359,45 @@ def cpu_oracle_timed(budget_s):
     return tot_flops / tot_time / 1e12, cores, sample, tot_time
 
 
+# ------------------------------------------------------------------------------ one case
+def run_case(torch, ga, args, warmup, flush, peaks, c):
+    """One workload alone (steps and warm-up as given); prints its JSON line."""
+    if args.case == "prefill":
+        B = args.batch or c.batch
+        q = device_bf16(torch, c.seed, "q", (B, c.n_heads, c.Tq, c.d))
+        k = device_bf16(torch, c.seed, "k", (B, c.n_kv, c.Tk, c.d))
+        v = device_bf16(torch, c.seed, "v", (B, c.n_kv, c.Tk, c.d))
+        out = torch.empty_like(q)
+        t = timed_steps(torch, lambda: ga.ga_attend(q, k, v, out), args.steps, warmup, flush)
+        flops = 4 * c.d * c.n_heads * B * causal_pairs(c.Tq, c.Tk)
+        ms = statistics.mean(t)
+        res = {"prefill": {"workload": f"dense causal B{B} H{c.n_heads} Hkv{c.n_kv} d{c.d} T{c.Tq}",
+                           "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12, "flops": flops}}
+    elif args.case in ("decode", "chunk"):
+        res = part_decode_and_chunk(torch, ga, args.steps, warmup, flush, peaks, batch=args.batch,
+                                    which=(args.case,))
+    elif args.case == "window":
+        res = part_window_sink(torch, ga, args.steps, warmup, flush, peaks)
+    else:
+        res = part_sparse(torch, ga, args.steps, warmup, flush, peaks)
+    print(json.dumps({"case": args.case, "steps": args.steps, "warmup": warmup, **res}))
+    return 0
+
+
 # ------------------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="all",
+                    choices=["all", "prefill", "decode", "chunk", "window", "sparse"],
+                    help="run one workload alone and print its own JSON line (for profiling)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="with --case prefill/decode/chunk: a smaller batch (profiling captures)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
 
@@ -389,6 +451,9 @@ def main():
     def flush():
         flush_buf.fill_(1)
 
+    if args.case != "all":
+        return run_case(torch, ga, args, warmup, flush, peaks, c)
+
     B, H, n_kv, d, T = c.batch, c.n_heads, c.n_kv, c.d, c.Tq
     q = device_bf16(torch, c.seed, "q", (B, H, T, d))
     k = device_bf16(torch, c.seed, "k", (B, n_kv, T, d))
@@ -408,6 +473,7 @@ def main():
     with ClockSampler(local) as clk:
         ev = []
         s = torch.cuda.current_stream()
+        clk.mark_start()
         for _ in range(args.steps):
             flush()
             a = torch.cuda.Event(enable_timing=True)
@@ -417,6 +483,7 @@ def main():
             b_.record(s)
             ev.append((a, b_))
         torch.cuda.synchronize()
+        clk.mark_end()
     if dist:
         dist.barrier()
     times = [a.elapsed_time(b_) for a, b_ in ev]
@@ -470,7 +537,7 @@ def main():
 
     if not args.no_parts and world == 1:
         parts = {}
-        ps, pw = max(3, args.steps // 4), 3
+        ps, pw = max(3, min(20, args.steps // 4)), 3
         for name, fn in (("decode_chunk", part_decode_and_chunk), ("window_sink", part_window_sink),
                          ("sparse_128k", part_sparse)):
             try:

@@ -15,6 +15,7 @@
 #include "blocks.cuh"
 #include "common.cuh"
 #include "decode.cuh"
+#include "prefill_pair.cuh"
 #include "prefill_tc.cuh"
 
 namespace ga {
@@ -244,10 +245,13 @@ int ga_attend(const void* q, const void* k, const void* v, void* out, int batch,
     (void)BN;
     dim3 grid((Tq + 127) / 128, n_heads, batch);
     if (d == 128) {
-      using C = PrefillCfg<128, 128>;
-      static int ok = set_smem(prefill_tc_kernel<128, 128>, C::SMEM_BYTES);
+      using C = PairCfg;
+      static int ok = set_smem(prefill_pair_kernel, C::SMEM_BYTES);
       if (ok != GA_OK) return ok;
-      prefill_tc_kernel<128, 128><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, ob, lse, sh);
+      const long long n_pairs = (Tq + 2 * C::BM - 1) / (2 * C::BM);
+      const long long n_cta = n_pairs * n_heads * batch;
+      if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+      prefill_pair_kernel<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, ob, lse, sh);
     } else {
       using C = PrefillCfg<256, 64>;
       static int ok = set_smem(prefill_tc_kernel<256, 64>, C::SMEM_BYTES);
