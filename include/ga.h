@@ -57,7 +57,8 @@ typedef enum {
   GA_ERR_UNSUPPORTED = -2,     /* valid, but outside what the kernels implement          */
   GA_ERR_CUDA = -3,            /* a CUDA runtime or driver call failed                   */
   GA_ERR_DEVICE_TIMEOUT = -4,  /* a device-side wait ran past its limit (sticky status)  */
-  GA_ERR_WORKSPACE = -5        /* workspace pointer missing or smaller than required     */
+  GA_ERR_WORKSPACE = -5,       /* workspace pointer missing or smaller than required     */
+  GA_ERR_SCRATCH_LIMIT = -6    /* needs more than the static scratch array holds         */
 } ga_status;
 
 /*
@@ -100,6 +101,41 @@ int ga_attend(const void* q, const void* k, const void* v, void* out,
  * its running max and sum. */
 size_t ga_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk_max,
                          ga_dtype dtype);
+
+/* Size of the device array that ga_attend_decode_static uses as its scratch (16 MiB). */
+#define GA_DECODE_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * ga_attend_decode_static -- the split-K decode of ga_attend, for callers that cannot
+ * allocate device memory.  (No counterpart on the pages: this entry point exists only for
+ * such callers.)  Examples: a plugin that runs inside an engine which owns all device
+ * memory through its own pool and forbids outside allocations, and a latency-bound loop
+ * where cudaMalloc/cudaFree are off limits because they can synchronise the device.  Such a
+ * caller has no workspace to pass, so this call keeps its partial results in a
+ * library-owned array instead.
+ *
+ * Computes exactly what ga_attend computes with dtype GA_BF16, block_mask NULL and a
+ * workspace, for shapes on the split-K decode path: d = 64 or 128 and
+ * (n_heads / n_kv) * Tq <= 16.  Other shapes return GA_ERR_UNSUPPORTED.  The other
+ * arguments, layouts and errors are those of ga_attend.
+ *
+ * Scratch: a file-scope __device__ array of GA_DECODE_STATIC_SCRATCH_BYTES, which every GPU
+ * that loads the library holds until the process exits.  Shapes that would need more than
+ * that (ga_workspace_size(...) > GA_DECODE_STATIC_SCRATCH_BYTES) return
+ * GA_ERR_SCRATCH_LIMIT before any CUDA call.
+ *   - The first call on a device does its set-up with that device current: it looks up
+ *     the array's device address and sets the decode kernels' shared-memory limit.  Make
+ *     that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents.  Nothing in it
+ *     needs to start at zero: each call writes every scratch slot before it reads it.
+ *   - Calls that overlap on the GPU race on the array: on different streams, or from host
+ *     threads with no ordering between them.  Order such calls on one stream or with events.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+int ga_attend_decode_static(const void* q, const void* k, const void* v, void* out,
+                            int batch, int n_heads, int n_kv, int d, int Tq, int Tk_max,
+                            const int32_t* k_lens, int causal, int window, const float* sink,
+                            float* lse, ga_stream_t stream);
 
 /*
  * ga_block_stats -- centroid and maximum radius of every key block.

@@ -24,10 +24,13 @@ __all__ = [
     "ga_select_blocks", "ga_read_device_status", "ga_set_wait_timeout_ns",
     "ga_selftest_wait_timeout", "ga_status_string", "ga_version", "GA_OK", "GA_ERR_INVALID_ARG",
     "GA_ERR_UNSUPPORTED", "GA_ERR_CUDA", "GA_ERR_DEVICE_TIMEOUT", "GA_ERR_WORKSPACE",
+    "GA_ERR_SCRATCH_LIMIT", "GA_DECODE_STATIC_SCRATCH_BYTES", "ga_attend_decode_static",
 ]
 
 GA_OK, GA_ERR_INVALID_ARG, GA_ERR_UNSUPPORTED = 0, -1, -2
 GA_ERR_CUDA, GA_ERR_DEVICE_TIMEOUT, GA_ERR_WORKSPACE = -3, -4, -5
+GA_ERR_SCRATCH_LIMIT = -6
+GA_DECODE_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -57,6 +60,9 @@ def lib() -> ctypes.CDLL:
     L.ga_attend.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32, vp, vp, i32,
                             i32, vp, i32, vp, sz, vp]
     L.ga_attend.restype = i32
+    L.ga_attend_decode_static.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32,
+                                          vp, vp, vp]
+    L.ga_attend_decode_static.restype = i32
     L.ga_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.ga_workspace_size.restype = sz
     L.ga_block_stats.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp]
@@ -155,6 +161,36 @@ def ga_attend(q, k, v, out=None, *, k_lens=None, causal=True, window=0, sink=Non
                      int(k_block), _ptr(lse), _DTYPES[q.dtype], _ptr(workspace), ws_bytes,
                      _stream(stream))
     _check(st, "ga_attend")
+    return out
+
+
+def ga_attend_decode_static(q, k, v, out=None, *, k_lens=None, causal=True, window=0, sink=None,
+                            lse=None, stream=None):
+    """Split-K decode (bf16) that allocates no device memory of its own: its scratch is the
+    library's static array of GA_DECODE_STATIC_SCRATCH_BYTES, shared by every call.  For
+    callers that cannot allocate (or pass) a workspace.  Calls that overlap on the GPU race
+    on that array; the first call on a device should come before any stream capture.
+    ``out`` is allocated here when None; pass it to allocate nothing at all."""
+    L = lib()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, H, Tq, d = q.shape
+    n_kv, Tk_max = k.shape[1], k.shape[2]
+    if k.shape != (B, n_kv, Tk_max, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [batch, n_kv, Tk_max, d] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4)
+    if k_lens is not None:
+        _need(k_lens, "k_lens", torch.int32, 1)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, 1)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    st = L.ga_attend_decode_static(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tq, Tk_max,
+                                   _ptr(k_lens), int(bool(causal)), int(window), _ptr(sink), _ptr(lse),
+                                   _stream(stream))
+    _check(st, "ga_attend_decode_static")
     return out
 
 

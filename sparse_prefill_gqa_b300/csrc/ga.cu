@@ -107,6 +107,38 @@ __global__ void selftest_wait_kernel(const volatile int* flag, uint64_t timeout_
 
 __device__ int g_never_set_flag = 0;
 
+// Scratch of ga_attend_decode_static: the split-K partial rows and their (max, sum) pairs.
+// Every device that loads the library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_decode_static_scratch[GA_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_decode_static_scratch on the current device.  Host code must not use
+// the symbol itself as a pointer (on the host it names a stand-in, not device memory), so
+// the address is looked up once per device, with that device current, and cached.
+constexpr int kMaxDevices = 128;
+std::mutex g_static_mu;
+void* g_static_scratch_addr[kMaxDevices] = {};
+
+int static_scratch_setup(void** addr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_static_scratch) != cudaSuccess || p == nullptr)
+      return GA_ERR_CUDA;
+    if (set_smem(decode_splitk_kernel<128>, DecodeCfg<128>::SMEM_BYTES) != GA_OK ||
+        set_smem(decode_splitk_kernel<64>, DecodeCfg<64>::SMEM_BYTES) != GA_OK)
+      return GA_ERR_CUDA;
+    g_static_scratch_addr[dev] = p;
+  }
+  *addr = g_static_scratch_addr[dev];
+  return GA_OK;
+}
+
+}  // namespace
+
 }  // namespace ga
 
 using namespace ga;
@@ -123,6 +155,9 @@ const char* ga_status_string(int status) {
     case GA_ERR_CUDA: return "GA_ERR_CUDA: a CUDA call failed";
     case GA_ERR_DEVICE_TIMEOUT: return "GA_ERR_DEVICE_TIMEOUT: a device-side wait ran past its limit";
     case GA_ERR_WORKSPACE: return "GA_ERR_WORKSPACE: workspace missing or too small";
+    case GA_ERR_SCRATCH_LIMIT:
+      return "GA_ERR_SCRATCH_LIMIT: the shape needs more scratch than the library's static array "
+             "(GA_DECODE_STATIC_SCRATCH_BYTES) holds";
     default: return "unknown ga_status";
   }
 }
@@ -265,6 +300,68 @@ int ga_attend(const void* q, const void* k, const void* v, void* out, int batch,
   dim3 grid((Tq + kSimtWarps - 1) / kSimtWarps, n_heads, batch);
   attend_simt_kernel<__nv_bfloat16><<<grid, 32 * kSimtWarps, 0, stream>>>(
       qb, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, ob, lse, sh);
+  return launch_status();
+}
+
+int ga_attend_decode_static(const void* q, const void* k, const void* v, void* out, int batch,
+                            int n_heads, int n_kv, int d, int Tq, int Tk_max, const int32_t* k_lens,
+                            int causal, int window, const float* sink, float* lse,
+                            ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  // ---- host-side checks, before any CUDA call -------------------------------------------
+  if (!q || !k || !v || !out) return GA_ERR_INVALID_ARG;
+  if (batch < 1 || n_heads < 1 || n_kv < 1 || n_kv > n_heads || n_heads % n_kv != 0)
+    return GA_ERR_INVALID_ARG;
+  if (d < 1 || d > 256 || Tq < 1 || Tk_max < Tq) return GA_ERR_INVALID_ARG;
+  if ((causal != 0 && causal != 1) || window < 0 || (window > 0 && !causal)) return GA_ERR_INVALID_ARG;
+  if (batch > 65535 || n_heads > 65535) return GA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (lse && !aligned16(lse)) || (sink && !aligned16(sink)) || (k_lens && !aligned16(k_lens)))
+    return GA_ERR_INVALID_ARG;
+  if (!decode_eligible(n_heads, n_kv, d, Tq, GA_BF16, nullptr)) return GA_ERR_UNSUPPORTED;
+  const size_t need = ga_workspace_size(batch, n_heads, n_kv, d, Tq, Tk_max, GA_BF16);
+  if (need > (size_t)GA_DECODE_STATIC_SCRATCH_BYTES) return GA_ERR_SCRATCH_LIMIT;
+
+  // ---- once per device: the scratch array's device address -------------------------------
+  void* scratch = nullptr;
+  const int st0 = static_scratch_setup(&scratch);
+  if (st0 != GA_OK) return st0;
+
+  AttnShape sh{};
+  sh.batch = batch; sh.n_heads = n_heads; sh.n_kv = n_kv; sh.d = d; sh.Tq = Tq; sh.Tk_max = Tk_max;
+  sh.k_lens = k_lens; sh.causal = causal; sh.window = window; sh.sink = sink;
+  sh.block_mask = nullptr; sh.q_block = 1; sh.k_block = 1; sh.nQb = 0; sh.nKb = 0;
+  sh.timeout_ns = g_timeout_ns;
+  DecodeShape ds{};
+  ds.a = sh;
+  ds.g = n_heads / n_kv;
+  ds.rows = ds.g * Tq;
+  ds.chunk_len = decode_chunk_len(batch, n_kv, Tk_max);
+  ds.n_chunks = (Tk_max + ds.chunk_len - 1) / ds.chunk_len;
+  if (ds.n_chunks == 1) ds.chunk_len = (Tk_max + 63) / 64 * 64;
+  // partial rows first, then the (max, sum) pairs: the same layout as a caller's workspace
+  float* ws_o = need ? static_cast<float*>(scratch) : nullptr;
+  float* ws_ml = need ? ws_o + (size_t)batch * n_heads * Tq * ds.n_chunks * d : nullptr;
+  const __nv_bfloat16* qb = (const __nv_bfloat16*)q;
+  __nv_bfloat16* ob = (__nv_bfloat16*)out;
+  CUtensorMap tk, tv;
+  if (!make_map_bf16(&tk, k, d, Tk_max, (long long)batch * n_kv, 64) ||
+      !make_map_bf16(&tv, v, d, Tk_max, (long long)batch * n_kv, 64))
+    return GA_ERR_CUDA;
+  dim3 grid(ds.n_chunks, n_kv, batch);
+  if (d == 128)
+    decode_splitk_kernel<128><<<grid, DecodeCfg<128>::THREADS, DecodeCfg<128>::SMEM_BYTES, stream>>>(
+        tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
+  else
+    decode_splitk_kernel<64><<<grid, DecodeCfg<64>::THREADS, DecodeCfg<64>::SMEM_BYTES, stream>>>(
+        tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
+  int st = launch_status();
+  if (st != GA_OK || ds.n_chunks == 1) return st;
+  dim3 cgrid(Tq, n_heads, batch);
+  if (d == 128)
+    decode_combine_kernel<128><<<cgrid, 128, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
+  else
+    decode_combine_kernel<64><<<cgrid, 64, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
   return launch_status();
 }
 
