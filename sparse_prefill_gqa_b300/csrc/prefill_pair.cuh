@@ -202,130 +202,129 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc_s_full = idesc_bf16_f32(128, BN, false);
-    constexpr uint32_t idesc_s_half = idesc_bf16_f32(128, 64, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-    const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-    bool ok = true;
-    for (int x = 0; x < 2 && ok; ++x)
-      if ((x ? r1 : r0).rows) ok = warp_wait(&bars->q_full[x], 0, tmo, abort_flag);
-    int n_pv[2] = {0, 0};           // PV steps issued per query tile (same in every lane)
-    int pv_total[2] = {0, 0};       // key tiles each query tile uses
-    bool o_started[2] = {false, false};   // lane 0: O_X holds an accumulated value
-    for (int j = pair_next(r0, r1, sh, kt_begin - 1, kt_end); j < kt_end; j = pair_next(r0, r1, sh, j, kt_end)) {
-      if (pair_half_mask(r0, sh, j)) ++pv_total[0];
-      if (pair_half_mask(r1, sh, j)) ++pv_total[1];
-    }
+    // One thread runs the whole issue loop: a tcgen05.mma costs the issuing thread about
+    // as long as a 128x128x16 MMA takes to execute, so this thread does nothing else
+    // (descriptors are built once and advanced by constant offsets; waits are one thread's).
+    if (lane == 0) {
+      constexpr uint32_t idesc_s_full = idesc_bf16_f32(128, BN, false);
+      constexpr uint32_t idesc_s_half = idesc_bf16_f32(128, 64, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(sV), BN * 128, 1024);
+      bool ok = true;
+      if (r0.rows) ok = mbar_wait(&bars->q_full[0], 0, tmo, abort_flag);
+      if (ok && r1.rows) ok = mbar_wait(&bars->q_full[1], 0, tmo, abort_flag);
+      int pv_total0 = 0, pv_total1 = 0;   // key tiles each query tile uses
+      for (int j = pair_next(r0, r1, sh, kt_begin - 1, kt_end); j < kt_end; j = pair_next(r0, r1, sh, j, kt_end)) {
+        pv_total0 += pair_half_mask(r0, sh, j) ? 1 : 0;
+        pv_total1 += pair_half_mask(r1, sh, j) ? 1 : 0;
+      }
+      int n_pv0 = 0, n_pv1 = 0;
+      uint32_t o_acc0 = 0u, o_acc1 = 0u;  // O_X already holds an accumulated value
 
-    // S_X = Q_X K^T for key tile j in stage st (one N=128 MMA, or N=64 per used half)
-    auto issue_s = [&](int x, int j, int st, uint32_t hm) {
-      const uint32_t qb = q_addr + x * C::QT_BYTES;
-      const uint32_t kb = k_addr + st * C::KV_BYTES;
-      const uint32_t d_s = tmem + C::COL_S + x * BN;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t a = sdesc_sw128(qb + (kk >> 2) * C::BM * 128 + (kk & 3) * 32, 16, 1024);
-        const uint32_t boff = (kk >> 2) * BN * 128 + (kk & 3) * 32;
+      // S_X = Q_X K^T for the key tile in stage st (N=128, or N=64 per used half)
+      auto issue_s = [&](int x, int st, uint32_t hm) {
+        const uint64_t aq = dq0 + (uint64_t)((x * C::QT_BYTES) >> 4);
+        const uint64_t bk = dk0 + (uint64_t)((st * C::KV_BYTES) >> 4);
+        const uint32_t d_s = tmem + C::COL_S + x * BN;
         if (hm == 3u) {
-          umma_bf16_ss(d_s, a, sdesc_sw128(kb + boff, 16, 1024), idesc_s_full, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
+            const uint64_t offb = (uint64_t)(((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4);
+            umma_bf16_ss(d_s, aq + off, bk + offb, idesc_s_full, kk > 0);
+          }
         } else {
+#pragma unroll 1
+          for (int hf = 0; hf < C::HALVES; ++hf) {
+            if (!((hm >> hf) & 1)) continue;
 #pragma unroll
-          for (int hf = 0; hf < C::HALVES; ++hf)
-            if ((hm >> hf) & 1)
-              umma_bf16_ss(d_s + 64 * hf, a, sdesc_sw128(kb + boff + hf * 64 * 128, 16, 1024),
-                           idesc_s_half, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
+              const uint64_t offb = (uint64_t)(((kk >> 2) * BN * 128 + (kk & 3) * 32 + hf * 64 * 128) >> 4);
+              umma_bf16_ss(d_s + 64 * hf, aq + off, bk + offb, idesc_s_half, kk > 0);
+            }
+          }
         }
-      }
-      umma_commit(&bars->s_full[x]);
-    };
-    // O_X += P_X V for key tile j in stage st (P_X in TMEM over S_X's first 64 columns)
-    auto issue_pv = [&](int x, int st, uint32_t hm, bool last) {
-      const uint32_t vb = v_addr + st * C::KV_BYTES;
-      const uint32_t p_col = tmem + C::COL_S + x * BN;
-      const uint32_t d_o = tmem + C::COL_O + x * D;
+        umma_commit(&bars->s_full[x]);
+      };
+      // O_X += P_X V for the key tile in stage st (P_X in TMEM over S_X's first 64 columns)
+      auto issue_pv = [&](int x, int st, uint32_t hm, uint32_t& o_acc) {
+        const uint64_t bv = dv0 + (uint64_t)((st * C::KV_BYTES) >> 4);
+        const uint32_t p_col = tmem + C::COL_S + x * BN;
+        const uint32_t d_o = tmem + C::COL_O + x * D;
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk) {
-        if (!((hm >> (kk >> 2)) & 1)) continue;
-        const uint64_t bd = sdesc_sw128(vb + kk * 2048, BN * 128, 1024);
-        umma_bf16_ts(d_o, p_col + kk * 8, bd, idesc_pv, o_started[x] ? 1u : 0u);
-        o_started[x] = true;
-      }
-      if (last) umma_commit(&bars->o_final[x]);
-    };
-    // zero value rows at or past the sequence end in the used halves (P is 0 there, but
-    // 0 * NaN = NaN for an uninitialised cache)
-    auto clear_v_tail = [&](int j, int st, uint32_t hm) {
-      const int key0 = j * BN;
-      if (key0 + BN <= Tk) return;
-      unsigned char* vs = sV + st * C::KV_BYTES;
-      const int first = max(0, Tk - key0);
-      for (int e = lane; e < (BN - first) * C::SLABS * 8; e += 32) {
-        const int row = first + e / (C::SLABS * 8);
-        const int rest = e % (C::SLABS * 8);
-        const int s = rest / 8, chunk = rest % 8;
-        if (!((hm >> (row / 64)) & 1)) continue;
-        *reinterpret_cast<uint4*>(vs + s * BN * 128 + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-    };
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          if (!((hm >> (kk >> 2)) & 1)) continue;
+          umma_bf16_ts(d_o, p_col + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), idesc_pv, o_acc);
+          o_acc = 1u;
+        }
+      };
+      // zero value rows at or past the sequence end in the used halves (P is 0 there, but
+      // 0 * NaN = NaN for an uninitialised cache); only a sequence's last tile needs it
+      auto clear_v_tail = [&](int j, int st, uint32_t hm) {
+        const int key0 = j * BN;
+        if (key0 + BN <= Tk) return;
+        unsigned char* vs = sV + st * C::KV_BYTES;
+        for (int row = max(0, Tk - key0); row < BN; ++row) {
+          if (!((hm >> (row / 64)) & 1)) continue;
+          for (int sl = 0; sl < C::SLABS; ++sl)
+            for (int chunk = 0; chunk < 8; ++chunk)
+              *reinterpret_cast<uint4*>(vs + sl * BN * 128 + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      };
 
-    int j = pair_next(r0, r1, sh, kt_begin - 1, kt_end);
-    if (ok && j < kt_end) {
-      ok = warp_wait(&bars->k_full[0], 0, tmo, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        if (lane == 0) {
+      int j = pair_next(r0, r1, sh, kt_begin - 1, kt_end);
+      if (ok && j < kt_end) {
+        ok = mbar_wait(&bars->k_full[0], 0, tmo, abort_flag);
+        if (ok) {
+          tc_fence_after();
           const uint32_t h0 = pair_half_mask(r0, sh, j), h1 = pair_half_mask(r1, sh, j);
-          if (h0) issue_s(0, j, 0, h0);
-          if (h1) issue_s(1, j, 0, h1);
+          if (h0) issue_s(0, 0, h0);
+          if (h1) issue_s(1, 0, h1);
           umma_commit(&bars->k_empty[0]);
         }
-        __syncwarp();
       }
-    }
-    for (int u = 0; ok && j < kt_end; ++u) {
-      const int st = u & 1, stn = (u + 1) & 1;
-      const int jn = pair_next(r0, r1, sh, j, kt_end);
-      const uint32_t h0 = pair_half_mask(r0, sh, j), h1 = pair_half_mask(r1, sh, j);
-      const uint32_t n0 = jn < kt_end ? pair_half_mask(r0, sh, jn) : 0u;
-      const uint32_t n1 = jn < kt_end ? pair_half_mask(r1, sh, jn) : 0u;
-      if (!(ok = warp_wait(&bars->v_full[st], (u >> 1) & 1, tmo, abort_flag))) break;
-      clear_v_tail(j, st, h0 | h1);
-      if (h0) {
-        if (!(ok = warp_wait(&bars->p_full[0], n_pv[0] & 1, tmo, abort_flag))) break;
-        tc_fence_after();
-        if (lane == 0) issue_pv(0, st, h0, n_pv[0] + 1 == pv_total[0]);
-        ++n_pv[0];
-        __syncwarp();
-      }
-      if (jn < kt_end) {
-        if (!(ok = warp_wait(&bars->k_full[stn], ((u + 1) >> 1) & 1, tmo, abort_flag))) break;
-        tc_fence_after();
-        if (lane == 0 && n0) issue_s(0, jn, stn, n0);
-        __syncwarp();
-      }
-      if (h1) {
-        if (!(ok = warp_wait(&bars->p_full[1], n_pv[1] & 1, tmo, abort_flag))) break;
-        tc_fence_after();
-        if (lane == 0) issue_pv(1, st, h1, n_pv[1] + 1 == pv_total[1]);
-        ++n_pv[1];
-        __syncwarp();
-      }
-      if (lane == 0) {
+      uint32_t h0 = ok && j < kt_end ? pair_half_mask(r0, sh, j) : 0u;
+      uint32_t h1 = ok && j < kt_end ? pair_half_mask(r1, sh, j) : 0u;
+      for (int u = 0; ok && j < kt_end; ++u) {
+        const int st = u & 1, stn = st ^ 1;
+        const int jn = pair_next(r0, r1, sh, j, kt_end);
+        const uint32_t n0 = jn < kt_end ? pair_half_mask(r0, sh, jn) : 0u;
+        const uint32_t n1 = jn < kt_end ? pair_half_mask(r1, sh, jn) : 0u;
+        if (!(ok = mbar_wait(&bars->v_full[st], (u >> 1) & 1, tmo, abort_flag))) break;
+        clear_v_tail(j, st, h0 | h1);
+        if (h0) {
+          if (!(ok = mbar_wait(&bars->p_full[0], n_pv0 & 1, tmo, abort_flag))) break;
+          tc_fence_after();
+          issue_pv(0, st, h0, o_acc0);
+          if (++n_pv0 == pv_total0) umma_commit(&bars->o_final[0]);
+        }
+        if (jn < kt_end) {
+          if (!(ok = mbar_wait(&bars->k_full[stn], ((u + 1) >> 1) & 1, tmo, abort_flag))) break;
+          tc_fence_after();
+          if (n0) issue_s(0, stn, n0);
+        }
+        if (h1) {
+          if (!(ok = mbar_wait(&bars->p_full[1], n_pv1 & 1, tmo, abort_flag))) break;
+          tc_fence_after();
+          issue_pv(1, st, h1, o_acc1);
+          if (++n_pv1 == pv_total1) umma_commit(&bars->o_final[1]);
+        }
         umma_commit(&bars->v_empty[st]);
         if (jn < kt_end) {
-          if (n1) issue_s(1, jn, stn, n1);
+          if (n1) issue_s(1, stn, n1);
           umma_commit(&bars->k_empty[stn]);
         }
+        j = jn; h0 = n0; h1 = n1;
       }
-      __syncwarp();
-      j = jn;
+      // Drain: every MMA this thread issued has completed before TMEM can be released.
+      umma_commit(&bars->mma_drain);
+      mbar_wait(&bars->mma_drain, 0, tmo, nullptr);
     }
-    // Drain: every MMA this thread issued has completed before TMEM can be released.
-    if (lane == 0) umma_commit(&bars->mma_drain);
     __syncwarp();
-    warp_wait(&bars->mma_drain, 0, tmo, nullptr);
   } else {
     // ------------------------------------------------------------------ softmax warps 0-7
     const int x = warp >> 2;                          // query tile of this warpgroup
@@ -365,31 +364,40 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             sv[c] = okc ? sv[c] : -INFINITY;
           }
         }
-        float mx[8];
+        // row max: 3-input max over 128 values in 4 independent chains
+        static_assert(BN % 8 == 0, "max chains take 8 columns per step");
+        float mx[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = sv[u];
+        for (int u = 0; u < 4; ++u) mx[u] = fmaxf(sv[u], sv[u + 4]);
 #pragma unroll
-        for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
-        const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * scale_log2;
+        for (int c = 8; c < BN; c += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mx[u] = fmax3(mx[u], sv[c + u], sv[c + u + 4]);
+        const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * scale_log2;
         const bool need = m_tile > m_run + 8.0f;
         const float m_new = need ? m_tile : m_run;
         const float alpha = need ? ex2(m_run - m_new) : 1.0f;   // ex2(-inf) = 0
         const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // p = 2^(s * scale_log2 - m): the scale-and-shift two columns per instruction
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // four independent pairs
 #pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float p0 = ex2(fmaf(sv[c0 + c], scale_log2, -m_use));
-            const float p1 = ex2(fmaf(sv[c0 + c + 1], scale_log2, -m_use));
-            ls[(c >> 1) & 3] += p0 + p1;
+          for (int c = 0; c < 32; c += 4) {
+            float t0, t1, t2, t3;
+            ffma2(t0, t1, sv[c0 + c], sv[c0 + c + 1], scale_log2, scale_log2, -m_use, -m_use);
+            ffma2(t2, t3, sv[c0 + c + 2], sv[c0 + c + 3], scale_log2, scale_log2, -m_use, -m_use);
+            const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+            const int q = (c >> 1) & 2;
+            fadd2(ls[q], ls[q + 1], ls[q], ls[q + 1], p0, p1);
+            fadd2(ls[q + 4], ls[q + 5], ls[q + 4], ls[q + 5], p2, p3);
             pk[c >> 1] = pack_bf16x2(p0, p1);
+            pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
           }
           tmem_st16(t_s + c0 / 2, pk);
         }
-        l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
         m_run = m_new;
         // S_X complete => PV_X of the previous tile complete: O_X may be rescaled now (after
         // P is out of registers, so the score row and the O chunk are never live together)
