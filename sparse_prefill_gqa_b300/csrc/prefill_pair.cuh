@@ -12,7 +12,10 @@
 //   warps 0-3  softmax of tile 0 (thread r = query row r = TMEM lane r);
 //   warps 4-7  softmax of tile 1;
 //   warp 8     TMA producer: Q0, Q1 once; K and V tiles of 128 keys into 2-stage rings;
-//   warp 9     MMA issuer (one lane).
+//   warp 9     MMA issuer (one lane);
+//   warps 10-11  idle (they complete the third warpgroup, whose registers move to the
+//              softmax warpgroups: 168 per thread at launch; 200 for warps 0-7 and 96 for
+//              warps 8-11 after setmaxnreg, 256 x 200 + 128 x 96 = 63488 <= 384 x 168).
 // Tensor memory (512 columns): O0 [0,128), O1 [128,256), S0 [256,384), S1 [384,512).  The
 // softmax writes P (bf16, two per 32-bit column) over the first 64 columns of its own S
 // buffer and the PV MMA reads it from there (A operand in TMEM).  tcgen05 operations of one
@@ -47,7 +50,10 @@ struct PairCfg {
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;
+  static constexpr int LAUNCH_REGS = 168;        // ptxas register count at launch (384 threads)
+  static constexpr int SOFTMAX_REGS = 200, OTHER_REGS = 96;
+  static_assert(256 * SOFTMAX_REGS + 128 * OTHER_REGS <= THREADS * LAUNCH_REGS, "register split");
   static constexpr uint32_t COL_O = 0, COL_S = 2 * D;  // O_X at X*D, S_X at 2D + X*BN
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -87,19 +93,26 @@ __device__ __forceinline__ TileRange pair_range(const AttnShape& sh, int b, int 
 
 __device__ __forceinline__ uint32_t pair_half_mask(const TileRange& r, const AttnShape& sh, int j) {
   if (r.rows == 0 || j < r.kt_lo || j >= r.kt_hi) return 0u;
+  // without a block mask every tile strictly inside the range uses both halves
+  if (r.mrow == nullptr && j > r.kt_lo && j + 1 < r.kt_hi) return 3u;
   return tile_half_mask<PairCfg::BN>(r, sh, j);
 }
 
 // Next key tile after j that either query tile uses (kt_end when none).
 __device__ __forceinline__ int pair_next(const TileRange& r0, const TileRange& r1, const AttnShape& sh,
                                          int j, int kt_end) {
-  for (++j; j < kt_end; ++j)
+  ++j;
+  // without a block mask, the next tile inside either contiguous range is used
+  if (r0.mrow == nullptr && r1.mrow == nullptr && j < kt_end &&
+      ((j >= r0.kt_lo && j < r0.kt_hi) || (j >= r1.kt_lo && j < r1.kt_hi)))
+    return j;
+  for (; j < kt_end; ++j)
     if (pair_half_mask(r0, sh, j) | pair_half_mask(r1, sh, j)) return j;
   return kt_end;
 }
 
-// grid: (n_pairs * n_heads * batch); block: 320 threads; 1 CTA per SM.
-__global__ void __launch_bounds__(320, 1)
+// grid: (n_pairs * n_heads * batch); block: 384 threads; 1 CTA per SM.
+__global__ void __launch_bounds__(384, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, AttnShape sh) {
@@ -151,6 +164,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  if (warp >= 8) {
+  // warps 8-11: one warpgroup gives registers back, then takes the producer / MMA roles
+  regs_dec<C::OTHER_REGS>();
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -325,8 +341,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_wait(&bars->mma_drain, 0, tmo, nullptr);
     }
     __syncwarp();
+  }
   } else {
     // ------------------------------------------------------------------ softmax warps 0-7
+    regs_inc<C::SOFTMAX_REGS>();
     const int x = warp >> 2;                          // query tile of this warpgroup
     const TileRange& r = x ? r1 : r0;
     const int row = threadIdx.x & 127;                // row within the tile = TMEM lane

@@ -89,6 +89,21 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 // ---------------------------------------------------------------------------------------
+// Register reallocation between warpgroups (all four warps of a warpgroup execute it).
+// The sum over warpgroups of (128 x registers) must stay within what the CTA was launched
+// with, or an increase waits forever: callers check that sum against the kernel's
+// launch register count.
+// ---------------------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+
+// ---------------------------------------------------------------------------------------
 // Proxy fences
 // ---------------------------------------------------------------------------------------
 // Makes generic-proxy writes to shared memory visible to the async proxy (TMA, tcgen05.mma).
