@@ -251,31 +251,39 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const uint64_t offb = (uint64_t)(((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4);
             umma_bf16_ss(d_s, aq + off, bk + offb, idesc_s_full, kk > 0);
           }
-        } else {
-#pragma unroll 1
-          for (int hf = 0; hf < C::HALVES; ++hf) {
-            if (!((hm >> hf) & 1)) continue;
+        } else {                               // one used 64-key half: N = 64
+          const int hf = hm == 2u ? 1 : 0;
+          const uint64_t bh = bk + (uint64_t)((hf * 64 * 128) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t off = (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
-              const uint64_t offb = (uint64_t)(((kk >> 2) * BN * 128 + (kk & 3) * 32 + hf * 64 * 128) >> 4);
-              umma_bf16_ss(d_s + 64 * hf, aq + off, bk + offb, idesc_s_half, kk > 0);
-            }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
+            const uint64_t offb = (uint64_t)(((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4);
+            umma_bf16_ss(d_s + 64 * hf, aq + off, bh + offb, idesc_s_half, kk > 0);
           }
         }
         umma_commit(&bars->s_full[x]);
       };
       // O_X += P_X V for the key tile in stage st (P_X in TMEM over S_X's first 64 columns)
+      // (one branch per group: the MMAs of a group are issued straight-line)
       auto issue_pv = [&](int x, int st, uint32_t hm, uint32_t& o_acc) {
         const uint64_t bv = dv0 + (uint64_t)((st * C::KV_BYTES) >> 4);
         const uint32_t p_col = tmem + C::COL_S + x * BN;
         const uint32_t d_o = tmem + C::COL_O + x * D;
+        if (hm == 3u) {
+          umma_bf16_ts(d_o, p_col, bv, idesc_pv, o_acc);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          if (!((hm >> (kk >> 2)) & 1)) continue;
-          umma_bf16_ts(d_o, p_col + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), idesc_pv, o_acc);
-          o_acc = 1u;
+          for (int kk = 1; kk < BN / 16; ++kk)
+            umma_bf16_ts(d_o, p_col + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), idesc_pv, 1u);
+        } else {
+          const int k0 = hm == 2u ? 4 : 0;     // the one used 64-key half
+          const uint64_t bh = bv + (uint64_t)((k0 * 2048) >> 4);
+          const uint32_t ph = p_col + k0 * 8;
+          umma_bf16_ts(d_o, ph, bh, idesc_pv, o_acc);
+#pragma unroll
+          for (int kk = 1; kk < 4; ++kk)
+            umma_bf16_ts(d_o, ph + kk * 8, bh + (uint64_t)((kk * 2048) >> 4), idesc_pv, 1u);
         }
+        o_acc = 1u;
       };
       // zero value rows at or past the sequence end in the used halves (P is 0 there, but
       // 0 * NaN = NaN for an uninitialised cache); only a sequence's last tile needs it
@@ -310,7 +318,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int jn = pair_next(r0, r1, sh, j, kt_end);
         const uint32_t n0 = jn < kt_end ? pair_half_mask(r0, sh, jn) : 0u;
         const uint32_t n1 = jn < kt_end ? pair_half_mask(r1, sh, jn) : 0u;
+        // both TMA waits first (the loads were released two tiles ago), so that each PV
+        // and the following S go to the tensor core back to back
         if (!(ok = mbar_wait(&bars->v_full[st], (u >> 1) & 1, tmo, abort_flag))) break;
+        if (jn < kt_end && !(ok = mbar_wait(&bars->k_full[stn], ((u + 1) >> 1) & 1, tmo, abort_flag))) break;
+        tc_fence_after();
         clear_v_tail(j, st, h0 | h1);
         if (h0) {
           if (!(ok = mbar_wait(&bars->p_full[0], n_pv0 & 1, tmo, abort_flag))) break;
@@ -318,11 +330,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           issue_pv(0, st, h0, o_acc0);
           if (++n_pv0 == pv_total0) umma_commit(&bars->o_final[0]);
         }
-        if (jn < kt_end) {
-          if (!(ok = mbar_wait(&bars->k_full[stn], ((u + 1) >> 1) & 1, tmo, abort_flag))) break;
-          tc_fence_after();
-          if (n0) issue_s(0, stn, n0);
-        }
+        if (n0) issue_s(0, stn, n0);
         if (h1) {
           if (!(ok = mbar_wait(&bars->p_full[1], n_pv1 & 1, tmo, abort_flag))) break;
           tc_fence_after();
