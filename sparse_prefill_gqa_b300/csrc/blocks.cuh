@@ -68,6 +68,93 @@ block_stats_kernel(const T* __restrict__ k, const int32_t* __restrict__ k_lens, 
 }
 
 // ---------------------------------------------------------------------------------------
+// Block statistics, bf16 keys with d = 8 * L (L = 1, 2, 4, 8, 16 or 32): one warp per key
+// block.  Lane l reads 16 bytes (8 dimensions, 8 * (l % L) ..) of rows l / L, l / L + 32 / L,
+// ...; the per-dimension sums meet by shuffles across the lanes of equal l % L.  Pass 2
+// re-reads the block (L1 hits) and keeps the largest squared distance to the centroid.
+// Each key byte crosses HBM once, in 16-byte loads.
+// ---------------------------------------------------------------------------------------
+constexpr int kStatsVecWarps = 4;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <int L>
+__global__ void __launch_bounds__(32 * kStatsVecWarps)
+block_stats_vec_kernel(const __nv_bfloat16* __restrict__ k, const int32_t* __restrict__ k_lens,
+                       int batch, int n_kv, int Tk_max, int k_block, int nKb,
+                       float* __restrict__ centroid, float* __restrict__ radius) {
+  constexpr int D = 8 * L, RP = 32 / L;          // head dim, rows per warp-wide load
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long blk = (long long)blockIdx.x * kStatsVecWarps + warp;   // (b, kvh, beta)
+  if (blk >= (long long)batch * n_kv * nKb) return;
+  const int beta = (int)(blk % nKb);
+  const int bk = (int)(blk / nKb);               // b * n_kv + kvh
+  const int b = bk / n_kv;
+  const int Tk = seq_keys(k_lens, b, Tk_max);
+  const long long j0 = (long long)beta * k_block;
+  const int n = (int)max(0LL, min((long long)k_block, (long long)Tk - j0));
+  float* c_out = centroid + blk * D;
+  const int col = 8 * (lane % L), r0 = lane / L;
+  if (n == 0) {
+    if (r0 == 0) {
+      *reinterpret_cast<float4*>(c_out + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(c_out + col + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (lane == 0) radius[blk] = 0.0f;
+    return;
+  }
+  const __nv_bfloat16* kb = k + ((size_t)bk * Tk_max + j0) * D + col;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int r = r0; r < n; r += RP) {
+    float f[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(kb + (size_t)r * D)), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += f[i];
+  }
+#pragma unroll
+  for (int o = L; o < 32; o <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  const float inv_n = 1.0f / (float)n;
+  float c[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c[i] = acc[i] * inv_n;
+  if (r0 == 0) {
+    *reinterpret_cast<float4*>(c_out + col) = make_float4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<float4*>(c_out + col + 4) = make_float4(c[4], c[5], c[6], c[7]);
+  }
+  float best = 0.0f;
+#pragma unroll 4
+  for (int rb = 0; rb < n; rb += RP) {           // every lane runs the same trip count
+    const int r = rb + r0;
+    float part = 0.0f;
+    if (r < n) {
+      float f[8];
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(kb + (size_t)r * D)), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float e = f[i] - c[i];
+        part = fmaf(e, e, part);
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    best = fmaxf(best, part);
+  }
+#pragma unroll
+  for (int o = L; o < 32; o <<= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if (lane == 0) radius[blk] = sqrtf(best);
+}
+
+// ---------------------------------------------------------------------------------------
 // Block selection.  One CTA per (group of kSelQT query blocks, query head, sequence).
 //   1. radius mean and population std over the kv head's key blocks, in fp64 (fixed tree,
 //      so every CTA of the kv head gets identical values), and the rescue flags;

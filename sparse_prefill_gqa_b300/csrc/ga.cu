@@ -376,6 +376,22 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
   if (!aligned16(k) || !aligned16(centroid) || !aligned16(radius) || (k_lens && !aligned16(k_lens)))
     return GA_ERR_INVALID_ARG;
   const int nKb = (Tk_max + k_block - 1) / k_block;
+  if (dtype == GA_BF16 && d % 8 == 0 && 32 % (d / 8) == 0) {
+    const long long n_blk = (long long)batch * n_kv * nKb;
+    const long long n_cta = (n_blk + kStatsVecWarps - 1) / kStatsVecWarps;
+    if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+    const dim3 vgrid((unsigned)n_cta);
+    const __nv_bfloat16* kp = (const __nv_bfloat16*)k;
+    switch (d / 8) {
+      case 1: block_stats_vec_kernel<1><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
+      case 2: block_stats_vec_kernel<2><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
+      case 4: block_stats_vec_kernel<4><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
+      case 8: block_stats_vec_kernel<8><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
+      case 16: block_stats_vec_kernel<16><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
+      default: block_stats_vec_kernel<32><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
+    }
+    return launch_status();
+  }
   dim3 grid(nKb, n_kv, batch);
   if (dtype == GA_BF16)
     block_stats_kernel<__nv_bfloat16><<<grid, kStatsThreads, 0, stream>>>(

@@ -26,10 +26,15 @@
 // The running output is rescaled only when the running max grows by more than 2^8 (P <= 256
 // in bf16 never overflows), which is rare after the first tiles of a row.
 // Key tiles left empty by the causal rule, the window, the sequence length or the block mask
-// are skipped before any load, per query tile; an unselected 64-key half is neither loaded
-// nor multiplied.  CTAs are numbered heaviest first (the last 256 rows of every head first).
+// are skipped before any load; an unselected 64-key unit is neither loaded nor multiplied.
+// With a block mask, the selected 64-key units are compacted at the start of the CTA into a
+// list of full 128-key tiles (units both query tiles use, then those only tile 0 uses, then
+// those only tile 1 uses, paired within each group), so sparse work runs on full-width MMAs
+// and costs in proportion to the selected units.  CTAs are numbered heaviest first (the
+// last 256 rows of every head first).
 //
-// Shared memory: Q 2 x 32 KB, K 2 x 32 KB, V 2 x 32 KB (128-byte swizzle), barriers.
+// Shared memory: Q 2 x 32 KB, K 2 x 32 KB, V 2 x 32 KB (128-byte swizzle), barriers, and the
+// tile list (2 x 2048 unit indices).
 #pragma once
 
 #include "common.cuh"
@@ -49,7 +54,10 @@ struct PairCfg {
   static constexpr int OFF_K = OFF_Q + 2 * QT_BYTES;
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
-  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int LIST_MAX = 2048;          // tiles in the shared-memory list
+  static constexpr int OFF_LIST = OFF_BAR + BAR_BYTES;
+  static constexpr int SMEM_BYTES = OFF_LIST + 2 * LIST_MAX * 4 + 1024;
   static constexpr int THREADS = 384;
   static constexpr int LAUNCH_REGS = 168;        // ptxas register count at launch (384 threads)
   static constexpr int SOFTMAX_REGS = 200, OTHER_REGS = 96;
@@ -65,6 +73,8 @@ struct PairBars {
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
+  int lcnt[3];                  // tile-list build: units per group
+  int lwarp[3][12];             // tile-list build: units per group and warp in a chunk
 };
 
 // Key range, rows and mask row of query tile X of the CTA (rows <= 0: the tile is empty).
@@ -109,6 +119,65 @@ __device__ __forceinline__ int pair_next(const TileRange& r0, const TileRange& r
   for (; j < kt_end; ++j)
     if (pair_half_mask(r0, sh, j) | pair_half_mask(r1, sh, j)) return j;
   return kt_end;
+}
+
+// The CTA's key-tile schedule.  A tile is two 64-key units ua, ub (keys 64*ua .. 64*ua+63
+// and 64*ub ..) and, per query tile X, the halves it uses (bit 0: ua, bit 1: ub).
+//   dense: tile j is units 2j, 2j+1 over the contiguous key ranges of the two query tiles
+//          (no block mask, or a block mask whose list would not fit);
+//   list:  tiles [0, c0) are used by both query tiles, [c0, c1) by tile 0 only, [c1, n) by
+//          tile 1 only; lb = kNoUnit marks a tile holding one unit.
+constexpr uint32_t kNoUnit = 0xFFFFFFFFu;
+
+struct PairSched {
+  int list;
+  int kt_begin, kt_end;
+  int n, c0, c1;
+  const uint32_t* la;
+  const uint32_t* lb;
+};
+
+struct PairTile {
+  int ua, ub;
+  uint32_t h0, h1;
+};
+
+__device__ __forceinline__ PairTile sched_tile(const PairSched& s, const TileRange& r0, const TileRange& r1,
+                                               const AttnShape& sh, int pos) {
+  PairTile t;
+  if (!s.list) {
+    t.ua = 2 * pos;
+    t.ub = 2 * pos + 1;
+    t.h0 = pair_half_mask(r0, sh, pos);
+    t.h1 = pair_half_mask(r1, sh, pos);
+  } else {
+    const uint32_t b = s.lb[pos];
+    const uint32_t present = b == kNoUnit ? 1u : 3u;
+    t.ua = (int)s.la[pos];
+    t.ub = b == kNoUnit ? t.ua : (int)b;
+    t.h0 = pos < s.c1 ? present : 0u;
+    t.h1 = (pos < s.c0 || pos >= s.c1) ? present : 0u;
+  }
+  return t;
+}
+
+// x < 0: the tiles either query tile uses; x = 0 / 1: the tiles query tile x uses.
+__device__ __forceinline__ int sched_end(const PairSched& s, const TileRange& r0, const TileRange& r1, int x) {
+  if (!s.list) return x < 0 ? s.kt_end : (x == 0 ? r0.kt_hi : r1.kt_hi);
+  return x == 0 ? s.c1 : s.n;
+}
+
+// The position after pos (pos = -1: the first), or sched_end when none is left.
+__device__ __forceinline__ int sched_next(const PairSched& s, const TileRange& r0, const TileRange& r1,
+                                          const AttnShape& sh, int pos, int x) {
+  if (!s.list) {
+    if (x < 0) return pair_next(r0, r1, sh, pos < 0 ? s.kt_begin - 1 : pos, s.kt_end);
+    const TileRange& r = x == 0 ? r0 : r1;
+    return pair_next(r, r, sh, pos < 0 ? r.kt_lo - 1 : pos, r.kt_hi);
+  }
+  int p = pos + 1;
+  if (x == 1 && p == s.c0) p = s.c1;
+  return p;
 }
 
 // grid: (n_pairs * n_heads * batch); block: 384 threads; 1 CTA per SM.
@@ -164,6 +233,79 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // ---- schedule: with a block mask, compact the selected units into a tile list ---------
+  PairSched sched;
+  sched.list = 0;
+  sched.kt_begin = kt_begin;
+  sched.kt_end = kt_end;
+  sched.n = sched.c0 = sched.c1 = 0;
+  uint32_t* list_a = reinterpret_cast<uint32_t*>(smem + C::OFF_LIST);
+  uint32_t* list_b = list_a + C::LIST_MAX;
+  sched.la = list_a;
+  sched.lb = list_b;
+  if (sh.block_mask) {
+    const int u_lo = (r1.rows ? min(r0.key_lo, r1.key_lo) : r0.key_lo) / 64;
+    const int u_hi = ((r1.rows ? max(r0.key_hi, r1.key_hi) : r0.key_hi) + 63) / 64;
+    // group of unit u: 0 both query tiles use it, 1 only tile 0, 2 only tile 1, -1 neither
+    auto unit_group = [&](int u) -> int {
+      if (u >= u_hi) return -1;
+      const int k0 = 64 * u;
+      const bool s0 = r0.rows && k0 < r0.key_hi && k0 + 64 > r0.key_lo && r0.mrow[k0 / sh.k_block] != 0;
+      const bool s1 = r1.rows && k0 < r1.key_hi && k0 + 64 > r1.key_lo && r1.mrow[k0 / sh.k_block] != 0;
+      return s0 && s1 ? 0 : (s0 ? 1 : (s1 ? 2 : -1));
+    };
+    if (threadIdx.x < 3) bars->lcnt[threadIdx.x] = 0;
+    __syncthreads();
+    for (int u = u_lo + (int)threadIdx.x; u < u_hi; u += C::THREADS) {
+      const int g = unit_group(u);
+      if (g >= 0) atomicAdd(&bars->lcnt[g], 1);
+    }
+    __syncthreads();
+    const int cnt0 = bars->lcnt[0], cnt1 = bars->lcnt[1], cnt2 = bars->lcnt[2];
+    const int tiles0 = (cnt0 + 1) / 2, tiles1 = (cnt1 + 1) / 2, tiles2 = (cnt2 + 1) / 2;
+    if (tiles0 + tiles1 + tiles2 <= C::LIST_MAX) {
+      sched.list = 1;
+      sched.c0 = tiles0;
+      sched.c1 = tiles0 + tiles1;
+      sched.n = sched.c1 + tiles2;
+      int run0 = 0, run1 = 0, run2 = 0;             // units placed per group (same in all threads)
+      const uint32_t lt = (1u << lane) - 1u;
+      for (int base = u_lo; base < u_hi; base += C::THREADS) {   // ordered compaction
+        const int u = base + (int)threadIdx.x;
+        const int g = unit_group(u);
+        const uint32_t bal0 = __ballot_sync(0xffffffffu, g == 0);
+        const uint32_t bal1 = __ballot_sync(0xffffffffu, g == 1);
+        const uint32_t bal2 = __ballot_sync(0xffffffffu, g == 2);
+        if (lane == 0) {
+          bars->lwarp[0][warp] = __popc(bal0);
+          bars->lwarp[1][warp] = __popc(bal1);
+          bars->lwarp[2][warp] = __popc(bal2);
+        }
+        __syncthreads();
+        if (g >= 0) {
+          const uint32_t bal = g == 0 ? bal0 : (g == 1 ? bal1 : bal2);
+          int rank = (g == 0 ? run0 : (g == 1 ? run1 : run2)) + __popc(bal & lt);
+          for (int w = 0; w < warp; ++w) rank += bars->lwarp[g][w];
+          const int tb = g == 0 ? 0 : (g == 1 ? sched.c0 : sched.c1);
+          (rank & 1 ? list_b : list_a)[tb + (rank >> 1)] = (uint32_t)u;
+        }
+        for (int w = 0; w < C::THREADS / 32; ++w) {
+          run0 += bars->lwarp[0][w];
+          run1 += bars->lwarp[1][w];
+          run2 += bars->lwarp[2][w];
+        }
+        __syncthreads();
+      }
+      // a group's odd last unit stands alone in its tile
+      if (threadIdx.x == 0) {
+        if (cnt0 & 1) list_b[cnt0 / 2] = kNoUnit;
+        if (cnt1 & 1) list_b[sched.c0 + cnt1 / 2] = kNoUnit;
+        if (cnt2 & 1) list_b[sched.c1 + cnt2 / 2] = kNoUnit;
+      }
+      __syncthreads();
+    }
+  }
+
   if (warp >= 8) {
   // warps 8-11: one warpgroup gives registers back, then takes the producer / MMA roles
   regs_dec<C::OTHER_REGS>();
@@ -184,9 +326,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         q_loaded[x] = true;
       }
       int u = 0, k_issued = 0, v_issued = 0;
-      for (int j = pair_next(r0, r1, sh, kt_begin - 1, kt_end); j < kt_end;
-           j = pair_next(r0, r1, sh, j, kt_end), ++u) {
-        const uint32_t hm = pair_half_mask(r0, sh, j) | pair_half_mask(r1, sh, j);
+      const int pend = sched_end(sched, r0, r1, -1);
+      for (int pos = sched_next(sched, r0, r1, sh, -1, -1); pos < pend;
+           pos = sched_next(sched, r0, r1, sh, pos, -1), ++u) {
+        const PairTile ti = sched_tile(sched, r0, r1, sh, pos);
+        const uint32_t hm = ti.h0 | ti.h1;
         const int st = u & 1;
         const uint32_t bytes = (uint32_t)__popc(hm) * 64u * D * 2u;
         if (u >= 2 && !mbar_wait(&bars->k_empty[st], ((u >> 1) + 1) & 1, tmo, abort_flag)) break;
@@ -196,7 +340,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (!((hm >> hf) & 1)) continue;
           for (int s = 0; s < C::SLABS; ++s)
             tma_load_3d(sK + st * C::KV_BYTES + s * BN * 128 + hf * 64 * 128, &tm_k, &bars->k_full[st],
-                        64 * s, j * BN + 64 * hf, kz);
+                        64 * s, 64 * (hf ? ti.ub : ti.ua), kz);
         }
         if (u >= 2 && !mbar_wait(&bars->v_empty[st], ((u >> 1) + 1) & 1, tmo, abort_flag)) break;
         mbar_arrive_expect_tx(&bars->v_full[st], bytes);
@@ -205,7 +349,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (!((hm >> hf) & 1)) continue;
           for (int s = 0; s < C::SLABS; ++s)
             tma_load_3d(sV + st * C::KV_BYTES + s * BN * 128 + hf * 64 * 128, &tm_v, &bars->v_full[st],
-                        64 * s, j * BN + 64 * hf, kz);
+                        64 * s, 64 * (hf ? ti.ub : ti.ua), kz);
         }
       }
       // Drain: every load this thread issued has landed before the CTA may exit.
@@ -231,10 +375,16 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       bool ok = true;
       if (r0.rows) ok = mbar_wait(&bars->q_full[0], 0, tmo, abort_flag);
       if (ok && r1.rows) ok = mbar_wait(&bars->q_full[1], 0, tmo, abort_flag);
+      const int pend = sched_end(sched, r0, r1, -1);
       int pv_total0 = 0, pv_total1 = 0;   // key tiles each query tile uses
-      for (int j = pair_next(r0, r1, sh, kt_begin - 1, kt_end); j < kt_end; j = pair_next(r0, r1, sh, j, kt_end)) {
-        pv_total0 += pair_half_mask(r0, sh, j) ? 1 : 0;
-        pv_total1 += pair_half_mask(r1, sh, j) ? 1 : 0;
+      if (sched.list) {
+        pv_total0 = sched.c1;
+        pv_total1 = sched.c0 + (sched.n - sched.c1);
+      } else {
+        for (int j = sched_next(sched, r0, r1, sh, -1, -1); j < pend; j = sched_next(sched, r0, r1, sh, j, -1)) {
+          pv_total0 += pair_half_mask(r0, sh, j) ? 1 : 0;
+          pv_total1 += pair_half_mask(r1, sh, j) ? 1 : 0;
+        }
       }
       int n_pv0 = 0, n_pv1 = 0;
       uint32_t o_acc0 = 0u, o_acc1 = 0u;  // O_X already holds an accumulated value
@@ -287,43 +437,45 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       };
       // zero value rows at or past the sequence end in the used halves (P is 0 there, but
       // 0 * NaN = NaN for an uninitialised cache); only a sequence's last tile needs it
-      auto clear_v_tail = [&](int j, int st, uint32_t hm) {
-        const int key0 = j * BN;
-        if (key0 + BN <= Tk) return;
+      auto clear_v_tail = [&](const PairTile& ti, int st, uint32_t hm) {
+        bool any = false;
         unsigned char* vs = sV + st * C::KV_BYTES;
-        for (int row = max(0, Tk - key0); row < BN; ++row) {
-          if (!((hm >> (row / 64)) & 1)) continue;
-          for (int sl = 0; sl < C::SLABS; ++sl)
-            for (int chunk = 0; chunk < 8; ++chunk)
-              *reinterpret_cast<uint4*>(vs + sl * BN * 128 + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+        for (int hf = 0; hf < C::HALVES; ++hf) {
+          const int key0 = 64 * (hf ? ti.ub : ti.ua);
+          if (!((hm >> hf) & 1) || key0 + 64 <= Tk) continue;
+          any = true;
+          for (int row = max(0, Tk - key0); row < 64; ++row)
+            for (int sl = 0; sl < C::SLABS; ++sl)
+              for (int chunk = 0; chunk < 8; ++chunk)
+                *reinterpret_cast<uint4*>(vs + sl * BN * 128 + (hf * 64 + row) * 128 + chunk * 16) =
+                    make_uint4(0, 0, 0, 0);
         }
-        fence_proxy_async_smem();
+        if (any) fence_proxy_async_smem();
       };
 
-      int j = pair_next(r0, r1, sh, kt_begin - 1, kt_end);
-      if (ok && j < kt_end) {
+      int j = sched_next(sched, r0, r1, sh, -1, -1);
+      PairTile ti = j < pend ? sched_tile(sched, r0, r1, sh, j) : PairTile{0, 0, 0u, 0u};
+      if (ok && j < pend) {
         ok = mbar_wait(&bars->k_full[0], 0, tmo, abort_flag);
         if (ok) {
           tc_fence_after();
-          const uint32_t h0 = pair_half_mask(r0, sh, j), h1 = pair_half_mask(r1, sh, j);
-          if (h0) issue_s(0, 0, h0);
-          if (h1) issue_s(1, 0, h1);
+          if (ti.h0) issue_s(0, 0, ti.h0);
+          if (ti.h1) issue_s(1, 0, ti.h1);
           umma_commit(&bars->k_empty[0]);
         }
       }
-      uint32_t h0 = ok && j < kt_end ? pair_half_mask(r0, sh, j) : 0u;
-      uint32_t h1 = ok && j < kt_end ? pair_half_mask(r1, sh, j) : 0u;
-      for (int u = 0; ok && j < kt_end; ++u) {
+      for (int u = 0; ok && j < pend; ++u) {
         const int st = u & 1, stn = st ^ 1;
-        const int jn = pair_next(r0, r1, sh, j, kt_end);
-        const uint32_t n0 = jn < kt_end ? pair_half_mask(r0, sh, jn) : 0u;
-        const uint32_t n1 = jn < kt_end ? pair_half_mask(r1, sh, jn) : 0u;
+        const uint32_t h0 = ti.h0, h1 = ti.h1;
+        const int jn = sched_next(sched, r0, r1, sh, j, -1);
+        const PairTile tn = jn < pend ? sched_tile(sched, r0, r1, sh, jn) : PairTile{0, 0, 0u, 0u};
+        const uint32_t n0 = tn.h0, n1 = tn.h1;
         // both TMA waits first (the loads were released two tiles ago), so that each PV
         // and the following S go to the tensor core back to back
         if (!(ok = mbar_wait(&bars->v_full[st], (u >> 1) & 1, tmo, abort_flag))) break;
-        if (jn < kt_end && !(ok = mbar_wait(&bars->k_full[stn], ((u + 1) >> 1) & 1, tmo, abort_flag))) break;
+        if (jn < pend && !(ok = mbar_wait(&bars->k_full[stn], ((u + 1) >> 1) & 1, tmo, abort_flag))) break;
         tc_fence_after();
-        clear_v_tail(j, st, h0 | h1);
+        clear_v_tail(ti, st, h0 | h1);
         if (h0) {
           if (!(ok = mbar_wait(&bars->p_full[0], n_pv0 & 1, tmo, abort_flag))) break;
           tc_fence_after();
@@ -338,11 +490,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (++n_pv1 == pv_total1) umma_commit(&bars->o_final[1]);
         }
         umma_commit(&bars->v_empty[st]);
-        if (jn < kt_end) {
+        if (jn < pend) {
           if (n1) issue_s(1, stn, n1);
           umma_commit(&bars->k_empty[stn]);
         }
-        j = jn; h0 = n0; h1 = n1;
+        j = jn;
+        ti = tn;
       }
       // Drain: every MMA this thread issued has completed before TMEM can be released.
       umma_commit(&bars->mma_drain);
@@ -370,7 +523,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     int n = 0;
     if (r.rows > 0) {
-      for (int j = pair_next(r, r, sh, r.kt_lo - 1, r.kt_hi); j < r.kt_hi; j = pair_next(r, r, sh, j, r.kt_hi), ++n) {
+      const int pend = sched_end(sched, r0, r1, x);
+      for (int pos = sched_next(sched, r0, r1, sh, -1, x); pos < pend; pos = sched_next(sched, r0, r1, sh, pos, x), ++n) {
         if (!warp_wait(&bars->s_full[x], n & 1, tmo, abort_flag)) break;
         tc_fence_after();
         float sv[BN];
@@ -379,13 +533,15 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           tmem_ld32(t_s + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
         tmem_wait_ld();
 
-        const uint32_t hm = pair_half_mask(r, sh, j);
-        const int key0 = j * BN;
-        const bool interior = hm == 3u && key0 >= lo_all && key0 + BN <= hi_all;
+        const PairTile ti = sched_tile(sched, r0, r1, sh, pos);
+        const uint32_t hm = x ? ti.h1 : ti.h0;
+        const int kb0 = 64 * ti.ua, kb1 = 64 * ti.ub;   // first key of each 64-key half
+        const bool interior = hm == 3u && kb0 >= lo_all && kb0 + 64 <= hi_all && kb1 >= lo_all &&
+                              kb1 + 64 <= hi_all;
         if (!interior) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) {
-            const int jj = key0 + c;
+            const int jj = (c < 64 ? kb0 : kb1) + (c & 63);
             const bool okc = jj >= lo && jj < hi && ((hm >> (c >> 6)) & 1);
             sv[c] = okc ? sv[c] : -INFINITY;
           }
