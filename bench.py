@@ -254,7 +254,7 @@ def part_window_sink(torch, ga, steps, warmup, flush, peaks):
             "composite_5to1": {"TFLOP/s": (5 * fw + ff) / ((5 * tw + tf) * 1e-3) / 1e12}}
 
 
-def part_sparse(torch, ga, steps, warmup, flush, peaks):
+def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
     from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
     c = get_config(5)
     B, H, n_kv, d, T, qb, kb = c.batch, c.n_heads, c.n_kv, c.d, c.Tq, c.q_block, c.k_block
@@ -299,6 +299,8 @@ def part_sparse(torch, ga, steps, warmup, flush, peaks):
     sel_bytes = q.numel() * 2 + cen.numel() * 4 + mask.numel()
     res["block_select"] = {"ms": statistics.mean(tsel),
                            "GB/s": sel_bytes / (statistics.mean(tsel) * 1e-3) / 1e9}
+    if select_only:
+        return res
     # tau for target densities (bisection on the measured density)
     targets = [0.05, 0.1, 0.2, 0.4]
     sweep = []
@@ -379,7 +381,7 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
     elif args.case == "window":
         res = part_window_sink(torch, ga, args.steps, warmup, flush, peaks)
     else:
-        res = part_sparse(torch, ga, args.steps, warmup, flush, peaks)
+        res = part_sparse(torch, ga, args.steps, warmup, flush, peaks, select_only=args.case == "select")
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": warmup, **res}))
     return 0
 
@@ -394,7 +396,7 @@ def main():
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="all",
-                    choices=["all", "prefill", "decode", "chunk", "window", "sparse"],
+                    choices=["all", "prefill", "decode", "chunk", "window", "sparse", "select"],
                     help="run one workload alone and print its own JSON line (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --case prefill/decode/chunk: a smaller batch (profiling captures)")

@@ -252,26 +252,61 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
   }
 
   // ---- 2. mean query row of each query block of this CTA --------------------------------
-  const int groups = min(kSelBT, max(1, kSelThreads / d));
-  const int gidx = tid / d, dim = tid % d;
-  for (int a = 0; a < kSelQT; ++a) {
-    const int alpha = a0 + a;
-    if (alpha >= s.nQb) break;
-    const int t0 = alpha * s.q_block, t1 = min(s.Tq, t0 + s.q_block);
-    const T* qb = q + (((size_t)b * s.n_heads + h) * s.Tq) * d;
-    for (int c = dim; c < d; c += (d > kSelThreads ? kSelThreads : d)) {
-      float acc = 0.0f;
-      if (gidx < groups)
-        for (int t = t0 + gidx; t < t1; t += groups) acc += to_f32(qb[(size_t)t * d + c]);
-      if (gidx < groups) ct[gidx * D4 + c] = acc;   // ct used as scratch here
+  const int vec_l = d / 8;                       // lanes per row for 16-byte bf16 loads
+  if (sizeof(T) == 2 && d % 8 == 0 && 32 % vec_l == 0) {
+    // 16-byte loads: lane l reads dims 8*(l % L) .. of rows l / L, l / L + 32/L, ... of the
+    // warp's share; sums meet by shuffles, then across the 8 warps in shared memory
+    const int rpw = 32 / vec_l;                  // rows per warp-wide load
+    const int col = 8 * (lane % vec_l), r0 = lane / vec_l;
+    for (int a = 0; a < kSelQT; ++a) {
+      const int alpha = a0 + a;
+      if (alpha >= s.nQb) break;
+      const int t0 = alpha * s.q_block, t1 = min(s.Tq, t0 + s.q_block);
+      const T* qb = q + (((size_t)b * s.n_heads + h) * s.Tq) * d + col;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int t = t0 + warp * rpw + r0; t < t1; t += (kSelThreads / 32) * rpw) {
+        float f[8];
+        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(qb + (size_t)t * d)), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+      }
+      for (int o = vec_l; o < 32; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+      if (r0 == 0)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ct[warp * D4 + col + i] = acc[i];   // ct used as scratch here
+      __syncthreads();
+      for (int c = tid; c < d; c += kSelThreads) {
+        float sum = 0.0f;
+        for (int w = 0; w < kSelThreads / 32; ++w) sum += ct[w * D4 + c];
+        qm[a * D4 + c] = sum / (float)(t1 - t0);
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    for (int c = tid; c < d; c += kSelThreads) {
-      float acc = 0.0f;
-      for (int g = 0; g < groups; ++g) acc += ct[g * D4 + c];
-      qm[a * D4 + c] = acc / (float)(t1 - t0);
+  } else {
+    const int groups = min(kSelBT, max(1, kSelThreads / d));
+    const int gidx = tid / d, dim = tid % d;
+    for (int a = 0; a < kSelQT; ++a) {
+      const int alpha = a0 + a;
+      if (alpha >= s.nQb) break;
+      const int t0 = alpha * s.q_block, t1 = min(s.Tq, t0 + s.q_block);
+      const T* qb = q + (((size_t)b * s.n_heads + h) * s.Tq) * d;
+      for (int c = dim; c < d; c += (d > kSelThreads ? kSelThreads : d)) {
+        float acc = 0.0f;
+        if (gidx < groups)
+          for (int t = t0 + gidx; t < t1; t += groups) acc += to_f32(qb[(size_t)t * d + c]);
+        if (gidx < groups) ct[gidx * D4 + c] = acc;   // ct used as scratch here
+      }
+      __syncthreads();
+      for (int c = tid; c < d; c += kSelThreads) {
+        float acc = 0.0f;
+        for (int g = 0; g < groups; ++g) acc += ct[g * D4 + c];
+        qm[a * D4 + c] = acc / (float)(t1 - t0);
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
   // rowmax holds an order-preserving integer image of the float maximum during pass A
   for (int c = tid; c < kSelQT; c += kSelThreads) {
