@@ -155,20 +155,27 @@ block_stats_vec_kernel(const __nv_bfloat16* __restrict__ k, const int32_t* __res
 }
 
 // ---------------------------------------------------------------------------------------
-// Block selection.  One CTA per (group of kSelQT query blocks, query head, sequence).
+// Block selection.  One CTA per (kSelQT query blocks, query head, sequence), 8 warps.
 //   1. radius mean and population std over the kv head's key blocks, in fp64 (fixed tree,
 //      so every CTA of the kv head gets identical values), and the rescue flags;
-//   2. the mean query row of each query block (q read once, coalesced);
-//   3. pass A: every visible (query block, key block) score q_mean . c / sqrt(d) in fp32,
-//      reduced to the row maximum;
-//   4. pass B: the same scores recomputed bit for bit, thresholded, OR-ed with the rescue
-//      and diagonal flags, and written as the mask row (0 beyond the visible range).
-// Scores are not stored, so the kernel takes any number of key blocks in little shared
+//   2. the mean query row of each query block (q read once, 16-byte loads), stored
+//      dimension-major: qmt[c][a];
+//   3. per query block, the visible key-block range [vlo, vhi) and the diagonal range;
+//   4. pass A: the scores q_mean . c / sqrt(d) of tiles of kSelBT key blocks (centroids
+//      staged dimension-major, ctt[c][beta]); warp w owns query blocks 4w .. 4w+3 and lane
+//      l key blocks 4l .. 4l+3 of the tile, so each step is one broadcast 16-byte load of
+//      four query means and one 16-byte load of four centroids for 16 FMAs; the row
+//      maximum over visible blocks needs no atomics (one warp owns the row);
+//   5. pass B: the same scores recomputed bit for bit (same operations, same order),
+//      thresholded, OR-ed with the rescue and diagonal flags, written as the mask row.
+// Scores are not stored, so any number of key blocks fits in a fixed amount of shared
 // memory; the recomputation doubles a cost that is small next to the attention itself.
 // ---------------------------------------------------------------------------------------
 constexpr int kSelThreads = 256;
-constexpr int kSelQT = 16;        // query blocks per CTA (2 per thread row group)
-constexpr int kSelBT = 64;        // key blocks per centroid tile (2 per thread)
+constexpr int kSelQT = 32;        // query blocks per CTA (4 per warp)
+constexpr int kSelBT = 128;       // key blocks per centroid tile (4 per lane)
+constexpr int kSelQS = kSelQT + 4;   // row stride (floats) of qmt
+constexpr int kSelCS = kSelBT + 4;   // row stride (floats) of ctt
 
 struct SelectShape {
   int batch, n_heads, n_kv, d, Tq, Tk, nKb_out, q_block, k_block, causal, window;
@@ -176,35 +183,11 @@ struct SelectShape {
   float tau_mean, lambda_radius;
 };
 
-__device__ __forceinline__ bool block_visible(const SelectShape& s, int alpha, int beta) {
-  if (!s.causal) return beta < s.nKb;
-  const long long t0 = (long long)alpha * s.q_block;
-  const long long t1 = min((long long)s.Tq, t0 + s.q_block);
-  const long long i_first = (long long)s.Tk - s.Tq + t0, i_last = (long long)s.Tk - s.Tq + t1 - 1;
-  const long long j_lo = (long long)beta * s.k_block;
-  const long long j_hi = min(j_lo + s.k_block, (long long)s.Tk) - 1;
-  if (beta >= s.nKb || j_lo > i_last) return false;
-  if (s.window > 0 && j_hi <= i_first - s.window) return false;
-  return true;
+// shared memory: qmt [d][kSelQS] | ctt [d][kSelCS] | red [8] double | rowmax [QT] | nsel [QT]
+// | ranges [QT][4] | rescue [nKb]
+__host__ __device__ inline size_t select_smem_bytes(int d, int nKb) {
+  return (size_t)d * (kSelQS + kSelCS) * 4 + (kSelThreads / 32) * 8 + kSelQT * 4 * 6 + (size_t)nKb + 16;
 }
-
-__device__ __forceinline__ bool block_diagonal(const SelectShape& s, int alpha, int beta) {
-  const long long t0 = (long long)alpha * s.q_block;
-  const long long t1 = min((long long)s.Tq, t0 + s.q_block);
-  const long long i_first = (long long)s.Tk - s.Tq + t0, i_last = (long long)s.Tk - s.Tq + t1 - 1;
-  const long long j_lo = (long long)beta * s.k_block;
-  const long long j_hi = min(j_lo + s.k_block, (long long)s.Tk) - 1;
-  return j_lo <= i_last && j_hi >= i_first;
-}
-
-template <int D4>   // padded row stride (floats) of the shared q_mean / centroid tiles
-struct SelectSmem {
-  float qm[kSelQT][D4];
-  float ct[kSelBT][D4];
-  double red[kSelThreads / 32];
-  float rowmax[kSelQT];
-  int nsel[kSelQT];
-};
 
 template <typename T>
 __global__ void __launch_bounds__(kSelThreads)
@@ -212,18 +195,18 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
                      const float* __restrict__ radius, uint8_t* __restrict__ block_mask,
                      int32_t* __restrict__ n_selected, SelectShape s) {
   extern __shared__ __align__(16) unsigned char sel_smem_raw[];
-  const int D4 = (s.d + 3) / 4 * 4 + 4;
-  float* qm = reinterpret_cast<float*>(sel_smem_raw);                 // [kSelQT][D4]
-  float* ct = qm + kSelQT * D4;                                       // [kSelBT][D4]
-  double* red = reinterpret_cast<double*>(ct + kSelBT * D4);          // [kSelThreads/32]
-  float* rowmax = reinterpret_cast<float*>(red + kSelThreads / 32);   // [kSelQT]
-  int* nsel = reinterpret_cast<int*>(rowmax + kSelQT);                // [kSelQT]
-  uint8_t* rescue = reinterpret_cast<uint8_t*>(nsel + kSelQT);        // [nKb]
+  const int d = s.d;
+  float* qmt = reinterpret_cast<float*>(sel_smem_raw);                 // [d][kSelQS]
+  float* ctt = qmt + (size_t)d * kSelQS;                               // [d][kSelCS]
+  double* red = reinterpret_cast<double*>(ctt + (size_t)d * kSelCS);   // [8]
+  float* rowmax = reinterpret_cast<float*>(red + kSelThreads / 32);    // [QT]
+  int* nsel = reinterpret_cast<int*>(rowmax + kSelQT);                 // [QT]
+  int* rng = nsel + kSelQT;                                            // [QT][4]
+  uint8_t* rescue = reinterpret_cast<uint8_t*>(rng + 4 * kSelQT);      // [nKb]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int a0 = blockIdx.x * kSelQT, h = blockIdx.y, b = blockIdx.z;
   const int kvh = h / (s.n_heads / s.n_kv);
-  const int d = s.d;
   const float* rrow = radius + ((size_t)b * s.n_kv + kvh) * s.nKb_out;
   const float* cbase = centroid + ((size_t)b * s.n_kv + kvh) * (size_t)s.nKb_out * d;
 
@@ -247,163 +230,179 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
     part += e * e;
   }
   const double sigma = sqrt(block_sum(part) / s.nKb);
-  for (int x = tid; x < s.nKb; x += kSelThreads) {
+  for (int x = tid; x < s.nKb; x += kSelThreads)
     rescue[x] = (sigma > 0.0 && ((double)rrow[x] - mu) / sigma >= (double)s.lambda_radius) ? 1 : 0;
-  }
 
-  // ---- 2. mean query row of each query block of this CTA --------------------------------
-  const int vec_l = d / 8;                       // lanes per row for 16-byte bf16 loads
-  if (sizeof(T) == 2 && d % 8 == 0 && 32 % vec_l == 0) {
-    // 16-byte loads: lane l reads dims 8*(l % L) .. of rows l / L, l / L + 32/L, ... of the
-    // warp's share; sums meet by shuffles, then across the 8 warps in shared memory
-    const int rpw = 32 / vec_l;                  // rows per warp-wide load
-    const int col = 8 * (lane % vec_l), r0 = lane / vec_l;
-    for (int a = 0; a < kSelQT; ++a) {
-      const int alpha = a0 + a;
-      if (alpha >= s.nQb) break;
-      const int t0 = alpha * s.q_block, t1 = min(s.Tq, t0 + s.q_block);
-      const T* qb = q + (((size_t)b * s.n_heads + h) * s.Tq) * d + col;
+  // ---- 2. mean query row of each query block of this CTA -> qmt[c][a] --------------------
+  // Warp w pools query blocks 4w .. 4w+3 on its own (no CTA-wide barrier between blocks).
+  const int vec_l = d / 8;
+  for (int i = 0; i < 4; ++i) {
+    const int a = 4 * warp + i, alpha = a0 + a;
+    if (alpha >= s.nQb) {                                             // padding rows: zeros
+      for (int c = lane; c < d; c += 32) qmt[c * kSelQS + a] = 0.0f;
+      continue;
+    }
+    const int t0 = alpha * s.q_block, t1 = min(s.Tq, t0 + s.q_block);
+    const float inv_n = 1.0f / (float)(t1 - t0);
+    const T* qb = q + (((size_t)b * s.n_heads + h) * s.Tq) * d;
+    if (sizeof(T) == 2 && d % 8 == 0 && 32 % vec_l == 0) {
+      // 16-byte loads: lane l reads dims 8*(l % L) .. of rows l / L, l / L + 32/L, ...
+      const int rpw = 32 / vec_l, col = 8 * (lane % vec_l), r0 = lane / vec_l;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int t = t0 + warp * rpw + r0; t < t1; t += (kSelThreads / 32) * rpw) {
+#pragma unroll 8
+      for (int t = t0 + r0; t < t1; t += rpw) {
         float f[8];
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(qb + (size_t)t * d)), f);
+        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(qb + (size_t)t * d + col)), f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        for (int k = 0; k < 8; ++k) acc[k] += f[k];
       }
       for (int o = vec_l; o < 32; o <<= 1)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+        for (int k = 0; k < 8; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
       if (r0 == 0)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ct[warp * D4 + col + i] = acc[i];   // ct used as scratch here
-      __syncthreads();
-      for (int c = tid; c < d; c += kSelThreads) {
-        float sum = 0.0f;
-        for (int w = 0; w < kSelThreads / 32; ++w) sum += ct[w * D4 + c];
-        qm[a * D4 + c] = sum / (float)(t1 - t0);
-      }
-      __syncthreads();
-    }
-  } else {
-    const int groups = min(kSelBT, max(1, kSelThreads / d));
-    const int gidx = tid / d, dim = tid % d;
-    for (int a = 0; a < kSelQT; ++a) {
-      const int alpha = a0 + a;
-      if (alpha >= s.nQb) break;
-      const int t0 = alpha * s.q_block, t1 = min(s.Tq, t0 + s.q_block);
-      const T* qb = q + (((size_t)b * s.n_heads + h) * s.Tq) * d;
-      for (int c = dim; c < d; c += (d > kSelThreads ? kSelThreads : d)) {
+        for (int k = 0; k < 8; ++k) qmt[(col + k) * kSelQS + a] = acc[k] * inv_n;
+    } else {
+      for (int c = lane; c < d; c += 32) {
         float acc = 0.0f;
-        if (gidx < groups)
-          for (int t = t0 + gidx; t < t1; t += groups) acc += to_f32(qb[(size_t)t * d + c]);
-        if (gidx < groups) ct[gidx * D4 + c] = acc;   // ct used as scratch here
-      }
-      __syncthreads();
-      for (int c = tid; c < d; c += kSelThreads) {
-        float acc = 0.0f;
-        for (int g = 0; g < groups; ++g) acc += ct[g * D4 + c];
-        qm[a * D4 + c] = acc / (float)(t1 - t0);
-      }
-      __syncthreads();
-    }
-  }
-  // rowmax holds an order-preserving integer image of the float maximum during pass A
-  for (int c = tid; c < kSelQT; c += kSelThreads) {
-    reinterpret_cast<int*>(rowmax)[c] = INT_MIN;
-    nsel[c] = 0;
-  }
-  if (tid < kSelQT) {
-    for (int c = d; c < D4; ++c) qm[tid * D4 + c] = 0.0f;
-  }
-
-  // key-block range seen by any query block of the CTA
-  const int a_last = min(s.nQb, a0 + kSelQT) - 1;
-  int beta_hi = s.nKb;
-  if (s.causal) {
-    const long long t1 = min((long long)s.Tq, (long long)(a_last + 1) * s.q_block);
-    const long long i_last = (long long)s.Tk - s.Tq + t1 - 1;
-    beta_hi = (int)min((long long)s.nKb, i_last / s.k_block + 1);
-  }
-  int beta_lo = 0;
-  if (s.causal && s.window > 0) {
-    const long long i_first = (long long)s.Tk - s.Tq + (long long)a0 * s.q_block;
-    beta_lo = (int)max(0LL, (i_first - s.window + 1) / s.k_block);
-  }
-  const float scale = 1.0f / sqrtf((float)d);
-  // thread -> 2 query blocks x 2 key blocks of the tile
-  const int ta = 2 * (tid / (kSelBT / 2));
-  const int tb = 2 * (tid % (kSelBT / 2));
-
-  for (int pass = 0; pass < 2; ++pass) {
-    __syncthreads();
-    for (int bt = beta_lo; bt < beta_hi; bt += kSelBT) {
-      // stage centroid tile [kSelBT][d] (zero-padded) into shared memory
-      for (int e = tid; e < kSelBT * D4; e += kSelThreads) {
-        const int r = e / D4, c = e % D4;
-        const int beta = bt + r;
-        ct[e] = (beta < beta_hi && c < d) ? cbase[(size_t)beta * d + c] : 0.0f;
-      }
-      __syncthreads();
-      float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      const float* q0 = qm + ta * D4;
-      const float* q1 = qm + (ta + 1) * D4;
-      const float* c0 = ct + tb * D4;
-      const float* c1 = ct + (tb + 1) * D4;
-      for (int c = 0; c < D4; c += 4) {
-        const float4 x0 = *reinterpret_cast<const float4*>(q0 + c);
-        const float4 x1 = *reinterpret_cast<const float4*>(q1 + c);
-        const float4 y0 = *reinterpret_cast<const float4*>(c0 + c);
-        const float4 y1 = *reinterpret_cast<const float4*>(c1 + c);
-        acc[0][0] = __fmaf_rn(x0.x, y0.x, acc[0][0]); acc[0][0] = __fmaf_rn(x0.y, y0.y, acc[0][0]);
-        acc[0][0] = __fmaf_rn(x0.z, y0.z, acc[0][0]); acc[0][0] = __fmaf_rn(x0.w, y0.w, acc[0][0]);
-        acc[0][1] = __fmaf_rn(x0.x, y1.x, acc[0][1]); acc[0][1] = __fmaf_rn(x0.y, y1.y, acc[0][1]);
-        acc[0][1] = __fmaf_rn(x0.z, y1.z, acc[0][1]); acc[0][1] = __fmaf_rn(x0.w, y1.w, acc[0][1]);
-        acc[1][0] = __fmaf_rn(x1.x, y0.x, acc[1][0]); acc[1][0] = __fmaf_rn(x1.y, y0.y, acc[1][0]);
-        acc[1][0] = __fmaf_rn(x1.z, y0.z, acc[1][0]); acc[1][0] = __fmaf_rn(x1.w, y0.w, acc[1][0]);
-        acc[1][1] = __fmaf_rn(x1.x, y1.x, acc[1][1]); acc[1][1] = __fmaf_rn(x1.y, y1.y, acc[1][1]);
-        acc[1][1] = __fmaf_rn(x1.z, y1.z, acc[1][1]); acc[1][1] = __fmaf_rn(x1.w, y1.w, acc[1][1]);
-      }
-#pragma unroll
-      for (int ia = 0; ia < 2; ++ia) {
-        const int alpha = a0 + ta + ia;
-        if (alpha >= s.nQb) continue;
-#pragma unroll
-        for (int ib = 0; ib < 2; ++ib) {
-          const int beta = bt + tb + ib;
-          if (beta >= beta_hi || !block_visible(s, alpha, beta)) continue;
-          const float score = __fmul_rn(acc[ia][ib], scale);
-          if (pass == 0) {
-            // scores are finite; order-preserving integer max on the float bits
-            atomicMax(reinterpret_cast<int*>(&rowmax[ta + ia]),
-                      __float_as_int(score) >= 0 ? __float_as_int(score) : (int)(0x80000000u ^ ~__float_as_uint(score)));
-          } else {
-            const bool keep = score >= rowmax[ta + ia] - s.tau_mean || rescue[beta] ||
-                              block_diagonal(s, alpha, beta);
-            block_mask[(((size_t)b * s.n_heads + h) * s.nQb + alpha) * s.nKb_out + beta] = keep;
-            if (keep) atomicAdd(&nsel[ta + ia], 1);
-          }
-        }
-      }
-      __syncthreads();
-    }
-    if (pass == 0) {
-      __syncthreads();
-      if (tid < kSelQT) {   // decode the order-preserving integer back to the float
-        const int x = reinterpret_cast<int*>(rowmax)[tid];
-        rowmax[tid] = x >= 0 ? __int_as_float(x) : __uint_as_float(~((unsigned)x ^ 0x80000000u));
+        for (int t = t0; t < t1; ++t) acc += to_f32(qb[(size_t)t * d + c]);
+        qmt[c * kSelQS + a] = acc * inv_n;
       }
     }
   }
   __syncthreads();
-  // zero the rest of each mask row (invisible key blocks and blocks without keys)
+
+  // ---- 3. visible and diagonal key-block ranges of each query block ----------------------
+  if (tid < kSelQT) {
+    const int alpha = a0 + tid;
+    int vlo = 0, vhi = 0, dlo = 1, dhi = 0;                            // empty by default
+    if (alpha < s.nQb) {
+      const long long t0 = (long long)alpha * s.q_block;
+      const long long t1 = min((long long)s.Tq, t0 + s.q_block);
+      const long long i_first = (long long)s.Tk - s.Tq + t0, i_last = (long long)s.Tk - s.Tq + t1 - 1;
+      vhi = s.causal ? (int)min((long long)s.nKb, i_last / s.k_block + 1) : s.nKb;
+      if (s.causal && s.window > 0) {
+        const long long x = i_first - s.window + 1;                    // first key a row may see
+        vlo = x <= 0 ? 0 : (int)(x / s.k_block);
+      }
+      dlo = (int)(i_first / s.k_block);
+      dhi = (int)min((long long)s.nKb - 1, i_last / s.k_block);
+    }
+    rng[4 * tid + 0] = vlo; rng[4 * tid + 1] = vhi; rng[4 * tid + 2] = dlo; rng[4 * tid + 3] = dhi;
+    rowmax[tid] = -INFINITY;
+    nsel[tid] = 0;
+  }
+  __syncthreads();
+  int beta_lo = s.nKb, beta_hi = 0;                                   // union over the CTA
+  for (int a = 0; a < kSelQT; ++a) {
+    if (rng[4 * a + 1] > rng[4 * a]) {
+      beta_lo = min(beta_lo, rng[4 * a]);
+      beta_hi = max(beta_hi, rng[4 * a + 1]);
+    }
+  }
+  if (beta_hi <= beta_lo) beta_lo = beta_hi = 0;
+  int my_vlo[4], my_vhi[4], my_dlo[4], my_dhi[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int a = 4 * warp + i;
+    my_vlo[i] = rng[4 * a]; my_vhi[i] = rng[4 * a + 1]; my_dlo[i] = rng[4 * a + 2]; my_dhi[i] = rng[4 * a + 3];
+  }
+  const float scale = 1.0f / sqrtf((float)d);
+  const bool vec_mask = (s.nKb_out % 4) == 0 && (reinterpret_cast<uintptr_t>(block_mask) & 3) == 0;
+
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int bt = beta_lo; bt < beta_hi; bt += kSelBT) {
+      // stage centroids of key blocks bt .. bt+127 dimension-major (zeros past beta_hi)
+      __syncthreads();
+      if (d % 4 == 0) {                                               // rows are 16-byte aligned
+        for (int e = tid; e < kSelBT * (d / 4); e += kSelThreads) {
+          const int r = e % kSelBT, c4 = e / kSelBT;
+          const int beta = bt + r;
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (beta < beta_hi) v = *reinterpret_cast<const float4*>(cbase + (size_t)beta * d + 4 * c4);
+          ctt[(4 * c4 + 0) * kSelCS + r] = v.x;
+          ctt[(4 * c4 + 1) * kSelCS + r] = v.y;
+          ctt[(4 * c4 + 2) * kSelCS + r] = v.z;
+          ctt[(4 * c4 + 3) * kSelCS + r] = v.w;
+        }
+      } else {
+        for (int e = tid; e < kSelBT * d; e += kSelThreads) {
+          const int r = e % kSelBT, c = e / kSelBT;
+          const int beta = bt + r;
+          ctt[c * kSelCS + r] = beta < beta_hi ? cbase[(size_t)beta * d + c] : 0.0f;
+        }
+      }
+      __syncthreads();
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.0f;
+      const float* qp = qmt + 4 * warp;
+      const float* cp = ctt + 4 * lane;
+#pragma unroll 4
+      for (int c = 0; c < d; ++c) {       // fused multiply-adds in dimension order, two per op
+        const float4 x = *reinterpret_cast<const float4*>(qp + c * kSelQS);
+        const float4 y = *reinterpret_cast<const float4*>(cp + c * kSelCS);
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ffma2(acc[i][0], acc[i][1], y.x, y.y, xs[i], xs[i], acc[i][0], acc[i][1]);
+          ffma2(acc[i][2], acc[i][3], y.z, y.w, xs[i], xs[i], acc[i][2], acc[i][3]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int a = 4 * warp + i, alpha = a0 + a;
+        if (alpha >= s.nQb) continue;                                  // warp-uniform
+        if (pass == 0) {
+          float m = -INFINITY;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int beta = bt + 4 * lane + jj;
+            if (beta >= my_vlo[i] && beta < my_vhi[i]) m = fmaxf(m, __fmul_rn(acc[i][jj], scale));
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) rowmax[a] = fmaxf(rowmax[a], m);
+        } else {
+          const float thr = rowmax[a] - s.tau_mean;
+          uint32_t bytes = 0u;
+          int kept = 0;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int beta = bt + 4 * lane + jj;
+            const bool vis = beta >= my_vlo[i] && beta < my_vhi[i];
+            const bool keep = vis && (__fmul_rn(acc[i][jj], scale) >= thr || rescue[beta] != 0 ||
+                                      (beta >= my_dlo[i] && beta <= my_dhi[i]));
+            bytes |= (keep ? 1u : 0u) << (8 * jj);
+            kept += keep ? 1 : 0;
+          }
+          uint8_t* mrow = block_mask + (((size_t)b * s.n_heads + h) * s.nQb + alpha) * s.nKb_out;
+          const int beta0 = bt + 4 * lane;
+          if (vec_mask && beta0 + 3 < s.nKb_out) {
+            *reinterpret_cast<uint32_t*>(mrow + beta0) = bytes;
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              if (beta0 + jj < s.nKb_out) mrow[beta0 + jj] = (uint8_t)((bytes >> (8 * jj)) & 1u);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
+          if (lane == 0) nsel[a] += kept;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // zero the rest of each mask row (key blocks outside the CTA's tiles)
+  const int tiles_end = beta_lo + ((beta_hi - beta_lo + kSelBT - 1) / kSelBT) * kSelBT;
   for (int a = 0; a < kSelQT; ++a) {
     const int alpha = a0 + a;
     if (alpha >= s.nQb) break;
     uint8_t* mrow = block_mask + (((size_t)b * s.n_heads + h) * s.nQb + alpha) * s.nKb_out;
-    for (int beta = tid; beta < s.nKb_out; beta += kSelThreads) {
-      if (beta < beta_lo || beta >= beta_hi || !block_visible(s, alpha, beta)) mrow[beta] = 0;
-    }
+    for (int beta = tid; beta < s.nKb_out; beta += kSelThreads)
+      if (beta < beta_lo || beta >= tiles_end) mrow[beta] = 0;
     if (tid == 0 && n_selected) n_selected[((size_t)b * s.n_heads + h) * s.nQb + alpha] = nsel[a];
   }
 }

@@ -425,10 +425,10 @@ int ga_select_blocks(const void* q, const float* centroid, const float* radius, 
   s.nKb_out = nKb_out; s.q_block = q_block; s.k_block = k_block; s.causal = causal;
   s.window = window; s.nQb = (Tq + q_block - 1) / q_block; s.nKb = (int)nKb;
   s.tau_mean = tau_mean; s.lambda_radius = lambda_radius;
-  const int D4 = (d + 3) / 4 * 4 + 4;
-  const size_t smem = (size_t)(kSelQT + kSelBT) * D4 * 4 + (kSelThreads / 32) * 8 + kSelQT * 8 + nKb + 16;
-  static int ok_bf = set_smem(select_blocks_kernel<__nv_bfloat16>, 200 * 1024);
-  static int ok_f = set_smem(select_blocks_kernel<float>, 200 * 1024);
+  const size_t smem = select_smem_bytes(d, (int)nKb);
+  if (smem > 220 * 1024) return GA_ERR_UNSUPPORTED;
+  static int ok_bf = set_smem(select_blocks_kernel<__nv_bfloat16>, 220 * 1024);
+  static int ok_f = set_smem(select_blocks_kernel<float>, 220 * 1024);
   if (ok_bf != GA_OK || ok_f != GA_OK) return GA_ERR_CUDA;
   dim3 grid((s.nQb + kSelQT - 1) / kSelQT, n_heads, batch);
   if (dtype == GA_BF16)
