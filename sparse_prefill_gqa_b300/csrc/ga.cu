@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "decode.cuh"
 #include "prefill_pair.cuh"
+#include "prefill_wide.cuh"
 #include "prefill_tc.cuh"
 
 namespace ga {
@@ -279,7 +280,18 @@ int ga_attend(const void* q, const void* k, const void* v, void* out, int batch,
       return GA_ERR_CUDA;
     (void)BN;
     dim3 grid((Tq + 127) / 128, n_heads, batch);
-    if (d == 128) {
+    if (d == 128 && block_mask == nullptr) {
+      using C = WideCfg<128>;
+      CUtensorMap tk2, tv2;                             // boxes of 128 keys (K) and VK = 128 keys (V)
+      if (!make_map_bf16(&tk2, k, d, Tk_max, (long long)batch * n_kv, 128) ||
+          !make_map_bf16(&tv2, v, d, Tk_max, (long long)batch * n_kv, C::VK))
+        return GA_ERR_CUDA;
+      static int ok = set_smem(prefill_wide_kernel<128>, C::SMEM_BYTES);
+      if (ok != GA_OK) return ok;
+      const long long n_cta = (long long)((Tq + C::BM - 1) / C::BM) * n_heads * batch;
+      if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+      prefill_wide_kernel<128><<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk2, tv2, ob, lse, sh);
+    } else if (d == 128) {
       using C = PairCfg;
       static int ok = set_smem(prefill_pair_kernel, C::SMEM_BYTES);
       if (ok != GA_OK) return ok;
@@ -287,6 +299,16 @@ int ga_attend(const void* q, const void* k, const void* v, void* out, int batch,
       const long long n_cta = n_pairs * n_heads * batch;
       if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
       prefill_pair_kernel<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, ob, lse, sh);
+    } else if (block_mask == nullptr) {
+      using C = WideCfg<256>;
+      CUtensorMap tk2;                                  // K boxes of 128 keys; V boxes of VK = 64 keys (tv)
+      static_assert(WideCfg<256>::VK == 64, "the V map's box is 64 keys");
+      if (!make_map_bf16(&tk2, k, d, Tk_max, (long long)batch * n_kv, 128)) return GA_ERR_CUDA;
+      static int ok = set_smem(prefill_wide_kernel<256>, C::SMEM_BYTES);
+      if (ok != GA_OK) return ok;
+      const long long n_cta = (long long)((Tq + C::BM - 1) / C::BM) * n_heads * batch;
+      if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+      prefill_wide_kernel<256><<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk2, tv, ob, lse, sh);
     } else {
       using C = PrefillCfg<256, 64>;
       static int ok = set_smem(prefill_tc_kernel<256, 64>, C::SMEM_BYTES);

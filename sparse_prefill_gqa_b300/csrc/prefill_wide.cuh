@@ -1,0 +1,380 @@
+// prefill_wide.cuh -- bf16 attention prefill, one 128-row query tile per CTA, head dim 128 or
+// 256 (dense, causal, window, sink).
+//
+// What it computes: the same attention as the other prefill kernels ("Attention in Code",
+// "one function all designs use": scores q.k/sqrt(d), masked positions removed, optional sink
+// logit in the normaliser, weighted sum of values; section 1 head grouping; the
+// absolute-position causal rule; the sliding window of section 2).
+//
+// One CTA per (128-row query tile, query head, sequence), heaviest causal tiles first.
+//   warps 0-3  softmax: thread r = query row r = TMEM lane r;
+//   warp 4     TMA producer (one lane): Q once, then K and V through a ring of 32 KB chunks
+//              (6 for d = 128, 4 for d = 256) -- a K chunk is 128 keys x 128 dims, a V chunk
+//              16384/d keys x d dims -- K one tile ahead of V;
+//   warp 5     MMA issuer (one lane).
+// Tensor memory: O [0,d), S buffers [d,d+128) and [d+128,d+256), N = 128 keys.
+// The issuer runs S(j+1) = Q K(j+1)^T before PV(j), so the softmax of tile j overlaps a whole
+// tile of tensor work; P(j) (bf16) is written over the first 64 columns of S buffer j&1 and
+// read from there by the PV MMA.  Since one thread issues every MMA and they complete in
+// order, S(j+2) overwrites P(j) only after PV(j) read it.  When the softmax of tile j must
+// rescale O, PV(j-1) may still run (S(j) was issued before it), so it waits for that one PV;
+// PV(j-2) is complete (S(j) was issued after it), so a parity wait on the per-PV barrier is
+// exact.  The epilogue waits on its own barrier, committed after the last PV.
+// Value rows past a sequence's end are zeroed by the producer before the chunk is published
+// (P is 0 there, but 0 * NaN = NaN for an uninitialised cache).
+#pragma once
+
+#include "common.cuh"
+#include "prefill_tc.cuh"
+
+namespace ga {
+
+template <int D_>
+struct WideCfg {
+  static constexpr int D = D_;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int Q_BYTES = BM * D * 2;            // D/64 slabs of 128 rows x 128 B
+  static constexpr int CHUNK = 32768;                   // ring chunk
+  static constexpr int KCH = D / 128;                   // K chunks per key tile (128 dims each)
+  static constexpr int VCH = D / 128;                   // V chunks per key tile
+  static constexpr int VK = 16384 / D;                  // keys per V chunk
+  static constexpr int RING = D == 128 ? 6 : 4;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = OFF_Q + Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + RING * CHUNK;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t COL_O = 0, COL_S = D;       // O [0,D), S_b at D + 128 b
+  static_assert(D == 128 || D == 256, "head dim");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(D + 2 * BN <= 512, "tensor memory budget");
+};
+
+struct WideBars {
+  uint64_t q_full;
+  uint64_t full[6], empty[6];
+  uint64_t s_full[2], p_full, o_done, o_final, v_tail, mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// grid: (n_qt * n_heads * batch); block: 192 threads; 1 CTA per SM.
+template <int D_>
+__global__ void __launch_bounds__(192, 1)
+prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+                    float* __restrict__ lse, AttnShape sh) {
+  using C = WideCfg<D_>;
+  constexpr int D = C::D, BN = C::BN;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = smem + C::OFF_Q;
+  unsigned char* sR = smem + C::OFF_RING;
+  WideBars* bars = reinterpret_cast<WideBars*>(smem + C::OFF_BAR);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_qt = (sh.Tq + C::BM - 1) / C::BM;
+  const int hb = sh.n_heads * sh.batch;
+  const int qr = (int)(blockIdx.x / hb), rem = (int)(blockIdx.x % hb);
+  const int h = rem % sh.n_heads, b = rem / sh.n_heads;
+  const int qt = n_qt - 1 - qr;                          // heaviest causal tiles first
+  const int kvh = h / (sh.n_heads / sh.n_kv);
+  const uint64_t tmo = sh.timeout_ns;
+  const int Tk = seq_keys(sh.k_lens, b, sh.Tk_max);
+
+  // key range of the tile's rows and its 128-key tiles
+  const int t0 = qt * C::BM;
+  const int rows = min(C::BM, sh.Tq - t0);
+  const long long i_first = (long long)Tk - sh.Tq + t0, i_last = i_first + rows - 1;
+  const int key_lo = sh.window > 0 ? (int)max(0LL, i_first - sh.window + 1) : 0;
+  int key_hi = sh.causal ? (int)min((long long)Tk, i_last + 1) : Tk;
+  if (key_hi < key_lo) key_hi = key_lo;
+  const int kt_lo = key_lo / BN;
+  const int n_tiles = key_hi > key_lo ? (key_hi + BN - 1) / BN - kt_lo : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::RING; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_final, 1);
+    mbar_init(&bars->v_tail, 1);
+    mbar_init(&bars->mma_drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 5) tmem_alloc(&bars->tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int qz = b * sh.n_heads + h, kz = b * sh.n_kv + kvh;
+      mbar_arrive_expect_tx(&bars->q_full, C::Q_BYTES);
+      for (int s = 0; s < D / 64; ++s)
+        tma_load_3d(sQ + s * C::BM * 128, &tm_q, &bars->q_full, 64 * s, t0, qz);
+      int cnt = 0, n_tail = 0;                           // chunks issued, tail chunks
+      bool ok = true;
+      // acquire ring slot for chunk number cnt
+      auto slot_acquire = [&](int& slot) -> bool {
+        slot = cnt % C::RING;
+        if (cnt >= C::RING && !mbar_wait(&bars->empty[slot], ((cnt / C::RING) + 1) & 1, tmo, abort_flag))
+          return false;
+        return true;
+      };
+      auto load_k = [&](int j) -> bool {                 // K(j): chunks of 128 dims
+        for (int c = 0; c < C::KCH; ++c) {
+          int slot;
+          if (!slot_acquire(slot)) return false;
+          unsigned char* dst = sR + slot * C::CHUNK;
+          mbar_arrive_expect_tx(&bars->full[slot], C::CHUNK);
+          for (int s = 0; s < 2; ++s)
+            tma_load_3d(dst + s * BN * 128, &tm_k, &bars->full[slot], 128 * c + 64 * s, (kt_lo + j) * BN, kz);
+          ++cnt;
+        }
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {                 // V(j): chunks of VK keys x D dims
+        for (int c = 0; c < C::VCH; ++c) {
+          int slot;
+          if (!slot_acquire(slot)) return false;
+          unsigned char* dst = sR + slot * C::CHUNK;
+          const int key0 = (kt_lo + j) * BN + C::VK * c;
+          const bool tail = key0 + C::VK > Tk;
+          uint64_t* bar = tail ? &bars->v_tail : &bars->full[slot];
+          mbar_arrive_expect_tx(bar, C::CHUNK);
+          for (int s = 0; s < D / 64; ++s) tma_load_3d(dst + s * C::VK * 128, &tm_v, bar, 64 * s, key0, kz);
+          if (tail) {
+            if (!mbar_wait(&bars->v_tail, n_tail & 1, tmo, abort_flag)) return false;
+            ++n_tail;
+            for (int row = max(0, Tk - key0); row < C::VK; ++row)
+              for (int s = 0; s < D / 64; ++s)
+                for (int q16 = 0; q16 < 8; ++q16)
+                  *reinterpret_cast<uint4*>(dst + s * C::VK * 128 + row * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->full[slot]);
+          }
+          ++cnt;
+        }
+        return true;
+      };
+      if (n_tiles > 0) ok = load_k(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) ok = load_k(j + 1);
+        if (ok) ok = load_v(j);
+      }
+      // Drain: the most recent chunk of every slot has landed before the CTA may exit.
+      mbar_wait(&bars->q_full, 0, tmo, nullptr);
+      for (int k = max(0, cnt - C::RING); k < cnt; ++k)
+        mbar_wait(&bars->full[k % C::RING], (k / C::RING) & 1, tmo, nullptr);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dr_k = sdesc_sw128(smem_u32(sR), 16, 1024);       // K chunks: K-major
+      const uint64_t dr_v = sdesc_sw128(smem_u32(sR), C::VK * 128, 1024);   // V chunks: MN-major
+      int cnt = 0;
+      bool ok = mbar_wait(&bars->q_full, 0, tmo, abort_flag);
+      // S(j) into buffer j & 1 from K(j)'s chunks
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t d_s = tmem + C::COL_S + (j & 1) * BN;
+        for (int c = 0; c < C::KCH; ++c) {
+          const int slot = cnt % C::RING;
+          if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
+          tc_fence_after();
+          const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
+#pragma unroll
+          for (int k8 = 0; k8 < 8; ++k8) {                // 8 steps of 16 dims in this chunk
+            const int kk = 8 * c + k8;
+            const uint64_t aq = dq + (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
+            const uint64_t bo = bk + (uint64_t)(((k8 >> 2) * BN * 128 + (k8 & 3) * 32) >> 4);
+            umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->empty[slot]);
+          ++cnt;
+        }
+        umma_commit(&bars->s_full[j & 1]);
+        return true;
+      };
+      // O += P(j) V(j), P in the first 64 columns of S buffer j & 1
+      uint32_t o_acc = 0u;
+      auto issue_pv = [&](int j) -> bool {
+        const uint32_t p_col = tmem + C::COL_S + (j & 1) * BN;
+        for (int c = 0; c < C::VCH; ++c) {
+          const int slot = cnt % C::RING;
+          if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
+          tc_fence_after();
+          const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
+#pragma unroll
+          for (int k4 = 0; k4 < C::VK / 16; ++k4) {       // steps of 16 keys in this chunk
+            const int kk = (C::VK / 16) * c + k4;
+            umma_bf16_ts(tmem + C::COL_O, p_col + kk * 8, bv + (uint64_t)((k4 * 2048) >> 4), idesc_pv,
+                         (o_acc | (uint32_t)k4) ? 1u : 0u);
+          }
+          o_acc = 1u;
+          umma_commit(&bars->empty[slot]);
+          ++cnt;
+        }
+        return true;
+      };
+      if (ok && n_tiles > 0) ok = issue_s(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
+        if (!(ok = mbar_wait(&bars->p_full, j & 1, tmo, abort_flag))) break;
+        tc_fence_after();
+        if (!(ok = issue_pv(j))) break;
+        umma_commit(&bars->o_done);
+        if (j + 1 == n_tiles) umma_commit(&bars->o_final);
+      }
+      // Drain: every MMA this thread issued has completed before TMEM can be released.
+      umma_commit(&bars->mma_drain);
+      mbar_wait(&bars->mma_drain, 0, tmo, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax warps 0-3
+    const int row = threadIdx.x;                      // query row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_o = tmem + C::COL_O + lane_off;
+    const long long i = i_first + row;                // absolute position of this row
+    const int lo = sh.window > 0 ? (int)max(0LL, i - sh.window + 1) : 0;
+    const int hi = sh.causal ? (int)min((long long)Tk, i + 1) : Tk;
+    const int lo_all = sh.window > 0 ? (int)max(0LL, i_last - sh.window + 1) : 0;
+    const int hi_all = sh.causal ? (int)min((long long)Tk, i_first + 1) : Tk;
+    const float scale_log2 = kLog2e / sqrtf((float)D);
+    float m_run = -INFINITY, l_run = 0.0f;
+    if (sh.sink) { m_run = sh.sink[h] * kLog2e; l_run = 1.0f; }
+
+    int n = 0;
+    for (; n < n_tiles; ++n) {
+      if (!warp_wait(&bars->s_full[n & 1], (n >> 1) & 1, tmo, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t t_s = tmem + C::COL_S + (n & 1) * BN + lane_off;
+      float sv[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+        tmem_ld32(t_s + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
+      tmem_wait_ld();
+      const int key0 = (kt_lo + n) * BN;
+      const bool interior = key0 >= lo_all && key0 + BN <= hi_all;
+      if (!interior) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const int jj = key0 + c;
+          sv[c] = (jj >= lo && jj < hi) ? sv[c] : -INFINITY;
+        }
+      }
+      float mx[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(sv[u], sv[u + 4]);
+#pragma unroll
+      for (int c = 8; c < BN; c += 8)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx[u] = fmax3(mx[u], sv[c + u], sv[c + u + 4]);
+      const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * scale_log2;
+      const bool need = m_tile > m_run + 8.0f;
+      const float m_new = need ? m_tile : m_run;
+      const float alpha = need ? ex2(m_run - m_new) : 1.0f;   // ex2(-inf) = 0
+      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          float e0, e1, e2, e3;
+          ffma2(e0, e1, sv[c0 + c], sv[c0 + c + 1], scale_log2, scale_log2, -m_use, -m_use);
+          ffma2(e2, e3, sv[c0 + c + 2], sv[c0 + c + 3], scale_log2, scale_log2, -m_use, -m_use);
+          const float p0 = ex2(e0), p1 = ex2(e1), p2 = ex2(e2), p3 = ex2(e3);
+          const int q = (c >> 1) & 2;
+          fadd2(ls[q], ls[q + 1], ls[q], ls[q + 1], p0, p1);
+          fadd2(ls[q + 4], ls[q + 5], ls[q + 4], ls[q + 5], p2, p3);
+          pk[c >> 1] = pack_bf16x2(p0, p1);
+          pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st16(t_s + c0 / 2, pk);
+      }
+      l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+      m_run = m_new;
+      if (n > 0 && __any_sync(0xffffffffu, need)) {
+        // PV(n-1) may still accumulate into O: wait for it (PV(n-2) is already complete)
+        if (!warp_wait(&bars->o_done, (n - 1) & 1, tmo, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] *= alpha;
+          tmem_st32(t_o + c, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full);
+    }
+
+    // ---- epilogue: O / l from TMEM to global ------------------------------------------
+    bool ok = __all_sync(0xffffffffu, *abort_flag == 0);
+    if (ok && n_tiles > 0) ok = warp_wait(&bars->o_final, 0, tmo, abort_flag);
+    tc_fence_after();
+    const int t = t0 + row;
+    const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    __nv_bfloat16* orow = out + (((size_t)b * sh.n_heads + h) * sh.Tq + t) * D;
+    if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float o[32];
+        if (n_tiles > 0) {
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] = 0.0f;
+        }
+        if (row < rows) {
+#pragma unroll
+          for (int u = 0; u < 32; u += 8) {
+            uint4 pk;
+            pk.x = pack_bf16x2(o[u + 0] * inv_l, o[u + 1] * inv_l);
+            pk.y = pack_bf16x2(o[u + 2] * inv_l, o[u + 3] * inv_l);
+            pk.z = pack_bf16x2(o[u + 4] * inv_l, o[u + 5] * inv_l);
+            pk.w = pack_bf16x2(o[u + 6] * inv_l, o[u + 7] * inv_l);
+            *reinterpret_cast<uint4*>(orow + c + u) = pk;
+          }
+        }
+      }
+      if (lse && row < rows)
+        lse[((size_t)b * sh.n_heads + h) * sh.Tq + t] =
+            l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace ga
