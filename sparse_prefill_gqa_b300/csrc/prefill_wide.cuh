@@ -9,17 +9,23 @@
 // One CTA per (128-row query tile, query head, sequence), heaviest causal tiles first.
 //   warps 0-3  softmax: thread r = query row r = TMEM lane r;
 //   warp 4     TMA producer (one lane): Q once, then K and V through a ring of 32 KB chunks
-//              (6 for d = 128, 4 for d = 256) -- a K chunk is 128 keys x 128 dims, a V chunk
+//              (4 slots) -- a K chunk is 128 keys x 128 dims, a V chunk
 //              16384/d keys x d dims -- K one tile ahead of V;
-//   warp 5     MMA issuer (one lane).
+//   warp 5     S issuer (one lane): S(j) = Q K(j)^T into S buffer j & 1;
+//   warp 6     PV issuer (one lane): O += P(j) V(j).
+// Two issuers (d = 128), because the tensor core's queue is short: a thread that issues an
+// MMA waits while earlier MMAs execute, so one thread that also waits for P would leave the
+// pipe idle.  For d = 256 a tile keeps the tensor core busy twice as long and warp 5 alone
+// issues everything, S(j+1) before PV(j) in issue order (in-order completion then makes S
+// overwrite P only after PV read it, without the per-buffer wait).
 // Tensor memory: O [0,d), S buffers [d,d+128) and [d+128,d+256), N = 128 keys.
-// The issuer runs S(j+1) = Q K(j+1)^T before PV(j), so the softmax of tile j overlaps a whole
-// tile of tensor work; P(j) (bf16) is written over the first 64 columns of S buffer j&1 and
-// read from there by the PV MMA.  Since one thread issues every MMA and they complete in
-// order, S(j+2) overwrites P(j) only after PV(j) read it.  When the softmax of tile j must
-// rescale O, PV(j-1) may still run (S(j) was issued before it), so it waits for that one PV;
-// PV(j-2) is complete (S(j) was issued after it), so a parity wait on the per-PV barrier is
-// exact.  The epilogue waits on its own barrier, committed after the last PV.
+// P(j) (bf16) is written over the first 64 columns of S buffer j&1 and read from there by the
+// PV MMA.  S(j+2) overwrites P(j), so the S issuer waits for PV(j) to complete (a per-buffer
+// barrier) before it issues S(j+2); the softmax of tile j therefore overlaps PV(j-1) and
+// S(j+1).  When the softmax of tile j must rescale O, PV(j-1) may still run, so it waits for
+// that one PV; PV(j-2) is complete (S(j) was issued after it completed), so a parity wait on
+// the per-PV barrier is exact.  The epilogue waits on its own barrier, committed after the
+// last PV.
 // Value rows past a sequence's end are zeroed by the producer before the chunk is published
 // (P is 0 there, but 0 * NaN = NaN for an uninitialised cache).
 #pragma once
@@ -38,12 +44,15 @@ struct WideCfg {
   static constexpr int KCH = D / 128;                   // K chunks per key tile (128 dims each)
   static constexpr int VCH = D / 128;                   // V chunks per key tile
   static constexpr int VK = 16384 / D;                  // keys per V chunk
-  static constexpr int RING = D == 128 ? 6 : 4;
+  static constexpr int RING = 4;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = OFF_Q + Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + RING * CHUNK;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-  static constexpr int THREADS = 192;
+  // d = 128: two issuers (S and PV); d = 256, whose tiles keep the tensor core busy longer,
+  // keeps a single issuer that runs S(j+1) before PV(j) in issue order.
+  static constexpr bool SPLIT_ISSUE = D == 128;
+  static constexpr int THREADS = SPLIT_ISSUE ? 224 : 192;
   static constexpr uint32_t COL_O = 0, COL_S = D;       // O [0,D), S_b at D + 128 b
   static_assert(D == 128 || D == 256, "head dim");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -53,14 +62,15 @@ struct WideCfg {
 struct WideBars {
   uint64_t q_full;
   uint64_t full[6], empty[6];
-  uint64_t s_full[2], p_full, o_done, o_final, v_tail, mma_drain;
+  uint64_t s_full[2], p_full, o_done, o_final, v_tail, mma_drain[2];
+  uint64_t p_free[2];           // PV of the tile in S buffer b has completed
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// grid: (n_qt * n_heads * batch); block: 192 threads; 1 CTA per SM.
+// grid: (n_qt * n_heads * batch); block: 224 threads (d = 128) or 192 (d = 256); 1 CTA per SM.
 template <int D_>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(WideCfg<D_>::THREADS, 1)
 prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, AttnShape sh) {
@@ -106,7 +116,10 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_final, 1);
     mbar_init(&bars->v_tail, 1);
-    mbar_init(&bars->mma_drain, 1);
+    mbar_init(&bars->mma_drain[0], 1);
+    mbar_init(&bars->mma_drain[1], 1);
+    mbar_init(&bars->p_free[0], 1);
+    mbar_init(&bars->p_free[1], 1);
     bars->abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -182,70 +195,138 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       for (int k = max(0, cnt - C::RING); k < cnt; ++k)
         mbar_wait(&bars->full[k % C::RING], (k / C::RING) & 1, tmo, nullptr);
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dr_k = sdesc_sw128(smem_u32(sR), 16, 1024);       // K chunks: K-major
-      const uint64_t dr_v = sdesc_sw128(smem_u32(sR), C::VK * 128, 1024);   // V chunks: MN-major
-      int cnt = 0;
-      bool ok = mbar_wait(&bars->q_full, 0, tmo, abort_flag);
-      // S(j) into buffer j & 1 from K(j)'s chunks
-      auto issue_s = [&](int j) -> bool {
-        const uint32_t d_s = tmem + C::COL_S + (j & 1) * BN;
-        for (int c = 0; c < C::KCH; ++c) {
-          const int slot = cnt % C::RING;
-          if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
-          tc_fence_after();
-          const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
-#pragma unroll
-          for (int k8 = 0; k8 < 8; ++k8) {                // 8 steps of 16 dims in this chunk
-            const int kk = 8 * c + k8;
-            const uint64_t aq = dq + (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
-            const uint64_t bo = bk + (uint64_t)(((k8 >> 2) * BN * 128 + (k8 & 3) * 32) >> 4);
-            umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
+  } else if (warp == 5 || warp == 6) {
+    // Warps 5 and 6 issue MMAs and nothing else; only warps 0-3 reach the softmax branch.
+    if (!C::SPLIT_ISSUE) {
+      // ------------------------------------------------------------------ one MMA issuer (d = 256)
+      if (lane == 0 && warp == 5) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+        const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dr_k = sdesc_sw128(smem_u32(sR), 16, 1024);       // K chunks: K-major
+        const uint64_t dr_v = sdesc_sw128(smem_u32(sR), C::VK * 128, 1024);   // V chunks: MN-major
+        int cnt = 0;
+        bool ok = mbar_wait(&bars->q_full, 0, tmo, abort_flag);
+        // S(j) into buffer j & 1 from K(j)'s chunks
+        auto issue_s = [&](int j) -> bool {
+          const uint32_t d_s = tmem + C::COL_S + (j & 1) * BN;
+          for (int c = 0; c < C::KCH; ++c) {
+            const int slot = cnt % C::RING;
+            if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
+            tc_fence_after();
+            const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
+  #pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {                // 8 steps of 16 dims in this chunk
+              const int kk = 8 * c + k8;
+              const uint64_t aq = dq + (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
+              const uint64_t bo = bk + (uint64_t)(((k8 >> 2) * BN * 128 + (k8 & 3) * 32) >> 4);
+              umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&bars->empty[slot]);
+            ++cnt;
           }
-          umma_commit(&bars->empty[slot]);
-          ++cnt;
-        }
-        umma_commit(&bars->s_full[j & 1]);
-        return true;
-      };
-      // O += P(j) V(j), P in the first 64 columns of S buffer j & 1
-      uint32_t o_acc = 0u;
-      auto issue_pv = [&](int j) -> bool {
-        const uint32_t p_col = tmem + C::COL_S + (j & 1) * BN;
-        for (int c = 0; c < C::VCH; ++c) {
-          const int slot = cnt % C::RING;
-          if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
-          tc_fence_after();
-          const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
-#pragma unroll
-          for (int k4 = 0; k4 < C::VK / 16; ++k4) {       // steps of 16 keys in this chunk
-            const int kk = (C::VK / 16) * c + k4;
-            umma_bf16_ts(tmem + C::COL_O, p_col + kk * 8, bv + (uint64_t)((k4 * 2048) >> 4), idesc_pv,
-                         (o_acc | (uint32_t)k4) ? 1u : 0u);
+          umma_commit(&bars->s_full[j & 1]);
+          return true;
+        };
+        // O += P(j) V(j), P in the first 64 columns of S buffer j & 1
+        uint32_t o_acc = 0u;
+        auto issue_pv = [&](int j) -> bool {
+          const uint32_t p_col = tmem + C::COL_S + (j & 1) * BN;
+          for (int c = 0; c < C::VCH; ++c) {
+            const int slot = cnt % C::RING;
+            if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
+            tc_fence_after();
+            const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
+  #pragma unroll
+            for (int k4 = 0; k4 < C::VK / 16; ++k4) {       // steps of 16 keys in this chunk
+              const int kk = (C::VK / 16) * c + k4;
+              umma_bf16_ts(tmem + C::COL_O, p_col + kk * 8, bv + (uint64_t)((k4 * 2048) >> 4), idesc_pv,
+                           (o_acc | (uint32_t)k4) ? 1u : 0u);
+            }
+            o_acc = 1u;
+            umma_commit(&bars->empty[slot]);
+            ++cnt;
           }
-          o_acc = 1u;
-          umma_commit(&bars->empty[slot]);
-          ++cnt;
+          return true;
+        };
+        if (ok && n_tiles > 0) ok = issue_s(0);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
+          if (!(ok = mbar_wait(&bars->p_full, j & 1, tmo, abort_flag))) break;
+          tc_fence_after();
+          if (!(ok = issue_pv(j))) break;
+          umma_commit(&bars->o_done);
+          if (j + 1 == n_tiles) umma_commit(&bars->o_final);
         }
-        return true;
-      };
-      if (ok && n_tiles > 0) ok = issue_s(0);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(&bars->p_full, j & 1, tmo, abort_flag))) break;
-        tc_fence_after();
-        if (!(ok = issue_pv(j))) break;
-        umma_commit(&bars->o_done);
-        if (j + 1 == n_tiles) umma_commit(&bars->o_final);
+        // Drain: every MMA this thread issued has completed before TMEM can be released.
+        umma_commit(&bars->mma_drain[0]);
+        mbar_wait(&bars->mma_drain[0], 0, tmo, nullptr);
       }
-      // Drain: every MMA this thread issued has completed before TMEM can be released.
-      umma_commit(&bars->mma_drain);
-      mbar_wait(&bars->mma_drain, 0, tmo, nullptr);
+    } else {
+      // ------------------------------------------------------------------ MMA issuers (d = 128)
+      // Both find their chunks in the ring from the producer's order: K(0), then K(j+1), V(j)
+      // for j = 0, 1, ... (K(n) is not loaded), C::KCH = C::VCH chunks each.
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+        const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dr_k = sdesc_sw128(smem_u32(sR), 16, 1024);       // K chunks: K-major
+        const uint64_t dr_v = sdesc_sw128(smem_u32(sR), C::VK * 128, 1024);   // V chunks: MN-major
+        const int xi = warp - 5;                         // 0: S issuer, 1: PV issuer
+        auto kpos = [&](int j) { return C::KCH * (j == 0 ? 0 : 2 * j - 1); };
+        auto vpos = [&](int j) { return C::KCH * (j + 1 < n_tiles ? 2 * j + 2 : 2 * j + 1); };
+        bool ok = xi == 1 || mbar_wait(&bars->q_full, 0, tmo, abort_flag);
+        uint32_t o_acc = 0u;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          if (xi == 0) {
+            // S(j) into buffer j & 1, once PV(j-2) has read the P held there
+            if (j >= 2 && !(ok = mbar_wait(&bars->p_free[j & 1], ((j >> 1) - 1) & 1, tmo, abort_flag))) break;
+            const uint32_t d_s = tmem + C::COL_S + (j & 1) * BN;
+            for (int c = 0; c < C::KCH; ++c) {
+              const int pos = kpos(j) + c, slot = pos % C::RING;
+              if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
+              tc_fence_after();
+              const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
+  #pragma unroll
+              for (int k8 = 0; k8 < 8; ++k8) {              // 8 steps of 16 dims in this chunk
+                const int kk = 8 * c + k8;
+                const uint64_t aq = dq + (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
+                const uint64_t bo = bk + (uint64_t)(((k8 >> 2) * BN * 128 + (k8 & 3) * 32) >> 4);
+                umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&bars->empty[slot]);
+            }
+            if (!ok) break;
+            umma_commit(&bars->s_full[j & 1]);
+          } else {
+            // O += P(j) V(j), P in the first 64 columns of S buffer j & 1
+            if (!(ok = mbar_wait(&bars->p_full, j & 1, tmo, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t p_col = tmem + C::COL_S + (j & 1) * BN;
+            for (int c = 0; c < C::VCH; ++c) {
+              const int pos = vpos(j) + c, slot = pos % C::RING;
+              if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
+              tc_fence_after();
+              const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
+  #pragma unroll
+              for (int k4 = 0; k4 < C::VK / 16; ++k4) {     // steps of 16 keys in this chunk
+                const int kk = (C::VK / 16) * c + k4;
+                umma_bf16_ts(tmem + C::COL_O, p_col + kk * 8, bv + (uint64_t)((k4 * 2048) >> 4), idesc_pv,
+                             (o_acc | (uint32_t)k4) ? 1u : 0u);
+              }
+              o_acc = 1u;
+              umma_commit(&bars->empty[slot]);
+            }
+            if (!ok) break;
+            umma_commit(&bars->p_free[j & 1]);
+            umma_commit(&bars->o_done);
+            if (j + 1 == n_tiles) umma_commit(&bars->o_final);
+          }
+        }
+        // Drain: every MMA this thread issued has completed before TMEM can be released.
+        umma_commit(&bars->mma_drain[xi]);
+        mbar_wait(&bars->mma_drain[xi], 0, tmo, nullptr);
+      }
     }
     __syncwarp();
   } else {

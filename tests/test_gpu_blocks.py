@@ -99,5 +99,9 @@ def test_sparse_prefill_end_to_end():
     assert 0.0 < density < 0.9
     dense_mask, _ = ga.ga_select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=math.inf)
     a = ga.ga_attend(q, k, v, block_mask=dense_mask, q_block=qb, k_block=kb)
-    b = ga.ga_attend(q, k, v)
+    ones = torch.ones_like(dense_mask)
+    b = ga.ga_attend(q, k, v, block_mask=ones, q_block=qb, k_block=kb)
+    # tau = inf selects every visible block: the same tiles as an all-ones mask, same bits
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # and dense attention (another kernel at d = 128) within the bf16 tolerance
+    assert_close(to_f64(a), to_f64(ga.ga_attend(q, k, v)), "bf16", "tau = inf vs dense")
