@@ -331,7 +331,7 @@ def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
         t = statistics.mean(timed_steps(torch, lambda: ga.ga_attend(q, k, v, out, block_mask=mask,
                                                                     q_block=qb, k_block=kb),
                                         max(2, steps // 2), min(warmup, 2), flush))
-        sweep.append({"tau_mean": tau, "density": dens, "ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12})
+        sweep.append({"tau_mean": tau if math.isfinite(tau) else "inf", "density": dens, "ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12})
     dens = np.array([s["density"] for s in sweep])
     tms = np.array([s["ms"] for s in sweep])
     A = np.vstack([dens, np.ones_like(dens)]).T
