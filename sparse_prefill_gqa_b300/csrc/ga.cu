@@ -69,6 +69,16 @@ int set_smem(K kernel, int bytes) {
              : GA_ERR_CUDA;
 }
 
+// Kernels that move registers between warpgroups with setmaxnreg: the increase waits until the
+// registers exist, so the CTA must have been launched with at least `need` registers in all.
+template <typename K>
+int set_smem_split(K kernel, int bytes, int threads, int need) {
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return GA_ERR_CUDA;
+  if (attr.numRegs * threads < need) return GA_ERR_UNSUPPORTED;
+  return set_smem(kernel, bytes);
+}
+
 int launch_status() { return cudaGetLastError() == cudaSuccess ? GA_OK : GA_ERR_CUDA; }
 
 // ---- split-K decode geometry (shared by ga_workspace_size and ga_attend) -----------------
@@ -286,14 +296,16 @@ int ga_attend(const void* q, const void* k, const void* v, void* out, int batch,
       if (!make_map_bf16(&tk2, k, d, Tk_max, (long long)batch * n_kv, 128) ||
           !make_map_bf16(&tv2, v, d, Tk_max, (long long)batch * n_kv, C::VK))
         return GA_ERR_CUDA;
-      static int ok = set_smem(prefill_wide_kernel<128>, C::SMEM_BYTES);
+      static int ok = set_smem_split(prefill_wide_kernel<128>, C::SMEM_BYTES, C::THREADS,
+                                     256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS);
       if (ok != GA_OK) return ok;
       const long long n_cta = (long long)((Tq + C::BM - 1) / C::BM) * n_heads * batch;
       if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
       prefill_wide_kernel<128><<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk2, tv2, ob, lse, sh);
     } else if (d == 128) {
       using C = PairCfg;
-      static int ok = set_smem(prefill_pair_kernel, C::SMEM_BYTES);
+      static int ok = set_smem_split(prefill_pair_kernel, C::SMEM_BYTES, C::THREADS,
+                                     256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS);
       if (ok != GA_OK) return ok;
       const long long n_pairs = (Tq + 2 * C::BM - 1) / (2 * C::BM);
       const long long n_cta = n_pairs * n_heads * batch;

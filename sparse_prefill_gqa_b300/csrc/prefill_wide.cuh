@@ -7,25 +7,34 @@
 // absolute-position causal rule; the sliding window of section 2).
 //
 // One CTA per (128-row query tile, query head, sequence), heaviest causal tiles first.
-//   warps 0-3  softmax: thread r = query row r = TMEM lane r;
-//   warp 4     TMA producer (one lane): Q once, then K and V through a ring of 32 KB chunks
-//              (4 slots) -- a K chunk is 128 keys x 128 dims, a V chunk
-//              16384/d keys x d dims -- K one tile ahead of V;
-//   warp 5     S issuer (one lane): S(j) = Q K(j)^T into S buffer j & 1;
-//   warp 6     PV issuer (one lane): O += P(j) V(j).
-// Two issuers (d = 128), because the tensor core's queue is short: a thread that issues an
-// MMA waits while earlier MMAs execute, so one thread that also waits for P would leave the
-// pipe idle.  For d = 256 a tile keeps the tensor core busy twice as long and warp 5 alone
-// issues everything, S(j+1) before PV(j) in issue order (in-order completion then makes S
-// overwrite P only after PV read it, without the per-buffer wait).
-// Tensor memory: O [0,d), S buffers [d,d+128) and [d+128,d+256), N = 128 keys.
-// P(j) (bf16) is written over the first 64 columns of S buffer j&1 and read from there by the
-// PV MMA.  S(j+2) overwrites P(j), so the S issuer waits for PV(j) to complete (a per-buffer
-// barrier) before it issues S(j+2); the softmax of tile j therefore overlaps PV(j-1) and
-// S(j+1).  When the softmax of tile j must rescale O, PV(j-1) may still run, so it waits for
-// that one PV; PV(j-2) is complete (S(j) was issued after it completed), so a parity wait on
-// the per-PV barrier is exact.  The epilogue waits on its own barrier, committed after the
-// last PV.
+//
+// d = 128 (12 warps): two softmax warpgroups split the key tiles of the query tile between them,
+// warpgroup 0 the even tiles and warpgroup 1 the odd ones, each with its own running max and sum
+// and its own output accumulator in tensor memory; the epilogue merges the two partial results
+// by the log-sum-exp rule (the same re-association as split-K decode).  The two softmaxes run
+// concurrently, so each scheduler holds two softmax warps and the tensor core sees tile j+1
+// ready while tile j is still being exponentiated.
+//   warps 0-3, 4-7  softmax of even / odd tiles: thread r of a warpgroup = query row r = TMEM lane r;
+//   warp 8          TMA producer (one lane): Q once, then K and V through a ring of 32 KB chunks
+//                   (4 slots), K one tile ahead of V;
+//   warp 9          S issuer (one lane): S(j) = Q K(j)^T into S buffer j & 1;
+//   warp 10         PV issuer (one lane): O_(j&1) += P(j) V(j);
+//   warp 11         idle (completes the warpgroup whose registers move to the softmax).
+// Two issuers, because the tensor core's queue is short: a thread that issues an MMA waits while
+// earlier MMAs execute, so one thread that also waited for P would leave the pipe idle.
+// Tensor memory: O_0 [0,128), O_1 [128,256), S buffers [256,384) and [384,512).
+// P(j) (bf16) is written over the first 64 columns of S buffer j&1 and read from there by the PV
+// MMA, in two halves of 64 keys: the PV issuer starts on the first half while the softmax still
+// exponentiates the second.  S(j+2) overwrites P(j), so the S issuer waits for PV(j) to complete
+// before it issues S(j+2); by the time a warpgroup sees S(j+2), its previous PV into the same
+// accumulator is therefore complete, and a rescale of that accumulator (done right after the row
+// maximum, before P is produced) needs no further wait.
+//
+// d = 256 (6 warps): one softmax warpgroup (warps 0-3) takes every tile, warp 4 is the producer,
+// warp 5 alone issues S(j+1) before PV(j) (a tile keeps the tensor core busy twice as long, and
+// in-order completion makes S overwrite P only after PV read it).  Tensor memory: O [0,256),
+// S buffers [256,384) and [384,512).  A rescale waits for PV(j-1) on a per-PV barrier.
+//
 // Value rows past a sequence's end are zeroed by the producer before the chunk is published
 // (P is 0 there, but 0 * NaN = NaN for an uninitialised cache).
 #pragma once
@@ -48,27 +57,36 @@ struct WideCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = OFF_Q + Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + RING * CHUNK;
-  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-  // d = 128: two issuers (S and PV); d = 256, whose tiles keep the tensor core busy longer,
-  // keeps a single issuer that runs S(j+1) before PV(j) in issue order.
-  static constexpr bool SPLIT_ISSUE = D == 128;
-  static constexpr int THREADS = SPLIT_ISSUE ? 224 : 192;
-  static constexpr uint32_t COL_O = 0, COL_S = D;       // O [0,D), S_b at D + 128 b
+  static constexpr int OFF_XCH = OFF_BAR + 256;         // epilogue (m, l) exchange (d = 128)
+  static constexpr int SMEM_BYTES = OFF_XCH + 2 * BM * 8 + 1024;
+  // d = 128: two softmax warpgroups on alternate key tiles, separate S and PV issuers.
+  // d = 256 (O alone fills half of tensor memory): one softmax warpgroup, one issuer.
+  static constexpr bool DUAL = D == 128;
+  static constexpr int NWG = DUAL ? 2 : 1;              // softmax warpgroups
+  static constexpr int W_PROD = 4 * NWG;                // producer warp
+  static constexpr int W_S = W_PROD + 1;                // S issuer (the only issuer for d = 256)
+  static constexpr int W_PV = W_PROD + 2;               // PV issuer (d = 128)
+  static constexpr int THREADS = DUAL ? 384 : 192;
+  static constexpr uint32_t COL_O = 0, COL_S = 256;     // O_b at 128 b (d = 128); S_b at 256 + 128 b
+  // register split (d = 128): launched at 168 a thread (384 threads, one CTA per SM)
+  static constexpr int LAUNCH_REGS = 168, SOFTMAX_REGS = 200, OTHER_REGS = 96;
+  static_assert(!DUAL || 256 * SOFTMAX_REGS + 128 * OTHER_REGS <= THREADS * LAUNCH_REGS, "register split");
   static_assert(D == 128 || D == 256, "head dim");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(D + 2 * BN <= 512, "tensor memory budget");
+  static_assert(NWG * D + 2 * BN <= 512 && COL_S == NWG * D, "tensor memory budget");
 };
 
 struct WideBars {
   uint64_t q_full;
   uint64_t full[6], empty[6];
-  uint64_t s_full[2], p_full, o_done, o_final, v_tail, mma_drain[2];
-  uint64_t p_free[2];           // PV of the tile in S buffer b has completed
+  uint64_t s_full[2], p_full[2][2], o_done, o_final, v_tail, mma_drain[2];
+  uint64_t p_free[2];           // PV of the tile in S buffer b has completed (d = 128)
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(WideBars) <= 256, "barrier area");
 
-// grid: (n_qt * n_heads * batch); block: 224 threads (d = 128) or 192 (d = 256); 1 CTA per SM.
+// grid: (n_qt * n_heads * batch); block: 384 threads (d = 128) or 192 (d = 256); 1 CTA per SM.
 template <int D_>
 __global__ void __launch_bounds__(WideCfg<D_>::THREADS, 1)
 prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -112,7 +130,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     mbar_init(&bars->s_full[0], 1);
     mbar_init(&bars->s_full[1], 1);
-    mbar_init(&bars->p_full, 4);
+    for (int b2 = 0; b2 < 4; ++b2) mbar_init(&bars->p_full[b2 >> 1][b2 & 1], 4);
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_final, 1);
     mbar_init(&bars->v_tail, 1);
@@ -124,230 +142,233 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 5) tmem_alloc(&bars->tmem_base, 512);
+  if (warp == C::W_S) tmem_alloc(&bars->tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const int qz = b * sh.n_heads + h, kz = b * sh.n_kv + kvh;
-      mbar_arrive_expect_tx(&bars->q_full, C::Q_BYTES);
-      for (int s = 0; s < D / 64; ++s)
-        tma_load_3d(sQ + s * C::BM * 128, &tm_q, &bars->q_full, 64 * s, t0, qz);
-      int cnt = 0, n_tail = 0;                           // chunks issued, tail chunks
-      bool ok = true;
-      // acquire ring slot for chunk number cnt
-      auto slot_acquire = [&](int& slot) -> bool {
-        slot = cnt % C::RING;
-        if (cnt >= C::RING && !mbar_wait(&bars->empty[slot], ((cnt / C::RING) + 1) & 1, tmo, abort_flag))
-          return false;
-        return true;
-      };
-      auto load_k = [&](int j) -> bool {                 // K(j): chunks of 128 dims
-        for (int c = 0; c < C::KCH; ++c) {
-          int slot;
-          if (!slot_acquire(slot)) return false;
-          unsigned char* dst = sR + slot * C::CHUNK;
-          mbar_arrive_expect_tx(&bars->full[slot], C::CHUNK);
-          for (int s = 0; s < 2; ++s)
-            tma_load_3d(dst + s * BN * 128, &tm_k, &bars->full[slot], 128 * c + 64 * s, (kt_lo + j) * BN, kz);
-          ++cnt;
-        }
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {                 // V(j): chunks of VK keys x D dims
-        for (int c = 0; c < C::VCH; ++c) {
-          int slot;
-          if (!slot_acquire(slot)) return false;
-          unsigned char* dst = sR + slot * C::CHUNK;
-          const int key0 = (kt_lo + j) * BN + C::VK * c;
-          const bool tail = key0 + C::VK > Tk;
-          uint64_t* bar = tail ? &bars->v_tail : &bars->full[slot];
-          mbar_arrive_expect_tx(bar, C::CHUNK);
-          for (int s = 0; s < D / 64; ++s) tma_load_3d(dst + s * C::VK * 128, &tm_v, bar, 64 * s, key0, kz);
-          if (tail) {
-            if (!mbar_wait(&bars->v_tail, n_tail & 1, tmo, abort_flag)) return false;
-            ++n_tail;
-            for (int row = max(0, Tk - key0); row < C::VK; ++row)
-              for (int s = 0; s < D / 64; ++s)
-                for (int q16 = 0; q16 < 8; ++q16)
-                  *reinterpret_cast<uint4*>(dst + s * C::VK * 128 + row * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->full[slot]);
-          }
-          ++cnt;
-        }
-        return true;
-      };
-      if (n_tiles > 0) ok = load_k(0);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) ok = load_k(j + 1);
-        if (ok) ok = load_v(j);
-      }
-      // Drain: the most recent chunk of every slot has landed before the CTA may exit.
-      mbar_wait(&bars->q_full, 0, tmo, nullptr);
-      for (int k = max(0, cnt - C::RING); k < cnt; ++k)
-        mbar_wait(&bars->full[k % C::RING], (k / C::RING) & 1, tmo, nullptr);
-    }
-  } else if (warp == 5 || warp == 6) {
-    // Warps 5 and 6 issue MMAs and nothing else; only warps 0-3 reach the softmax branch.
-    if (!C::SPLIT_ISSUE) {
-      // ------------------------------------------------------------------ one MMA issuer (d = 256)
-      if (lane == 0 && warp == 5) {
-        constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-        const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
-        const uint64_t dr_k = sdesc_sw128(smem_u32(sR), 16, 1024);       // K chunks: K-major
-        const uint64_t dr_v = sdesc_sw128(smem_u32(sR), C::VK * 128, 1024);   // V chunks: MN-major
-        int cnt = 0;
-        bool ok = mbar_wait(&bars->q_full, 0, tmo, abort_flag);
-        // S(j) into buffer j & 1 from K(j)'s chunks
-        auto issue_s = [&](int j) -> bool {
-          const uint32_t d_s = tmem + C::COL_S + (j & 1) * BN;
-          for (int c = 0; c < C::KCH; ++c) {
-            const int slot = cnt % C::RING;
-            if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
-            tc_fence_after();
-            const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
-  #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {                // 8 steps of 16 dims in this chunk
-              const int kk = 8 * c + k8;
-              const uint64_t aq = dq + (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
-              const uint64_t bo = bk + (uint64_t)(((k8 >> 2) * BN * 128 + (k8 & 3) * 32) >> 4);
-              umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&bars->empty[slot]);
-            ++cnt;
-          }
-          umma_commit(&bars->s_full[j & 1]);
-          return true;
-        };
-        // O += P(j) V(j), P in the first 64 columns of S buffer j & 1
-        uint32_t o_acc = 0u;
-        auto issue_pv = [&](int j) -> bool {
-          const uint32_t p_col = tmem + C::COL_S + (j & 1) * BN;
-          for (int c = 0; c < C::VCH; ++c) {
-            const int slot = cnt % C::RING;
-            if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
-            tc_fence_after();
-            const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
-  #pragma unroll
-            for (int k4 = 0; k4 < C::VK / 16; ++k4) {       // steps of 16 keys in this chunk
-              const int kk = (C::VK / 16) * c + k4;
-              umma_bf16_ts(tmem + C::COL_O, p_col + kk * 8, bv + (uint64_t)((k4 * 2048) >> 4), idesc_pv,
-                           (o_acc | (uint32_t)k4) ? 1u : 0u);
-            }
-            o_acc = 1u;
-            umma_commit(&bars->empty[slot]);
-            ++cnt;
-          }
-          return true;
-        };
-        if (ok && n_tiles > 0) ok = issue_s(0);
-        for (int j = 0; ok && j < n_tiles; ++j) {
-          if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
-          if (!(ok = mbar_wait(&bars->p_full, j & 1, tmo, abort_flag))) break;
-          tc_fence_after();
-          if (!(ok = issue_pv(j))) break;
-          umma_commit(&bars->o_done);
-          if (j + 1 == n_tiles) umma_commit(&bars->o_final);
-        }
-        // Drain: every MMA this thread issued has completed before TMEM can be released.
-        umma_commit(&bars->mma_drain[0]);
-        mbar_wait(&bars->mma_drain[0], 0, tmo, nullptr);
-      }
-    } else {
-      // ------------------------------------------------------------------ MMA issuers (d = 128)
-      // Both find their chunks in the ring from the producer's order: K(0), then K(j+1), V(j)
-      // for j = 0, 1, ... (K(n) is not loaded), C::KCH = C::VCH chunks each.
+  if (warp >= C::W_PROD) {
+    if constexpr (C::DUAL) regs_dec<C::OTHER_REGS>();
+    if (warp == C::W_PROD) {
+      // ------------------------------------------------------------------ TMA producer
       if (lane == 0) {
-        constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-        const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
-        const uint64_t dr_k = sdesc_sw128(smem_u32(sR), 16, 1024);       // K chunks: K-major
-        const uint64_t dr_v = sdesc_sw128(smem_u32(sR), C::VK * 128, 1024);   // V chunks: MN-major
-        const int xi = warp - 5;                         // 0: S issuer, 1: PV issuer
-        auto kpos = [&](int j) { return C::KCH * (j == 0 ? 0 : 2 * j - 1); };
-        auto vpos = [&](int j) { return C::KCH * (j + 1 < n_tiles ? 2 * j + 2 : 2 * j + 1); };
-        bool ok = xi == 1 || mbar_wait(&bars->q_full, 0, tmo, abort_flag);
-        uint32_t o_acc = 0u;
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        const int qz = b * sh.n_heads + h, kz = b * sh.n_kv + kvh;
+        mbar_arrive_expect_tx(&bars->q_full, C::Q_BYTES);
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_3d(sQ + s * C::BM * 128, &tm_q, &bars->q_full, 64 * s, t0, qz);
+        int cnt = 0, n_tail = 0;                           // chunks issued, tail chunks
+        bool ok = true;
+        // acquire ring slot for chunk number cnt
+        auto slot_acquire = [&](int& slot) -> bool {
+          slot = cnt % C::RING;
+          if (cnt >= C::RING && !mbar_wait(&bars->empty[slot], ((cnt / C::RING) + 1) & 1, tmo, abort_flag))
+            return false;
+          return true;
+        };
+        auto load_k = [&](int j) -> bool {                 // K(j): chunks of 128 dims
+          for (int c = 0; c < C::KCH; ++c) {
+            int slot;
+            if (!slot_acquire(slot)) return false;
+            unsigned char* dst = sR + slot * C::CHUNK;
+            mbar_arrive_expect_tx(&bars->full[slot], C::CHUNK);
+            for (int s = 0; s < 2; ++s)
+              tma_load_3d(dst + s * BN * 128, &tm_k, &bars->full[slot], 128 * c + 64 * s, (kt_lo + j) * BN, kz);
+            ++cnt;
+          }
+          return true;
+        };
+        auto load_v = [&](int j) -> bool {                 // V(j): chunks of VK keys x D dims
+          for (int c = 0; c < C::VCH; ++c) {
+            int slot;
+            if (!slot_acquire(slot)) return false;
+            unsigned char* dst = sR + slot * C::CHUNK;
+            const int key0 = (kt_lo + j) * BN + C::VK * c;
+            const bool tail = key0 + C::VK > Tk;
+            uint64_t* bar = tail ? &bars->v_tail : &bars->full[slot];
+            mbar_arrive_expect_tx(bar, C::CHUNK);
+            for (int s = 0; s < D / 64; ++s) tma_load_3d(dst + s * C::VK * 128, &tm_v, bar, 64 * s, key0, kz);
+            if (tail) {
+              if (!mbar_wait(&bars->v_tail, n_tail & 1, tmo, abort_flag)) return false;
+              ++n_tail;
+              for (int row = max(0, Tk - key0); row < C::VK; ++row)
+                for (int s = 0; s < D / 64; ++s)
+                  for (int q16 = 0; q16 < 8; ++q16)
+                    *reinterpret_cast<uint4*>(dst + s * C::VK * 128 + row * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+              fence_proxy_async_smem();
+              mbar_arrive(&bars->full[slot]);
+            }
+            ++cnt;
+          }
+          return true;
+        };
+        if (n_tiles > 0) ok = load_k(0);
         for (int j = 0; ok && j < n_tiles; ++j) {
-          if (xi == 0) {
-            // S(j) into buffer j & 1, once PV(j-2) has read the P held there
-            if (j >= 2 && !(ok = mbar_wait(&bars->p_free[j & 1], ((j >> 1) - 1) & 1, tmo, abort_flag))) break;
+          if (j + 1 < n_tiles) ok = load_k(j + 1);
+          if (ok) ok = load_v(j);
+        }
+        // Drain: the most recent chunk of every slot has landed before the CTA may exit.
+        mbar_wait(&bars->q_full, 0, tmo, nullptr);
+        for (int k = max(0, cnt - C::RING); k < cnt; ++k)
+          mbar_wait(&bars->full[k % C::RING], (k / C::RING) & 1, tmo, nullptr);
+      }
+    } else if (warp == C::W_S || warp == C::W_PV) {
+      // The issuer warps issue MMAs and nothing else.
+      if constexpr (!C::DUAL) {
+        // ------------------------------------------------------------------ one MMA issuer (d = 256)
+        if (lane == 0 && warp == C::W_S) {
+          constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
+          constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+          const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+          const uint64_t dr_k = sdesc_sw128(smem_u32(sR), 16, 1024);       // K chunks: K-major
+          const uint64_t dr_v = sdesc_sw128(smem_u32(sR), C::VK * 128, 1024);   // V chunks: MN-major
+          int cnt = 0;
+          bool ok = mbar_wait(&bars->q_full, 0, tmo, abort_flag);
+          // S(j) into buffer j & 1 from K(j)'s chunks
+          auto issue_s = [&](int j) -> bool {
             const uint32_t d_s = tmem + C::COL_S + (j & 1) * BN;
             for (int c = 0; c < C::KCH; ++c) {
-              const int pos = kpos(j) + c, slot = pos % C::RING;
-              if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
+              const int slot = cnt % C::RING;
+              if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
               tc_fence_after();
               const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
-  #pragma unroll
-              for (int k8 = 0; k8 < 8; ++k8) {              // 8 steps of 16 dims in this chunk
+    #pragma unroll
+              for (int k8 = 0; k8 < 8; ++k8) {                // 8 steps of 16 dims in this chunk
                 const int kk = 8 * c + k8;
                 const uint64_t aq = dq + (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
                 const uint64_t bo = bk + (uint64_t)(((k8 >> 2) * BN * 128 + (k8 & 3) * 32) >> 4);
                 umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
               }
               umma_commit(&bars->empty[slot]);
+              ++cnt;
             }
-            if (!ok) break;
             umma_commit(&bars->s_full[j & 1]);
-          } else {
-            // O += P(j) V(j), P in the first 64 columns of S buffer j & 1
-            if (!(ok = mbar_wait(&bars->p_full, j & 1, tmo, abort_flag))) break;
-            tc_fence_after();
+            return true;
+          };
+          // O += P(j) V(j), P in the first 64 columns of S buffer j & 1
+          uint32_t o_acc = 0u;
+          auto issue_pv = [&](int j) -> bool {
             const uint32_t p_col = tmem + C::COL_S + (j & 1) * BN;
             for (int c = 0; c < C::VCH; ++c) {
-              const int pos = vpos(j) + c, slot = pos % C::RING;
-              if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
+              const int slot = cnt % C::RING;
+              if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
               tc_fence_after();
               const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
-  #pragma unroll
-              for (int k4 = 0; k4 < C::VK / 16; ++k4) {     // steps of 16 keys in this chunk
+    #pragma unroll
+              for (int k4 = 0; k4 < C::VK / 16; ++k4) {       // steps of 16 keys in this chunk
                 const int kk = (C::VK / 16) * c + k4;
                 umma_bf16_ts(tmem + C::COL_O, p_col + kk * 8, bv + (uint64_t)((k4 * 2048) >> 4), idesc_pv,
                              (o_acc | (uint32_t)k4) ? 1u : 0u);
               }
               o_acc = 1u;
               umma_commit(&bars->empty[slot]);
+              ++cnt;
             }
-            if (!ok) break;
-            umma_commit(&bars->p_free[j & 1]);
+            return true;
+          };
+          if (ok && n_tiles > 0) ok = issue_s(0);
+          for (int j = 0; ok && j < n_tiles; ++j) {
+            if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
+            if (!(ok = mbar_wait(&bars->p_full[0][0], j & 1, tmo, abort_flag))) break;
+            tc_fence_after();
+            if (!(ok = issue_pv(j))) break;
             umma_commit(&bars->o_done);
             if (j + 1 == n_tiles) umma_commit(&bars->o_final);
           }
+          // Drain: every MMA this thread issued has completed before TMEM can be released.
+          umma_commit(&bars->mma_drain[0]);
+          mbar_wait(&bars->mma_drain[0], 0, tmo, nullptr);
         }
-        // Drain: every MMA this thread issued has completed before TMEM can be released.
-        umma_commit(&bars->mma_drain[xi]);
-        mbar_wait(&bars->mma_drain[xi], 0, tmo, nullptr);
+      } else {
+        // ------------------------------------------------------------------ MMA issuers (d = 128)
+        // Both find their chunks in the ring from the producer's order: K(0), then K(j+1), V(j)
+        // for j = 0, 1, ... (K(n) is not loaded), one chunk each.
+        static_assert(C::KCH == 1 && C::VCH == 1 && C::VK == C::BN, "d = 128 chunk layout");
+        if (lane == 0) {
+          constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
+          constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+          const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+          const uint64_t dr_k = sdesc_sw128(smem_u32(sR), 16, 1024);       // K chunks: K-major
+          const uint64_t dr_v = sdesc_sw128(smem_u32(sR), C::VK * 128, 1024);   // V chunks: MN-major
+          const int xi = warp - C::W_S;                    // 0: S issuer, 1: PV issuer
+          auto kpos = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };
+          auto vpos = [&](int j) { return j + 1 < n_tiles ? 2 * j + 2 : 2 * j + 1; };
+          bool ok = xi == 1 || mbar_wait(&bars->q_full, 0, tmo, abort_flag);
+          for (int j = 0; ok && j < n_tiles; ++j) {
+            const int buf = j & 1;
+            if (xi == 0) {
+              // S(j) into buffer j & 1, once PV(j-2) has read the P held there.  K(j) is waited
+              // for first: it has usually landed long before, so only the PV wait is exposed.
+              const int pos = kpos(j), slot = pos % C::RING;
+              if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
+              if (j >= 2 && !(ok = mbar_wait(&bars->p_free[buf], ((j >> 1) - 1) & 1, tmo, abort_flag))) break;
+              tc_fence_after();
+              const uint32_t d_s = tmem + C::COL_S + buf * BN;
+              const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
+    #pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {                 // 8 steps of 16 dims
+                const uint64_t aq = dq + (uint64_t)(((kk >> 2) * C::BM * 128 + (kk & 3) * 32) >> 4);
+                const uint64_t bo = bk + (uint64_t)(((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4);
+                umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&bars->empty[slot]);
+              umma_commit(&bars->s_full[buf]);
+            } else {
+              // O_(j&1) += P(j) V(j), P in the first 64 columns of S buffer j & 1.  The softmax
+              // publishes P in two halves of 64 keys; the first half's MMAs run while the
+              // second half is exponentiated.
+              const int pos = vpos(j), slot = pos % C::RING;
+              if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
+              const uint32_t p_col = tmem + C::COL_S + buf * BN;
+              const uint32_t d_o = tmem + C::COL_O + buf * D;
+              const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
+              for (int half = 0; ok && half < 2; ++half) {
+                if (!(ok = mbar_wait(&bars->p_full[buf][half], (j >> 1) & 1, tmo, abort_flag))) break;
+                tc_fence_after();
+    #pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {               // 4 steps of 16 keys
+                  const int kk = 4 * half + k4;
+                  umma_bf16_ts(d_o, p_col + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                               (j >= 2 || kk > 0) ? 1u : 0u);
+                }
+              }
+              if (!ok) break;
+              umma_commit(&bars->empty[slot]);
+              umma_commit(&bars->p_free[buf]);
+              if (j + 1 == n_tiles) umma_commit(&bars->o_final);
+            }
+          }
+          // Drain: every MMA this thread issued has completed before TMEM can be released.
+          umma_commit(&bars->mma_drain[xi]);
+          mbar_wait(&bars->mma_drain[xi], 0, tmo, nullptr);
+        }
       }
-    }
-    __syncwarp();
+      __syncwarp();
+  }
   } else {
-    // ------------------------------------------------------------------ softmax warps 0-3
-    const int row = threadIdx.x;                      // query row within the tile = TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_o = tmem + C::COL_O + lane_off;
+    // ------------------------------------------------------------------ softmax warpgroups
+    if constexpr (C::DUAL) regs_inc<C::SOFTMAX_REGS>();
+    const int wg = warp >> 2;                         // key tiles wg, wg + NWG, wg + 2 NWG, ...
+    const int row = threadIdx.x & 127;                // query row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_o = tmem + C::COL_O + wg * D + lane_off;
     const long long i = i_first + row;                // absolute position of this row
     const int lo = sh.window > 0 ? (int)max(0LL, i - sh.window + 1) : 0;
     const int hi = sh.causal ? (int)min((long long)Tk, i + 1) : Tk;
     const int lo_all = sh.window > 0 ? (int)max(0LL, i_last - sh.window + 1) : 0;
     const int hi_all = sh.causal ? (int)min((long long)Tk, i_first + 1) : Tk;
     const float scale_log2 = kLog2e / sqrtf((float)D);
-    float m_run = -INFINITY, l_run = 0.0f;
-    if (sh.sink) { m_run = sh.sink[h] * kLog2e; l_run = 1.0f; }
+    float m_run = -INFINITY, l_run = 0.0f;            // this warpgroup's share of the keys
+    if (sh.sink && wg == 0) { m_run = sh.sink[h] * kLog2e; l_run = 1.0f; }
 
-    int n = 0;
-    for (; n < n_tiles; ++n) {
-      if (!warp_wait(&bars->s_full[n & 1], (n >> 1) & 1, tmo, abort_flag)) break;
+    for (int n = wg; n < n_tiles; n += C::NWG) {
+      const int buf = n & 1;
+      if (!warp_wait(&bars->s_full[buf], (n >> 1) & 1, tmo, abort_flag)) break;
       tc_fence_after();
-      const uint32_t t_s = tmem + C::COL_S + (n & 1) * BN + lane_off;
+      const uint32_t t_s = tmem + C::COL_S + buf * BN + lane_off;
       float sv[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c)
@@ -374,9 +395,32 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const float m_new = need ? m_tile : m_run;
       const float alpha = need ? ex2(m_run - m_new) : 1.0f;   // ex2(-inf) = 0
       const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+      auto rescale_o = [&]() {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] *= alpha;
+          tmem_st32(t_o + c, o);
+        }
+      };
+      // d = 128: the accumulator's previous PV, PV(n-2), completed before S(n) was issued, so
+      // the rescale can run before P is produced (PV(n) must see the rescaled accumulator).
+      if constexpr (C::DUAL)
+        if (n >= C::NWG && __any_sync(0xffffffffu, need)) rescale_o();
       float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) {
+        if constexpr (C::DUAL) {
+          if (c0 == BN / 2) {                           // keys [0, 64) of P are in place
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full[buf][0]);
+          }
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
@@ -394,24 +438,19 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
       m_run = m_new;
-      if (n > 0 && __any_sync(0xffffffffu, need)) {
-        // PV(n-1) may still accumulate into O: wait for it (PV(n-2) is already complete)
-        if (!warp_wait(&bars->o_done, (n - 1) & 1, tmo, abort_flag)) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          float o[32];
-          tmem_ld32(t_o + c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 32; ++u) o[u] *= alpha;
-          tmem_st32(t_o + c, o);
+      if constexpr (!C::DUAL) {
+        // d = 256: PV(n-1) may still accumulate into O, so the rescale waits for it (PV(n-2)
+        // is complete) and runs last.
+        if (n >= C::NWG && __any_sync(0xffffffffu, need)) {
+          if (!warp_wait(&bars->o_done, (n - 1) & 1, tmo, abort_flag)) break;
+          tc_fence_after();
+          rescale_o();
         }
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);
+      if (lane == 0) mbar_arrive(C::DUAL ? &bars->p_full[buf][1] : &bars->p_full[0][0]);
     }
 
     // ---- epilogue: O / l from TMEM to global ------------------------------------------
@@ -419,40 +458,80 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (ok && n_tiles > 0) ok = warp_wait(&bars->o_final, 0, tmo, abort_flag);
     tc_fence_after();
     const int t = t0 + row;
-    const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
     __nv_bfloat16* orow = out + (((size_t)b * sh.n_heads + h) * sh.Tq + t) * D;
-    if (ok) {
-#pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        float o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(t_o + c, o);
-          tmem_wait_ld();
-        } else {
+    auto store32 = [&](int c, const float (&o)[32], float s0) {
+      if (row < rows) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) o[u] = 0.0f;
-        }
-        if (row < rows) {
-#pragma unroll
-          for (int u = 0; u < 32; u += 8) {
-            uint4 pk;
-            pk.x = pack_bf16x2(o[u + 0] * inv_l, o[u + 1] * inv_l);
-            pk.y = pack_bf16x2(o[u + 2] * inv_l, o[u + 3] * inv_l);
-            pk.z = pack_bf16x2(o[u + 4] * inv_l, o[u + 5] * inv_l);
-            pk.w = pack_bf16x2(o[u + 6] * inv_l, o[u + 7] * inv_l);
-            *reinterpret_cast<uint4*>(orow + c + u) = pk;
-          }
+        for (int u = 0; u < 32; u += 8) {
+          uint4 pk;
+          pk.x = pack_bf16x2(o[u + 0] * s0, o[u + 1] * s0);
+          pk.y = pack_bf16x2(o[u + 2] * s0, o[u + 3] * s0);
+          pk.z = pack_bf16x2(o[u + 4] * s0, o[u + 5] * s0);
+          pk.w = pack_bf16x2(o[u + 6] * s0, o[u + 7] * s0);
+          *reinterpret_cast<uint4*>(orow + c + u) = pk;
         }
       }
-      if (lse && row < rows)
-        lse[((size_t)b * sh.n_heads + h) * sh.Tq + t] =
-            l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+    };
+    if constexpr (C::DUAL) {
+      // Merge the warpgroups' partial results (running max m_w, sum l_w, accumulator O_w, all
+      // relative to 2^m_w): out = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w.  The warpgroups
+      // swap (m, l) through shared memory; warpgroup w then writes columns [64 w, 64 w + 64).
+      float2* xch = reinterpret_cast<float2*>(smem + C::OFF_XCH);
+      if (ok) xch[wg * C::BM + row] = make_float2(m_run, l_run);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const float2 other = xch[(wg ^ 1) * C::BM + row];
+      const float m0 = wg == 0 ? m_run : other.x, l0 = wg == 0 ? l_run : other.y;
+      const float m1 = wg == 0 ? other.x : m_run, l1 = wg == 0 ? other.y : l_run;
+      const float M = fmaxf(m0, m1);
+      const float a0 = M == -INFINITY ? 0.0f : ex2(m0 - M);
+      const float a1 = M == -INFINITY ? 0.0f : ex2(m1 - M);
+      const float L = l0 * a0 + l1 * a1;
+      const float inv_l = L > 0.0f ? 1.0f / L : 0.0f;
+      const float s0 = a0 * inv_l, s1 = a1 * inv_l;
+      if (ok) {
+        const uint32_t t_o0 = tmem + C::COL_O + lane_off, t_o1 = t_o0 + D;
+#pragma unroll 1
+        for (int c = 64 * wg; c < 64 * wg + 64; c += 32) {
+          float o0[32], o1[32];
+          if (n_tiles > 0) tmem_ld32(t_o0 + c, o0);
+          if (n_tiles > 1) tmem_ld32(t_o1 + c, o1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float x0 = n_tiles > 0 ? o0[u] : 0.0f, x1 = n_tiles > 1 ? o1[u] : 0.0f;
+            o0[u] = fmaf(x0, s0, x1 * s1);
+          }
+          store32(c, o0, 1.0f);
+        }
+        if (lse && wg == 0 && row < rows)
+          lse[((size_t)b * sh.n_heads + h) * sh.Tq + t] =
+              L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+      }
+    } else {
+      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      if (ok) {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(t_o + c, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = 0.0f;
+          }
+          store32(c, o, inv_l);
+        }
+        if (lse && row < rows)
+          lse[((size_t)b * sh.n_heads + h) * sh.Tq + t] =
+              l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      }
     }
     tc_fence_before();
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::W_S) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
