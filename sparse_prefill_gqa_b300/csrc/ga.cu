@@ -15,9 +15,7 @@
 #include "blocks.cuh"
 #include "common.cuh"
 #include "decode.cuh"
-#include "prefill_pair.cuh"
 #include "prefill_wide.cuh"
-#include "prefill_tc.cuh"
 
 namespace ga {
 
@@ -282,50 +280,33 @@ int ga_attend(const void* q, const void* k, const void* v, void* out, int batch,
 
   // ---- tensor-core prefill ---------------------------------------------------------------
   if (tc_eligible(d, dtype, q, k, v, out, block_mask, q_block, k_block)) {
-    CUtensorMap tq, tk, tv;
-    const int BN = d == 128 ? 128 : 64;
+    // 64-column SW128 boxes: Q 128 rows; K 128 keys and 64 keys; V 16384/d keys and 64 keys
+    const long long kvz = (long long)batch * n_kv;
+    const int vk = 16384 / d;
+    CUtensorMap tq, tk, tv, tk64, tv64;
     if (!make_map_bf16(&tq, q, d, Tq, (long long)batch * n_heads, 128) ||
-        !make_map_bf16(&tk, k, d, Tk_max, (long long)batch * n_kv, 64) ||
-        !make_map_bf16(&tv, v, d, Tk_max, (long long)batch * n_kv, 64))
+        !make_map_bf16(&tk, k, d, Tk_max, kvz, 128) || !make_map_bf16(&tv, v, d, Tk_max, kvz, vk) ||
+        !make_map_bf16(&tk64, k, d, Tk_max, kvz, 64) || !make_map_bf16(&tv64, v, d, Tk_max, kvz, 64))
       return GA_ERR_CUDA;
-    (void)BN;
-    dim3 grid((Tq + 127) / 128, n_heads, batch);
-    if (d == 128 && block_mask == nullptr) {
+    const long long n_cta = (long long)((Tq + 127) / 128) * n_heads * batch;
+    if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+    if (d == 128) {
       using C = WideCfg<128>;
-      CUtensorMap tk2, tv2;                             // boxes of 128 keys (K) and VK = 128 keys (V)
-      if (!make_map_bf16(&tk2, k, d, Tk_max, (long long)batch * n_kv, 128) ||
-          !make_map_bf16(&tv2, v, d, Tk_max, (long long)batch * n_kv, C::VK))
-        return GA_ERR_CUDA;
-      static int ok = set_smem_split(prefill_wide_kernel<128>, C::SMEM_BYTES, C::THREADS,
-                                     256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS);
-      if (ok != GA_OK) return ok;
-      const long long n_cta = (long long)((Tq + C::BM - 1) / C::BM) * n_heads * batch;
-      if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
-      prefill_wide_kernel<128><<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk2, tv2, ob, lse, sh);
-    } else if (d == 128) {
-      using C = PairCfg;
-      static int ok = set_smem_split(prefill_pair_kernel, C::SMEM_BYTES, C::THREADS,
-                                     256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS);
-      if (ok != GA_OK) return ok;
-      const long long n_pairs = (Tq + 2 * C::BM - 1) / (2 * C::BM);
-      const long long n_cta = n_pairs * n_heads * batch;
-      if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
-      prefill_pair_kernel<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, ob, lse, sh);
-    } else if (block_mask == nullptr) {
-      using C = WideCfg<256>;
-      CUtensorMap tk2;                                  // K boxes of 128 keys; V boxes of VK = 64 keys (tv)
-      static_assert(WideCfg<256>::VK == 64, "the V map's box is 64 keys");
-      if (!make_map_bf16(&tk2, k, d, Tk_max, (long long)batch * n_kv, 128)) return GA_ERR_CUDA;
-      static int ok = set_smem(prefill_wide_kernel<256>, C::SMEM_BYTES);
-      if (ok != GA_OK) return ok;
-      const long long n_cta = (long long)((Tq + C::BM - 1) / C::BM) * n_heads * batch;
-      if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
-      prefill_wide_kernel<256><<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk2, tv, ob, lse, sh);
+      static_assert(C::VK == 128, "V map box");
+      constexpr int need = 256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS;
+      static int ok0 = set_smem_split(prefill_wide_kernel<128, false>, C::SMEM_BYTES, C::THREADS, need);
+      static int ok1 = set_smem_split(prefill_wide_kernel<128, true>, C::SMEM_BYTES, C::THREADS, need);
+      if (ok0 != GA_OK || ok1 != GA_OK) return ok0 != GA_OK ? ok0 : ok1;
+      auto kern = block_mask ? prefill_wide_kernel<128, true> : prefill_wide_kernel<128, false>;
+      kern<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh);
     } else {
-      using C = PrefillCfg<256, 64>;
-      static int ok = set_smem(prefill_tc_kernel<256, 64>, C::SMEM_BYTES);
-      if (ok != GA_OK) return ok;
-      prefill_tc_kernel<256, 64><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, ob, lse, sh);
+      using C = WideCfg<256>;
+      static_assert(C::VK == 64, "V map box");
+      static int ok0 = set_smem(prefill_wide_kernel<256, false>, C::SMEM_BYTES);
+      static int ok1 = set_smem(prefill_wide_kernel<256, true>, C::SMEM_BYTES);
+      if (ok0 != GA_OK || ok1 != GA_OK) return ok0 != GA_OK ? ok0 : ok1;
+      auto kern = block_mask ? prefill_wide_kernel<256, true> : prefill_wide_kernel<256, false>;
+      kern<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh);
     }
     return launch_status();
   }

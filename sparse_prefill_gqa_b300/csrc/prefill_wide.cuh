@@ -1,10 +1,17 @@
 // prefill_wide.cuh -- bf16 attention prefill, one 128-row query tile per CTA, head dim 128 or
-// 256 (dense, causal, window, sink).
+// 256: causal, window, sink, and block-sparse (a block mask over 64-key units).
 //
-// What it computes: the same attention as the other prefill kernels ("Attention in Code",
-// "one function all designs use": scores q.k/sqrt(d), masked positions removed, optional sink
-// logit in the normaliser, weighted sum of values; section 1 head grouping; the
-// absolute-position causal rule; the sliding window of section 2).
+// What it computes ("Attention in Code", "one function all designs use": scores q.k/sqrt(d),
+// masked positions removed, optional sink logit in the normaliser, weighted sum of values;
+// section 1 head grouping; the absolute-position causal rule; the sliding window of section 2),
+// restricted to the selected key blocks when a block mask is given ("RBS-Attention review":
+// attention is computed only over the blocks the selection keeps).
+//
+// Block masks: the CTA first lists the selected 64-key units of its query tile, in key order,
+// and pairs them into 128-key tiles; each half of a tile is loaded as its own 64-key box and
+// masked from its own key base, so the work is proportional to the selected units and the MMAs
+// stay full width.  Launches without a block mask use the instantiation UNITS = false, which
+// has no list and loads contiguous 128-key tiles.
 //
 // One CTA per (128-row query tile, query head, sequence), heaviest causal tiles first.
 //
@@ -40,7 +47,6 @@
 #pragma once
 
 #include "common.cuh"
-#include "prefill_tc.cuh"
 
 namespace ga {
 
@@ -58,7 +64,9 @@ struct WideCfg {
   static constexpr int OFF_RING = OFF_Q + Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + RING * CHUNK;
   static constexpr int OFF_XCH = OFF_BAR + 256;         // epilogue (m, l) exchange (d = 128)
-  static constexpr int SMEM_BYTES = OFF_XCH + 2 * BM * 8 + 1024;
+  static constexpr int LIST_MAX = 2048;                 // block-mask tile list: tiles (2 units each)
+  static constexpr int OFF_LIST = OFF_XCH + 2 * BM * 8;
+  static constexpr int SMEM_BYTES = OFF_LIST + 2 * LIST_MAX * 4 + 1024;
   // d = 128: two softmax warpgroups on alternate key tiles, separate S and PV issuers.
   // d = 256 (O alone fills half of tensor memory): one softmax warpgroup, one issuer.
   static constexpr bool DUAL = D == 128;
@@ -86,11 +94,19 @@ struct WideBars {
 };
 static_assert(sizeof(WideBars) <= 256, "barrier area");
 
+// A list entry naming no unit: the tile holds one unit, in its first half.
+constexpr uint32_t kUnitNone = 0xFFFFFFFFu;
+
 // grid: (n_qt * n_heads * batch); block: 384 threads (d = 128) or 192 (d = 256); 1 CTA per SM.
-template <int D_>
+// Tensor maps (64-column SW128 boxes): tm_q 128 rows; tm_k 128 keys; tm_v 16384/d keys;
+// tm_k64 and tm_v64 64 keys (the 64-key units of a block-masked tile).
+// UNITS: the launch has a block mask (tiles are lists of 64-key units); without one the
+// kernel compiles to contiguous 128-key tiles only.
+template <int D_, bool UNITS>
 __global__ void __launch_bounds__(WideCfg<D_>::THREADS, 1)
 prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k64,
+                    const __grid_constant__ CUtensorMap tm_v64, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, AttnShape sh) {
   using C = WideCfg<D_>;
   constexpr int D = C::D, BN = C::BN;
@@ -120,7 +136,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   int key_hi = sh.causal ? (int)min((long long)Tk, i_last + 1) : Tk;
   if (key_hi < key_lo) key_hi = key_lo;
   const int kt_lo = key_lo / BN;
-  const int n_tiles = key_hi > key_lo ? (key_hi + BN - 1) / BN - kt_lo : 0;
+  int n_tiles = key_hi > key_lo ? (key_hi + BN - 1) / BN - kt_lo : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -148,6 +164,71 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // ---- block mask: the selected 64-key units of this query tile, in key order, paired into
+  // 128-key tiles (unit list_a[t] in the first half of tile t, list_b[t] in the second).  Keys
+  // of a tile need not be adjacent -- the softmax masks each half from its own base -- and the
+  // order of tiles does not change the result, so the work is proportional to the selected
+  // units.  A list that would not fit leaves the contiguous tiles, masked per half.
+  const uint8_t* mrow = UNITS && sh.block_mask
+      ? sh.block_mask + (((size_t)b * sh.n_heads + h) * sh.nQb + t0 / sh.q_block) * sh.nKb
+      : nullptr;
+  uint32_t* list_a = reinterpret_cast<uint32_t*>(smem + C::OFF_LIST);
+  uint32_t* list_b = list_a + C::LIST_MAX;
+  bool list = false;
+  if (UNITS && mrow != nullptr && n_tiles > 0) {
+    int* cnt = reinterpret_cast<int*>(smem + C::OFF_XCH);   // [0] total, [1 + w] per warp
+    const int u_lo = key_lo / 64, u_hi = (key_hi + 63) / 64;
+    auto selected = [&](int u) -> bool { return u < u_hi && mrow[(64 * u) / sh.k_block] != 0; };
+    if (threadIdx.x == 0) cnt[0] = 0;
+    __syncthreads();
+    int mine = 0;
+    for (int u = u_lo + (int)threadIdx.x; u < u_hi; u += C::THREADS) mine += selected(u) ? 1 : 0;
+    mine = __reduce_add_sync(0xffffffffu, mine);
+    if (lane == 0 && mine) atomicAdd(&cnt[0], mine);
+    __syncthreads();
+    const int total = cnt[0];
+    if (total <= 2 * C::LIST_MAX) {
+      list = true;
+      int run = 0;                                   // units placed so far (same in all threads)
+      const uint32_t lt = (1u << lane) - 1u;
+      for (int base = u_lo; base < u_hi; base += C::THREADS) {
+        const int u = base + (int)threadIdx.x;
+        const bool sel = selected(u);
+        const uint32_t bal = __ballot_sync(0xffffffffu, sel);
+        if (lane == 0) cnt[1 + warp] = __popc(bal);
+        __syncthreads();
+        if (sel) {
+          int rank = run + __popc(bal & lt);
+          for (int w = 0; w < warp; ++w) rank += cnt[1 + w];
+          (rank & 1 ? list_b : list_a)[rank >> 1] = (uint32_t)u;
+        }
+        for (int w = 0; w < C::THREADS / 32; ++w) run += cnt[1 + w];
+        __syncthreads();
+      }
+      if (threadIdx.x == 0 && (total & 1)) list_b[total >> 1] = kUnitNone;
+      __syncthreads();
+      n_tiles = (total + 1) / 2;
+    }
+  }
+  // Tile t: the 64-key units of its two halves and which halves hold keys of this query tile
+  // (bit 0: first half, bit 1: second).  A lone unit is loaded into both halves, the second
+  // masked, so that no half ever holds unloaded data.
+  auto tile_units = [&](int t, int& ua, int& ub, uint32_t& present) {
+    if (UNITS && list) {
+      const uint32_t lb = list_b[t];
+      ua = (int)list_a[t];
+      ub = lb == kUnitNone ? ua : (int)lb;
+      present = lb == kUnitNone ? 1u : 3u;
+    } else {
+      ua = 2 * (kt_lo + t);
+      ub = ua + 1;
+      present = 3u;
+      if (UNITS && mrow != nullptr)
+        present = (mrow[(64 * ua) / sh.k_block] ? 1u : 0u) |
+                  ((64 * ub < sh.Tk_max && mrow[(64 * ub) / sh.k_block]) ? 2u : 0u);
+    }
+  };
+
   if (warp >= C::W_PROD) {
     if constexpr (C::DUAL) regs_dec<C::OTHER_REGS>();
     if (warp == C::W_PROD) {
@@ -169,35 +250,62 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             return false;
           return true;
         };
+        // With a block mask every half of a tile is a 64-key unit of its own (64-row boxes);
+        // otherwise tile j is the contiguous keys 128 (kt_lo + j) ... (128-row boxes).
+        constexpr bool units = UNITS;
         auto load_k = [&](int j) -> bool {                 // K(j): chunks of 128 dims
+          int ua, ub;
+          uint32_t pr;
+          tile_units(j, ua, ub, pr);
           for (int c = 0; c < C::KCH; ++c) {
             int slot;
             if (!slot_acquire(slot)) return false;
             unsigned char* dst = sR + slot * C::CHUNK;
             mbar_arrive_expect_tx(&bars->full[slot], C::CHUNK);
-            for (int s = 0; s < 2; ++s)
-              tma_load_3d(dst + s * BN * 128, &tm_k, &bars->full[slot], 128 * c + 64 * s, (kt_lo + j) * BN, kz);
+            for (int s = 0; s < 2; ++s) {
+              if (!units) {
+                tma_load_3d(dst + s * BN * 128, &tm_k, &bars->full[slot], 128 * c + 64 * s, (kt_lo + j) * BN, kz);
+              } else {
+                tma_load_3d(dst + s * BN * 128, &tm_k64, &bars->full[slot], 128 * c + 64 * s, 64 * ua, kz);
+                tma_load_3d(dst + s * BN * 128 + 64 * 128, &tm_k64, &bars->full[slot], 128 * c + 64 * s, 64 * ub, kz);
+              }
+            }
             ++cnt;
           }
           return true;
         };
         auto load_v = [&](int j) -> bool {                 // V(j): chunks of VK keys x D dims
+          int ua, ub;
+          uint32_t pr;
+          tile_units(j, ua, ub, pr);
+          constexpr int PARTS = C::VK / 64;                // 64-key units per chunk
           for (int c = 0; c < C::VCH; ++c) {
             int slot;
             if (!slot_acquire(slot)) return false;
             unsigned char* dst = sR + slot * C::CHUNK;
-            const int key0 = (kt_lo + j) * BN + C::VK * c;
-            const bool tail = key0 + C::VK > Tk;
+            // unit of part p: half PARTS * c + p of the tile
+            auto part_unit = [&](int p) { return (PARTS * c + p) == 0 ? ua : ub; };
+            bool tail = false;
+            for (int p = 0; p < PARTS; ++p) tail |= 64 * part_unit(p) + 64 > Tk;
             uint64_t* bar = tail ? &bars->v_tail : &bars->full[slot];
             mbar_arrive_expect_tx(bar, C::CHUNK);
-            for (int s = 0; s < D / 64; ++s) tma_load_3d(dst + s * C::VK * 128, &tm_v, bar, 64 * s, key0, kz);
+            for (int s = 0; s < D / 64; ++s) {
+              if (!units) {
+                tma_load_3d(dst + s * C::VK * 128, &tm_v, bar, 64 * s, (kt_lo + j) * BN + C::VK * c, kz);
+              } else {
+                for (int p = 0; p < PARTS; ++p)
+                  tma_load_3d(dst + s * C::VK * 128 + p * 64 * 128, &tm_v64, bar, 64 * s, 64 * part_unit(p), kz);
+              }
+            }
             if (tail) {
               if (!mbar_wait(&bars->v_tail, n_tail & 1, tmo, abort_flag)) return false;
               ++n_tail;
-              for (int row = max(0, Tk - key0); row < C::VK; ++row)
-                for (int s = 0; s < D / 64; ++s)
-                  for (int q16 = 0; q16 < 8; ++q16)
-                    *reinterpret_cast<uint4*>(dst + s * C::VK * 128 + row * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+              for (int p = 0; p < PARTS; ++p)
+                for (int row = max(0, Tk - 64 * part_unit(p)); row < 64; ++row)
+                  for (int s = 0; s < D / 64; ++s)
+                    for (int q16 = 0; q16 < 8; ++q16)
+                      *reinterpret_cast<uint4*>(dst + s * C::VK * 128 + (p * 64 + row) * 128 + q16 * 16) =
+                          make_uint4(0, 0, 0, 0);
               fence_proxy_async_smem();
               mbar_arrive(&bars->full[slot]);
             }
@@ -374,13 +482,19 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       for (int c = 0; c < BN / 32; ++c)
         tmem_ld32(t_s + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
       tmem_wait_ld();
-      const int key0 = (kt_lo + n) * BN;
-      const bool interior = key0 >= lo_all && key0 + BN <= hi_all;
+      // keys of the two 64-column halves start at 64 ua and 64 ub
+      int ua, ub;
+      uint32_t pr;
+      tile_units(n, ua, ub, pr);
+      const int kb0 = 64 * ua, kb1 = 64 * ub;
+      const bool interior = UNITS ? pr == 3u && kb0 >= lo_all && kb0 + 64 <= hi_all && kb1 >= lo_all && kb1 + 64 <= hi_all
+                                  : kb0 >= lo_all && kb0 + BN <= hi_all;
       if (!interior) {
+        const int lo0 = (pr & 1u) ? lo : 0x7fffffff, lo1 = (pr & 2u) ? lo : 0x7fffffff;   // absent half: no key
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
-          const int jj = key0 + c;
-          sv[c] = (jj >= lo && jj < hi) ? sv[c] : -INFINITY;
+          const int jj = c < 64 ? kb0 + c : kb1 + (c - 64);
+          sv[c] = (jj >= (c < 64 ? lo0 : lo1) && jj < hi) ? sv[c] : -INFINITY;
         }
       }
       float mx[4];
