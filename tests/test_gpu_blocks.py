@@ -42,6 +42,8 @@ def compare_masks(gpu_mask, ref_mask, mean_margin, z_margin, what):
     ("bf16", 1, 3, 777, 256, 64, None),
     ("f32", 1, 2, 300, 40, 17, [250]),
     ("bf16", 1, 1, 4096, 128, 128, None),
+    ("bf16", 2, 2, 700, 64, 64, [700, 333]),      # register-resident kernel, d = 64
+    ("bf16", 1, 2, 517, 32, 48, [517]),           # d = 32, blocks of 48 keys, partial last block
 ])
 def test_block_stats(dtype, B, n_kv, T, d, kb, lens):
     k, kr = host_tensor(51, "k", (B, n_kv, T, d), dtype)
