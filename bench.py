@@ -263,6 +263,42 @@ def part_window_sink(torch, ga, steps, warmup, flush, peaks):
             "composite_5to1": {"TFLOP/s": (5 * fw + ff) / ((5 * tw + tf) * 1e-3) / 1e12}}
 
 
+def part_ring(torch, ga, steps, warmup, flush, peaks):
+    """Decode over W-slot ring caches (the decode side of the window + sink workload): its
+    heads (H16 Hkv8 d256), window W = 1024 and sink, a decode batch of 64 sequences (the
+    batch of the KV-cache decode workload) whose token counters n are drawn from U[W/2, 4W],
+    so most rings have wrapped.  A ring is any set of W keys in any order, so its contents
+    are seeded N(0, 1) draws.  Timed: ga_attend_ring (K/V bytes = min(n, W) keys per
+    sequence and kv head); the append of one token per sequence is timed on its own."""
+    from workloads import get_config
+    c = get_config(4)
+    B, H, n_kv, d, W = 64, c.n_heads, c.n_kv, c.d, c.window
+    q = device_bf16(torch, c.seed, "ring_q", (B, H, 1, d))
+    k_ring = device_bf16(torch, c.seed, "ring_k", (B, n_kv, W, d))
+    v_ring = device_bf16(torch, c.seed, "ring_v", (B, n_kv, W, d))
+    rng = np.random.Generator(np.random.PCG64(c.seed + 17))
+    n = rng.integers(W // 2, 4 * W + 1, size=B).astype(np.int32)
+    n_seen = torch.from_numpy(n).cuda()
+    sink = torch.from_numpy(rng.standard_normal(H).astype(np.float32)).cuda()
+    out = torch.empty_like(q)
+    ws = torch.empty(max(1, ga.ga_workspace_size(B, H, n_kv, d, 1, W, torch.bfloat16)),
+                     dtype=torch.uint8, device="cuda")
+    t = timed_steps(torch, lambda: ga.ga_attend_ring(q, k_ring, v_ring, n_seen, out, sink=sink,
+                                                     workspace=ws), steps, warmup, flush)
+    kv_bytes = 2 * 2 * d * n_kv * int(np.minimum(n, W).sum())
+    ms = statistics.mean(t)
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    k_new = device_bf16(torch, c.seed, "ring_k_new", (B, n_kv, 1, d)).view(B, n_kv, d)
+    v_new = device_bf16(torch, c.seed, "ring_v_new", (B, n_kv, 1, d)).view(B, n_kv, d)
+    n_app = n_seen.clone()
+    ta = statistics.mean(timed_steps(torch, lambda: ga.ga_ring_append(k_ring, v_ring, k_new, v_new, n_app),
+                                     steps, warmup, flush))
+    return {"ring_decode": {"workload": "bf16 ring-buffer decode B64 H16 Hkv8 d256 W1024 + sink, "
+                                        "counters U[512, 4096]", "ms": ms, "GB/s": gbs,
+                            "frac_hbm": gbs / peaks["hbm_gbs"], "kv_bytes": kv_bytes,
+                            "append_us": ta * 1e3}}
+
+
 def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
     from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
     c = get_config(5)
@@ -389,6 +425,8 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
                                     which=(args.case,))
     elif args.case == "window":
         res = part_window_sink(torch, ga, args.steps, warmup, flush, peaks)
+    elif args.case == "ring":
+        res = part_ring(torch, ga, args.steps, warmup, flush, peaks)
     else:
         res = part_sparse(torch, ga, args.steps, warmup, flush, peaks, select_only=args.case == "select")
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": warmup, **res}))
@@ -405,7 +443,7 @@ def main():
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="all",
-                    choices=["all", "prefill", "decode", "chunk", "window", "sparse", "select"],
+                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "sparse", "select"],
                     help="run one workload alone and print its own JSON line (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --case prefill/decode/chunk: a smaller batch (profiling captures)")
@@ -550,7 +588,7 @@ def main():
         parts = {}
         ps, pw = max(3, min(20, args.steps // 4)), 3
         for name, fn in (("decode_chunk", part_decode_and_chunk), ("window_sink", part_window_sink),
-                         ("sparse_128k", part_sparse)):
+                         ("ring", part_ring), ("sparse_128k", part_sparse)):
             try:
                 parts.update(fn(torch, ga, ps, pw, flush, peaks))
             except Exception as e:  # report, never hide

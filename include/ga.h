@@ -115,7 +115,7 @@ size_t ga_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk
  * library-owned array instead.
  *
  * Computes exactly what ga_attend computes with dtype GA_BF16, block_mask NULL and a
- * workspace, for shapes on the split-K decode path: d = 64 or 128 and
+ * workspace, for shapes on the split-K decode path: d = 64, 128 or 256 and
  * (n_heads / n_kv) * Tq <= 16.  Other shapes return GA_ERR_UNSUPPORTED.  The other
  * arguments, layouts and errors are those of ga_attend.
  *
@@ -136,6 +136,48 @@ int ga_attend_decode_static(const void* q, const void* k, const void* v, void* o
                             int batch, int n_heads, int n_kv, int d, int Tq, int Tk_max,
                             const int32_t* k_lens, int causal, int window, const float* sink,
                             float* lse, ga_stream_t stream);
+
+/*
+ * ga_ring_append -- write one new token per sequence into a sliding-window ring cache.
+ * ("Attention in Code", section 2: a layer that only looks at the last W tokens keeps a
+ * cache of W slots per kv head; token number n, counting from 0, goes to slot n mod W and
+ * overwrites the oldest token once the cache is full.)
+ *
+ *   k_ring, v_ring  device bf16 [batch, n_kv, W, d], caller-owned, updated in place.
+ *   k_new, v_new    device bf16 [batch, n_kv, d]: the new token's key and value per kv head.
+ *   n_seen          device int32 [batch]: tokens written so far.  Slot n_seen[b] mod W of
+ *                   every kv head of sequence b receives the new token, then n_seen[b] is
+ *                   incremented.  Must be >= 0 (not checked on the host; a negative value
+ *                   writes nothing and leaves the counter unchanged).
+ *   batch >= 1, n_kv >= 1, W >= 1, d a multiple of 8 in 8..256; the rings and new tokens
+ *   16-byte aligned, n_seen 4-byte aligned.
+ *   Asynchronous on stream; allocates nothing.  Calls that touch the same sequences must be
+ *   ordered (one stream or events): each reads and increments the counter.
+ */
+int ga_ring_append(void* k_ring, void* v_ring, const void* k_new, const void* v_new,
+                   int32_t* n_seen, int batch, int n_kv, int d, int W, ga_stream_t stream);
+
+/*
+ * ga_attend_ring -- decode attention of one query token per sequence over a ring cache.
+ * ("Attention in Code", section 2.)  For the query at absolute position n_seen[b] - 1 with a
+ * window of W positions, the keys it may use are exactly the min(n_seen[b], W) filled slots
+ * of the ring; their order in the ring does not matter, because a softmax over a set of keys
+ * does not depend on the order of the keys.  The result equals ga_attend with causal = 1 and
+ * window = W over the whole key sequence.
+ *
+ *   q, out          device bf16 [batch, n_heads, 1, d].
+ *   k_ring, v_ring  as in ga_ring_append, after the query token's own key and value were
+ *                   appended.
+ *   n_seen          device int32 [batch], >= 1 (values above W use all W slots).
+ *   sink, lse       as in ga_attend.
+ *   workspace       device scratch of ga_workspace_size(batch, n_heads, n_kv, d, 1, W,
+ *                   GA_BF16) bytes (may be NULL when that is 0).
+ *   d: 64, 128 or 256; n_heads / n_kv <= 16; other arguments and errors as in ga_attend.
+ */
+int ga_attend_ring(const void* q, const void* k_ring, const void* v_ring, void* out,
+                   int batch, int n_heads, int n_kv, int d, int W, const int32_t* n_seen,
+                   const float* sink, float* lse, void* workspace, size_t workspace_bytes,
+                   ga_stream_t stream);
 
 /*
  * ga_block_stats -- centroid and maximum radius of every key block.

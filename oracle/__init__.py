@@ -24,7 +24,7 @@ Modules:
 """
 from .attention import attend, positions, visible
 from .blocks import allowed_blocks, block_stats, radius_zscores, select_blocks
-from .ring import ring_decode
+from .ring import ring_contents, ring_decode
 
 __all__ = ["attend", "positions", "visible", "allowed_blocks", "block_stats",
-           "radius_zscores", "select_blocks", "ring_decode"]
+           "radius_zscores", "select_blocks", "ring_contents", "ring_decode"]

@@ -13,7 +13,7 @@ import math
 
 import numpy as np
 
-__all__ = ["ring_decode"]
+__all__ = ["ring_contents", "ring_decode"]
 
 
 def ring_decode(q, k, v, window: int, sink=None):
@@ -44,3 +44,18 @@ def ring_decode(q, k, v, window: int, sink=None):
             Z = w.sum() + (0.0 if sink is None else math.exp(float(sink[h]) - m))
             out[h, t] = (w @ ring_v[h // g, :filled]) / Z
     return out
+
+
+def ring_contents(k, v, window: int, n_tokens: int | None = None):
+    """The ring caches after tokens 0 .. n_tokens-1 of k, v [n_kv, T, d] were written, token t
+    into slot t mod W ("Attention in Code", section 2).  Slots never written stay zero.
+    Returns (ring_k, ring_v), each [n_kv, W, d]."""
+    k = np.asarray(k)
+    v = np.asarray(v)
+    n = k.shape[1] if n_tokens is None else n_tokens
+    ring_k = np.zeros((k.shape[0], window, k.shape[2]), dtype=k.dtype)
+    ring_v = np.zeros((v.shape[0], window, v.shape[2]), dtype=v.dtype)
+    for t in range(n):
+        ring_k[:, t % window] = k[:, t]
+        ring_v[:, t % window] = v[:, t]
+    return ring_k, ring_v

@@ -25,6 +25,7 @@ __all__ = [
     "ga_selftest_wait_timeout", "ga_status_string", "ga_version", "GA_OK", "GA_ERR_INVALID_ARG",
     "GA_ERR_UNSUPPORTED", "GA_ERR_CUDA", "GA_ERR_DEVICE_TIMEOUT", "GA_ERR_WORKSPACE",
     "GA_ERR_SCRATCH_LIMIT", "GA_DECODE_STATIC_SCRATCH_BYTES", "ga_attend_decode_static",
+    "ga_ring_append", "ga_attend_ring",
 ]
 
 GA_OK, GA_ERR_INVALID_ARG, GA_ERR_UNSUPPORTED = 0, -1, -2
@@ -63,6 +64,10 @@ def lib() -> ctypes.CDLL:
     L.ga_attend_decode_static.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32,
                                           vp, vp, vp]
     L.ga_attend_decode_static.restype = i32
+    L.ga_ring_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    L.ga_ring_append.restype = i32
+    L.ga_attend_ring.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    L.ga_attend_ring.restype = i32
     L.ga_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.ga_workspace_size.restype = sz
     L.ga_block_stats.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp]
@@ -191,6 +196,54 @@ def ga_attend_decode_static(q, k, v, out=None, *, k_lens=None, causal=True, wind
                                    _ptr(k_lens), int(bool(causal)), int(window), _ptr(sink), _ptr(lse),
                                    _stream(stream))
     _check(st, "ga_attend_decode_static")
+    return out
+
+
+def ga_ring_append(k_ring, v_ring, k_new, v_new, n_seen, *, stream=None):
+    """Write one token per sequence into the W-slot ring caches: k_new, v_new [B, n_kv, d]
+    go to slot n_seen[b] % W of k_ring, v_ring [B, n_kv, W, d]; n_seen [B] (int32) is then
+    incremented on the device."""
+    L = lib()
+    for t, n in ((k_ring, "k_ring"), (v_ring, "v_ring")):
+        _need(t, n, torch.bfloat16, 4)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, torch.bfloat16, 3)
+    _need(n_seen, "n_seen", torch.int32, 1)
+    B, n_kv, W, d = k_ring.shape
+    if v_ring.shape != k_ring.shape or k_new.shape != (B, n_kv, d) or v_new.shape != k_new.shape \
+            or n_seen.shape != (B,):
+        raise ValueError("ring shapes: rings [B, n_kv, W, d], new tokens [B, n_kv, d], n_seen [B]")
+    st = L.ga_ring_append(_ptr(k_ring), _ptr(v_ring), _ptr(k_new), _ptr(v_new), _ptr(n_seen),
+                          B, n_kv, d, W, _stream(stream))
+    _check(st, "ga_ring_append")
+
+
+def ga_attend_ring(q, k_ring, v_ring, n_seen, out=None, *, sink=None, lse=None, workspace=None,
+                   stream=None):
+    """Decode attention of the newest token of every sequence (q [B, n_heads, 1, d]) over its
+    ring cache: the min(n_seen[b], W) filled slots, after that token was appended."""
+    L = lib()
+    for t, n in ((q, "q"), (k_ring, "k_ring"), (v_ring, "v_ring")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(n_seen, "n_seen", torch.int32, 1)
+    B, H, Tq, d = q.shape
+    n_kv, W = k_ring.shape[1], k_ring.shape[2]
+    if Tq != 1 or k_ring.shape != (B, n_kv, W, d) or v_ring.shape != k_ring.shape or n_seen.shape != (B,):
+        raise ValueError("q [B, n_heads, 1, d], rings [B, n_kv, W, d], n_seen [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, 1)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    need = ga_workspace_size(B, H, n_kv, d, 1, W, q.dtype) if H % max(n_kv, 1) == 0 else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = L.ga_attend_ring(_ptr(q), _ptr(k_ring), _ptr(v_ring), _ptr(out), B, H, n_kv, d, W, _ptr(n_seen),
+                          _ptr(sink), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "ga_attend_ring")
     return out
 
 

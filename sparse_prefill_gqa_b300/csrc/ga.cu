@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "decode.cuh"
 #include "prefill_wide.cuh"
+#include "ring.cuh"
 
 namespace ga {
 
@@ -82,7 +83,7 @@ int launch_status() { return cudaGetLastError() == cudaSuccess ? GA_OK : GA_ERR_
 // ---- split-K decode geometry (shared by ga_workspace_size and ga_attend) -----------------
 bool decode_eligible(int n_heads, int n_kv, int d, int Tq, ga_dtype dtype, const void* block_mask) {
   const int g = n_heads / n_kv;
-  return dtype == GA_BF16 && block_mask == nullptr && (d == 64 || d == 128) && (long long)g * Tq <= 16;
+  return dtype == GA_BF16 && block_mask == nullptr && (d == 64 || d == 128 || d == 256) && (long long)g * Tq <= 16;
 }
 
 int decode_chunk_len(int batch, int n_kv, int Tk_max) {
@@ -137,13 +138,39 @@ int static_scratch_setup(void** addr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_static_scratch) != cudaSuccess || p == nullptr)
       return GA_ERR_CUDA;
-    if (set_smem(decode_splitk_kernel<128>, DecodeCfg<128>::SMEM_BYTES) != GA_OK ||
+    if (set_smem(decode_splitk_kernel<256>, DecodeCfg<256>::SMEM_BYTES) != GA_OK ||
+        set_smem(decode_splitk_kernel<128>, DecodeCfg<128>::SMEM_BYTES) != GA_OK ||
         set_smem(decode_splitk_kernel<64>, DecodeCfg<64>::SMEM_BYTES) != GA_OK)
       return GA_ERR_CUDA;
     g_static_scratch_addr[dev] = p;
   }
   *addr = g_static_scratch_addr[dev];
   return GA_OK;
+}
+
+// Launches the split-K decode (d in {64, 128, 256}) and, for more than one chunk, the combine.
+// The caller has validated the shape and placed the partial-result workspace.
+template <int D>
+int launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfloat16* qb,
+                    __nv_bfloat16* ob, float* lse, float* ws_o, float* ws_ml, const DecodeShape& ds,
+                    cudaStream_t stream) {
+  static int ok = set_smem(decode_splitk_kernel<D>, DecodeCfg<D>::SMEM_BYTES);
+  if (ok != GA_OK) return ok;
+  const dim3 grid(ds.n_chunks, ds.a.n_kv, ds.a.batch);
+  decode_splitk_kernel<D><<<grid, DecodeCfg<D>::THREADS, DecodeCfg<D>::SMEM_BYTES, stream>>>(
+      tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
+  const int st = launch_status();
+  if (st != GA_OK || ds.n_chunks == 1) return st;
+  decode_combine_kernel<D><<<dim3(ds.a.Tq, ds.a.n_heads, ds.a.batch), D, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
+  return launch_status();
+}
+
+int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfloat16* qb,
+                  __nv_bfloat16* ob, float* lse, float* ws_o, float* ws_ml, const DecodeShape& ds,
+                  cudaStream_t stream) {
+  if (d == 256) return launch_decode_d<256>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+  if (d == 128) return launch_decode_d<128>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+  return launch_decode_d<64>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
 }
 
 }  // namespace
@@ -256,26 +283,7 @@ int ga_attend(const void* q, const void* k, const void* v, void* out, int batch,
     if (!make_map_bf16(&tk, k, d, Tk_max, (long long)batch * n_kv, 64) ||
         !make_map_bf16(&tv, v, d, Tk_max, (long long)batch * n_kv, 64))
       return GA_ERR_CUDA;
-    dim3 grid(ds.n_chunks, n_kv, batch);
-    if (d == 128) {
-      static int ok = set_smem(decode_splitk_kernel<128>, DecodeCfg<128>::SMEM_BYTES);
-      if (ok != GA_OK) return ok;
-      decode_splitk_kernel<128><<<grid, DecodeCfg<128>::THREADS, DecodeCfg<128>::SMEM_BYTES, stream>>>(
-          tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
-    } else {
-      static int ok = set_smem(decode_splitk_kernel<64>, DecodeCfg<64>::SMEM_BYTES);
-      if (ok != GA_OK) return ok;
-      decode_splitk_kernel<64><<<grid, DecodeCfg<64>::THREADS, DecodeCfg<64>::SMEM_BYTES, stream>>>(
-          tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
-    }
-    int st = launch_status();
-    if (st != GA_OK || ds.n_chunks == 1) return st;
-    dim3 cgrid(Tq, n_heads, batch);
-    if (d == 128)
-      decode_combine_kernel<128><<<cgrid, 128, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
-    else
-      decode_combine_kernel<64><<<cgrid, 64, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
-    return launch_status();
+    return launch_decode(d, tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
   }
 
   // ---- tensor-core prefill ---------------------------------------------------------------
@@ -363,21 +371,35 @@ int ga_attend_decode_static(const void* q, const void* k, const void* v, void* o
   if (!make_map_bf16(&tk, k, d, Tk_max, (long long)batch * n_kv, 64) ||
       !make_map_bf16(&tv, v, d, Tk_max, (long long)batch * n_kv, 64))
     return GA_ERR_CUDA;
-  dim3 grid(ds.n_chunks, n_kv, batch);
-  if (d == 128)
-    decode_splitk_kernel<128><<<grid, DecodeCfg<128>::THREADS, DecodeCfg<128>::SMEM_BYTES, stream>>>(
-        tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
-  else
-    decode_splitk_kernel<64><<<grid, DecodeCfg<64>::THREADS, DecodeCfg<64>::SMEM_BYTES, stream>>>(
-        tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
-  int st = launch_status();
-  if (st != GA_OK || ds.n_chunks == 1) return st;
-  dim3 cgrid(Tq, n_heads, batch);
-  if (d == 128)
-    decode_combine_kernel<128><<<cgrid, 128, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
-  else
-    decode_combine_kernel<64><<<cgrid, 64, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
+  return launch_decode(d, tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+}
+
+int ga_ring_append(void* k_ring, void* v_ring, const void* k_new, const void* v_new, int32_t* n_seen,
+                   int batch, int n_kv, int d, int W, ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!k_ring || !v_ring || !k_new || !v_new || !n_seen) return GA_ERR_INVALID_ARG;
+  if (batch < 1 || n_kv < 1 || W < 1 || d < 8 || d > 256 || d % 8 != 0) return GA_ERR_INVALID_ARG;
+  if (batch > 0x7fffffff / 2) return GA_ERR_UNSUPPORTED;
+  if (!aligned16(k_ring) || !aligned16(v_ring) || !aligned16(k_new) || !aligned16(v_new) ||
+      (reinterpret_cast<uintptr_t>(n_seen) & 3) != 0)
+    return GA_ERR_INVALID_ARG;
+  ring_append_kernel<<<batch, kRingThreads, 0, stream>>>(
+      (__nv_bfloat16*)k_ring, (__nv_bfloat16*)v_ring, (const __nv_bfloat16*)k_new,
+      (const __nv_bfloat16*)v_new, n_seen, n_kv, d, W);
   return launch_status();
+}
+
+int ga_attend_ring(const void* q, const void* k_ring, const void* v_ring, void* out, int batch,
+                   int n_heads, int n_kv, int d, int W, const int32_t* n_seen, const float* sink,
+                   float* lse, void* workspace, size_t workspace_bytes, ga_stream_t stream) {
+  if (!n_seen || W < 1 || n_heads < 1 || n_kv < 1 || n_heads % n_kv != 0) return GA_ERR_INVALID_ARG;
+  if (!(d == 64 || d == 128 || d == 256) || n_heads / n_kv > 16) return GA_ERR_UNSUPPORTED;
+  // The query is the newest token, at absolute position n_seen - 1 of its sequence; with a
+  // window of W positions the keys it may use are exactly the min(n_seen, W) filled slots.
+  // Over the ring that is a causal decode row whose key count is n_seen clamped to W (the
+  // kernels clamp every length to [0, Tk_max] = [0, W]).
+  return ga_attend(q, k_ring, v_ring, out, batch, n_heads, n_kv, d, 1, W, n_seen, 1, 0, sink, nullptr,
+                   1, 1, lse, GA_BF16, workspace, workspace_bytes, stream);
 }
 
 int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, int d, int Tk_max,

@@ -92,3 +92,19 @@ def test_block_calls_reject_invalid_arguments(L):
     bad = list(args)
     bad[16] = None                              # no output
     assert L.ga_select_blocks(*bad) == ga.GA_ERR_INVALID_ARG
+
+
+def test_ring_calls_reject_invalid_arguments(L):
+    p = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4098)                 # not 4-byte aligned
+    # ga_ring_append(k_ring, v_ring, k_new, v_new, n_seen, batch, n_kv, d, W, stream)
+    assert L.ga_ring_append(p, p, p, p, p, 1, 2, 128, 0, None) == ga.GA_ERR_INVALID_ARG      # W = 0
+    assert L.ga_ring_append(p, p, p, p, p, 1, 2, 100, 8, None) == ga.GA_ERR_INVALID_ARG      # d % 8
+    assert L.ga_ring_append(p, p, p, p, None, 1, 2, 128, 8, None) == ga.GA_ERR_INVALID_ARG   # no counter
+    assert L.ga_ring_append(p, p, p, p, odd, 1, 2, 128, 8, None) == ga.GA_ERR_INVALID_ARG    # misaligned
+    # ga_attend_ring(q, k_ring, v_ring, out, batch, n_heads, n_kv, d, W, n_seen, sink, lse, ws, bytes, stream)
+    assert L.ga_attend_ring(p, p, p, p, 1, 8, 2, 128, 0, p, None, None, None, 0, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_attend_ring(p, p, p, p, 1, 8, 3, 128, 8, p, None, None, None, 0, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_attend_ring(p, p, p, p, 1, 8, 2, 96, 8, p, None, None, None, 0, None) == ga.GA_ERR_UNSUPPORTED
+    assert L.ga_attend_ring(p, p, p, p, 1, 64, 2, 128, 8, p, None, None, None, 0, None) == ga.GA_ERR_UNSUPPORTED
+    assert L.ga_attend_ring(p, p, p, p, 1, 8, 2, 128, 8, None, None, None, None, 0, None) == ga.GA_ERR_INVALID_ARG

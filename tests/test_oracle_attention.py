@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import attend, positions, ring_decode, visible
+from oracle import attend, positions, ring_contents, ring_decode, visible
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -239,6 +239,30 @@ def test_ring_cache_equals_window_mask_and_forgets_token_zero():
     assert np.max(np.abs(masked2[0, :, :W] - masked[0, :, :W])) > 1.0
     ring2 = ring_decode(q, k, v2, W)
     assert np.array_equal(ring2[:, W:], ring[:, W:])
+
+
+def test_ring_contents_slot_rule_and_decode_consistency():
+    """"Attention in Code" s.2: after n tokens slot s holds the newest token t < n with
+    t mod W = s (checked by enumerating the tokens), never-written slots stay zero, and the
+    last ring_decode output is plain attention over the min(n, W) filled slots in slot order."""
+    n_kv, T, d, W = 2, 23, 4, 8
+    k = _rand((n_kv, T, d), 64)
+    v = _rand((n_kv, T, d), 65)
+    for n in (0, 3, 8, 9, 23):
+        rk, rv = ring_contents(k, v, W, n)
+        for slot in range(W):
+            owners = [t for t in range(n) if t % W == slot]
+            if owners:
+                assert np.array_equal(rk[:, slot], k[:, max(owners)])
+                assert np.array_equal(rv[:, slot], v[:, max(owners)])
+            else:
+                assert not rk[:, slot].any() and not rv[:, slot].any()
+    H = 4
+    q = _rand((H, T, d), 66)
+    ring = ring_decode(q, k, v, W)
+    rk, rv = ring_contents(k, v, W)
+    last, _ = attend(q[None, :, T - 1:], rk[None], rv[None], causal=False)
+    assert np.max(np.abs(ring[:, T - 1] - last[0, :, 0])) <= 1e-13
 
 
 def test_sink_closed_forms():
