@@ -86,23 +86,49 @@ def allowed_blocks(alpha: int, Tq: int, Tk: int, q_block: int, k_block: int,
     return ok
 
 
-def radius_zscores(radius_row: np.ndarray):
-    """z-scores of one (sequence, kv head) row of radii: (r - mean) / population std.
+# Consistency factor of the median absolute deviation for normally distributed data:
+# 1 / (the 0.75 quantile of the standard normal), so that 1.4826 * MAD estimates sigma.
+MAD_NORMAL = 1.4826
 
-    Returns None when the std is zero (every block has the same radius: nothing stands out).
+
+def radius_zscores(radius_row: np.ndarray, rule: str = "z"):
+    """How unusual each radius of one (sequence, kv head) row is, judged against the row's
+    own distribution ("RBS-Attention review": a radius is large relative to the prompt,
+    layer and head).
+
+    rule "z":   (r - mean) / population std.
+    rule "mad": (r - median) / (1.4826 * median(|r - median|)), the robust form: a few very
+                large radii cannot inflate the scale and hide themselves.
+    Returns None when the scale is zero (nothing stands out).
     """
     r = np.asarray(radius_row, dtype=np.float64)
-    mu = r.mean()
-    sigma = math.sqrt(((r - mu) ** 2).mean())
-    if sigma == 0.0:
-        return None
-    return (r - mu) / sigma
+    if rule == "z":
+        mu = r.mean()
+        sigma = math.sqrt(((r - mu) ** 2).mean())
+        if sigma == 0.0:
+            return None
+        return (r - mu) / sigma
+    if rule == "mad":
+        med = float(np.median(r))
+        mad = float(np.median(np.abs(r - med)))
+        if mad == 0.0:
+            return None
+        return (r - med) / (MAD_NORMAL * mad)
+    raise ValueError(f"unknown radius rule {rule!r}")
 
 
 def select_blocks(q, centroid, radius, *, Tk: int, q_block: int = 128, k_block: int = 64,
                   causal: bool = True, window: int = 0, tau_mean: float = math.inf,
-                  lambda_radius: float = 3.0, return_margins: bool = False):
+                  lambda_radius: float = 3.0, return_margins: bool = False,
+                  radius_rule: str = "z", tau_bound: float | None = None):
     """Union of the mean-score branch and the radius-rescue branch, plus the diagonal.
+
+    radius_rule: "z" or "mad" (see radius_zscores).  tau_bound: when given, a third branch
+    keeps block beta if the Cauchy-Schwarz bound on the pooled query's score over the
+    block's keys, (q_mean . c + |q_mean| r) / sqrt(d) >= max_j q_mean . k_j / sqrt(d), is at
+    least the best visible mean score minus tau_bound: a block whose keys could score that
+    high is kept however low its mean.  With return_margins the bound branch's margins are
+    returned as a fifth array.
 
     q: [B, H, Tq, d]; centroid: [B, n_kv, >=nKb, d]; radius: [B, n_kv, >=nKb] with
     nKb = ceil(Tk / k_block).  Returns (mask uint8 [B, H, nQb, nKb], n_selected int32
@@ -121,9 +147,10 @@ def select_blocks(q, centroid, radius, *, Tk: int, q_block: int = 128, k_block: 
     mask = np.zeros((B, H, nQb, nKb), dtype=np.uint8)
     mean_margin = np.full((B, H, nQb, nKb), np.nan)
     z_margin = np.full((B, H, nQb, nKb), np.nan)
+    bound_margin = np.full((B, H, nQb, nKb), np.nan)
     for b in range(B):
         for kvh in range(n_kv):
-            z = radius_zscores(radius[b, kvh, :nKb])
+            z = radius_zscores(radius[b, kvh, :nKb], radius_rule)
             rescue = np.zeros(nKb, dtype=bool) if z is None else z >= lambda_radius
             c = centroid[b, kvh, :nKb]
             for h in range(kvh * g, (kvh + 1) * g):
@@ -135,15 +162,22 @@ def select_blocks(q, centroid, radius, *, Tk: int, q_block: int = 128, k_block: 
                     s = (c @ q_mean) * scale
                     top = s[allowed].max()
                     keep_mean = s >= top - tau_mean
+                    keep_bound = np.zeros(nKb, dtype=bool)
+                    if tau_bound is not None:
+                        ub = (c @ q_mean + np.linalg.norm(q_mean) * radius[b, kvh, :nKb]) * scale
+                        keep_bound = ub >= top - tau_bound
+                        bound_margin[b, h, alpha] = ub - (top - tau_bound)
                     j_lo = np.arange(nKb, dtype=np.int64) * k_block
                     j_hi = np.minimum(j_lo + k_block, Tk) - 1
                     diagonal = (j_lo <= i_last) & (j_hi >= i_first)
-                    sel = allowed & (keep_mean | rescue | diagonal)
+                    sel = allowed & (keep_mean | keep_bound | rescue | diagonal)
                     mask[b, h, alpha] = sel
                     mean_margin[b, h, alpha] = s - (top - tau_mean)
                     if z is not None:
                         z_margin[b, h, alpha] = z - lambda_radius
     n_selected = mask.sum(axis=3, dtype=np.int32)
     if return_margins:
+        if tau_bound is not None:
+            return mask, n_selected, mean_margin, z_margin, bound_margin
         return mask, n_selected, mean_margin, z_margin
     return mask, n_selected

@@ -197,3 +197,75 @@ def test_radius_branch_rescues_planted_outliers_that_the_mean_misses():
         s = mm[0, h, last]
         top = set(np.argsort(-s)[:len(s) // 10])
         assert len(top & set(hit)) <= len(hit) // 2
+
+
+def test_mad_rule_by_hand_and_its_robustness():
+    """Robust radius rule: median and median absolute deviation worked by hand on small rows
+    (odd and even counts), and the reason for the rule: when one block in ten is an outlier,
+    the outliers inflate the population std until none reaches z >= 3, while the median and
+    MAD still place every outlier far out."""
+    z = radius_zscores(np.array([1.0, 2.0, 3.0, 4.0, 100.0]), "mad")
+    # median 3, deviations 2 1 0 1 97 -> MAD 1
+    assert np.allclose(z, (np.array([1, 2, 3, 4, 100]) - 3.0) / 1.4826)
+    z = radius_zscores(np.array([1.0, 2.0, 4.0, 10.0]), "mad")
+    # median (2 + 4) / 2 = 3, deviations 2 1 1 7 -> MAD (1 + 2) / 2 = 1.5
+    assert np.allclose(z, (np.array([1, 2, 4, 10]) - 3.0) / (1.4826 * 1.5))
+    assert radius_zscores(np.array([5.0, 5.0, 5.0, 9.0]), "mad") is None   # MAD 0: nothing stands out
+    r = 13.0 + 0.5 * _rand(200, 151)
+    r[::10] = 20.0                                                         # 20 planted outliers
+    assert np.sum(radius_zscores(r, "z")[::10] >= 3.0) == 0
+    assert np.all(radius_zscores(r, "mad")[::10] >= 3.0)
+
+
+def test_bound_branch_bounds_the_block_scores_and_contains_the_mean_branch():
+    """The bound branch's score (q_mean . c + |q_mean| r) / sqrt(d) is at least the pooled
+    query's score against every key of the block (checked key by key); so at equal
+    thresholds the bound branch keeps every block the mean branch keeps, infinite tau_bound
+    keeps every visible block, and a brute-force union matches."""
+    B, H, n_kv, T, d, qb, kb = 1, 4, 2, 256, 8, 32, 16
+    q = _rand((B, H, T, d), 161)
+    k = _rand((B, n_kv, T, d), 162)
+    k[0, 1, 90] *= 7.0
+    c, r = block_stats(k, None, kb)
+    nKb = T // kb
+    for h in range(H):
+        kvh = h // (H // n_kv)
+        for alpha in range(T // qb):
+            qm = q[0, h, alpha * qb:(alpha + 1) * qb].mean(axis=0)
+            ub = (c[0, kvh] @ qm + np.linalg.norm(qm) * r[0, kvh]) / math.sqrt(d)
+            best = (k[0, kvh].reshape(nKb, kb, d) @ qm).max(axis=1) / math.sqrt(d)
+            assert np.all(ub >= best - 1e-12)
+    for tau in (0.0, 0.3, 1.0):
+        m_mean, _ = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=tau, lambda_radius=math.inf)
+        m_both, _ = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=-math.inf,
+                                  lambda_radius=math.inf, tau_bound=tau)
+        m_mean_only = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=-math.inf,
+                                    lambda_radius=math.inf)[0]                   # diagonal only
+        assert np.all(m_both >= m_mean)
+        assert np.all(m_both >= m_mean_only)
+    dense, _ = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=-math.inf,
+                             lambda_radius=math.inf, tau_bound=math.inf)
+    for alpha in range(T // qb):
+        assert np.array_equal(dense[0, :, alpha], np.repeat(allowed_blocks(alpha, T, T, qb, kb, True, 0)[None], H, 0))
+    # brute force of the three-branch union with the robust rule
+    tau, tb, lam = 0.05, 0.2, 2.0
+    mask, _ = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=tau, lambda_radius=lam,
+                            radius_rule="mad", tau_bound=tb)
+    for h in range(H):
+        kvh = h // (H // n_kv)
+        rr = r[0, kvh]
+        med = sorted(rr)[nKb // 2 - 1: nKb // 2 + 1]
+        med = (med[0] + med[1]) / 2
+        dev = sorted(abs(x - med) for x in rr)
+        mad = (dev[nKb // 2 - 1] + dev[nKb // 2]) / 2
+        for alpha in range(T // qb):
+            qm = q[0, h, alpha * qb:(alpha + 1) * qb].mean(axis=0)
+            vis = allowed_blocks(alpha, T, T, qb, kb, True, 0)
+            s = c[0, kvh] @ qm / math.sqrt(d)
+            top = s[vis].max()
+            for x in range(nKb):
+                ub = s[x] + np.linalg.norm(qm) * rr[x] / math.sqrt(d)
+                own = alpha * qb // kb <= x <= ((alpha + 1) * qb - 1) // kb
+                keep = vis[x] and (s[x] >= top - tau or ub >= top - tb or
+                                   (rr[x] - med) / (1.4826 * mad) >= lam or own)
+                assert mask[0, h, alpha, x] == keep
