@@ -344,6 +344,25 @@ def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
     sel_bytes = q.numel() * 2 + cen.numel() * 4 + mask.numel()
     res["block_select"] = {"ms": statistics.mean(tsel),
                            "GB/s": sel_bytes / (statistics.mean(tsel) * 1e-3) / 1e9}
+    # Selection variants at tau_mean = 0.02 (about density 0.1): the mean branch alone, with the
+    # radius rescue (z-score or median/MAD, lambda from the workload), and with the bound branch
+    # as the rescue instead (bound >= best mean score + 3, no radius branch); time, density and
+    # the recall of the planted outlier blocks (visible (query block, planted block) pairs kept).
+    planted = torch.zeros(n_kv, nKb, dtype=torch.bool, device="cuda")
+    for kvh, blk, tok, vec in planted_outliers(c.seed, n_kv, T, d, kb, c.planted_fraction):
+        planted[kvh, blk] = True
+    target = planted.repeat_interleave(H // n_kv, dim=0)[:, None, :] & (pairs > 0)[None]
+    variants = {}
+    for name, rule, lm, tb in (("mean only", "z", math.inf, None), ("z rescue", "z", lam, None),
+                               ("mad rescue", "mad", lam, None), ("bound rescue", "z", math.inf, -3.0)):
+        fn = lambda: ga.ga_select_blocks(q, cen, rad, Tk=T, q_block=qb, k_block=kb, tau_mean=0.02,
+                                         lambda_radius=lm, block_mask=mask, n_selected=nsel,
+                                         radius_rule=rule, tau_bound=tb)
+        tv = statistics.mean(timed_steps(torch, fn, max(3, steps // 2), min(warmup, 2), flush))
+        fn()
+        recall = float((mask[0].bool() & target).sum()) / max(1, int(target.sum()))
+        variants[name] = {"ms": tv, "density": density(), "planted_recall": recall}
+    res["block_select_variants"] = variants
     if select_only:
         return res
     # tau for target densities (bisection on the measured density)

@@ -233,6 +233,39 @@ int ga_select_blocks(const void* q, const float* centroid, const float* radius,
                      uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype,
                      ga_stream_t stream);
 
+/* Radius rules of ga_select_blocks_ex. */
+typedef enum {
+  GA_RADIUS_ZSCORE = 0,   /* (r - mean) / population std, as ga_select_blocks */
+  GA_RADIUS_MAD = 1       /* (r - median) / (1.4826 * median |r - median|): a few very large
+                             radii cannot inflate the scale and hide themselves */
+} ga_radius_rule;
+
+/*
+ * ga_select_blocks_ex -- ga_select_blocks with a choice of radius rule and a third branch.
+ * ("RBS-Attention review": the radius is judged against the head's own radius
+ * distribution; the method's name, radius-bounded, and the maximum key-block radius.)
+ *
+ *   radius_rule  GA_RADIUS_ZSCORE: the radius branch of ga_select_blocks.
+ *                GA_RADIUS_MAD: z = (r - median) / (1.4826 * MAD) over the radii of the
+ *                ceil(Tk/k_block) blocks of (b, kvh), median and MAD (median absolute
+ *                deviation) of an even count being the mean of the two middle values, fp64;
+ *                nothing is rescued when MAD == 0.  Needs ceil(Tk/k_block) <= 16384.
+ *   tau_bound    bound branch: keep beta if
+ *                  (mean_rows(q) . centroid[beta] + |mean_rows(q)| * radius[beta]) / sqrt(d)
+ *                    >= max_{visible} s - tau_bound.
+ *                The left side bounds the pooled query's score over every key of the block
+ *                (Cauchy-Schwarz: |k - c| <= radius), so a block whose keys could score that
+ *                high is kept however low its mean is.  -INFINITY: no bound branch.
+ *   block_mask = visible && (mean || bound || radius || diagonal).  Everything else as in
+ *   ga_select_blocks; NaN thresholds and unknown rules give GA_ERR_INVALID_ARG.
+ */
+int ga_select_blocks_ex(const void* q, const float* centroid, const float* radius,
+                        int batch, int n_heads, int n_kv, int d, int Tq, int Tk, int nKb_out,
+                        int q_block, int k_block, int causal, int window,
+                        float tau_mean, float lambda_radius, int radius_rule, float tau_bound,
+                        uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype,
+                        ga_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device status: GA_OK, or
  * GA_ERR_DEVICE_TIMEOUT when some kernel gave up on a wait since the last read.  Returns
  * GA_ERR_CUDA when the synchronisation itself fails. */

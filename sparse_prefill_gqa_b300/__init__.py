@@ -25,13 +25,14 @@ __all__ = [
     "ga_selftest_wait_timeout", "ga_status_string", "ga_version", "GA_OK", "GA_ERR_INVALID_ARG",
     "GA_ERR_UNSUPPORTED", "GA_ERR_CUDA", "GA_ERR_DEVICE_TIMEOUT", "GA_ERR_WORKSPACE",
     "GA_ERR_SCRATCH_LIMIT", "GA_DECODE_STATIC_SCRATCH_BYTES", "ga_attend_decode_static",
-    "ga_ring_append", "ga_attend_ring",
+    "ga_ring_append", "ga_attend_ring", "GA_RADIUS_ZSCORE", "GA_RADIUS_MAD",
 ]
 
 GA_OK, GA_ERR_INVALID_ARG, GA_ERR_UNSUPPORTED = 0, -1, -2
 GA_ERR_CUDA, GA_ERR_DEVICE_TIMEOUT, GA_ERR_WORKSPACE = -3, -4, -5
 GA_ERR_SCRATCH_LIMIT = -6
 GA_DECODE_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
+GA_RADIUS_ZSCORE, GA_RADIUS_MAD = 0, 1
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -75,6 +76,9 @@ def lib() -> ctypes.CDLL:
     L.ga_select_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                    f32, f32, vp, vp, i32, vp]
     L.ga_select_blocks.restype = i32
+    L.ga_select_blocks_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                      f32, f32, i32, f32, vp, vp, i32, vp]
+    L.ga_select_blocks_ex.restype = i32
     L.ga_read_device_status.argtypes = [vp]
     L.ga_read_device_status.restype = i32
     L.ga_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -269,8 +273,11 @@ def ga_block_stats(k, k_block=64, *, k_lens=None, centroid=None, radius=None, st
 
 def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, causal=True,
                      window=0, tau_mean=math.inf, lambda_radius=3.0, block_mask=None,
-                     n_selected=None, n_kv=None, stream=None):
-    """Block mask (uint8 [B, H, nQb, nKb]) and per-row counts (int32 [B, H, nQb])."""
+                     n_selected=None, n_kv=None, radius_rule="z", tau_bound=None, stream=None):
+    """Block mask (uint8 [B, H, nQb, nKb]) and per-row counts (int32 [B, H, nQb]).
+
+    radius_rule: "z" (mean and population std) or "mad" (median and 1.4826 * MAD);
+    tau_bound: threshold of the Cauchy-Schwarz bound branch, None for no bound branch."""
     L = lib()
     _need(q, "q", None, 4)
     B, H, Tq, d = q.shape
@@ -282,10 +289,12 @@ def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, c
         block_mask = torch.empty(B, H, nQb, nKb_out, dtype=torch.uint8, device=q.device)
     if n_selected is None:
         n_selected = torch.empty(B, H, nQb, dtype=torch.int32, device=q.device)
-    st = L.ga_select_blocks(_ptr(q), _ptr(centroid), _ptr(radius), B, H, n_kv, d, Tq, int(Tk),
-                            nKb_out, int(q_block), int(k_block), int(bool(causal)), int(window),
-                            float(tau_mean), float(lambda_radius), _ptr(block_mask), _ptr(n_selected),
-                            _DTYPES[q.dtype], _stream(stream))
+    rule = {"z": GA_RADIUS_ZSCORE, "mad": GA_RADIUS_MAD}[radius_rule]
+    tb = -math.inf if tau_bound is None else float(tau_bound)
+    st = L.ga_select_blocks_ex(_ptr(q), _ptr(centroid), _ptr(radius), B, H, n_kv, d, Tq, int(Tk),
+                               nKb_out, int(q_block), int(k_block), int(bool(causal)), int(window),
+                               float(tau_mean), float(lambda_radius), rule, tb, _ptr(block_mask),
+                               _ptr(n_selected), _DTYPES[q.dtype], _stream(stream))
     _check(st, "ga_select_blocks")
     return block_mask, n_selected
 

@@ -290,12 +290,37 @@ struct SelectShape {
   int batch, n_heads, n_kv, d, Tq, Tk, nKb_out, q_block, k_block, causal, window;
   int nQb, nKb;                   // query blocks, key blocks holding keys (ceil(Tk/k_block))
   float tau_mean, lambda_radius;
+  int radius_rule;                // 0: z-score (mean, population std); 1: median and MAD
+  int sort_len;                   // rule 1: power of two >= nKb (the sort buffer); else 0
+  float tau_bound;                // bound branch threshold; -inf: no bound branch
 };
 
-// shared memory: qmt [d][kSelQS] | ctt [d][kSelCS] | red [8] double | rowmax [QT] | nsel [QT]
-// | ranges [QT][4] | rescue [nKb]
-__host__ __device__ inline size_t select_smem_bytes(int d, int nKb) {
-  return (size_t)d * (kSelQS + kSelCS) * 4 + (kSelThreads / 32) * 8 + kSelQT * 4 * 6 + (size_t)nKb + 16;
+// shared memory: qmt [d][kSelQS] | ctt [d][kSelCS] | red [8] double | sortbuf [sort_len] double
+// | rowmax [QT] | qnrm [QT] | nsel [QT] | ranges [QT][4] | rescue [nKb]
+__host__ __device__ inline size_t select_smem_bytes(int d, int nKb, int sort_len) {
+  return (size_t)d * (kSelQS + kSelCS) * 4 + (kSelThreads / 32) * 8 + (size_t)sort_len * 8 +
+         kSelQT * 4 * 7 + (size_t)nKb + 16;
+}
+
+// Ascending bitonic sort of buf[0, n) (n a power of two) by the CTA's kSelThreads threads.
+__device__ inline void select_sort(double* buf, int n) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kSelThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const double a = buf[i], b = buf[ixj];
+          if ((a > b) == ((i & k) == 0)) { buf[i] = b; buf[ixj] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Median of a sorted buf[0, n): the middle value, or the mean of the two middle values.
+__device__ inline double sorted_median(const double* buf, int n) {
+  return (n & 1) ? buf[n / 2] : (buf[n / 2 - 1] + buf[n / 2]) * 0.5;
 }
 
 template <typename T>
@@ -308,8 +333,10 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
   float* qmt = reinterpret_cast<float*>(sel_smem_raw);                 // [d][kSelQS]
   float* ctt = qmt + (size_t)d * kSelQS;                               // [d][kSelCS]
   double* red = reinterpret_cast<double*>(ctt + (size_t)d * kSelCS);   // [8]
-  float* rowmax = reinterpret_cast<float*>(red + kSelThreads / 32);    // [QT]
-  int* nsel = reinterpret_cast<int*>(rowmax + kSelQT);                 // [QT]
+  double* sortbuf = red + kSelThreads / 32;                            // [sort_len]
+  float* rowmax = reinterpret_cast<float*>(sortbuf + s.sort_len);      // [QT]
+  float* qnrm = rowmax + kSelQT;                                       // [QT]
+  int* nsel = reinterpret_cast<int*>(qnrm + kSelQT);                   // [QT]
   int* rng = nsel + kSelQT;                                            // [QT][4]
   uint8_t* rescue = reinterpret_cast<uint8_t*>(rng + 4 * kSelQT);      // [nKb]
 
@@ -330,17 +357,34 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
     for (int w = 0; w < kSelThreads / 32; ++w) tot += red[w];
     return tot;
   };
-  double part = 0.0;
-  for (int x = tid; x < s.nKb; x += kSelThreads) part += (double)rrow[x];
-  const double mu = block_sum(part) / s.nKb;
-  part = 0.0;
-  for (int x = tid; x < s.nKb; x += kSelThreads) {
-    const double e = (double)rrow[x] - mu;
-    part += e * e;
+  if (s.radius_rule == 0) {
+    double part = 0.0;
+    for (int x = tid; x < s.nKb; x += kSelThreads) part += (double)rrow[x];
+    const double mu = block_sum(part) / s.nKb;
+    part = 0.0;
+    for (int x = tid; x < s.nKb; x += kSelThreads) {
+      const double e = (double)rrow[x] - mu;
+      part += e * e;
+    }
+    const double sigma = sqrt(block_sum(part) / s.nKb);
+    for (int x = tid; x < s.nKb; x += kSelThreads)
+      rescue[x] = (sigma > 0.0 && ((double)rrow[x] - mu) / sigma >= (double)s.lambda_radius) ? 1 : 0;
+  } else {
+    // robust form: (r - median) / (1.4826 MAD), median and MAD by sorting (fp64, exact)
+    for (int x = tid; x < s.sort_len; x += kSelThreads) sortbuf[x] = x < s.nKb ? (double)rrow[x] : INFINITY;
+    __syncthreads();
+    select_sort(sortbuf, s.sort_len);
+    const double med = sorted_median(sortbuf, s.nKb);
+    __syncthreads();
+    for (int x = tid; x < s.sort_len; x += kSelThreads)
+      sortbuf[x] = x < s.nKb ? fabs((double)rrow[x] - med) : INFINITY;
+    __syncthreads();
+    select_sort(sortbuf, s.sort_len);
+    const double mad = sorted_median(sortbuf, s.nKb);
+    const double scale_r = 1.4826 * mad;   // consistency factor of the MAD for normal data
+    for (int x = tid; x < s.nKb; x += kSelThreads)
+      rescue[x] = (mad > 0.0 && ((double)rrow[x] - med) / scale_r >= (double)s.lambda_radius) ? 1 : 0;
   }
-  const double sigma = sqrt(block_sum(part) / s.nKb);
-  for (int x = tid; x < s.nKb; x += kSelThreads)
-    rescue[x] = (sigma > 0.0 && ((double)rrow[x] - mu) / sigma >= (double)s.lambda_radius) ? 1 : 0;
 
   // ---- 2. mean query row of each query block of this CTA -> qmt[c][a] --------------------
   // Warp w pools query blocks 4w .. 4w+3 on its own (no CTA-wide barrier between blocks).
@@ -400,6 +444,9 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
     rng[4 * tid + 0] = vlo; rng[4 * tid + 1] = vhi; rng[4 * tid + 2] = dlo; rng[4 * tid + 3] = dhi;
     rowmax[tid] = -INFINITY;
     nsel[tid] = 0;
+    float n2 = 0.0f;                                                   // |q_mean| of the block
+    for (int c = 0; c < d; ++c) n2 = fmaf(qmt[c * kSelQS + tid], qmt[c * kSelQS + tid], n2);
+    qnrm[tid] = sqrtf(n2);
   }
   __syncthreads();
   int beta_lo = s.nKb, beta_hi = 0;                                   // union over the CTA
@@ -476,14 +523,18 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
           if (lane == 0) rowmax[a] = fmaxf(rowmax[a], m);
         } else {
           const float thr = rowmax[a] - s.tau_mean;
+          // bound branch: (q_mean . c + |q_mean| r) / sqrt(d) >= best mean score - tau_bound
+          const bool bound = s.tau_bound != -INFINITY;
+          const float thr_b = rowmax[a] - s.tau_bound, qn = qnrm[a];
           uint32_t bytes = 0u;
           int kept = 0;
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int beta = bt + 4 * lane + jj;
             const bool vis = beta >= my_vlo[i] && beta < my_vhi[i];
-            const bool keep = vis && (__fmul_rn(acc[i][jj], scale) >= thr || rescue[beta] != 0 ||
-                                      (beta >= my_dlo[i] && beta <= my_dhi[i]));
+            const float sc = __fmul_rn(acc[i][jj], scale);
+            bool keep = vis && (sc >= thr || rescue[beta] != 0 || (beta >= my_dlo[i] && beta <= my_dhi[i]));
+            if (bound && vis && !keep) keep = __fmaf_rn(qn, __fmul_rn(rrow[beta], scale), sc) >= thr_b;
             bytes |= (keep ? 1u : 0u) << (8 * jj);
             kept += keep ? 1 : 0;
           }

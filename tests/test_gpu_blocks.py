@@ -107,3 +107,38 @@ def test_sparse_prefill_end_to_end():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     # and dense attention (another kernel at d = 128) within the bf16 tolerance
     assert_close(to_f64(a), to_f64(ga.ga_attend(q, k, v)), "bf16", "tau = inf vs dense")
+
+
+@pytest.mark.parametrize("B,H,n_kv,Tq,Tk,d,qb,kb,W,tau,lam,rule,tb", [
+    (1, 8, 2, 4096, 4096, 128, 128, 64, 0, 0.02, 3.0, "mad", None),             # robust rule
+    (1, 4, 2, 2048, 2048, 128, 128, 64, 0, -math.inf, math.inf, "z", 0.5),      # bound branch alone
+    (1, 4, 2, 3000, 3000, 128, 256, 128, 700, 0.015, 2.5, "mad", 0.3),          # all, with a window
+    (2, 4, 1, 1000, 3000, 128, 128, 64, 0, 0.01, 2.0, "mad", 0.2),              # chunk at an offset
+])
+def test_select_blocks_variants(B, H, n_kv, Tq, Tk, d, qb, kb, W, tau, lam, rule, tb):
+    """Robust (median / MAD) radius rule and the Cauchy-Schwarz bound branch.  The oracle gets
+    the GPU's own centroids and radii (fp32, widened exactly), so the radius decisions of the
+    two sides are the same fp64 arithmetic on the same inputs; score decisions may differ only
+    within the band."""
+    q, qr = host_tensor(63, "q", (B, H, Tq, d), "bf16")
+    k, _ = planted_keys(64, B, n_kv, Tk, d, kb)
+    c, r = ga.ga_block_stats(k, kb)
+    mask, nsel = ga.ga_select_blocks(q, c, r, Tk=Tk, q_block=qb, k_block=kb, window=W, tau_mean=tau,
+                                     lambda_radius=lam, radius_rule=rule, tau_bound=tb)
+    out = oracle.select_blocks(qr, to_f64(c), to_f64(r), Tk=Tk, q_block=qb, k_block=kb, window=W,
+                               tau_mean=tau, lambda_radius=lam, return_margins=True,
+                               radius_rule=rule, tau_bound=tb)
+    mref, nref, mm, zm = out[:4]
+    bm = out[4] if tb is not None else np.full_like(mm, np.nan)
+    gm = mask.cpu().numpy()
+    diff = gm != mref
+    near = (np.abs(np.nan_to_num(mm, nan=np.inf)) < BAND) | (np.abs(np.nan_to_num(bm, nan=np.inf)) < BAND)
+    # radius decisions are not in the band: the two sides compute them identically
+    assert not (diff & ~near).any(), f"{int((diff & ~near).sum())} decisions differ outside the band"
+    if tb is not None:   # the bound (>= the mean score) keeps every block the mean branch keeps at tau_bound
+        m_mean, _ = ga.ga_select_blocks(q, c, r, Tk=Tk, q_block=qb, k_block=kb, window=W, tau_mean=tb,
+                                        lambda_radius=math.inf)
+        assert np.all(gm >= m_mean.cpu().numpy())
+    assert np.array_equal(nsel.cpu().numpy(), gm.sum(axis=3))
+    if not diff.any():
+        assert np.array_equal(nsel.cpu().numpy(), nref)
