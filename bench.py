@@ -299,6 +299,28 @@ def part_ring(torch, ga, steps, warmup, flush, peaks):
                             "append_us": ta * 1e3}}
 
 
+def part_diff(torch, ga, steps, warmup, flush, peaks):
+    """Differential attention (A1 - lam A2) V on the dense workload's shape (B2 H32 Hkv8 d128
+    T8192, causal), lam = 0.8: two attention passes over the same values, the second fusing the
+    fp32 difference into its epilogue.  Algorithmic FLOPs: twice the causal attention's."""
+    from workloads import get_config
+    c = get_config(2)
+    B, H, n_kv, d, T = c.batch, c.n_heads, c.n_kv, c.d, c.Tq
+    q1 = device_bf16(torch, c.seed, "diff_q1", (B, H, T, d))
+    q2 = device_bf16(torch, c.seed, "diff_q2", (B, H, T, d))
+    k1 = device_bf16(torch, c.seed, "diff_k1", (B, n_kv, T, d))
+    k2 = device_bf16(torch, c.seed, "diff_k2", (B, n_kv, T, d))
+    v = device_bf16(torch, c.seed, "diff_v", (B, n_kv, T, d))
+    out = torch.empty_like(q1)
+    ws = torch.empty(B * H * T * d * 4, dtype=torch.uint8, device="cuda")
+    t = statistics.mean(timed_steps(torch, lambda: ga.ga_attend_diff(q1, k1, q2, k2, v, 0.8, out, workspace=ws),
+                                    steps, warmup, flush))
+    flops = 2 * 4 * d * H * B * causal_pairs(T, T)
+    return {"diff_attention": {"workload": "bf16 differential attention B2 H32 Hkv8 d128 T8192 causal, lambda 0.8",
+                               "ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12, "flops": flops,
+                               "launches_per_step": 2}}
+
+
 def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
     from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
     c = get_config(5)
@@ -446,6 +468,8 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
         res = part_window_sink(torch, ga, args.steps, warmup, flush, peaks)
     elif args.case == "ring":
         res = part_ring(torch, ga, args.steps, warmup, flush, peaks)
+    elif args.case == "diff":
+        res = part_diff(torch, ga, args.steps, warmup, flush, peaks)
     else:
         res = part_sparse(torch, ga, args.steps, warmup, flush, peaks, select_only=args.case == "select")
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": warmup, **res}))
@@ -462,7 +486,7 @@ def main():
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="all",
-                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "sparse", "select"],
+                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "diff", "sparse", "select"],
                     help="run one workload alone and print its own JSON line (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --case prefill/decode/chunk: a smaller batch (profiling captures)")
@@ -607,7 +631,7 @@ def main():
         parts = {}
         ps, pw = max(3, min(20, args.steps // 4)), 3
         for name, fn in (("decode_chunk", part_decode_and_chunk), ("window_sink", part_window_sink),
-                         ("ring", part_ring), ("sparse_128k", part_sparse)):
+                         ("ring", part_ring), ("diff", part_diff), ("sparse_128k", part_sparse)):
             try:
                 parts.update(fn(torch, ga, ps, pw, flush, peaks))
             except Exception as e:  # report, never hide

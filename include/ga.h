@@ -138,6 +138,26 @@ int ga_attend_decode_static(const void* q, const void* k, const void* v, void* o
                             float* lse, ga_stream_t stream);
 
 /*
+ * ga_attend_diff -- differential attention, out = (A1 - lam * A2) v.
+ * ("Attention Variants", differential attention: two attention maps from two query/key
+ * pairs over the same values, the second scaled by a mixing coefficient and subtracted.)
+ *
+ *   A1 = softmax(q1 k1^T / sqrt(d) + mask), A2 = softmax(q2 k2^T / sqrt(d) + mask), the mask
+ *   being ga_attend's (k_lens, causal, window) applied to both maps.
+ *   q1, q2, out     device bf16 [batch, n_heads, Tq, d];  k1, k2, v: [batch, n_kv, Tk_max, d].
+ *   lam             the mixing coefficient (finite).
+ *   workspace       device scratch of at least batch * n_heads * Tq * d * 4 bytes, 16-byte
+ *                   aligned: A1 v in fp32.  The difference is formed in fp32 and rounded to
+ *                   bf16 once (the two terms may nearly cancel).
+ *   d: 128 or 256 (the tensor-core path); other shapes GA_ERR_UNSUPPORTED.  Other arguments
+ *   and errors as in ga_attend.
+ */
+int ga_attend_diff(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                   void* out, int batch, int n_heads, int n_kv, int d, int Tq, int Tk_max,
+                   const int32_t* k_lens, int causal, int window, float lam, void* workspace,
+                   size_t workspace_bytes, ga_stream_t stream);
+
+/*
  * ga_ring_append -- write one new token per sequence into a sliding-window ring cache.
  * ("Attention in Code", section 2: a layer that only looks at the last W tokens keeps a
  * cache of W slots per kv head; token number n, counting from 0, goes to slot n mod W and

@@ -25,7 +25,7 @@ __all__ = [
     "ga_selftest_wait_timeout", "ga_status_string", "ga_version", "GA_OK", "GA_ERR_INVALID_ARG",
     "GA_ERR_UNSUPPORTED", "GA_ERR_CUDA", "GA_ERR_DEVICE_TIMEOUT", "GA_ERR_WORKSPACE",
     "GA_ERR_SCRATCH_LIMIT", "GA_DECODE_STATIC_SCRATCH_BYTES", "ga_attend_decode_static",
-    "ga_ring_append", "ga_attend_ring", "GA_RADIUS_ZSCORE", "GA_RADIUS_MAD",
+    "ga_ring_append", "ga_attend_ring", "ga_attend_diff", "GA_RADIUS_ZSCORE", "GA_RADIUS_MAD",
 ]
 
 GA_OK, GA_ERR_INVALID_ARG, GA_ERR_UNSUPPORTED = 0, -1, -2
@@ -65,6 +65,9 @@ def lib() -> ctypes.CDLL:
     L.ga_attend_decode_static.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32,
                                           vp, vp, vp]
     L.ga_attend_decode_static.restype = i32
+    L.ga_attend_diff.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32, f32,
+                                 vp, sz, vp]
+    L.ga_attend_diff.restype = i32
     L.ga_ring_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     L.ga_ring_append.restype = i32
     L.ga_attend_ring.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
@@ -200,6 +203,34 @@ def ga_attend_decode_static(q, k, v, out=None, *, k_lens=None, causal=True, wind
                                    _ptr(k_lens), int(bool(causal)), int(window), _ptr(sink), _ptr(lse),
                                    _stream(stream))
     _check(st, "ga_attend_decode_static")
+    return out
+
+
+def ga_attend_diff(q1, k1, q2, k2, v, lam, out=None, *, k_lens=None, causal=True, window=0,
+                   workspace=None, stream=None):
+    """Differential attention (A1 - lam A2) v with A_i = softmax(q_i k_i^T / sqrt(d) + mask);
+    bf16, d = 128 or 256.  workspace: >= batch * n_heads * Tq * d * 4 bytes (allocated here if
+    None): the first map's result in fp32."""
+    L = lib()
+    for t, n in ((q1, "q1"), (k1, "k1"), (q2, "q2"), (k2, "k2"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, H, Tq, d = q1.shape
+    n_kv, Tk_max = k1.shape[1], k1.shape[2]
+    if q2.shape != q1.shape or k1.shape != (B, n_kv, Tk_max, d) or k2.shape != k1.shape or v.shape != k1.shape:
+        raise ValueError("q1, q2 [B, H, Tq, d]; k1, k2, v [B, n_kv, Tk_max, d]")
+    if out is None:
+        out = torch.empty_like(q1)
+    _need(out, "out", torch.bfloat16, 4)
+    if k_lens is not None:
+        _need(k_lens, "k_lens", torch.int32, 1)
+    need = B * H * Tq * d * 4
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q1.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = L.ga_attend_diff(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), _ptr(out), B, H, n_kv, d, Tq,
+                          Tk_max, _ptr(k_lens), int(bool(causal)), int(window), float(lam), _ptr(workspace),
+                          ws_bytes, _stream(stream))
+    _check(st, "ga_attend_diff")
     return out
 
 

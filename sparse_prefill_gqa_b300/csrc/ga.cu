@@ -173,6 +173,54 @@ int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const __n
   return launch_decode_d<64>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
 }
 
+// The tensor-core prefill (bf16, d = 128 or 256): tensor maps, then prefill_wide_kernel with or
+// without block-mask unit lists.  The caller has validated the shape.
+int launch_prefill_tc(const void* q, const void* k, const void* v, __nv_bfloat16* ob, float* lse,
+                      const AttnShape& sh, bool masked, WideEpi epi, cudaStream_t stream) {
+  const int d = sh.d, Tq = sh.Tq, Tk_max = sh.Tk_max;
+  // 64-column SW128 boxes: Q 128 rows; K 128 keys and 64 keys; V 16384/d keys and 64 keys
+  const long long kvz = (long long)sh.batch * sh.n_kv;
+  const int vk = 16384 / d;
+  CUtensorMap tq, tk, tv, tk64, tv64;
+  if (!make_map_bf16(&tq, q, d, Tq, (long long)sh.batch * sh.n_heads, 128) ||
+      !make_map_bf16(&tk, k, d, Tk_max, kvz, 128) || !make_map_bf16(&tv, v, d, Tk_max, kvz, vk) ||
+      !make_map_bf16(&tk64, k, d, Tk_max, kvz, 64) || !make_map_bf16(&tv64, v, d, Tk_max, kvz, 64))
+    return GA_ERR_CUDA;
+  const long long n_cta = (long long)((Tq + 127) / 128) * sh.n_heads * sh.batch;
+  if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+  if (d == 128) {
+    using C = WideCfg<128>;
+    static_assert(C::VK == 128, "V map box");
+    constexpr int need = 256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS;
+    static int ok0 = set_smem_split(prefill_wide_kernel<128, false>, C::SMEM_BYTES, C::THREADS, need);
+    static int ok1 = set_smem_split(prefill_wide_kernel<128, true>, C::SMEM_BYTES, C::THREADS, need);
+    static int ok2 = set_smem_split(prefill_wide_kernel<128, false, 1>, C::SMEM_BYTES, C::THREADS, need);
+    static int ok3 = set_smem_split(prefill_wide_kernel<128, false, 2>, C::SMEM_BYTES, C::THREADS, need);
+    for (int o : {ok0, ok1, ok2, ok3})
+      if (o != GA_OK) return o;
+    auto kern = epi.mode == 1 ? prefill_wide_kernel<128, false, 1>
+              : epi.mode == 2 ? prefill_wide_kernel<128, false, 2>
+              : masked        ? prefill_wide_kernel<128, true>
+                              : prefill_wide_kernel<128, false>;
+    kern<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh, epi);
+  } else {
+    using C = WideCfg<256>;
+    static_assert(C::VK == 64, "V map box");
+    static int ok0 = set_smem(prefill_wide_kernel<256, false>, C::SMEM_BYTES);
+    static int ok1 = set_smem(prefill_wide_kernel<256, true>, C::SMEM_BYTES);
+    static int ok2 = set_smem(prefill_wide_kernel<256, false, 1>, C::SMEM_BYTES);
+    static int ok3 = set_smem(prefill_wide_kernel<256, false, 2>, C::SMEM_BYTES);
+    for (int o : {ok0, ok1, ok2, ok3})
+      if (o != GA_OK) return o;
+    auto kern = epi.mode == 1 ? prefill_wide_kernel<256, false, 1>
+              : epi.mode == 2 ? prefill_wide_kernel<256, false, 2>
+              : masked        ? prefill_wide_kernel<256, true>
+                              : prefill_wide_kernel<256, false>;
+    kern<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh, epi);
+  }
+  return launch_status();
+}
+
 }  // namespace
 
 }  // namespace ga
@@ -287,37 +335,9 @@ int ga_attend(const void* q, const void* k, const void* v, void* out, int batch,
   }
 
   // ---- tensor-core prefill ---------------------------------------------------------------
-  if (tc_eligible(d, dtype, q, k, v, out, block_mask, q_block, k_block)) {
-    // 64-column SW128 boxes: Q 128 rows; K 128 keys and 64 keys; V 16384/d keys and 64 keys
-    const long long kvz = (long long)batch * n_kv;
-    const int vk = 16384 / d;
-    CUtensorMap tq, tk, tv, tk64, tv64;
-    if (!make_map_bf16(&tq, q, d, Tq, (long long)batch * n_heads, 128) ||
-        !make_map_bf16(&tk, k, d, Tk_max, kvz, 128) || !make_map_bf16(&tv, v, d, Tk_max, kvz, vk) ||
-        !make_map_bf16(&tk64, k, d, Tk_max, kvz, 64) || !make_map_bf16(&tv64, v, d, Tk_max, kvz, 64))
-      return GA_ERR_CUDA;
-    const long long n_cta = (long long)((Tq + 127) / 128) * n_heads * batch;
-    if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
-    if (d == 128) {
-      using C = WideCfg<128>;
-      static_assert(C::VK == 128, "V map box");
-      constexpr int need = 256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS;
-      static int ok0 = set_smem_split(prefill_wide_kernel<128, false>, C::SMEM_BYTES, C::THREADS, need);
-      static int ok1 = set_smem_split(prefill_wide_kernel<128, true>, C::SMEM_BYTES, C::THREADS, need);
-      if (ok0 != GA_OK || ok1 != GA_OK) return ok0 != GA_OK ? ok0 : ok1;
-      auto kern = block_mask ? prefill_wide_kernel<128, true> : prefill_wide_kernel<128, false>;
-      kern<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh);
-    } else {
-      using C = WideCfg<256>;
-      static_assert(C::VK == 64, "V map box");
-      static int ok0 = set_smem(prefill_wide_kernel<256, false>, C::SMEM_BYTES);
-      static int ok1 = set_smem(prefill_wide_kernel<256, true>, C::SMEM_BYTES);
-      if (ok0 != GA_OK || ok1 != GA_OK) return ok0 != GA_OK ? ok0 : ok1;
-      auto kern = block_mask ? prefill_wide_kernel<256, true> : prefill_wide_kernel<256, false>;
-      kern<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh);
-    }
-    return launch_status();
-  }
+  if (tc_eligible(d, dtype, q, k, v, out, block_mask, q_block, k_block))
+    return launch_prefill_tc(q, k, v, ob, lse, sh, block_mask != nullptr, WideEpi{0, nullptr, nullptr, 0.0f},
+                             stream);
 
   // ---- everything else: CUDA-core kernel on bf16 storage --------------------------------
   dim3 grid((Tq + kSimtWarps - 1) / kSimtWarps, n_heads, batch);
@@ -372,6 +392,37 @@ int ga_attend_decode_static(const void* q, const void* k, const void* v, void* o
       !make_map_bf16(&tv, v, d, Tk_max, (long long)batch * n_kv, 64))
     return GA_ERR_CUDA;
   return launch_decode(d, tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+}
+
+int ga_attend_diff(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                   void* out, int batch, int n_heads, int n_kv, int d, int Tq, int Tk_max,
+                   const int32_t* k_lens, int causal, int window, float lam, void* workspace,
+                   size_t workspace_bytes, ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!q1 || !k1 || !q2 || !k2 || !v || !out) return GA_ERR_INVALID_ARG;
+  if (batch < 1 || n_heads < 1 || n_kv < 1 || n_kv > n_heads || n_heads % n_kv != 0)
+    return GA_ERR_INVALID_ARG;
+  if (Tq < 1 || Tk_max < Tq || !std::isfinite(lam)) return GA_ERR_INVALID_ARG;
+  if ((causal != 0 && causal != 1) || window < 0 || (window > 0 && !causal)) return GA_ERR_INVALID_ARG;
+  if (d != 128 && d != 256) return GA_ERR_UNSUPPORTED;
+  if (batch > 65535 || n_heads > 65535) return GA_ERR_UNSUPPORTED;
+  for (const void* p : {q1, k1, q2, k2, v, (const void*)out})
+    if (!aligned16(p)) return GA_ERR_INVALID_ARG;
+  if (k_lens && !aligned16(k_lens)) return GA_ERR_INVALID_ARG;
+  const size_t need = (size_t)batch * n_heads * Tq * d * sizeof(float);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GA_ERR_WORKSPACE;
+
+  AttnShape sh{};
+  sh.batch = batch; sh.n_heads = n_heads; sh.n_kv = n_kv; sh.d = d; sh.Tq = Tq; sh.Tk_max = Tk_max;
+  sh.k_lens = k_lens; sh.causal = causal; sh.window = window; sh.sink = nullptr;
+  sh.block_mask = nullptr; sh.q_block = 1; sh.k_block = 1; sh.nQb = 0; sh.nKb = 0;
+  sh.timeout_ns = g_timeout_ns;
+  float* a1v = static_cast<float*>(workspace);
+  __nv_bfloat16* ob = (__nv_bfloat16*)out;
+  // pass 1: A1 v in fp32; pass 2: out = A1 v - lam * A2 v, rounded once
+  int st = launch_prefill_tc(q1, k1, v, ob, nullptr, sh, false, WideEpi{1, a1v, nullptr, 0.0f}, stream);
+  if (st != GA_OK) return st;
+  return launch_prefill_tc(q2, k2, v, ob, nullptr, sh, false, WideEpi{2, nullptr, a1v, lam}, stream);
 }
 
 int ga_ring_append(void* k_ring, void* v_ring, const void* k_new, const void* v_new, int32_t* n_seen,

@@ -94,6 +94,17 @@ struct WideBars {
 };
 static_assert(sizeof(WideBars) <= 256, "barrier area");
 
+// What the epilogue writes.  Differential attention ("Attention Variants": (A1 - lambda A2) V)
+// runs the kernel twice: the first pass keeps its normalised output in fp32 (mode 1), the
+// second subtracts lambda times its own from it before the single rounding to bf16 (mode 2),
+// so the cancellation between the two maps happens in fp32.
+struct WideEpi {
+  int mode;             // 0: out (bf16); 1: out32 (fp32); 2: out = sub - lam * result (bf16)
+  float* out32;         // mode 1: [batch, n_heads, Tq, D]
+  const float* sub;     // mode 2: [batch, n_heads, Tq, D]
+  float lam;
+};
+
 // A list entry naming no unit: the tile holds one unit, in its first half.
 constexpr uint32_t kUnitNone = 0xFFFFFFFFu;
 
@@ -102,12 +113,14 @@ constexpr uint32_t kUnitNone = 0xFFFFFFFFu;
 // tm_k64 and tm_v64 64 keys (the 64-key units of a block-masked tile).
 // UNITS: the launch has a block mask (tiles are lists of 64-key units); without one the
 // kernel compiles to contiguous 128-key tiles only.
-template <int D_, bool UNITS>
+// EPI: the epilogue's mode (WideEpi::mode), fixed at compile time so that plain launches carry
+// none of the other modes' code.
+template <int D_, bool UNITS, int EPI = 0>
 __global__ void __launch_bounds__(WideCfg<D_>::THREADS, 1)
 prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k64,
                     const __grid_constant__ CUtensorMap tm_v64, __nv_bfloat16* __restrict__ out,
-                    float* __restrict__ lse, AttnShape sh) {
+                    float* __restrict__ lse, AttnShape sh, WideEpi epi) {
   using C = WideCfg<D_>;
   constexpr int D = C::D, BN = C::BN;
   extern __shared__ unsigned char smem_raw[];
@@ -572,16 +585,33 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (ok && n_tiles > 0) ok = warp_wait(&bars->o_final, 0, tmo, abort_flag);
     tc_fence_after();
     const int t = t0 + row;
-    __nv_bfloat16* orow = out + (((size_t)b * sh.n_heads + h) * sh.Tq + t) * D;
+    const size_t orow_off = (((size_t)b * sh.n_heads + h) * sh.Tq + t) * D;
+    __nv_bfloat16* orow = out + orow_off;
     auto store32 = [&](int c, const float (&o)[32], float s0) {
       if (row < rows) {
 #pragma unroll
         for (int u = 0; u < 32; u += 8) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = o[u + e] * s0;
+          if constexpr (EPI == 1) {
+            float* dst = epi.out32 + orow_off + c + u;
+            *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            continue;
+          }
+          if constexpr (EPI == 2) {
+            const float* src = epi.sub + orow_off + c + u;
+            const float4 a = *reinterpret_cast<const float4*>(src), b4 = *reinterpret_cast<const float4*>(src + 4);
+            const float y[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = fmaf(-epi.lam, x[e], y[e]);
+          }
           uint4 pk;
-          pk.x = pack_bf16x2(o[u + 0] * s0, o[u + 1] * s0);
-          pk.y = pack_bf16x2(o[u + 2] * s0, o[u + 3] * s0);
-          pk.z = pack_bf16x2(o[u + 4] * s0, o[u + 5] * s0);
-          pk.w = pack_bf16x2(o[u + 6] * s0, o[u + 7] * s0);
+          pk.x = pack_bf16x2(x[0], x[1]);
+          pk.y = pack_bf16x2(x[2], x[3]);
+          pk.z = pack_bf16x2(x[4], x[5]);
+          pk.w = pack_bf16x2(x[6], x[7]);
           *reinterpret_cast<uint4*>(orow + c + u) = pk;
         }
       }
