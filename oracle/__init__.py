@@ -17,17 +17,21 @@ Sources (web pages, cited by title and section):
     its W=4 diagram.
   * "Attention Masking" guide (devhandbook.co.kr): per-sequence length (padding) masks.
   * "Attention Variants" lesson: differential attention, (A1 - lambda A2) V.
+  * "Attention in Code" section 5: an indexer scores every cached token, attention reads the top k.
 
 Modules:
   attention  -- attend (dense / windowed / sink / block-masked / ragged), visibility rule
   blocks     -- block centroids and radii, mean-score + radius-rescue block selection
   ring       -- W-slot ring-buffer decode (the windowed cache of "Attention in Code" s.2)
   variants   -- differential attention ("Attention Variants", differential attention)
+  dsa        -- token top-k sparse attention with a lightning-style indexer ("Attention in Code" s.5)
 """
 from .attention import attend, positions, visible
 from .blocks import allowed_blocks, block_stats, radius_zscores, select_blocks
 from .ring import ring_contents, ring_decode
 from .variants import attention_weights, diff_attend
+from .dsa import dsa_decode, indexer_scores, sparse_attend, topk_indices
 
 __all__ = ["attend", "positions", "visible", "allowed_blocks", "block_stats",
-           "radius_zscores", "select_blocks", "ring_contents", "ring_decode", "attention_weights", "diff_attend"]
+           "radius_zscores", "select_blocks", "ring_contents", "ring_decode", "attention_weights", "diff_attend",
+           "dsa_decode", "indexer_scores", "sparse_attend", "topk_indices"]
