@@ -321,6 +321,57 @@ def part_diff(torch, ga, steps, warmup, flush, peaks):
                                "launches_per_step": 2}}
 
 
+def part_dsa(torch, ga, steps, warmup, flush, peaks):
+    """Token top-k sparse decode on the KV-cache decode workload (B64 H32 Hkv8 d128, lengths
+    U[16384, 32768]): an indexer of 8 heads x 128 dims scores every cached token, the top
+    k = 2048 are kept, and attention reads only those.  Stages timed one by one and together;
+    the dense decode of the same cache is timed beside it."""
+    from workloads import get_config, uniform_lengths
+    c = get_config(3)
+    B, H, n_kv, d, Tk = c.batch, c.n_heads, c.n_kv, c.d, c.Tk
+    Hi, di, topk = 8, 128, 2048
+    lens = uniform_lengths(c.seed, B, *c.k_len_range)
+    k = device_bf16(torch, c.seed, "k", (B, n_kv, Tk, d), lengths=lens)
+    v = device_bf16(torch, c.seed, "v", (B, n_kv, Tk, d), lengths=lens)
+    q = device_bf16(torch, c.seed, "q", (B, H, 1, d))
+    qi = device_bf16(torch, c.seed, "dsa_qi", (B, 1, Hi, di)).view(B, Hi, di)
+    ki = device_bf16(torch, c.seed, "dsa_ki", (B, 1, Tk, di), lengths=lens).view(B, Tk, di)
+    rng = np.random.Generator(np.random.PCG64(c.seed + 31))
+    wi = torch.from_numpy(np.abs(rng.standard_normal((B, Hi))).astype(np.float32)).cuda()
+    k_lens = torch.from_numpy(lens).cuda()
+    scores = torch.empty(B, Tk, dtype=torch.float32, device="cuda")
+    idx = torch.empty(B, topk, dtype=torch.int32, device="cuda")
+    n_sel = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    ws = torch.empty(int(ga.lib().ga_attend_gather_workspace_size(B, H, n_kv, d, topk)), dtype=torch.uint8,
+                     device="cuda")
+    t_idx = statistics.mean(timed_steps(torch, lambda: ga.ga_dsa_indexer(qi, wi, ki, k_lens, scores),
+                                        steps, warmup, flush))
+    t_top = statistics.mean(timed_steps(torch, lambda: ga.ga_topk_indices(scores, topk, k_lens, idx, n_sel),
+                                        steps, warmup, flush))
+    t_att = statistics.mean(timed_steps(torch, lambda: ga.ga_attend_gather(q, k, v, idx, n_sel, out, workspace=ws),
+                                        steps, warmup, flush))
+
+    def step():
+        ga.ga_dsa_indexer(qi, wi, ki, k_lens, scores)
+        ga.ga_topk_indices(scores, topk, k_lens, idx, n_sel)
+        ga.ga_attend_gather(q, k, v, idx, n_sel, out, workspace=ws)
+    t_all = statistics.mean(timed_steps(torch, step, steps, warmup, flush))
+    dws = torch.empty(max(1, ga.ga_workspace_size(B, H, n_kv, d, 1, Tk, torch.bfloat16)), dtype=torch.uint8,
+                      device="cuda")
+    dense_out = torch.empty_like(q)
+    t_dense = statistics.mean(timed_steps(torch, lambda: ga.ga_attend(q, k, v, dense_out, k_lens=k_lens,
+                                                                      workspace=dws), steps, warmup, flush))
+    idx_bytes = int(lens.sum()) * di * 2
+    sel_kv = B * n_kv * topk * d * 2 * 2                # selected K and V rows, read once
+    return {"dsa_decode": {"workload": "bf16 top-k sparse decode B64 H32 Hkv8 d128, lengths U[16384, 32768], "
+                                       "indexer 8 x 128, k 2048",
+                           "ms": t_all, "indexer_ms": t_idx, "indexer_GB/s": idx_bytes / (t_idx * 1e-3) / 1e9,
+                           "indexer_frac_hbm": idx_bytes / (t_idx * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "topk_ms": t_top, "gather_decode_ms": t_att, "selected_kv_bytes": sel_kv,
+                           "dense_decode_ms": t_dense, "launches_per_step": 5}}
+
+
 def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
     from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
     c = get_config(5)
@@ -470,6 +521,8 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
         res = part_ring(torch, ga, args.steps, warmup, flush, peaks)
     elif args.case == "diff":
         res = part_diff(torch, ga, args.steps, warmup, flush, peaks)
+    elif args.case == "dsa":
+        res = part_dsa(torch, ga, args.steps, warmup, flush, peaks)
     else:
         res = part_sparse(torch, ga, args.steps, warmup, flush, peaks, select_only=args.case == "select")
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": warmup, **res}))
@@ -486,7 +539,7 @@ def main():
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="all",
-                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "diff", "sparse", "select"],
+                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "diff", "dsa", "sparse", "select"],
                     help="run one workload alone and print its own JSON line (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --case prefill/decode/chunk: a smaller batch (profiling captures)")
@@ -631,7 +684,8 @@ def main():
         parts = {}
         ps, pw = max(3, min(20, args.steps // 4)), 3
         for name, fn in (("decode_chunk", part_decode_and_chunk), ("window_sink", part_window_sink),
-                         ("ring", part_ring), ("diff", part_diff), ("sparse_128k", part_sparse)):
+                         ("ring", part_ring), ("diff", part_diff), ("dsa", part_dsa),
+                         ("sparse_128k", part_sparse)):
             try:
                 parts.update(fn(torch, ga, ps, pw, flush, peaks))
             except Exception as e:  # report, never hide

@@ -158,6 +158,49 @@ int ga_attend_diff(const void* q1, const void* k1, const void* q2, const void* k
                    size_t workspace_bytes, ga_stream_t stream);
 
 /*
+ * Token top-k sparse attention for decode ("Attention in Code", section 5): a small indexer
+ * scores every cached token for the current query, and attention reads only the k tokens with
+ * the highest scores; the cache keeps every token.  Decode form: one query per sequence at
+ * position lens[b] - 1, which may see every cached token.  Three calls, in order:
+ *
+ * ga_dsa_indexer -- scores[b, s] = sum_j wi[b, j] * relu(qi[b, j] . ki[b, s]) for s < lens[b],
+ *   -inf for lens[b] <= s < L_max.
+ *   qi      device bf16 [batch, n_idx_heads, di]: the indexer's query heads.
+ *   wi      device float [batch, n_idx_heads]: their weights.
+ *   ki      device bf16 [batch, L_max, di]: one indexer key per cached token.
+ *   lens    device int32 [batch] (tokens cached; clamped to [0, L_max]) or NULL (= L_max).
+ *   scores  device float out [batch, L_max] (fp32 dot products and sums).
+ *   di: 64 or 128; n_idx_heads a power of two <= di / 8; others GA_ERR_UNSUPPORTED.
+ */
+int ga_dsa_indexer(const void* qi, const float* wi, const void* ki, const int32_t* lens, int batch,
+                   int n_idx_heads, int di, int L_max, float* scores, ga_stream_t stream);
+
+/*
+ * ga_topk_indices -- per sequence, the min(topk, lens[b]) positions with the highest scores,
+ *   in increasing position order; among equal scores at the boundary the lower positions are
+ *   kept.  idx device int32 out [batch, topk] (-1 past the count); n_sel device int32 out
+ *   [batch]: the count.  scores as produced by ga_dsa_indexer (NaN scores: undefined order).
+ */
+int ga_topk_indices(const float* scores, const int32_t* lens, int batch, int L_max, int topk,
+                    int32_t* idx, int32_t* n_sel, ga_stream_t stream);
+
+/* Bytes of workspace ga_attend_gather needs (SIZE_MAX for invalid sizes): the gathered keys and
+ * values, then the split-K decode's partial results. */
+size_t ga_attend_gather_workspace_size(int batch, int n_heads, int n_kv, int d, int topk);
+
+/*
+ * ga_attend_gather -- decode attention of q [batch, n_heads, 1, d] over the cached tokens
+ *   idx[b, 0 .. n_sel[b]-1] of k, v [batch, n_kv, Tk_max, d] (bf16): softmax over exactly
+ *   those keys (plus the optional sink), for every head of the sequence.  The selected rows
+ *   are gathered into the workspace, then the split-K decode runs over them.
+ *   d: 64, 128 or 256; n_heads / n_kv <= 16.  sink, lse as in ga_attend.
+ */
+int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int batch,
+                     int n_heads, int n_kv, int d, int Tk_max, const int32_t* idx,
+                     const int32_t* n_sel, int topk, const float* sink, float* lse,
+                     void* workspace, size_t workspace_bytes, ga_stream_t stream);
+
+/*
  * ga_ring_append -- write one new token per sequence into a sliding-window ring cache.
  * ("Attention in Code", section 2: a layer that only looks at the last W tokens keeps a
  * cache of W slots per kv head; token number n, counting from 0, goes to slot n mod W and

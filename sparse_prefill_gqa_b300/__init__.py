@@ -25,7 +25,8 @@ __all__ = [
     "ga_selftest_wait_timeout", "ga_status_string", "ga_version", "GA_OK", "GA_ERR_INVALID_ARG",
     "GA_ERR_UNSUPPORTED", "GA_ERR_CUDA", "GA_ERR_DEVICE_TIMEOUT", "GA_ERR_WORKSPACE",
     "GA_ERR_SCRATCH_LIMIT", "GA_DECODE_STATIC_SCRATCH_BYTES", "ga_attend_decode_static",
-    "ga_ring_append", "ga_attend_ring", "ga_attend_diff", "GA_RADIUS_ZSCORE", "GA_RADIUS_MAD",
+    "ga_ring_append", "ga_attend_ring", "ga_attend_diff", "ga_dsa_indexer", "ga_topk_indices",
+    "ga_attend_gather", "dsa_decode", "GA_RADIUS_ZSCORE", "GA_RADIUS_MAD",
 ]
 
 GA_OK, GA_ERR_INVALID_ARG, GA_ERR_UNSUPPORTED = 0, -1, -2
@@ -65,6 +66,14 @@ def lib() -> ctypes.CDLL:
     L.ga_attend_decode_static.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32,
                                           vp, vp, vp]
     L.ga_attend_decode_static.restype = i32
+    L.ga_dsa_indexer.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp]
+    L.ga_dsa_indexer.restype = i32
+    L.ga_topk_indices.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    L.ga_topk_indices.restype = i32
+    L.ga_attend_gather_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.ga_attend_gather_workspace_size.restype = sz
+    L.ga_attend_gather.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp, sz, vp]
+    L.ga_attend_gather.restype = i32
     L.ga_attend_diff.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32, f32,
                                  vp, sz, vp]
     L.ga_attend_diff.restype = i32
@@ -232,6 +241,80 @@ def ga_attend_diff(q1, k1, q2, k2, v, lam, out=None, *, k_lens=None, causal=True
                           ws_bytes, _stream(stream))
     _check(st, "ga_attend_diff")
     return out
+
+
+def ga_dsa_indexer(qi, wi, ki, lens=None, scores=None, *, stream=None):
+    """Indexer scores [B, L_max] (float32): sum_j wi[b, j] relu(qi[b, j] . ki[b, s]); -inf past
+    lens[b].  qi [B, Hi, di] and ki [B, L_max, di] bf16, wi [B, Hi] float32."""
+    L = lib()
+    _need(qi, "qi", torch.bfloat16, 3)
+    _need(ki, "ki", torch.bfloat16, 3)
+    _need(wi, "wi", torch.float32, 2)
+    B, Hi, di = qi.shape
+    L_max = ki.shape[1]
+    if ki.shape != (B, L_max, di) or wi.shape != (B, Hi):
+        raise ValueError("qi [B, Hi, di], ki [B, L_max, di], wi [B, Hi]")
+    if lens is not None:
+        _need(lens, "lens", torch.int32, 1)
+    if scores is None:
+        scores = torch.empty(B, L_max, dtype=torch.float32, device=qi.device)
+    _need(scores, "scores", torch.float32, 2)
+    _check(L.ga_dsa_indexer(_ptr(qi), _ptr(wi), _ptr(ki), _ptr(lens), B, Hi, di, L_max, _ptr(scores),
+                            _stream(stream)), "ga_dsa_indexer")
+    return scores
+
+
+def ga_topk_indices(scores, topk, lens=None, idx=None, n_sel=None, *, stream=None):
+    """Per sequence the min(topk, lens[b]) highest-scoring positions (increasing order, ties to
+    the lower position): (idx int32 [B, topk] with -1 padding, n_sel int32 [B])."""
+    L = lib()
+    _need(scores, "scores", torch.float32, 2)
+    B, L_max = scores.shape
+    if lens is not None:
+        _need(lens, "lens", torch.int32, 1)
+    if idx is None:
+        idx = torch.empty(B, topk, dtype=torch.int32, device=scores.device)
+    if n_sel is None:
+        n_sel = torch.empty(B, dtype=torch.int32, device=scores.device)
+    _check(L.ga_topk_indices(_ptr(scores), _ptr(lens), B, L_max, int(topk), _ptr(idx), _ptr(n_sel),
+                             _stream(stream)), "ga_topk_indices")
+    return idx, n_sel
+
+
+def ga_attend_gather(q, k, v, idx, n_sel, out=None, *, sink=None, lse=None, workspace=None, stream=None):
+    """Decode attention of q [B, H, 1, d] over the tokens idx[b, :n_sel[b]] of k, v."""
+    L = lib()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(idx, "idx", torch.int32, 2)
+    _need(n_sel, "n_sel", torch.int32, 1)
+    B, H, Tq, d = q.shape
+    n_kv, Tk_max = k.shape[1], k.shape[2]
+    topk = idx.shape[1]
+    if Tq != 1 or v.shape != k.shape or idx.shape[0] != B:
+        raise ValueError("q [B, H, 1, d], k, v [B, n_kv, Tk_max, d], idx [B, topk]")
+    if out is None:
+        out = torch.empty_like(q)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, 1)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    need = int(L.ga_attend_gather_workspace_size(B, H, n_kv, d, topk))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(L.ga_attend_gather(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tk_max, _ptr(idx),
+                              _ptr(n_sel), topk, _ptr(sink), _ptr(lse), _ptr(workspace), ws_bytes,
+                              _stream(stream)), "ga_attend_gather")
+    return out
+
+
+def dsa_decode(q, k, v, qi, wi, ki, topk, lens=None, *, sink=None, stream=None):
+    """Indexer, top-k and gathered decode in order; returns (out, idx, n_sel, scores)."""
+    scores = ga_dsa_indexer(qi, wi, ki, lens, stream=stream)
+    idx, n_sel = ga_topk_indices(scores, topk, lens, stream=stream)
+    out = ga_attend_gather(q, k, v, idx, n_sel, sink=sink, stream=stream)
+    return out, idx, n_sel, scores
 
 
 def ga_ring_append(k_ring, v_ring, k_new, v_new, n_seen, *, stream=None):

@@ -76,14 +76,6 @@ block_stats_kernel(const T* __restrict__ k, const int32_t* __restrict__ k_lens, 
 // ---------------------------------------------------------------------------------------
 constexpr int kStatsVecWarps = 4;
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
 
 template <int L>
 __global__ void __launch_bounds__(32 * kStatsVecWarps)

@@ -29,4 +29,14 @@ __device__ __forceinline__ int seq_keys(const int32_t* k_lens, int b, int Tk_max
   return k_lens ? min(max(k_lens[b], 0), Tk_max) : Tk_max;
 }
 
+// Widens 8 packed bf16 values (one 16-byte load) to fp32, exactly.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
 }  // namespace ga

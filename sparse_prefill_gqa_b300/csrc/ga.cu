@@ -15,6 +15,7 @@
 #include "blocks.cuh"
 #include "common.cuh"
 #include "decode.cuh"
+#include "dsa.cuh"
 #include "prefill_wide.cuh"
 #include "ring.cuh"
 
@@ -423,6 +424,88 @@ int ga_attend_diff(const void* q1, const void* k1, const void* q2, const void* k
   int st = launch_prefill_tc(q1, k1, v, ob, nullptr, sh, false, WideEpi{1, a1v, nullptr, 0.0f}, stream);
   if (st != GA_OK) return st;
   return launch_prefill_tc(q2, k2, v, ob, nullptr, sh, false, WideEpi{2, nullptr, a1v, lam}, stream);
+}
+
+int ga_dsa_indexer(const void* qi, const float* wi, const void* ki, const int32_t* lens, int batch,
+                   int n_idx_heads, int di, int L_max, float* scores, ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!qi || !wi || !ki || !scores || batch < 1 || L_max < 1) return GA_ERR_INVALID_ARG;
+  if (!(di == 64 || di == 128) || n_idx_heads < 1 || n_idx_heads > di / 8 ||
+      (n_idx_heads & (n_idx_heads - 1)) != 0)
+    return GA_ERR_UNSUPPORTED;
+  if (batch > 65535) return GA_ERR_UNSUPPORTED;
+  if (!aligned16(qi) || !aligned16(ki) || (reinterpret_cast<uintptr_t>(wi) & 3) ||
+      (reinterpret_cast<uintptr_t>(scores) & 3) || (lens && (reinterpret_cast<uintptr_t>(lens) & 3)))
+    return GA_ERR_INVALID_ARG;
+  const dim3 grid((L_max + kIdxWarps * kIdxKeysPerWarp - 1) / (kIdxWarps * kIdxKeysPerWarp), batch);
+  const auto* q = (const __nv_bfloat16*)qi;
+  const auto* kk = (const __nv_bfloat16*)ki;
+#define GA_IDX(DI, HI) dsa_indexer_kernel<DI, HI><<<grid, 32 * kIdxWarps, 0, stream>>>(q, wi, kk, lens, L_max, scores)
+  if (di == 128) {
+    switch (n_idx_heads) {
+      case 1: GA_IDX(128, 1); break;
+      case 2: GA_IDX(128, 2); break;
+      case 4: GA_IDX(128, 4); break;
+      case 8: GA_IDX(128, 8); break;
+      default: GA_IDX(128, 16); break;
+    }
+  } else {
+    switch (n_idx_heads) {
+      case 1: GA_IDX(64, 1); break;
+      case 2: GA_IDX(64, 2); break;
+      case 4: GA_IDX(64, 4); break;
+      default: GA_IDX(64, 8); break;
+    }
+  }
+#undef GA_IDX
+  return launch_status();
+}
+
+int ga_topk_indices(const float* scores, const int32_t* lens, int batch, int L_max, int topk,
+                    int32_t* idx, int32_t* n_sel, ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!scores || !idx || !n_sel || batch < 1 || L_max < 1 || topk < 1) return GA_ERR_INVALID_ARG;
+  if (batch > 0x7fffffff / 2) return GA_ERR_UNSUPPORTED;
+  for (const void* p : {(const void*)scores, (const void*)idx, (const void*)n_sel, (const void*)lens})
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3)) return GA_ERR_INVALID_ARG;
+  topk_select_kernel<<<batch, kTopkThreads, 0, stream>>>(scores, lens, L_max, topk, idx, n_sel);
+  return launch_status();
+}
+
+size_t ga_attend_gather_workspace_size(int batch, int n_heads, int n_kv, int d, int topk) {
+  if (batch < 1 || n_heads < 1 || n_kv < 1 || d < 1 || topk < 1 || n_heads % n_kv != 0) return SIZE_MAX;
+  const size_t cache = ((size_t)batch * n_kv * topk * d * 2 + 255) / 256 * 256;   // kc, then vc
+  const size_t dec = ga_workspace_size(batch, n_heads, n_kv, d, 1, topk, GA_BF16);
+  if (dec == SIZE_MAX) return SIZE_MAX;
+  return 2 * cache + dec;
+}
+
+int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int batch, int n_heads,
+                     int n_kv, int d, int Tk_max, const int32_t* idx, const int32_t* n_sel, int topk,
+                     const float* sink, float* lse, void* workspace, size_t workspace_bytes,
+                     ga_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!q || !k || !v || !out || !idx || !n_sel || topk < 1 || Tk_max < 1) return GA_ERR_INVALID_ARG;
+  if (batch < 1 || n_heads < 1 || n_kv < 1 || n_heads % n_kv != 0) return GA_ERR_INVALID_ARG;
+  if (!(d == 64 || d == 128 || d == 256) || n_heads / n_kv > 16 || batch > 65535) return GA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(n_sel) ||
+      (reinterpret_cast<uintptr_t>(idx) & 3))
+    return GA_ERR_INVALID_ARG;
+  const size_t need = ga_attend_gather_workspace_size(batch, n_heads, n_kv, d, topk);
+  if (need == SIZE_MAX) return GA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GA_ERR_WORKSPACE;
+  const size_t cache = ((size_t)batch * n_kv * topk * d * 2 + 255) / 256 * 256;
+  auto* kc = static_cast<__nv_bfloat16*>(workspace);
+  auto* vc = reinterpret_cast<__nv_bfloat16*>(static_cast<unsigned char*>(workspace) + cache);
+  void* ws_dec = static_cast<unsigned char*>(workspace) + 2 * cache;
+  const dim3 grid((topk + 7) / 8, n_kv, batch);
+  dsa_gather_kernel<<<grid, 256, 0, stream>>>((const __nv_bfloat16*)k, (const __nv_bfloat16*)v, idx, n_sel,
+                                              n_kv, d, Tk_max, topk, kc, vc);
+  const int st = launch_status();
+  if (st != GA_OK) return st;
+  // The query sees every selected token: a causal decode row over n_sel[b] compact keys.
+  return ga_attend(q, kc, vc, out, batch, n_heads, n_kv, d, 1, topk, n_sel, 1, 0, sink, nullptr, 1, 1, lse,
+                   GA_BF16, ws_dec, workspace_bytes - 2 * cache, stream_);
 }
 
 int ga_ring_append(void* k_ring, void* v_ring, const void* k_new, const void* v_new, int32_t* n_seen,

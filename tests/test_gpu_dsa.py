@@ -1,0 +1,135 @@
+"""GPU parity of token top-k sparse attention for decode ("Attention in Code", section 5):
+indexer scores against the float64 oracle; the top-k selection exactly (the oracle selects
+from the GPU's own fp32 scores, with the same tie rule); the gathered decode against the oracle
+over the same token sets; k >= L against full attention; and the bench's full-size workload on
+sampled sequences."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_prefill_gqa_b300 as ga
+from oracle.dsa import indexer_scores, topk_indices
+from tests.helpers import assert_close, host_tensor, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _indexer_inputs(B, Hi, di, L, seed):
+    qi, qir = host_tensor(seed, "qi", (B, 1, Hi, di), "bf16")
+    ki, kir = host_tensor(seed, "ki", (B, 1, L, di), "bf16")
+    wr = np.abs(np.random.default_rng(seed).standard_normal((B, Hi))).astype(np.float32)
+    return qi[:, 0].contiguous(), qir[:, 0], ki[:, 0].contiguous(), kir[:, 0], torch.from_numpy(wr).cuda(), wr
+
+
+@pytest.mark.parametrize("B,Hi,di,L,lens", [
+    (2, 8, 128, 1000, [1000, 611]),
+    (1, 4, 64, 777, None),
+    (1, 16, 128, 1300, None),
+    (2, 1, 64, 64, [64, 1]),
+])
+def test_indexer_scores(B, Hi, di, L, lens):
+    qi, qir, ki, kir, wi, wr = _indexer_inputs(B, Hi, di, L, seed=501 + Hi)
+    ln = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    sc = to_f64(ga.ga_dsa_indexer(qi, wi, ki, ln))
+    for b in range(B):
+        n = L if lens is None else lens[b]
+        ref = indexer_scores(qir[b][:, None], kir[b, :n], wr[b][:, None].astype(np.float64))[0]
+        assert np.max(np.abs(sc[b, :n] - ref)) <= 1e-5 * max(1.0, np.max(np.abs(ref)))
+        assert np.all(np.isneginf(sc[b, n:]))
+
+
+@pytest.mark.parametrize("B,L,topk,ties", [
+    (3, 5000, 512, False),
+    (2, 3000, 2048, True),       # integer-valued scores: many ties at the boundary
+    (2, 1000, 1500, False),      # topk > L: every token
+])
+def test_topk_indices_exact(B, L, topk, ties):
+    rng = np.random.default_rng(511)
+    s = rng.standard_normal((B, L)).astype(np.float32)
+    if ties:
+        s = np.floor(s * 3.0).astype(np.float32)
+    lens = [L, L // 2, L - 7][:B]
+    scores = torch.from_numpy(s).cuda()
+    idx, n_sel = ga.ga_topk_indices(scores, topk, torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    idx, n_sel = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for b in range(B):
+        ref = topk_indices(s[b, :lens[b]], np.ones(lens[b], bool), topk)
+        assert n_sel[b] == ref.size
+        assert np.array_equal(idx[b, :ref.size], ref)
+        assert np.all(idx[b, ref.size:] == -1)
+
+
+def _decode_inputs(B, H, n_kv, Lm, d, Hi, di, seed):
+    q, qr = host_tensor(seed, "q", (B, H, 1, d), "bf16")
+    k, kr = host_tensor(seed, "k", (B, n_kv, Lm, d), "bf16")
+    v, vr = host_tensor(seed, "v", (B, n_kv, Lm, d), "bf16")
+    qi, qir, ki, kir, wi, wr = _indexer_inputs(B, Hi, di, Lm, seed + 1)
+    return (q, k, v, qi, wi, ki), (qr, kr, vr, qir, kir, wr)
+
+
+@pytest.mark.parametrize("B,H,n_kv,Lm,d,Hi,di,topk,lens,use_sink", [
+    (2, 8, 2, 3000, 128, 8, 128, 512, [3000, 1234], False),
+    (2, 4, 1, 2000, 256, 4, 64, 300, [2000, 150], True),     # d = 256; a sequence shorter than k
+])
+def test_dsa_decode_matches_oracle(B, H, n_kv, Lm, d, Hi, di, topk, lens, use_sink):
+    dev, ref = _decode_inputs(B, H, n_kv, Lm, d, Hi, di, seed=521)
+    q, k, v, qi, wi, ki = dev
+    qr, kr, vr, qir, kir, wr = ref
+    sink = skr = None
+    if use_sink:
+        skr = np.random.default_rng(7).standard_normal(H).astype(np.float32)
+        sink = torch.from_numpy(skr).cuda()
+    ln = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out, idx, n_sel, scores = ga.dsa_decode(q, k, v, qi, wi, ki, topk, ln, sink=sink)
+    assert ga.ga_read_device_status() == ga.GA_OK
+    # the oracle attends over the tokens its own top-k picks from the GPU's scores
+    expect, chosen = oracle.dsa_decode(qr, kr, vr, qir, kir, wr, lens, topk, sink=skr, scores=to_f64(scores))
+    idx, n_sel = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for b in range(B):
+        assert np.array_equal(idx[b, :n_sel[b]], chosen[b])
+    assert_close(to_f64(out), expect, "bf16", "dsa decode")
+
+
+def test_dsa_topk_at_least_length_is_full_attention():
+    """k >= L: every cached token is read, and the result is full decode attention."""
+    B, H, n_kv, Lm, d = 2, 8, 2, 700, 128
+    dev, ref = _decode_inputs(B, H, n_kv, Lm, d, 8, 128, seed=531)
+    q, k, v, qi, wi, ki = dev
+    qr, kr, vr = ref[:3]
+    out, idx, n_sel, _ = ga.dsa_decode(q, k, v, qi, wi, ki, 1024)
+    assert n_sel.cpu().tolist() == [Lm, Lm]
+    full, _ = oracle.attend(qr, kr, vr, causal=True)
+    assert_close(to_f64(out), full, "bf16", "dsa k >= L")
+
+
+def test_dsa_full_size_sampled():
+    """The bench's workload (B64 H32 Hkv8 d128, lengths U[16384, 32768], indexer 8 heads x 128,
+    k = 2048): scores, selection and output checked on sampled sequences."""
+    from workloads import bf16_bits_to_f32, randn_bhtd, uniform_lengths
+    B, H, n_kv, Lm, d, Hi, di, topk = 64, 32, 8, 32768, 128, 8, 128, 2048
+    lens = uniform_lengths(541, B, 16384, 32768)
+    q, qr = host_tensor(541, "q", (B, H, 1, d), "bf16")
+    kb = randn_bhtd(541, "k", (B, n_kv, Lm, d), "bf16")      # bf16 bits; float64 only where sampled
+    vb = randn_bhtd(541, "v", (B, n_kv, Lm, d), "bf16")
+    k = torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).cuda()
+    v = torch.from_numpy(vb.view(np.int16)).view(torch.bfloat16).cuda()
+    qi, qir = host_tensor(542, "qi", (B, 1, Hi, di), "bf16")
+    qi, qir = qi[:, 0].contiguous(), qir[:, 0]
+    kib = randn_bhtd(542, "ki", (B, 1, Lm, di), "bf16")[:, 0]
+    ki = torch.from_numpy(np.ascontiguousarray(kib).view(np.int16)).view(torch.bfloat16).cuda()
+    wr = np.abs(np.random.default_rng(542).standard_normal((B, Hi))).astype(np.float32)
+    wi = torch.from_numpy(wr).cuda()
+    out, idx, n_sel, scores = ga.dsa_decode(q, k, v, qi, wi, ki, topk, torch.from_numpy(lens).cuda())
+    assert ga.ga_read_device_status() == ga.GA_OK
+    sc, idx, n_sel = to_f64(scores), idx.cpu().numpy(), n_sel.cpu().numpy()
+    f64 = lambda x: bf16_bits_to_f32(x).astype(np.float64)
+    for b in np.random.default_rng(543).choice(B, size=3, replace=False):
+        n = int(lens[b])
+        ref_sc = indexer_scores(qir[b][:, None], f64(kib[b, :n]), wr[b][:, None].astype(np.float64))[0]
+        assert np.max(np.abs(sc[b, :n] - ref_sc)) <= 1e-5 * max(1.0, np.max(np.abs(ref_sc)))
+        chosen = topk_indices(sc[b, :n], np.ones(n, bool), topk)
+        assert np.array_equal(idx[b, :n_sel[b]], chosen)
+        expect, _ = oracle.attend(qr[b:b + 1], f64(kb[b:b + 1, :, chosen]), f64(vb[b:b + 1, :, chosen]),
+                                  causal=False)
+        assert_close(to_f64(out[b:b + 1]), expect, "bf16", f"dsa full size b={b}")
