@@ -369,6 +369,8 @@ def part_dsa(torch, ga, steps, warmup, flush, peaks):
                            "ms": t_all, "indexer_ms": t_idx, "indexer_GB/s": idx_bytes / (t_idx * 1e-3) / 1e9,
                            "indexer_frac_hbm": idx_bytes / (t_idx * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "topk_ms": t_top, "gather_decode_ms": t_att, "selected_kv_bytes": sel_kv,
+                           "gather_decode_GB/s": sel_kv / (t_att * 1e-3) / 1e9,
+                           "gather_decode_frac_hbm": sel_kv / (t_att * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "dense_decode_ms": t_dense, "launches_per_step": 5}}
 
 
