@@ -374,6 +374,31 @@ def part_dsa(torch, ga, steps, warmup, flush, peaks):
                            "dense_decode_ms": t_dense, "launches_per_step": 5}}
 
 
+def part_mla(torch, ga, steps, warmup, flush, peaks):
+    """MLA decode, absorbed form, at DeepSeek-V2-Lite's sizes (16 heads, latent 512, rope 64, head
+    dims 128): a decode batch of 64 sequences (the batch of the KV-cache decode workload) with
+    cache lengths U[4096, 8192].  Bytes: the latent cache read once (576 bf16 per token)."""
+    from workloads import uniform_lengths
+    B, H, L_max, seed = 64, 16, 8192, 1006
+    lens = uniform_lengths(seed, B, 4096, 8192)
+    q_nope = device_bf16(torch, seed, "mla_qn", (B, 1, H, 128)).view(B, H, 128)
+    q_rope = device_bf16(torch, seed, "mla_qp", (B, 1, H, 64)).view(B, H, 64)
+    latent = device_bf16(torch, seed, "mla_lat", (B, 1, L_max, 576), lengths=lens).view(B, L_max, 576)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    w = torch.from_numpy((rng.standard_normal((2, H, 512, 128)) / np.sqrt(128)).astype(np.float32)).to(torch.bfloat16)
+    w_uk, w_uv = w[0].cuda().contiguous(), w[1].cuda().contiguous()
+    lens_t = torch.from_numpy(lens).cuda()
+    out = torch.empty(B, H, 128, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(int(ga.lib().ga_mla_decode_workspace_size(B, H, L_max)), dtype=torch.uint8, device="cuda")
+    t = statistics.mean(timed_steps(torch, lambda: ga.ga_mla_decode(q_nope, q_rope, latent, w_uk, w_uv, lens_t,
+                                                                   out, workspace=ws), steps, warmup, flush))
+    lat_bytes = int(lens.sum()) * 576 * 2
+    gbs = lat_bytes / (t * 1e-3) / 1e9
+    return {"mla_decode": {"workload": "bf16 MLA decode (absorbed) B64 H16, latent 512 + rope 64, lengths U[4096, 8192]",
+                           "ms": t, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "latent_bytes": lat_bytes,
+                           "launches_per_step": 4}}
+
+
 def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
     from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
     c = get_config(5)
@@ -525,6 +550,8 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
         res = part_diff(torch, ga, args.steps, warmup, flush, peaks)
     elif args.case == "dsa":
         res = part_dsa(torch, ga, args.steps, warmup, flush, peaks)
+    elif args.case == "mla":
+        res = part_mla(torch, ga, args.steps, warmup, flush, peaks)
     else:
         res = part_sparse(torch, ga, args.steps, warmup, flush, peaks, select_only=args.case == "select")
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": warmup, **res}))
@@ -541,7 +568,7 @@ def main():
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="all",
-                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "diff", "dsa", "sparse", "select"],
+                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "diff", "dsa", "mla", "sparse", "select"],
                     help="run one workload alone and print its own JSON line (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --case prefill/decode/chunk: a smaller batch (profiling captures)")
@@ -686,7 +713,7 @@ def main():
         parts = {}
         ps, pw = max(3, min(20, args.steps // 4)), 3
         for name, fn in (("decode_chunk", part_decode_and_chunk), ("window_sink", part_window_sink),
-                         ("ring", part_ring), ("diff", part_diff), ("dsa", part_dsa),
+                         ("ring", part_ring), ("diff", part_diff), ("dsa", part_dsa), ("mla", part_mla),
                          ("sparse_128k", part_sparse)):
             try:
                 parts.update(fn(torch, ga, ps, pw, flush, peaks))

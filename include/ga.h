@@ -201,6 +201,26 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
                      void* workspace, size_t workspace_bytes, ga_stream_t stream);
 
 /*
+ * ga_mla_decode -- multi-head latent attention, absorbed form, one new token per sequence.
+ * ("Attention in Code", section 4: store only the latent vectors and move the weights to the
+ * query side.)  With DeepSeek-V2-Lite's sizes: latent r = 512, rope key dr = 64, head dims
+ * dn = dv = 128, up to 16 heads sharing the latent cache:
+ *   q_lat = q_nope w_uk[h]^T, s_j = (q_lat . c_kv_j + q_rope . k_rope_j) / sqrt(dn + dr),
+ *   out   = (softmax(s) c_kv) w_uv[h], over every cached token j < lens[b].
+ *   q_nope   device bf16 [batch, n_heads, 128];  q_rope: [batch, n_heads, 64].
+ *   latent   device bf16 [batch, L_max, 576]: per token c_kv (512) then k_rope (64).
+ *   w_uk     device bf16 [n_heads, 512, 128];  w_uv: [n_heads, 512, 128].
+ *   lens     device int32 [batch] (clamped to [0, L_max]) or NULL (= L_max).
+ *   out      device bf16 [batch, n_heads, 128].
+ *   workspace of ga_mla_decode_workspace_size(batch, n_heads, L_max) bytes, 16-byte aligned.
+ *   n_heads <= 16 (GA_ERR_UNSUPPORTED otherwise).  q_lat is rounded to bf16 before the scores.
+ */
+size_t ga_mla_decode_workspace_size(int batch, int n_heads, int L_max);
+int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, const void* w_uk,
+                  const void* w_uv, const int32_t* lens, void* out, int batch, int n_heads,
+                  int L_max, void* workspace, size_t workspace_bytes, ga_stream_t stream);
+
+/*
  * ga_ring_append -- write one new token per sequence into a sliding-window ring cache.
  * ("Attention in Code", section 2: a layer that only looks at the last W tokens keeps a
  * cache of W slots per kv head; token number n, counting from 0, goes to slot n mod W and

@@ -25,6 +25,7 @@ Modules:
   ring       -- W-slot ring-buffer decode (the windowed cache of "Attention in Code" s.2)
   variants   -- differential attention ("Attention Variants", differential attention)
   dsa        -- token top-k sparse attention with a lightning-style indexer ("Attention in Code" s.5)
+  mla        -- multi-head latent attention, naive and absorbed ("Attention in Code" s.4)
 """
 from .attention import attend, positions, visible
 from .blocks import allowed_blocks, block_stats, radius_zscores, select_blocks

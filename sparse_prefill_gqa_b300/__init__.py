@@ -26,7 +26,7 @@ __all__ = [
     "GA_ERR_UNSUPPORTED", "GA_ERR_CUDA", "GA_ERR_DEVICE_TIMEOUT", "GA_ERR_WORKSPACE",
     "GA_ERR_SCRATCH_LIMIT", "GA_DECODE_STATIC_SCRATCH_BYTES", "ga_attend_decode_static",
     "ga_ring_append", "ga_attend_ring", "ga_attend_diff", "ga_dsa_indexer", "ga_topk_indices",
-    "ga_attend_gather", "dsa_decode", "GA_RADIUS_ZSCORE", "GA_RADIUS_MAD",
+    "ga_attend_gather", "dsa_decode", "ga_mla_decode", "GA_RADIUS_ZSCORE", "GA_RADIUS_MAD",
 ]
 
 GA_OK, GA_ERR_INVALID_ARG, GA_ERR_UNSUPPORTED = 0, -1, -2
@@ -74,6 +74,10 @@ def lib() -> ctypes.CDLL:
     L.ga_attend_gather_workspace_size.restype = sz
     L.ga_attend_gather.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp, sz, vp]
     L.ga_attend_gather.restype = i32
+    L.ga_mla_decode_workspace_size.argtypes = [i32, i32, i32]
+    L.ga_mla_decode_workspace_size.restype = sz
+    L.ga_mla_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]
+    L.ga_mla_decode.restype = i32
     L.ga_attend_diff.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32, f32,
                                  vp, sz, vp]
     L.ga_attend_diff.restype = i32
@@ -315,6 +319,33 @@ def dsa_decode(q, k, v, qi, wi, ki, topk, lens=None, *, sink=None, stream=None):
     idx, n_sel = ga_topk_indices(scores, topk, lens, stream=stream)
     out = ga_attend_gather(q, k, v, idx, n_sel, sink=sink, stream=stream)
     return out, idx, n_sel, scores
+
+
+def ga_mla_decode(q_nope, q_rope, latent, w_uk, w_uv, lens=None, out=None, *, workspace=None, stream=None):
+    """MLA decode, absorbed form: q_nope [B, H, 128], q_rope [B, H, 64], latent [B, L_max, 576]
+    (c_kv | k_rope per token), w_uk and w_uv [H, 512, 128], all bf16; returns out [B, H, 128]."""
+    L = lib()
+    _need(q_nope, "q_nope", torch.bfloat16, 3)
+    _need(q_rope, "q_rope", torch.bfloat16, 3)
+    _need(latent, "latent", torch.bfloat16, 3)
+    _need(w_uk, "w_uk", torch.bfloat16, 3)
+    _need(w_uv, "w_uv", torch.bfloat16, 3)
+    B, H, _ = q_nope.shape
+    L_max = latent.shape[1]
+    if q_nope.shape != (B, H, 128) or q_rope.shape != (B, H, 64) or latent.shape != (B, L_max, 576) \
+            or w_uk.shape != (H, 512, 128) or w_uv.shape != (H, 512, 128):
+        raise ValueError("MLA shapes: q_nope [B,H,128], q_rope [B,H,64], latent [B,L,576], w_uk/w_uv [H,512,128]")
+    if lens is not None:
+        _need(lens, "lens", torch.int32, 1)
+    if out is None:
+        out = torch.empty(B, H, 128, dtype=torch.bfloat16, device=q_nope.device)
+    need = int(L.ga_mla_decode_workspace_size(B, H, L_max))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_nope.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(L.ga_mla_decode(_ptr(q_nope), _ptr(q_rope), _ptr(latent), _ptr(w_uk), _ptr(w_uv), _ptr(lens), _ptr(out),
+                           B, H, L_max, _ptr(workspace), ws_bytes, _stream(stream)), "ga_mla_decode")
+    return out
 
 
 def ga_ring_append(k_ring, v_ring, k_new, v_new, n_seen, *, stream=None):

@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "decode.cuh"
 #include "dsa.cuh"
+#include "mla.cuh"
 #include "prefill_wide.cuh"
 #include "ring.cuh"
 
@@ -506,6 +507,66 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
   // The query sees every selected token: a causal decode row over n_sel[b] compact keys.
   return ga_attend(q, kc, vc, out, batch, n_heads, n_kv, d, 1, topk, n_sel, 1, 0, sink, nullptr, 1, 1, lse,
                    GA_BF16, ws_dec, workspace_bytes - 2 * cache, stream_);
+}
+
+namespace {
+// Token chunk of the MLA decode: about two waves of one CTA per SM over the batch at full
+// length, whole 64-token tiles.
+int mla_chunk_len(int batch, int L_max) {
+  long long c = (long long)L_max * batch / (148LL * 2);
+  c = c < 256 ? 256 : (c > 4096 ? 4096 : c);
+  return (int)((c + 63) / 64 * 64);
+}
+}  // namespace
+
+size_t ga_mla_decode_workspace_size(int batch, int n_heads, int L_max) {
+  if (batch < 1 || n_heads < 1 || n_heads > 16 || L_max < 1) return SIZE_MAX;
+  using C = MlaCfg;
+  const int chunk = mla_chunk_len(batch, L_max);
+  const size_t n_chunks = (L_max + chunk - 1) / chunk;
+  const size_t rows = (size_t)batch * n_heads;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  return up(rows * C::DK * 2) + up(rows * C::R * 4) + up(rows * n_chunks * C::R * 4) + up(rows * n_chunks * 2 * 4);
+}
+
+int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, const void* w_uk,
+                  const void* w_uv, const int32_t* lens, void* out, int batch, int n_heads, int L_max,
+                  void* workspace, size_t workspace_bytes, ga_stream_t stream_) {
+  using C = MlaCfg;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!q_nope || !q_rope || !latent || !w_uk || !w_uv || !out) return GA_ERR_INVALID_ARG;
+  if (batch < 1 || n_heads < 1 || L_max < 1) return GA_ERR_INVALID_ARG;
+  if (n_heads > 16 || batch > 65535) return GA_ERR_UNSUPPORTED;
+  for (const void* p : {q_nope, q_rope, latent, w_uk, w_uv, (const void*)out})
+    if (!aligned16(p)) return GA_ERR_INVALID_ARG;
+  if (lens && (reinterpret_cast<uintptr_t>(lens) & 3)) return GA_ERR_INVALID_ARG;
+  const size_t need = ga_mla_decode_workspace_size(batch, n_heads, L_max);
+  if (need == SIZE_MAX) return GA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GA_ERR_WORKSPACE;
+  MlaShape s{};
+  s.batch = batch; s.n_heads = n_heads; s.L_max = L_max; s.lens = lens; s.timeout_ns = g_timeout_ns;
+  s.chunk_len = mla_chunk_len(batch, L_max);
+  s.n_chunks = (L_max + s.chunk_len - 1) / s.chunk_len;
+  const size_t rows = (size_t)batch * n_heads;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  auto* q_abs = reinterpret_cast<__nv_bfloat16*>(w);
+  auto* o_lat = reinterpret_cast<float*>(w + up(rows * C::DK * 2));
+  auto* ws_o = reinterpret_cast<float*>(w + up(rows * C::DK * 2) + up(rows * C::R * 4));
+  auto* ws_ml = reinterpret_cast<float*>(w + up(rows * C::DK * 2) + up(rows * C::R * 4) +
+                                         up(rows * s.n_chunks * C::R * 4));
+  CUtensorMap tm;
+  if (!make_map_bf16(&tm, latent, C::DK, L_max, batch, C::TILE)) return GA_ERR_CUDA;
+  static int ok = set_smem(mla_decode_kernel, C::SMEM_BYTES);
+  if (ok != GA_OK) return ok;
+  mla_absorb_kernel<<<dim3(n_heads, batch), 256, 0, stream>>>(
+      (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_rope, (const __nv_bfloat16*)w_uk, q_abs, n_heads);
+  mla_decode_kernel<<<dim3(s.n_chunks, batch), C::THREADS, C::SMEM_BYTES, stream>>>(tm, q_abs, ws_o, ws_ml,
+                                                                                   o_lat, s);
+  if (s.n_chunks > 1) mla_combine_kernel<<<dim3(n_heads, batch), C::R, 0, stream>>>(ws_o, ws_ml, o_lat, s);
+  mla_expand_kernel<<<dim3(n_heads, batch), C::DV, 0, stream>>>(o_lat, (const __nv_bfloat16*)w_uv,
+                                                                 (__nv_bfloat16*)out, n_heads);
+  return launch_status();
 }
 
 int ga_ring_append(void* k_ring, void* v_ring, const void* k_new, const void* v_new, int32_t* n_seen,

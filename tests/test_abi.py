@@ -119,3 +119,12 @@ def test_select_ex_rejects_invalid_rule_and_nan_bound(L):
     bad = list(args)
     bad[17] = math.nan                          # NaN bound threshold
     assert L.ga_select_blocks_ex(*bad) == ga.GA_ERR_INVALID_ARG
+
+
+def test_mla_rejects_invalid_arguments(L):
+    p = ctypes.c_void_p(4096)
+    # ga_mla_decode(q_nope, q_rope, latent, w_uk, w_uv, lens, out, batch, n_heads, L_max, ws, bytes, stream)
+    assert L.ga_mla_decode(p, p, p, p, p, None, p, 1, 32, 64, p, 1 << 20, None) == ga.GA_ERR_UNSUPPORTED
+    assert L.ga_mla_decode(p, p, p, p, p, None, p, 0, 16, 64, p, 1 << 20, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_mla_decode(p, p, p, p, p, None, p, 1, 16, 64, p, 16, None) == ga.GA_ERR_WORKSPACE
+    assert L.ga_mla_decode_workspace_size(1, 17, 64) == 2 ** 64 - 1
