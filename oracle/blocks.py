@@ -120,7 +120,7 @@ def radius_zscores(radius_row: np.ndarray, rule: str = "z"):
 def select_blocks(q, centroid, radius, *, Tk: int, q_block: int = 128, k_block: int = 64,
                   causal: bool = True, window: int = 0, tau_mean: float = math.inf,
                   lambda_radius: float = 3.0, return_margins: bool = False,
-                  radius_rule: str = "z", tau_bound: float | None = None):
+                  radius_rule: str = "z", tau_bound: float | None = None, group_shared: bool = False):
     """Union of the mean-score branch and the radius-rescue branch, plus the diagonal.
 
     radius_rule: "z" or "mad" (see radius_zscores).  tau_bound: when given, a third branch
@@ -129,6 +129,9 @@ def select_blocks(q, centroid, radius, *, Tk: int, q_block: int = 128, k_block: 
     least the best visible mean score minus tau_bound: a block whose keys could score that
     high is kept however low its mean.  With return_margins the bound branch's margins are
     returned as a fifth array.
+
+    group_shared: one selection per kv head, from the query rows of all its g query heads pooled
+    together (the mean over heads and rows); every head of the group gets that mask.
 
     q: [B, H, Tq, d]; centroid: [B, n_kv, >=nKb, d]; radius: [B, n_kv, >=nKb] with
     nKb = ceil(Tk / k_block).  Returns (mask uint8 [B, H, nQb, nKb], n_selected int32
@@ -158,7 +161,10 @@ def select_blocks(q, centroid, radius, *, Tk: int, q_block: int = 128, k_block: 
                     t0, t1 = alpha * q_block, min(Tq, (alpha + 1) * q_block)
                     i_first, i_last = Tk - Tq + t0, Tk - Tq + t1 - 1
                     allowed = allowed_blocks(alpha, Tq, Tk, q_block, k_block, causal, window)
-                    q_mean = q[b, h, t0:t1].mean(axis=0)
+                    if group_shared:
+                        q_mean = q[b, kvh * g:(kvh + 1) * g, t0:t1].reshape(-1, d).mean(axis=0)
+                    else:
+                        q_mean = q[b, h, t0:t1].mean(axis=0)
                     s = (c @ q_mean) * scale
                     top = s[allowed].max()
                     keep_mean = s >= top - tau_mean

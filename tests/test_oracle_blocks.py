@@ -269,3 +269,24 @@ def test_bound_branch_bounds_the_block_scores_and_contains_the_mean_branch():
                 keep = vis[x] and (s[x] >= top - tau or ub >= top - tb or
                                    (rr[x] - med) / (1.4826 * mad) >= lam or own)
                 assert mask[0, h, alpha, x] == keep
+
+
+def test_group_shared_selection():
+    """One mask per kv head from the group-pooled query: with one query head per kv head it is
+    the per-head selection; otherwise every head of a group carries the same mask, equal to the
+    per-head selection of the pooled query (the mean of the group's rows), checked by brute force."""
+    B, n_kv, T, d, qb, kb = 1, 2, 256, 8, 32, 16
+    k = _rand((B, n_kv, T, d), 171)
+    k[0, 1, 77] *= 6.0
+    c, r = block_stats(k, None, kb)
+    q1 = _rand((B, n_kv, T, d), 172)
+    a, _ = select_blocks(q1, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=0.05, lambda_radius=2.0)
+    s, _ = select_blocks(q1, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=0.05, lambda_radius=2.0, group_shared=True)
+    assert np.array_equal(a, s)
+    g = 4
+    q = _rand((B, n_kv * g, T, d), 173)
+    m, _ = select_blocks(q, c, r, Tk=T, q_block=qb, k_block=kb, tau_mean=0.05, lambda_radius=2.0, group_shared=True)
+    pooled = q.reshape(B, n_kv, g, T, d).mean(axis=2)          # same block means as pooling g x rows
+    ref = _brute_select(pooled, c, r, T, qb, kb, 0, 0.05, 2.0)
+    for h in range(n_kv * g):
+        assert np.array_equal(m[0, h], ref[0, h // g])
