@@ -339,6 +339,10 @@ typedef enum {
  *                The left side bounds the pooled query's score over every key of the block
  *                (Cauchy-Schwarz: |k - c| <= radius), so a block whose keys could score that
  *                high is kept however low its mean is.  -INFINITY: no bound branch.
+ *   group_shared 1: one selection per kv head, from the query rows of its n_heads / n_kv heads
+ *                pooled together (mean_rows above is then the mean over those heads' rows);
+ *                every head of the group receives that mask and count (the heads of a group
+ *                then read the same key blocks).  0: per query head.
  *   block_mask = visible && (mean || bound || radius || diagonal).  Everything else as in
  *   ga_select_blocks; NaN thresholds and unknown rules give GA_ERR_INVALID_ARG.
  */
@@ -346,8 +350,8 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
                         int batch, int n_heads, int n_kv, int d, int Tq, int Tk, int nKb_out,
                         int q_block, int k_block, int causal, int window,
                         float tau_mean, float lambda_radius, int radius_rule, float tau_bound,
-                        uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype,
-                        ga_stream_t stream);
+                        int group_shared, uint8_t* block_mask, int32_t* n_selected,
+                        ga_dtype dtype, ga_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the sticky device status: GA_OK, or
  * GA_ERR_DEVICE_TIMEOUT when some kernel gave up on a wait since the last read.  Returns

@@ -93,7 +93,7 @@ def lib() -> ctypes.CDLL:
                                    f32, f32, vp, vp, i32, vp]
     L.ga_select_blocks.restype = i32
     L.ga_select_blocks_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                      f32, f32, i32, f32, vp, vp, i32, vp]
+                                      f32, f32, i32, f32, i32, vp, vp, i32, vp]
     L.ga_select_blocks_ex.restype = i32
     L.ga_read_device_status.argtypes = [vp]
     L.ga_read_device_status.restype = i32
@@ -418,11 +418,13 @@ def ga_block_stats(k, k_block=64, *, k_lens=None, centroid=None, radius=None, st
 
 def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, causal=True,
                      window=0, tau_mean=math.inf, lambda_radius=3.0, block_mask=None,
-                     n_selected=None, n_kv=None, radius_rule="z", tau_bound=None, stream=None):
+                     n_selected=None, n_kv=None, radius_rule="z", tau_bound=None, group_shared=False,
+                     stream=None):
     """Block mask (uint8 [B, H, nQb, nKb]) and per-row counts (int32 [B, H, nQb]).
 
     radius_rule: "z" (mean and population std) or "mad" (median and 1.4826 * MAD);
-    tau_bound: threshold of the Cauchy-Schwarz bound branch, None for no bound branch."""
+    tau_bound: threshold of the Cauchy-Schwarz bound branch, None for no bound branch;
+    group_shared: one selection per kv head from its heads' pooled query rows."""
     L = lib()
     _need(q, "q", None, 4)
     B, H, Tq, d = q.shape
@@ -438,7 +440,8 @@ def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, c
     tb = -math.inf if tau_bound is None else float(tau_bound)
     st = L.ga_select_blocks_ex(_ptr(q), _ptr(centroid), _ptr(radius), B, H, n_kv, d, Tq, int(Tk),
                                nKb_out, int(q_block), int(k_block), int(bool(causal)), int(window),
-                               float(tau_mean), float(lambda_radius), rule, tb, _ptr(block_mask),
+                               float(tau_mean), float(lambda_radius), rule, tb, int(bool(group_shared)),
+                               _ptr(block_mask),
                                _ptr(n_selected), _DTYPES[q.dtype], _stream(stream))
     _check(st, "ga_select_blocks")
     return block_mask, n_selected

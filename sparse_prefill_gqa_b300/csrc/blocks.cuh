@@ -285,6 +285,8 @@ struct SelectShape {
   int radius_rule;                // 0: z-score (mean, population std); 1: median and MAD
   int sort_len;                   // rule 1: power of two >= nKb (the sort buffer); else 0
   float tau_bound;                // bound branch threshold; -inf: no bound branch
+  int group_shared;               // 1: one selection per kv head (grid over kv heads), from the
+                                  // query rows of its g heads pooled; every head gets the mask
 };
 
 // shared memory: qmt [d][kSelQS] | ctt [d][kSelCS] | red [8] double | sortbuf [sort_len] double
@@ -333,8 +335,12 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
   uint8_t* rescue = reinterpret_cast<uint8_t*>(rng + 4 * kSelQT);      // [nKb]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int a0 = blockIdx.x * kSelQT, h = blockIdx.y, b = blockIdx.z;
-  const int kvh = h / (s.n_heads / s.n_kv);
+  const int a0 = blockIdx.x * kSelQT, b = blockIdx.z;
+  const int g = s.n_heads / s.n_kv;
+  // group-shared: blockIdx.y is the kv head and the pooled heads are its g query heads
+  const int h = s.group_shared ? blockIdx.y * g : blockIdx.y;        // first head of the CTA
+  const int n_pool = s.group_shared ? g : 1;                         // heads pooled and written
+  const int kvh = h / g;
   const float* rrow = radius + ((size_t)b * s.n_kv + kvh) * s.nKb_out;
   const float* cbase = centroid + ((size_t)b * s.n_kv + kvh) * (size_t)s.nKb_out * d;
 
@@ -388,18 +394,21 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
       continue;
     }
     const int t0 = alpha * s.q_block, t1 = min(s.Tq, t0 + s.q_block);
-    const float inv_n = 1.0f / (float)(t1 - t0);
+    const float inv_n = 1.0f / (float)((t1 - t0) * n_pool);
     const T* qb = q + (((size_t)b * s.n_heads + h) * s.Tq) * d;
     if (sizeof(T) == 2 && d % 8 == 0 && 32 % vec_l == 0) {
       // 16-byte loads: lane l reads dims 8*(l % L) .. of rows l / L, l / L + 32/L, ...
       const int rpw = 32 / vec_l, col = 8 * (lane % vec_l), r0 = lane / vec_l;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int hp = 0; hp < n_pool; ++hp) {                         // the pooled heads' rows
+        const T* qh = qb + (size_t)hp * s.Tq * d;
 #pragma unroll 8
-      for (int t = t0 + r0; t < t1; t += rpw) {
-        float f[8];
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(qb + (size_t)t * d + col)), f);
+        for (int t = t0 + r0; t < t1; t += rpw) {
+          float f[8];
+          bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(qh + (size_t)t * d + col)), f);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] += f[k];
+          for (int k = 0; k < 8; ++k) acc[k] += f[k];
+        }
       }
       for (int o = vec_l; o < 32; o <<= 1)
 #pragma unroll
@@ -410,7 +419,8 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
     } else {
       for (int c = lane; c < d; c += 32) {
         float acc = 0.0f;
-        for (int t = t0; t < t1; ++t) acc += to_f32(qb[(size_t)t * d + c]);
+        for (int hp = 0; hp < n_pool; ++hp)
+          for (int t = t0; t < t1; ++t) acc += to_f32(qb[((size_t)hp * s.Tq + t) * d + c]);
         qmt[c * kSelQS + a] = acc * inv_n;
       }
     }
@@ -530,14 +540,16 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
             bytes |= (keep ? 1u : 0u) << (8 * jj);
             kept += keep ? 1 : 0;
           }
-          uint8_t* mrow = block_mask + (((size_t)b * s.n_heads + h) * s.nQb + alpha) * s.nKb_out;
           const int beta0 = bt + 4 * lane;
-          if (vec_mask && beta0 + 3 < s.nKb_out) {
-            *reinterpret_cast<uint32_t*>(mrow + beta0) = bytes;
-          } else {
+          for (int hp = 0; hp < n_pool; ++hp) {                       // every head of the CTA
+            uint8_t* mrow = block_mask + (((size_t)b * s.n_heads + h + hp) * s.nQb + alpha) * s.nKb_out;
+            if (vec_mask && beta0 + 3 < s.nKb_out) {
+              *reinterpret_cast<uint32_t*>(mrow + beta0) = bytes;
+            } else {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-              if (beta0 + jj < s.nKb_out) mrow[beta0 + jj] = (uint8_t)((bytes >> (8 * jj)) & 1u);
+              for (int jj = 0; jj < 4; ++jj)
+                if (beta0 + jj < s.nKb_out) mrow[beta0 + jj] = (uint8_t)((bytes >> (8 * jj)) & 1u);
+            }
           }
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
@@ -552,10 +564,12 @@ select_blocks_kernel(const T* __restrict__ q, const float* __restrict__ centroid
   for (int a = 0; a < kSelQT; ++a) {
     const int alpha = a0 + a;
     if (alpha >= s.nQb) break;
-    uint8_t* mrow = block_mask + (((size_t)b * s.n_heads + h) * s.nQb + alpha) * s.nKb_out;
-    for (int beta = tid; beta < s.nKb_out; beta += kSelThreads)
-      if (beta < beta_lo || beta >= tiles_end) mrow[beta] = 0;
-    if (tid == 0 && n_selected) n_selected[((size_t)b * s.n_heads + h) * s.nQb + alpha] = nsel[a];
+    for (int hp = 0; hp < n_pool; ++hp) {
+      uint8_t* mrow = block_mask + (((size_t)b * s.n_heads + h + hp) * s.nQb + alpha) * s.nKb_out;
+      for (int beta = tid; beta < s.nKb_out; beta += kSelThreads)
+        if (beta < beta_lo || beta >= tiles_end) mrow[beta] = 0;
+      if (tid == 0 && n_selected) n_selected[((size_t)b * s.n_heads + h + hp) * s.nQb + alpha] = nsel[a];
+    }
   }
 }
 

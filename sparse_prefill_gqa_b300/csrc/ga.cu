@@ -648,14 +648,14 @@ int ga_select_blocks(const void* q, const float* centroid, const float* radius, 
                      uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype, ga_stream_t stream_) {
   return ga_select_blocks_ex(q, centroid, radius, batch, n_heads, n_kv, d, Tq, Tk, nKb_out, q_block,
                              k_block, causal, window, tau_mean, lambda_radius, GA_RADIUS_ZSCORE,
-                             -INFINITY, block_mask, n_selected, dtype, stream_);
+                             -INFINITY, 0, block_mask, n_selected, dtype, stream_);
 }
 
 int ga_select_blocks_ex(const void* q, const float* centroid, const float* radius, int batch,
                         int n_heads, int n_kv, int d, int Tq, int Tk, int nKb_out, int q_block,
                         int k_block, int causal, int window, float tau_mean, float lambda_radius,
-                        int radius_rule, float tau_bound, uint8_t* block_mask, int32_t* n_selected,
-                        ga_dtype dtype, ga_stream_t stream_) {
+                        int radius_rule, float tau_bound, int group_shared, uint8_t* block_mask,
+                        int32_t* n_selected, ga_dtype dtype, ga_stream_t stream_) {
   cudaStream_t stream = (cudaStream_t)stream_;
   if (!q || !centroid || !radius || !block_mask) return GA_ERR_INVALID_ARG;
   if (dtype != GA_F32 && dtype != GA_BF16) return GA_ERR_INVALID_ARG;
@@ -666,6 +666,7 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
   if ((causal != 0 && causal != 1) || window < 0 || (window > 0 && !causal)) return GA_ERR_INVALID_ARG;
   if (std::isnan(tau_mean) || std::isnan(lambda_radius) || std::isnan(tau_bound)) return GA_ERR_INVALID_ARG;
   if (radius_rule != GA_RADIUS_ZSCORE && radius_rule != GA_RADIUS_MAD) return GA_ERR_INVALID_ARG;
+  if (group_shared != 0 && group_shared != 1) return GA_ERR_INVALID_ARG;
   const long long nKb = ((long long)Tk + k_block - 1) / k_block;
   if (nKb_out < nKb) return GA_ERR_INVALID_ARG;
   if (nKb > 32768 || batch > 65535 || n_heads > 65535) return GA_ERR_UNSUPPORTED;
@@ -676,7 +677,7 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
   s.nKb_out = nKb_out; s.q_block = q_block; s.k_block = k_block; s.causal = causal;
   s.window = window; s.nQb = (Tq + q_block - 1) / q_block; s.nKb = (int)nKb;
   s.tau_mean = tau_mean; s.lambda_radius = lambda_radius;
-  s.radius_rule = radius_rule; s.tau_bound = tau_bound;
+  s.radius_rule = radius_rule; s.tau_bound = tau_bound; s.group_shared = group_shared;
   s.sort_len = 0;
   if (radius_rule == GA_RADIUS_MAD)
     for (s.sort_len = 1; s.sort_len < nKb; s.sort_len <<= 1) {}
@@ -685,7 +686,7 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
   static int ok_bf = set_smem(select_blocks_kernel<__nv_bfloat16>, 220 * 1024);
   static int ok_f = set_smem(select_blocks_kernel<float>, 220 * 1024);
   if (ok_bf != GA_OK || ok_f != GA_OK) return GA_ERR_CUDA;
-  dim3 grid((s.nQb + kSelQT - 1) / kSelQT, n_heads, batch);
+  dim3 grid((s.nQb + kSelQT - 1) / kSelQT, group_shared ? n_kv : n_heads, batch);
   if (dtype == GA_BF16)
     select_blocks_kernel<__nv_bfloat16><<<grid, kSelThreads, smem, stream>>>(
         (const __nv_bfloat16*)q, centroid, radius, block_mask, n_selected, s);

@@ -112,12 +112,15 @@ def test_ring_calls_reject_invalid_arguments(L):
 
 def test_select_ex_rejects_invalid_rule_and_nan_bound(L):
     p = ctypes.c_void_p(4096)
-    args = [p, p, p, 1, 8, 2, 128, 256, 256, 4, 128, 64, 1, 0, math.inf, 3.0, 0, -math.inf, p, None, 1, None]
+    args = [p, p, p, 1, 8, 2, 128, 256, 256, 4, 128, 64, 1, 0, math.inf, 3.0, 0, -math.inf, 0, p, None, 1, None]
     bad = list(args)
     bad[16] = 2                                 # unknown radius rule
     assert L.ga_select_blocks_ex(*bad) == ga.GA_ERR_INVALID_ARG
     bad = list(args)
     bad[17] = math.nan                          # NaN bound threshold
+    assert L.ga_select_blocks_ex(*bad) == ga.GA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[18] = 2                                 # group_shared is 0 or 1
     assert L.ga_select_blocks_ex(*bad) == ga.GA_ERR_INVALID_ARG
 
 

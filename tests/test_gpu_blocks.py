@@ -142,3 +142,28 @@ def test_select_blocks_variants(B, H, n_kv, Tq, Tk, d, qb, kb, W, tau, lam, rule
     assert np.array_equal(nsel.cpu().numpy(), gm.sum(axis=3))
     if not diff.any():
         assert np.array_equal(nsel.cpu().numpy(), nref)
+
+
+@pytest.mark.parametrize("B,H,n_kv,Tq,Tk,d,qb,kb,W,tau,lam", [
+    (1, 8, 2, 4096, 4096, 128, 128, 64, 0, 0.02, 3.0),
+    (1, 4, 1, 1000, 3000, 128, 128, 64, 0, 0.01, 2.0),        # chunk at an offset, MQA
+])
+def test_select_blocks_group_shared(B, H, n_kv, Tq, Tk, d, qb, kb, W, tau, lam):
+    """One selection per kv head from its heads' pooled query rows; every head of the group
+    carries the same mask."""
+    q, qr = host_tensor(65, "q", (B, H, Tq, d), "bf16")
+    k, _ = planted_keys(66, B, n_kv, Tk, d, kb)
+    c, r = ga.ga_block_stats(k, kb)
+    mask, nsel = ga.ga_select_blocks(q, c, r, Tk=Tk, q_block=qb, k_block=kb, window=W, tau_mean=tau,
+                                     lambda_radius=lam, group_shared=True)
+    mref, nref, mm, zm = oracle.select_blocks(qr, to_f64(c), to_f64(r), Tk=Tk, q_block=qb, k_block=kb, window=W,
+                                              tau_mean=tau, lambda_radius=lam, return_margins=True,
+                                              group_shared=True)
+    gm = mask.cpu().numpy()
+    g = H // n_kv
+    for h in range(H):                       # the group's heads carry one mask
+        assert np.array_equal(gm[:, h], gm[:, (h // g) * g])
+    n_diff = compare_masks(gm, mref, mm, zm, "group-shared select")
+    if n_diff == 0:
+        assert np.array_equal(nsel.cpu().numpy(), nref)
+    assert np.array_equal(nsel.cpu().numpy(), gm.sum(axis=3))
