@@ -10,90 +10,102 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace ga {
 
 constexpr int kIdxWarps = 8;
 constexpr int kIdxKeysPerWarp = 64;            // keys a warp scores per CTA
+constexpr int kIdxGroups = 2;                  // 16-key groups whose loads a lane keeps in flight
 
 // grid: (ceil(L_max / (kIdxWarps * kIdxKeysPerWarp)), batch); block: 32 * kIdxWarps.
 // DI = indexer key dim (64 or 128), HI = indexer heads (power of two, <= DI / 8).
-// Lane l of a warp holds dims 8 (l % LD) .. + 7 of every head (LD = DI / 8 lanes per key) and
-// scores keys l / LD, l / LD + 32 / LD, ...; scores past lens[b] are -inf.
+//
+// The scores of 16 keys are mma.sync m16n8k16 contractions, one per 16 dims: the keys are the 16
+// rows of A and the indexer heads the columns of B, eight per n-block (columns past HI hold zero
+// queries and zero weights).  At 8 FLOP per byte the kernel is bound by HBM; the tensor cores
+// only take the 1024 multiply-adds per key off the issue slots, so the loads stay in flight.
+// A dot product does not depend on the order of its dims, so each lane takes whole 16-byte
+// pieces of its key rows straight from global memory: lane (g, c) = (lane / 4, lane % 4) loads
+// pieces c, c + 4, ... of keys g and g + 8, and its query fragment (head g) the same pieces.
+// In the k16 step that covers dims 0..3 (or 4..7) of piece u, the lane's four dims of a row sit
+// at the k indices 2c, 2c + 1, 2c + 8, 2c + 9 that the fragment layout assigns to it, on the A
+// and the B side alike.  The result is C[key][head]; lane (g, c) holds heads 2c, 2c + 1 (of
+// each n-block) of keys g and g + 8, so the weighted relu sum over the heads takes two shuffles
+// within each group of four lanes.  Scores past lens[b] are -inf.
 template <int DI, int HI>
 __global__ void __launch_bounds__(32 * kIdxWarps)
 dsa_indexer_kernel(const __nv_bfloat16* __restrict__ qi, const float* __restrict__ wi,
                    const __nv_bfloat16* __restrict__ ki, const int32_t* __restrict__ lens,
                    int L_max, float* __restrict__ scores) {
-  constexpr int LD = DI / 8, RP = 32 / LD;
-  static_assert(HI >= 1 && HI <= LD && (HI & (HI - 1)) == 0, "indexer heads: power of two <= DI/8");
+  constexpr int NU = DI / 32;                  // 16-byte pieces per lane and key row
+  constexpr int NB = (HI + 7) / 8;             // n8 blocks of indexer heads
+  static_assert(HI >= 1 && HI <= DI / 8 && (HI & (HI - 1)) == 0, "indexer heads: power of two <= DI/8");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, b = blockIdx.y;
+  const int g = lane >> 2, c = lane & 3;
   const int L = seq_keys(lens, b, L_max);
-  const int col = 8 * (lane % LD), r0 = lane / LD;
-  float qreg[HI][8];
+  uint4 qf[NB][NU];
+  float w[NB][2];
 #pragma unroll
-  for (int j = 0; j < HI; ++j) {
-    float f[8];
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(qi + ((size_t)b * HI + j) * DI + col), f);
+  for (int nb = 0; nb < NB; ++nb) {
+    const int head = 8 * nb + g;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qreg[j][e] = f[e];
-  }
-  // after the butterfly, lane l holds head idx = (bits of l below HI); its weight
-  int idx = 0;
+    for (int u = 0; u < NU; ++u)
+      qf[nb][u] = head < HI
+          ? __ldg(reinterpret_cast<const uint4*>(qi + ((size_t)b * HI + head) * DI + 8 * (c + 4 * u)))
+          : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-  for (int o = 1, w = 1; o < HI; o <<= 1, w <<= 1) idx += ((lane & o) ? 1 : 0) * (HI / (2 * w));
-  const float wj = wi[(size_t)b * HI + idx];
-  const int key_base = (blockIdx.x * kIdxWarps + warp) * kIdxKeysPerWarp;
-  constexpr int BATCH = 8;                           // loads in flight per lane
-  for (int rb = 0; rb < kIdxKeysPerWarp; rb += BATCH * RP) {
-  uint4 xk[BATCH];
-#pragma unroll
-  for (int u = 0; u < BATCH; ++u) {
-    const int s = key_base + rb + u * RP + r0;
-    xk[u] = s < L ? __ldg(reinterpret_cast<const uint4*>(ki + ((size_t)b * L_max + s) * DI + col))
-                  : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int u = 0; u < BATCH; ++u) {
-    const int s = key_base + rb + u * RP + r0;
-    float part[HI];
-    if (s < L) {
-      float f[8];
-      bf16x8_to_f32(xk[u], f);
-#pragma unroll
-      for (int j = 0; j < HI; ++j) {
-        float a = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaf(qreg[j][e], f[e], a);
-        part[j] = a;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < HI; ++j) part[j] = 0.0f;
+    for (int e = 0; e < 2; ++e) {
+      const int hw = 8 * nb + 2 * c + e;
+      w[nb][e] = hw < HI ? wi[(size_t)b * HI + hw] : 0.0f;
     }
-    // transposed butterfly over the low lane bits: each stage halves the heads a lane holds
-    int cnt = HI;
+  }
+  const int key_base = (blockIdx.x * kIdxWarps + warp) * kIdxKeysPerWarp;
+  const __nv_bfloat16* kb = ki + (size_t)b * L_max * DI;
+  float* sb = scores + (size_t)b * L_max;
+  for (int rb = 0; rb < kIdxKeysPerWarp; rb += 16 * kIdxGroups) {
+    uint4 ka[kIdxGroups][2][NU];               // [group][key g or g + 8][piece]
 #pragma unroll
-    for (int o = 1; o < HI; o <<= 1) {
-      const bool upper = (lane & o) != 0;
-      cnt >>= 1;
+    for (int gi = 0; gi < kIdxGroups; ++gi)
 #pragma unroll
-      for (int j = 0; j < HI / 2; ++j) {
-        if (j < cnt) {
-          const float send = upper ? part[j] : part[j + cnt];
-          const float keep = upper ? part[j + cnt] : part[j];
-          part[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      for (int r = 0; r < 2; ++r) {
+        const int s = key_base + rb + 16 * gi + 8 * r + g;
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+          ka[gi][r][u] = s < L ? __ldg(reinterpret_cast<const uint4*>(kb + (size_t)s * DI + 8 * (c + 4 * u)))
+                               : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+    for (int gi = 0; gi < kIdxGroups; ++gi) {
+      float acc[NB][4];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        // A registers: (key g, k 2c..), (key g + 8, k 2c..), (key g, k 2c + 8..), (key g + 8, k 2c + 8..)
+        const uint32_t a_lo[4] = {ka[gi][0][u].x, ka[gi][1][u].x, ka[gi][0][u].y, ka[gi][1][u].y};
+        const uint32_t a_hi[4] = {ka[gi][0][u].z, ka[gi][1][u].z, ka[gi][0][u].w, ka[gi][1][u].w};
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          mma_bf16_16816(acc[nb], a_lo, qf[nb][u].x, qf[nb][u].y);
+          mma_bf16_16816(acc[nb], a_hi, qf[nb][u].z, qf[nb][u].w);
         }
       }
+      float s0 = 0.0f, s1 = 0.0f;              // keys g and g + 8 over this lane's heads
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        s0 = fmaf(w[nb][0], fmaxf(acc[nb][0], 0.0f), s0);
+        s0 = fmaf(w[nb][1], fmaxf(acc[nb][1], 0.0f), s0);
+        s1 = fmaf(w[nb][0], fmaxf(acc[nb][2], 0.0f), s1);
+        s1 = fmaf(w[nb][1], fmaxf(acc[nb][3], 0.0f), s1);
+      }
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      const int s = key_base + rb + 16 * gi + g + 8 * c;      // lane c = 0: key g, c = 1: key g + 8
+      if (c < 2 && s < L_max) sb[s] = s < L ? (c ? s1 : s0) : -INFINITY;
     }
-    float dot = part[0];                              // head idx, summed over HI lanes
-#pragma unroll
-    for (int o = HI; o < LD; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    float sc = wj * fmaxf(dot, 0.0f);
-#pragma unroll
-    for (int o = 1; o < HI; o <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
-    if (lane % LD == 0 && s < L_max) scores[(size_t)b * L_max + s] = s < L ? sc : -INFINITY;
-  }
   }
 }
 

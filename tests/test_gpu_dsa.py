@@ -27,6 +27,7 @@ def _indexer_inputs(B, Hi, di, L, seed):
     (1, 4, 64, 777, None),
     (1, 16, 128, 1300, None),
     (2, 1, 64, 64, [64, 1]),
+    (3, 8, 128, 530, [0, 17, 530]),    # an empty cache scores -inf everywhere
 ])
 def test_indexer_scores(B, Hi, di, L, lens):
     qi, qir, ki, kir, wi, wr = _indexer_inputs(B, Hi, di, L, seed=501 + Hi)
@@ -34,8 +35,9 @@ def test_indexer_scores(B, Hi, di, L, lens):
     sc = to_f64(ga.ga_dsa_indexer(qi, wi, ki, ln))
     for b in range(B):
         n = L if lens is None else lens[b]
-        ref = indexer_scores(qir[b][:, None], kir[b, :n], wr[b][:, None].astype(np.float64))[0]
-        assert np.max(np.abs(sc[b, :n] - ref)) <= 1e-5 * max(1.0, np.max(np.abs(ref)))
+        if n:
+            ref = indexer_scores(qir[b][:, None], kir[b, :n], wr[b][:, None].astype(np.float64))[0]
+            assert np.max(np.abs(sc[b, :n] - ref)) <= 1e-5 * max(1.0, np.max(np.abs(ref)))
         assert np.all(np.isneginf(sc[b, n:]))
 
 
