@@ -184,16 +184,19 @@ int ga_dsa_indexer(const void* qi, const float* wi, const void* ki, const int32_
 int ga_topk_indices(const float* scores, const int32_t* lens, int batch, int L_max, int topk,
                     int32_t* idx, int32_t* n_sel, ga_stream_t stream);
 
-/* Bytes of workspace ga_attend_gather needs (SIZE_MAX for invalid sizes): the gathered keys and
- * values, then the split-K decode's partial results. */
+/* Bytes of workspace ga_attend_gather needs (SIZE_MAX for invalid sizes): the split-K decode's
+ * partial results over topk keys; 0 when the decode runs as one chunk (workspace may be NULL). */
 size_t ga_attend_gather_workspace_size(int batch, int n_heads, int n_kv, int d, int topk);
 
 /*
  * ga_attend_gather -- decode attention of q [batch, n_heads, 1, d] over the cached tokens
  *   idx[b, 0 .. n_sel[b]-1] of k, v [batch, n_kv, Tk_max, d] (bf16): softmax over exactly
- *   those keys (plus the optional sink), for every head of the sequence.  The selected rows
- *   are gathered into the workspace, then the split-K decode runs over them.
- *   d: 64, 128 or 256; n_heads / n_kv <= 16.  sink, lse as in ga_attend.
+ *   those keys (plus the optional sink), for every head of the sequence.  The split-K decode
+ *   reads the selected rows straight from the cache (TMA copies of four indexed rows each); no
+ *   compact copy is made.  idx entries must lie in [0, Tk_max) (others are clamped into it);
+ *   idx 4-byte aligned, n_sel, lse and sink 16-byte aligned.
+ *   d: 64, 128 or 256; n_heads / n_kv <= 16; batch * n_kv * Tk_max < 2^31 (GA_ERR_UNSUPPORTED
+ *   otherwise).  sink, lse as in ga_attend.
  */
 int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int batch,
                      int n_heads, int n_kv, int d, int Tk_max, const int32_t* idx,

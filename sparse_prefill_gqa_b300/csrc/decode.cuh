@@ -34,7 +34,11 @@ struct DecodeCfg {
   static constexpr int BODY = OFF_BAR > MERGE_BYTES ? OFF_BAR : MERGE_BYTES;
   static constexpr int SMEM_BYTES = BODY + 256 + 1024;
   static constexpr int THREADS = 160;
+  // gathered form: the chunk's cache rows (at most kGatherMaxKeys), after the barriers
+  static constexpr int GATHER_SMEM_BYTES = SMEM_BYTES + 4 * 4096;
 };
+
+constexpr int kGatherMaxKeys = 4096;              // longest key chunk of the gathered form
 
 struct DecodeBars {
   uint64_t full[8], empty[8];
@@ -47,6 +51,11 @@ struct DecodeShape {
   int n_chunks;
   int rows;             // query rows per kv head: g * Tq (<= 16)
   int g;
+  // Gathered form only: key j of sequence b is cache row gidx[b * gidx_stride + j] of its kv
+  // head, whose cache holds cache_T rows (the tensor maps are 2-D over all B * n_kv * cache_T rows).
+  const int32_t* gidx;
+  int gidx_stride;
+  int cache_T;
 };
 
 // Key range [lo, hi) that any row of sequence b may use, and the chunk's share of it.
@@ -58,7 +67,11 @@ __device__ __forceinline__ void decode_chunk_range(const DecodeShape& s, int Tk,
 }
 
 // grid: (n_chunks, n_kv, batch); block: 160 threads.
-template <int D>
+// GATHER = false: keys kbeg.. of the chunk are consecutive cache rows (3-D maps, one box per slab).
+// GATHER = true: the keys are the cache rows that s.gidx names (2-D maps with one-row boxes); the
+// producer warp loads each 64-key tile with tile::gather4 copies, four rows per copy and 16 lanes
+// issuing, into the same swizzled layout, so the consumers do not change.
+template <int D, bool GATHER = false>
 __global__ void __launch_bounds__(160)
 decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out,
@@ -91,6 +104,55 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   }
   __syncthreads();
 
+  if (warp == 4 && GATHER) {
+    // ------------------------------------------------------------ TMA gather producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    // The cache rows of the whole chunk go to shared memory first (one load latency per CTA,
+    // not one per tile): rows past the chunk's end repeat its last key (the consumers mask them),
+    // and an index outside the cache is clamped into it.  The host keeps the chunk within
+    // kGatherMaxKeys keys.
+    const long long row0 = (long long)(b * s.a.n_kv + kvh) * s.cache_T;   // first cache row of the head
+    const int32_t* gi = s.gidx + (size_t)b * s.gidx_stride + kbeg;
+    int* rows = reinterpret_cast<int*>(smem + C::BODY + 256);
+    const int n_keys = kend - kbeg;
+#pragma unroll 8
+    for (int j = lane; j < n_tiles * C::TILE; j += 32) {
+      const int t = __ldg(gi + min(j, n_keys - 1));
+      rows[j] = (int)(row0 + min(max(t, 0), s.cache_T - 1));
+    }
+    __syncwarp();
+    int issued = 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int st = it % C::STAGES, use = it / C::STAGES;
+      int r[4];                                   // lane l < 16 copies tile rows 4l .. 4l + 3
+#pragma unroll
+      for (int e = 0; e < 4; ++e) r[e] = rows[it * C::TILE + (4 * lane + e) % C::TILE];
+      int ok = 1;
+      if (lane == 0) {
+        ok = it < C::STAGES || mbar_wait(&bars->empty[st], (use + 1) & 1, tmo, abort_flag);
+        if (ok) mbar_arrive_expect_tx(&bars->full[st], C::STAGE_BYTES);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      ++issued;
+      if (lane < 16) {
+        unsigned char* dk = smem + st * C::STAGE_BYTES + lane * 512;
+        unsigned char* dv = dk + C::TILE_BYTES;
+#pragma unroll
+        for (int sl = 0; sl < C::SLABS; ++sl) {
+          tma_gather4(dk + sl * C::TILE * 128, &tm_k, &bars->full[st], 64 * sl, r[0], r[1], r[2], r[3]);
+          tma_gather4(dv + sl * C::TILE * 128, &tm_v, &bars->full[st], 64 * sl, r[0], r[1], r[2], r[3]);
+        }
+      }
+    }
+    if (lane == 0)
+      for (int k = max(0, issued - C::STAGES); k < issued; ++k)
+        mbar_wait(&bars->full[k % C::STAGES], (k / C::STAGES) & 1, tmo, nullptr);
+    __syncthreads();
+    return;
+  }
   if (warp == 4) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {

@@ -6,7 +6,8 @@
 // with one small key ki[s] per token -- and attention then reads only the k tokens with the
 // highest scores.  The cache keeps every token; what shrinks is what attention reads.  Decode
 // form: one query per sequence at position L_b - 1, which may see every cached token.
-// Ties at the k-th score go to the lower token index.
+// Ties at the k-th score go to the lower token index.  The decode over the selected tokens is the
+// split-K decode kernel in its gathered form (decode.cuh), which loads the chosen cache rows itself.
 #pragma once
 
 #include "common.cuh"
@@ -194,27 +195,6 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
   }
   for (int j = k + threadIdx.x; j < topk; j += kTopkThreads) out[j] = -1;
   if (threadIdx.x == 0) n_sel[b] = k;
-}
-
-// ---------------------------------------------------------------------------------------
-// Gather: rows idx[b, i] (i < n_sel[b]) of K and V of every kv head into a compact cache
-// [batch, n_kv, topk, d], in the order of the index list.  grid: (ceil(topk / 8), n_kv, batch);
-// block: 256 threads = 8 rows x 32 threads, 16 bytes a thread and step.
-__global__ void __launch_bounds__(256)
-dsa_gather_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                  const int32_t* __restrict__ idx, const int32_t* __restrict__ n_sel, int n_kv, int d,
-                  int Tk_max, int topk, __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc) {
-  const int b = blockIdx.z, kvh = blockIdx.y;
-  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (i >= min(n_sel[b], topk)) return;
-  const int j = idx[(size_t)b * topk + i];
-  if (j < 0 || j >= Tk_max) return;
-  const size_t src = (((size_t)b * n_kv + kvh) * Tk_max + j) * d;
-  const size_t dst = (((size_t)b * n_kv + kvh) * topk + i) * d;
-  for (int c = 8 * (threadIdx.x & 31); c < d; c += 256) {
-    *reinterpret_cast<uint4*>(kc + dst + c) = *reinterpret_cast<const uint4*>(k + src + c);
-    *reinterpret_cast<uint4*>(vc + dst + c) = *reinterpret_cast<const uint4*>(v + src + c);
-  }
 }
 
 }  // namespace ga

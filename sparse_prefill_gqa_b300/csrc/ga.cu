@@ -63,6 +63,20 @@ bool make_map_bf16(CUtensorMap* map, const void* base, int cols, long long rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over a [rows, cols] row-major tensor with boxes of one row x 64 columns and the
+// 128-byte swizzle: the form that tile::gather4 copies (four rows chosen by index) take.
+bool make_map_rows_bf16(CUtensorMap* map, const void* base, int cols, long long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename K>
 int set_smem(K kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess
@@ -152,14 +166,15 @@ int static_scratch_setup(void** addr) {
 
 // Launches the split-K decode (d in {64, 128, 256}) and, for more than one chunk, the combine.
 // The caller has validated the shape and placed the partial-result workspace.
-template <int D>
+template <int D, bool GATHER>
 int launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfloat16* qb,
                     __nv_bfloat16* ob, float* lse, float* ws_o, float* ws_ml, const DecodeShape& ds,
                     cudaStream_t stream) {
-  static int ok = set_smem(decode_splitk_kernel<D>, DecodeCfg<D>::SMEM_BYTES);
+  constexpr int smem = GATHER ? DecodeCfg<D>::GATHER_SMEM_BYTES : DecodeCfg<D>::SMEM_BYTES;
+  static int ok = set_smem(decode_splitk_kernel<D, GATHER>, smem);
   if (ok != GA_OK) return ok;
   const dim3 grid(ds.n_chunks, ds.a.n_kv, ds.a.batch);
-  decode_splitk_kernel<D><<<grid, DecodeCfg<D>::THREADS, DecodeCfg<D>::SMEM_BYTES, stream>>>(
+  decode_splitk_kernel<D, GATHER><<<grid, DecodeCfg<D>::THREADS, smem, stream>>>(
       tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
   const int st = launch_status();
   if (st != GA_OK || ds.n_chunks == 1) return st;
@@ -169,10 +184,15 @@ int launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfl
 
 int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfloat16* qb,
                   __nv_bfloat16* ob, float* lse, float* ws_o, float* ws_ml, const DecodeShape& ds,
-                  cudaStream_t stream) {
-  if (d == 256) return launch_decode_d<256>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
-  if (d == 128) return launch_decode_d<128>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
-  return launch_decode_d<64>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+                  cudaStream_t stream, bool gather = false) {
+  if (gather) {
+    if (d == 256) return launch_decode_d<256, true>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+    if (d == 128) return launch_decode_d<128, true>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+    return launch_decode_d<64, true>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+  }
+  if (d == 256) return launch_decode_d<256, false>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+  if (d == 128) return launch_decode_d<128, false>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
+  return launch_decode_d<64, false>(tk, tv, qb, ob, lse, ws_o, ws_ml, ds, stream);
 }
 
 // The tensor-core prefill (bf16, d = 128 or 256): tensor maps, then prefill_wide_kernel with or
@@ -475,10 +495,7 @@ int ga_topk_indices(const float* scores, const int32_t* lens, int batch, int L_m
 
 size_t ga_attend_gather_workspace_size(int batch, int n_heads, int n_kv, int d, int topk) {
   if (batch < 1 || n_heads < 1 || n_kv < 1 || d < 1 || topk < 1 || n_heads % n_kv != 0) return SIZE_MAX;
-  const size_t cache = ((size_t)batch * n_kv * topk * d * 2 + 255) / 256 * 256;   // kc, then vc
-  const size_t dec = ga_workspace_size(batch, n_heads, n_kv, d, 1, topk, GA_BF16);
-  if (dec == SIZE_MAX) return SIZE_MAX;
-  return 2 * cache + dec;
+  return ga_workspace_size(batch, n_heads, n_kv, d, 1, topk, GA_BF16);   // the decode's partials
 }
 
 int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int batch, int n_heads,
@@ -489,24 +506,36 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
   if (!q || !k || !v || !out || !idx || !n_sel || topk < 1 || Tk_max < 1) return GA_ERR_INVALID_ARG;
   if (batch < 1 || n_heads < 1 || n_kv < 1 || n_heads % n_kv != 0) return GA_ERR_INVALID_ARG;
   if (!(d == 64 || d == 128 || d == 256) || n_heads / n_kv > 16 || batch > 65535) return GA_ERR_UNSUPPORTED;
+  if ((long long)batch * n_kv * Tk_max > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;   // int32 row coordinates
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(n_sel) ||
-      (reinterpret_cast<uintptr_t>(idx) & 3))
+      (reinterpret_cast<uintptr_t>(idx) & 3) || (lse && !aligned16(lse)) || (sink && !aligned16(sink)))
     return GA_ERR_INVALID_ARG;
   const size_t need = ga_attend_gather_workspace_size(batch, n_heads, n_kv, d, topk);
   if (need == SIZE_MAX) return GA_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GA_ERR_WORKSPACE;
-  const size_t cache = ((size_t)batch * n_kv * topk * d * 2 + 255) / 256 * 256;
-  auto* kc = static_cast<__nv_bfloat16*>(workspace);
-  auto* vc = reinterpret_cast<__nv_bfloat16*>(static_cast<unsigned char*>(workspace) + cache);
-  void* ws_dec = static_cast<unsigned char*>(workspace) + 2 * cache;
-  const dim3 grid((topk + 7) / 8, n_kv, batch);
-  dsa_gather_kernel<<<grid, 256, 0, stream>>>((const __nv_bfloat16*)k, (const __nv_bfloat16*)v, idx, n_sel,
-                                              n_kv, d, Tk_max, topk, kc, vc);
-  const int st = launch_status();
-  if (st != GA_OK) return st;
-  // The query sees every selected token: a causal decode row over n_sel[b] compact keys.
-  return ga_attend(q, kc, vc, out, batch, n_heads, n_kv, d, 1, topk, n_sel, 1, 0, sink, nullptr, 1, 1, lse,
-                   GA_BF16, ws_dec, workspace_bytes - 2 * cache, stream_);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return GA_ERR_WORKSPACE;
+  // The query sees every selected token: a causal decode row over n_sel[b] keys, key j being
+  // cache row idx[b, j] of the kv head.
+  AttnShape sh{};
+  sh.batch = batch; sh.n_heads = n_heads; sh.n_kv = n_kv; sh.d = d; sh.Tq = 1; sh.Tk_max = topk;
+  sh.k_lens = n_sel; sh.causal = 1; sh.window = 0; sh.sink = sink;
+  sh.block_mask = nullptr; sh.q_block = 1; sh.k_block = 1; sh.nQb = 0; sh.nKb = 0;
+  sh.timeout_ns = g_timeout_ns;
+  DecodeShape ds{};
+  ds.a = sh;
+  ds.g = n_heads / n_kv;
+  ds.rows = ds.g;
+  ds.chunk_len = decode_chunk_len(batch, n_kv, topk);
+  ds.n_chunks = (topk + ds.chunk_len - 1) / ds.chunk_len;
+  if (ds.n_chunks == 1) ds.chunk_len = (topk + 63) / 64 * 64;
+  ds.gidx = idx; ds.gidx_stride = topk; ds.cache_T = Tk_max;
+  if (ds.chunk_len > kGatherMaxKeys) return GA_ERR_UNSUPPORTED;    // not reached: chunks are <= 4096 keys
+  float* ws_o = need ? static_cast<float*>(workspace) : nullptr;
+  float* ws_ml = need ? ws_o + (size_t)batch * n_heads * ds.n_chunks * d : nullptr;
+  CUtensorMap tk, tv;
+  const long long rows = (long long)batch * n_kv * Tk_max;
+  if (!make_map_rows_bf16(&tk, k, d, rows) || !make_map_rows_bf16(&tv, v, d, rows)) return GA_ERR_CUDA;
+  return launch_decode(d, tk, tv, (const __nv_bfloat16*)q, (__nv_bfloat16*)out, lse, ws_o, ws_ml, ds, stream,
+                       /*gather=*/true);
 }
 
 namespace {

@@ -129,6 +129,20 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Four rows of a 2-D map, chosen by their row coordinates r0..r3, each from column x over the
+// box's width (the box is one row high); written to shared memory as four consecutive box rows
+// under the map's swizzle, which follows the shared-memory address, so copies placed at 512-byte
+// steps inside a 1024-byte-aligned tile lay the rows out exactly as one tile load would.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2),
+         "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------------------
 // tcgen05: tensor memory, UMMA, commit, TMEM <-> register moves
 // ---------------------------------------------------------------------------------------

@@ -73,6 +73,7 @@ def _decode_inputs(B, H, n_kv, Lm, d, Hi, di, seed):
 @pytest.mark.parametrize("B,H,n_kv,Lm,d,Hi,di,topk,lens,use_sink", [
     (2, 8, 2, 3000, 128, 8, 128, 512, [3000, 1234], False),
     (2, 4, 1, 2000, 256, 4, 64, 300, [2000, 150], True),     # d = 256; a sequence shorter than k
+    (1, 4, 4, 900, 64, 2, 64, 200, [600], False),            # d = 64; cache rows past the length hold NaN
 ])
 def test_dsa_decode_matches_oracle(B, H, n_kv, Lm, d, Hi, di, topk, lens, use_sink):
     dev, ref = _decode_inputs(B, H, n_kv, Lm, d, Hi, di, seed=521)
@@ -83,6 +84,9 @@ def test_dsa_decode_matches_oracle(B, H, n_kv, Lm, d, Hi, di, topk, lens, use_si
         skr = np.random.default_rng(7).standard_normal(H).astype(np.float32)
         sink = torch.from_numpy(skr).cuda()
     ln = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    for b, n in enumerate(lens):               # rows no selection may read
+        k[b, :, n:] = float("nan")
+        v[b, :, n:] = float("nan")
     out, idx, n_sel, scores = ga.dsa_decode(q, k, v, qi, wi, ki, topk, ln, sink=sink)
     assert ga.ga_read_device_status() == ga.GA_OK
     # the oracle attends over the tokens its own top-k picks from the GPU's scores
