@@ -9,7 +9,9 @@
 //
 // The work is bound by reading K and V once from HBM (every byte of a kv head serves all
 // its g query heads).  One CTA per (key chunk, kv head, sequence):
-//   warp 4   TMA producer: 64-key K and V tiles (128-byte swizzled) into a ring of stages;
+//   warp 4   TMA producer: 64-key K and V tiles (128-byte swizzled) into a ring of stages (in the
+//            gathered form, which reads the keys an index list names, the consumer warps load
+//            their own rows instead);
 //   warps 0-3  each takes 16 keys of every tile.  The rows of the MMA are the g * Tq query
 //            rows of the kv head (padded to 16); scores and the value sum run on the tensor
 //            cores through mma.sync m16n8k16 (a contraction of 16 x d x 16 per warp and tile,
@@ -34,8 +36,11 @@ struct DecodeCfg {
   static constexpr int BODY = OFF_BAR > MERGE_BYTES ? OFF_BAR : MERGE_BYTES;
   static constexpr int SMEM_BYTES = BODY + 256 + 1024;
   static constexpr int THREADS = 160;
-  // gathered form: the chunk's cache rows (at most kGatherMaxKeys), after the barriers
-  static constexpr int GATHER_SMEM_BYTES = SMEM_BYTES + 4 * 4096;
+  // gathered form: more stages (each warp keeps GSTAGES - 1 of its tiles in flight), then the
+  // barriers, then the chunk's cache rows (at most kGatherMaxKeys)
+  static constexpr int GSTAGES = D >= 256 ? 3 : (D >= 128 ? 6 : 12);
+  static constexpr int GBODY = GSTAGES * STAGE_BYTES > MERGE_BYTES ? GSTAGES * STAGE_BYTES : MERGE_BYTES;
+  static constexpr int GATHER_SMEM_BYTES = GBODY + 256 + 4 * 4096 + 1024;
 };
 
 constexpr int kGatherMaxKeys = 4096;              // longest key chunk of the gathered form
@@ -52,10 +57,12 @@ struct DecodeShape {
   int rows;             // query rows per kv head: g * Tq (<= 16)
   int g;
   // Gathered form only: key j of sequence b is cache row gidx[b * gidx_stride + j] of its kv
-  // head, whose cache holds cache_T rows (the tensor maps are 2-D over all B * n_kv * cache_T rows).
+  // head in gk / gv [batch, n_kv, cache_T, D] (the tensor maps are not used).
   const int32_t* gidx;
   int gidx_stride;
   int cache_T;
+  const __nv_bfloat16* gk;
+  const __nv_bfloat16* gv;
 };
 
 // Key range [lo, hi) that any row of sequence b may use, and the chunk's share of it.
@@ -67,10 +74,14 @@ __device__ __forceinline__ void decode_chunk_range(const DecodeShape& s, int Tk,
 }
 
 // grid: (n_chunks, n_kv, batch); block: 160 threads.
-// GATHER = false: keys kbeg.. of the chunk are consecutive cache rows (3-D maps, one box per slab).
-// GATHER = true: the keys are the cache rows that s.gidx names (2-D maps with one-row boxes); the
-// producer warp loads each 64-key tile with tile::gather4 copies, four rows per copy and 16 lanes
-// issuing, into the same swizzled layout, so the consumers do not change.
+// GATHER = false: keys kbeg.. of the chunk are consecutive cache rows, loaded by the TMA producer
+// warp (3-D maps, one box per slab).
+// GATHER = true: the keys are the cache rows that s.gidx names.  Each consumer warp reads only its
+// own 16 rows of every tile, so each loads them itself with 16-byte cp.async copies into the same
+// swizzled layout, GSTAGES - 1 tiles ahead, and needs nothing but __syncwarp; the producer warp
+// idles.  (Indexed TMA copies, tile::gather4, four 128-byte rows per copy issued by the producer
+// warp, were measured at about 6 bytes per clock per SM on this workload, half the rate of these
+// copies.)
 template <int D, bool GATHER = false>
 __global__ void __launch_bounds__(160)
 decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -78,10 +89,13 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                      float* __restrict__ lse, float* __restrict__ ws_o, float* __restrict__ ws_ml,
                      DecodeShape s) {
   using C = DecodeCfg<D>;
+  constexpr int NST = GATHER ? C::GSTAGES : C::STAGES;       // stages of the ring
+  constexpr int BODY = GATHER ? C::GBODY : C::BODY;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  DecodeBars* bars = reinterpret_cast<DecodeBars*>(smem + C::BODY);
+  DecodeBars* bars = reinterpret_cast<DecodeBars*>(smem + BODY);
+  int* rows = reinterpret_cast<int*>(smem + BODY + 256);     // gathered form: the chunk's cache rows
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,6 +107,18 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   const int n_tiles = (kend - kbeg + C::TILE - 1) / C::TILE;
   const uint64_t tmo = s.a.timeout_ns;
 
+  if constexpr (GATHER) {
+    // The chunk's cache rows, once per CTA: rows past the chunk's end repeat its last key (the
+    // consumers mask them), and an index outside the cache is clamped into it.  The host keeps
+    // the chunk within kGatherMaxKeys keys.
+    const long long row0 = (long long)(b * s.a.n_kv + kvh) * s.cache_T;
+    const int32_t* gi = s.gidx + (size_t)b * s.gidx_stride + kbeg;
+    const int n_keys = kend - kbeg;
+    for (int j = threadIdx.x; j < n_tiles * C::TILE; j += C::THREADS) {
+      const int t = __ldg(gi + min(j, n_keys - 1));
+      rows[j] = (int)(row0 + min(max(t, 0), s.cache_T - 1));
+    }
+  }
   if (threadIdx.x == 0) {
     for (int st = 0; st < C::STAGES; ++st) {
       mbar_init(&bars->full[st], 1);
@@ -104,52 +130,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   }
   __syncthreads();
 
-  if (warp == 4 && GATHER) {
-    // ------------------------------------------------------------ TMA gather producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-    }
-    // The cache rows of the whole chunk go to shared memory first (one load latency per CTA,
-    // not one per tile): rows past the chunk's end repeat its last key (the consumers mask them),
-    // and an index outside the cache is clamped into it.  The host keeps the chunk within
-    // kGatherMaxKeys keys.
-    const long long row0 = (long long)(b * s.a.n_kv + kvh) * s.cache_T;   // first cache row of the head
-    const int32_t* gi = s.gidx + (size_t)b * s.gidx_stride + kbeg;
-    int* rows = reinterpret_cast<int*>(smem + C::BODY + 256);
-    const int n_keys = kend - kbeg;
-#pragma unroll 8
-    for (int j = lane; j < n_tiles * C::TILE; j += 32) {
-      const int t = __ldg(gi + min(j, n_keys - 1));
-      rows[j] = (int)(row0 + min(max(t, 0), s.cache_T - 1));
-    }
-    __syncwarp();
-    int issued = 0;
-    for (int it = 0; it < n_tiles; ++it) {
-      const int st = it % C::STAGES, use = it / C::STAGES;
-      int r[4];                                   // lane l < 16 copies tile rows 4l .. 4l + 3
-#pragma unroll
-      for (int e = 0; e < 4; ++e) r[e] = rows[it * C::TILE + (4 * lane + e) % C::TILE];
-      int ok = 1;
-      if (lane == 0) {
-        ok = it < C::STAGES || mbar_wait(&bars->empty[st], (use + 1) & 1, tmo, abort_flag);
-        if (ok) mbar_arrive_expect_tx(&bars->full[st], C::STAGE_BYTES);
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      ++issued;
-      if (lane < 16) {
-        unsigned char* dk = smem + st * C::STAGE_BYTES + lane * 512;
-        unsigned char* dv = dk + C::TILE_BYTES;
-#pragma unroll
-        for (int sl = 0; sl < C::SLABS; ++sl) {
-          tma_gather4(dk + sl * C::TILE * 128, &tm_k, &bars->full[st], 64 * sl, r[0], r[1], r[2], r[3]);
-          tma_gather4(dv + sl * C::TILE * 128, &tm_v, &bars->full[st], 64 * sl, r[0], r[1], r[2], r[3]);
-        }
-      }
-    }
-    if (lane == 0)
-      for (int k = max(0, issued - C::STAGES); k < issued; ++k)
-        mbar_wait(&bars->full[k % C::STAGES], (k / C::STAGES) & 1, tmo, nullptr);
+  if (warp == 4 && GATHER) {                      // the consumers load their own rows
     __syncthreads();
     return;
   }
@@ -226,9 +207,36 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   float l_part[2] = {0.0f, 0.0f};                 // this lane's share of the row sums
 
   const uint32_t sbase = smem_u32(smem);
+  // gathered form: copy this warp's 16 rows of tile t (K and V) into stage t % NST, as one group
+  auto gather_rows = [&](int t) {
+    if (t < n_tiles) {
+      constexpr int CH = D / 8, LPR = CH < 32 ? CH : 32, RPP = 32 / LPR;   // 16-byte pieces per row
+      const int pc = lane % LPR;
+      const uint32_t kst = sbase + (t % NST) * C::STAGE_BYTES;
+#pragma unroll
+      for (int p = 0; p < 16 / RPP; ++p) {
+        const int kt = 16 * warp + p * RPP + lane / LPR;                    // row of the tile
+        const size_t src = (size_t)rows[t * C::TILE + kt] * D + 8 * pc;
+        const uint32_t off = (pc >> 3) * (C::TILE * 128) + kt * 128 + (((pc & 7) ^ (kt & 7)) << 4);
+        cp_async_16(kst + off, s.gk + src);
+        cp_async_16(kst + C::TILE_BYTES + off, s.gv + src);
+      }
+    }
+    cp_async_commit();                            // empty groups past the end keep the count
+  };
+  if constexpr (GATHER) {
+#pragma unroll 1
+    for (int t = 0; t < NST - 1; ++t) gather_rows(t);
+  }
   for (int it = 0; it < n_tiles; ++it) {
-    const int st = it % C::STAGES;
-    if (!warp_wait(&bars->full[st], (it / C::STAGES) & 1, tmo, abort_flag)) break;
+    const int st = it % NST;
+    if constexpr (GATHER) {
+      gather_rows(it + NST - 1);                  // into the stage this warp finished last
+      cp_async_wait<NST - 1>();                   // tile it has landed
+      __syncwarp();
+    } else {
+      if (!warp_wait(&bars->full[st], (it / C::STAGES) & 1, tmo, abort_flag)) break;
+    }
     const uint32_t kb = sbase + st * C::STAGE_BYTES;
     const uint32_t vb = kb + C::TILE_BYTES;
     const int key0 = kbeg + it * C::TILE + 16 * warp;   // this warp's 16 keys
@@ -326,8 +334,9 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->empty[st]);
+    if (!GATHER && lane == 0) mbar_arrive(&bars->empty[st]);
   }
+  if constexpr (GATHER) cp_async_wait_all();
   // row sums of this warp
 #pragma unroll
   for (int row = 0; row < 2; ++row) {

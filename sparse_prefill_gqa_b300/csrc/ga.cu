@@ -63,20 +63,6 @@ bool make_map_bf16(CUtensorMap* map, const void* base, int cols, long long rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D bf16 map over a [rows, cols] row-major tensor with boxes of one row x 64 columns and the
-// 128-byte swizzle: the form that tile::gather4 copies (four rows chosen by index) take.
-bool make_map_rows_bf16(CUtensorMap* map, const void* base, int cols, long long rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename K>
 int set_smem(K kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess
@@ -528,12 +514,13 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
   ds.n_chunks = (topk + ds.chunk_len - 1) / ds.chunk_len;
   if (ds.n_chunks == 1) ds.chunk_len = (topk + 63) / 64 * 64;
   ds.gidx = idx; ds.gidx_stride = topk; ds.cache_T = Tk_max;
+  ds.gk = (const __nv_bfloat16*)k; ds.gv = (const __nv_bfloat16*)v;
   if (ds.chunk_len > kGatherMaxKeys) return GA_ERR_UNSUPPORTED;    // not reached: chunks are <= 4096 keys
   float* ws_o = need ? static_cast<float*>(workspace) : nullptr;
   float* ws_ml = need ? ws_o + (size_t)batch * n_heads * ds.n_chunks * d : nullptr;
-  CUtensorMap tk, tv;
-  const long long rows = (long long)batch * n_kv * Tk_max;
-  if (!make_map_rows_bf16(&tk, k, d, rows) || !make_map_rows_bf16(&tv, v, d, rows)) return GA_ERR_CUDA;
+  CUtensorMap tk, tv;                             // not read by the gathered form
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
   return launch_decode(d, tk, tv, (const __nv_bfloat16*)q, (__nv_bfloat16*)out, lse, ws_o, ws_ml, ds, stream,
                        /*gather=*/true);
 }

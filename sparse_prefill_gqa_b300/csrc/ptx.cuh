@@ -129,19 +129,14 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Four rows of a 2-D map, chosen by their row coordinates r0..r3, each from column x over the
-// box's width (the box is one row high); written to shared memory as four consecutive box rows
-// under the map's swizzle, which follows the shared-memory address, so copies placed at 512-byte
-// steps inside a 1024-byte-aligned tile lay the rows out exactly as one tile load would.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                            int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-      :: "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2),
-         "r"(r3), "r"(smem_u32(bar))
-      : "memory");
+// 16-byte asynchronous copy global -> shared through L2 only, and its group bookkeeping.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------------------
 // tcgen05: tensor memory, UMMA, commit, TMEM <-> register moves
