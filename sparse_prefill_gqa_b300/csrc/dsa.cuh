@@ -122,30 +122,24 @@ __device__ __forceinline__ uint32_t order_key(float x) {     // larger float -> 
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix of `flag` over the CTA in thread order and the CTA total; wsum: 32 ints.
-__device__ __forceinline__ int cta_prefix(bool flag, int* wsum, int& total) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t bal = __ballot_sync(0xffffffffu, flag);
-  if (lane == 0) wsum[warp] = __popc(bal);
-  __syncthreads();
-  int before = 0;
-  total = 0;
-  for (int w = 0; w < kTopkThreads / 32; ++w) {
-    if (w < warp) before += wsum[w];
-    total += wsum[w];
-  }
-  __syncthreads();
-  return before + __popc(bal & ((1u << lane) - 1u));
-}
-
-// grid: (batch); block: kTopkThreads.
+// grid: (batch); block: kTopkThreads (32 warps).
+//   radix select: per 8-bit digit, a histogram of the keys that match the digits chosen so far
+//     (increments aggregated per warp over equal bins: the scores are non-negative, so the top
+//     digit falls into one or two bins), then warp 0 finds the bin that holds the k-th largest
+//     key by a suffix scan, each lane covering 8 bins from the top;
+//   compaction: warp w owns a contiguous segment of the scores; a first sweep counts its keys
+//     above and equal to the k-th, a second writes its selected indices at its offset, which
+//     keeps the indices in increasing order with one barrier in all.
 __global__ void __launch_bounds__(kTopkThreads)
 topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__ lens, int L_max, int topk,
                    int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
+  constexpr int NW = kTopkThreads / 32;
   __shared__ int hist[256];
-  __shared__ int wsum[32];
+  __shared__ int w_gt[NW], w_eq[NW];
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lt_mask = (1u << lane) - 1u;
   const int b = blockIdx.x;
   const int L = seq_keys(lens, b, L_max);
   const float* row = scores + (size_t)b * L_max;
@@ -157,7 +151,7 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
     if (threadIdx.x == 0) n_sel[b] = L;
     return;
   }
-  // radix select of the k-th largest key
+  // ---- radix select of the k-th largest key ------------------------------------------------
   if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
@@ -165,33 +159,75 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
     for (int i = threadIdx.x; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix;
-    for (int j = threadIdx.x; j < L; j += kTopkThreads) {
-      const uint32_t key = order_key(row[j]);
-      if ((key & hi_mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFFu], 1);
+    for (int base = 0; base < L; base += kTopkThreads) {       // uniform trip count per warp
+      const int j = base + (int)threadIdx.x;
+      const uint32_t key = j < L ? order_key(row[j]) : 0u;
+      const bool in = j < L && (key & hi_mask) == prefix;
+      const uint32_t act = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        const int bin = (key >> shift) & 0xFF;
+        const uint32_t peers = __match_any_sync(act, bin);
+        if ((uint32_t)(__ffs(peers) - 1) == (uint32_t)lane) atomicAdd(&hist[bin], __popc(peers));
+      }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {                      // walk the bins from the top
-      int need = s_need, bin = 255;
-      while (bin > 0 && hist[bin] < need) { need -= hist[bin]; --bin; }
-      s_prefix = prefix | ((uint32_t)bin << shift);
-      s_need = need;                             // how many of this bin's keys are in the top k
+    if (warp == 0) {
+      // lane l covers bins 255 - 8l down to 248 - 8l; the chosen bin is the highest b >= 1 whose
+      // suffix count (keys in bins >= b) reaches `need`, else 0
+      const int need = s_need;
+      int cnt = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) cnt += hist[255 - 8 * lane - e];
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const uint32_t reach = __ballot_sync(0xffffffffu, incl >= need);
+      const int ls = reach ? __ffs(reach) - 1 : 31;
+      if (lane == ls) {
+        int running = incl - cnt;                // keys in the bins above this lane's
+        int bin = 255 - 8 * lane;
+        while (bin > 0 && running + hist[bin] < need) { running += hist[bin]; --bin; }
+        s_prefix = prefix | ((uint32_t)bin << shift);
+        s_need = need - running;                 // how many of this bin's keys are in the top k
+      }
     }
     __syncthreads();
   }
   const uint32_t kth = s_prefix;                 // the k-th largest key
   const int quota = s_need;                      // keys equal to kth that are kept
-  int eq_run = 0, out_run = 0;
-  for (int base = 0; base < L; base += kTopkThreads) {
-    const int j = base + (int)threadIdx.x;
-    const uint32_t key = j < L ? order_key(row[j]) : 0u;
-    const bool gt = j < L && key > kth, eq = j < L && key == kth;
-    int eq_tot, sel_tot;
-    const int eq_rank = eq_run + cta_prefix(eq, wsum, eq_tot);
-    const bool sel = gt || (eq && eq_rank < quota);
-    const int pos = out_run + cta_prefix(sel, wsum, sel_tot);
-    if (sel) out[pos] = j;
-    eq_run += eq_tot;
-    out_run += sel_tot;
+  // ---- ordered compaction over per-warp segments ------------------------------------------
+  const int seg = (L + kTopkThreads - 1) / kTopkThreads * 32;   // a multiple of 32 keys
+  const int j0 = warp * seg, j1 = min(L, j0 + seg);
+  int n_gt = 0, n_eq = 0;
+  for (int base = j0; base < j1; base += 32) {
+    const int j = base + lane;
+    const uint32_t key = j < j1 ? order_key(row[j]) : 0u;
+    n_gt += __popc(__ballot_sync(0xffffffffu, j < j1 && key > kth));
+    n_eq += __popc(__ballot_sync(0xffffffffu, j < j1 && key == kth));
+  }
+  if (lane == 0) { w_gt[warp] = n_gt; w_eq[warp] = n_eq; }
+  __syncthreads();
+  int gt_before = lane < warp ? w_gt[lane] : 0;
+  int eq_run = lane < warp ? w_eq[lane] : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gt_before += __shfl_xor_sync(0xffffffffu, gt_before, o);
+    eq_run += __shfl_xor_sync(0xffffffffu, eq_run, o);
+  }
+  int out_run = gt_before + min(eq_run, quota);
+  for (int base = j0; base < j1; base += 32) {
+    const int j = base + lane;
+    const uint32_t key = j < j1 ? order_key(row[j]) : 0u;
+    const bool gt = j < j1 && key > kth, eq = j < j1 && key == kth;
+    const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
+    const bool sel = gt || (eq && eq_run + __popc(eq_bal & lt_mask) < quota);
+    const uint32_t sel_bal = __ballot_sync(0xffffffffu, sel);
+    if (sel) out[out_run + __popc(sel_bal & lt_mask)] = j;
+    eq_run += __popc(eq_bal);
+    out_run += __popc(sel_bal);
   }
   for (int j = k + threadIdx.x; j < topk; j += kTopkThreads) out[j] = -1;
   if (threadIdx.x == 0) n_sel[b] = k;
