@@ -24,6 +24,15 @@
 
 namespace ga {
 
+// 16-byte asynchronous copy global -> shared through L2 only, and its group bookkeeping.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 template <int D>
 struct DecodeCfg {
   static constexpr int TILE = 64;                       // keys per stage
