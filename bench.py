@@ -371,7 +371,8 @@ def part_dsa(torch, ga, steps, warmup, flush, peaks):
                            "topk_ms": t_top, "gather_decode_ms": t_att, "selected_kv_bytes": sel_kv,
                            "gather_decode_GB/s": sel_kv / (t_att * 1e-3) / 1e9,
                            "gather_decode_frac_hbm": sel_kv / (t_att * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                           "dense_decode_ms": t_dense, "launches_per_step": 5}}
+                           "dense_decode_ms": t_dense,
+                           "launches_per_step": 4}}       # indexer, top-k, gathered decode, combine
 
 
 def part_mla(torch, ga, steps, warmup, flush, peaks):

@@ -131,3 +131,65 @@ def test_mla_rejects_invalid_arguments(L):
     assert L.ga_mla_decode(p, p, p, p, p, None, p, 0, 16, 64, p, 1 << 20, None) == ga.GA_ERR_INVALID_ARG
     assert L.ga_mla_decode(p, p, p, p, p, None, p, 1, 16, 64, p, 16, None) == ga.GA_ERR_WORKSPACE
     assert L.ga_mla_decode_workspace_size(1, 17, 64) == 2 ** 64 - 1
+
+
+def test_diff_rejects_invalid_arguments(L):
+    p = ctypes.c_void_p(4096)
+
+    def diff(**kw):
+        a = dict(q1=p, k1=p, q2=p, k2=p, v=p, out=p, batch=1, n_heads=8, n_kv=2, d=128, Tq=16, Tk=32,
+                 causal=1, window=0, lam=0.5, ws=p, wsb=1 << 20)
+        a.update(kw)
+        return L.ga_attend_diff(a["q1"], a["k1"], a["q2"], a["k2"], a["v"], a["out"], a["batch"], a["n_heads"],
+                                a["n_kv"], a["d"], a["Tq"], a["Tk"], None, a["causal"], a["window"], a["lam"],
+                                a["ws"], a["wsb"], None)
+    assert diff(q2=None) == ga.GA_ERR_INVALID_ARG
+    assert diff(lam=float("nan")) == ga.GA_ERR_INVALID_ARG
+    assert diff(lam=float("inf")) == ga.GA_ERR_INVALID_ARG
+    assert diff(Tq=33) == ga.GA_ERR_INVALID_ARG                      # Tk_max < Tq
+    assert diff(causal=0, window=4) == ga.GA_ERR_INVALID_ARG
+    assert diff(k2=ctypes.c_void_p(4104)) == ga.GA_ERR_INVALID_ARG   # not 16-byte aligned
+    assert diff(d=64) == ga.GA_ERR_UNSUPPORTED                       # tensor-core head dims only
+    assert diff(ws=None) == ga.GA_ERR_WORKSPACE
+    assert diff(wsb=1 * 8 * 16 * 128 * 4 - 1) == ga.GA_ERR_WORKSPACE  # A1 v in fp32 needs B*H*Tq*d*4
+    assert diff(ws=ctypes.c_void_p(4104)) == ga.GA_ERR_WORKSPACE
+
+
+def test_topk_sparse_decode_calls_reject_invalid_arguments(L):
+    p = ctypes.c_void_p(4096)
+    # ga_dsa_indexer(qi, wi, ki, lens, batch, n_idx_heads, di, L_max, scores, stream)
+    assert L.ga_dsa_indexer(p, p, p, None, 1, 8, 96, 64, p, None) == ga.GA_ERR_UNSUPPORTED   # di
+    assert L.ga_dsa_indexer(p, p, p, None, 1, 3, 128, 64, p, None) == ga.GA_ERR_UNSUPPORTED  # not 2^n
+    assert L.ga_dsa_indexer(p, p, p, None, 1, 32, 128, 64, p, None) == ga.GA_ERR_UNSUPPORTED  # > di/8
+    assert L.ga_dsa_indexer(p, p, p, None, 0, 8, 128, 64, p, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_dsa_indexer(p, p, p, None, 1, 8, 128, 0, p, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_dsa_indexer(p, p, p, None, 1, 8, 128, 64, None, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_dsa_indexer(ctypes.c_void_p(4104), p, p, None, 1, 8, 128, 64, p, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_dsa_indexer(p, ctypes.c_void_p(4098), p, None, 1, 8, 128, 64, p, None) == ga.GA_ERR_INVALID_ARG
+    # ga_topk_indices(scores, lens, batch, L_max, topk, idx, n_sel, stream)
+    assert L.ga_topk_indices(p, None, 1, 64, 0, p, p, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_topk_indices(p, None, 0, 64, 8, p, p, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_topk_indices(p, None, 1, 64, 8, None, p, None) == ga.GA_ERR_INVALID_ARG
+    assert L.ga_topk_indices(ctypes.c_void_p(4098), None, 1, 64, 8, p, p, None) == ga.GA_ERR_INVALID_ARG
+
+    def gather(**kw):
+        a = dict(q=p, k=p, v=p, out=p, batch=1, n_heads=8, n_kv=2, d=128, Tk=32768, idx=p, n_sel=p,
+                 topk=8192, sink=None, lse=None, ws=p, wsb=1 << 24)
+        a.update(kw)
+        return L.ga_attend_gather(a["q"], a["k"], a["v"], a["out"], a["batch"], a["n_heads"], a["n_kv"], a["d"],
+                                  a["Tk"], a["idx"], a["n_sel"], a["topk"], a["sink"], a["lse"], a["ws"],
+                                  a["wsb"], None)
+    assert gather(d=96) == ga.GA_ERR_UNSUPPORTED
+    assert gather(n_heads=64) == ga.GA_ERR_UNSUPPORTED                 # 32 query heads per kv head
+    assert gather(batch=2, n_kv=8, n_heads=8, Tk=1 << 28) == ga.GA_ERR_UNSUPPORTED   # 2^32 cache rows
+    assert gather(topk=0) == ga.GA_ERR_INVALID_ARG
+    assert gather(idx=None) == ga.GA_ERR_INVALID_ARG
+    assert gather(idx=ctypes.c_void_p(4098)) == ga.GA_ERR_INVALID_ARG
+    assert gather(n_sel=ctypes.c_void_p(4100)) == ga.GA_ERR_INVALID_ARG
+    assert gather(lse=ctypes.c_void_p(4100)) == ga.GA_ERR_INVALID_ARG
+    assert gather(ws=None) == ga.GA_ERR_WORKSPACE                      # 16 key chunks: partials needed
+    assert gather(wsb=16) == ga.GA_ERR_WORKSPACE
+    # the gathered decode needs only the split-K partials over topk keys
+    need = L.ga_attend_gather_workspace_size(1, 8, 2, 128, 8192)
+    assert need > 0 and need == L.ga_workspace_size(1, 8, 2, 128, 1, 8192, 1)
+    assert L.ga_attend_gather_workspace_size(1, 6, 4, 128, 8192) == 2 ** 64 - 1
