@@ -572,6 +572,20 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
 
 
 # ------------------------------------------------------------------------------ main
+def max_over_ranks(torch, dist, total_ms, device):
+    """The job's timed total: the slowest rank's (every rank waits at the closing barrier)."""
+    if dist is None:
+        return total_ms
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_step, steps, total_ms):
+    """Whole-job throughput: each of the `world` ranks runs its own replica of the step."""
+    return world * flops_step * steps / (total_ms * 1e-3) / 1e12
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -674,13 +688,9 @@ def main():
     if dist:
         dist.barrier()
     times = [a.elapsed_time(b_) for a, b_ in ev]
-    total_ms = sum(times)
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, dist, sum(times), "cuda")
     ms_per_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, args.steps, total_ms)
     kern_tflops = flops_step / (statistics.mean(times) * 1e-3) / 1e12
 
     # end to end: pinned host buffers, copies inside the timed region
