@@ -24,6 +24,7 @@ metric (the pages give no GPU implementation to run).
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import math
@@ -400,13 +401,22 @@ def part_mla(torch, ga, steps, warmup, flush, peaks):
                            "launches_per_step": 4}}
 
 
-def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
+OUTLIER_SCALES = {"8sqrtd": "8*sqrt(d)*u", "8": "8*u (literal)"}
+
+
+def planted_scale(name, d):
+    """Norm of the 128K workload's planted key under each reading of "8x a random unit direction"."""
+    return 8.0 * math.sqrt(d) if name == "8sqrtd" else 8.0
+
+
+def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False, outlier_scale="8sqrtd"):
     from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
     c = get_config(5)
     B, H, n_kv, d, T, qb, kb = c.batch, c.n_heads, c.n_kv, c.d, c.Tq, c.q_block, c.k_block
+    scale_used = planted_scale(outlier_scale, d)
     q = device_bf16(torch, c.seed, "q", (B, H, T, d))
     kbits = randn_bhtd(c.seed, "k", (B, n_kv, T, d), "bf16")
-    for kvh, blk, tok, vec in planted_outliers(c.seed, n_kv, T, d, kb, c.planted_fraction):
+    for kvh, blk, tok, vec in planted_outliers(c.seed, n_kv, T, d, kb, c.planted_fraction, scale=scale_used):
         kbits[0, kvh, tok] = f32_to_bf16_bits(vec)
     k = torch.from_numpy(kbits.view(np.int16)).view(torch.bfloat16).cuda()
     del kbits
@@ -476,6 +486,34 @@ def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False):
         recall = float((mask[0].bool() & target).sum()) / max(1, int(target.sum()))
         variants[name] = {"ms": tv, "tau_mean": tau_v, "density": density(), "planted_recall": recall}
     res["block_select_variants"] = variants
+    # Both readings of the planted key's scale: the same blocks, slots and directions at norm
+    # 8 sqrt(d) and at norm 8; the radius z-scores of the planted blocks (population statistics
+    # over each kv head's blocks, as the radius branch takes them) and the share it rescues.
+    try:
+        readings = {}
+        for name, label in OUTLIER_SCALES.items():
+            sc = planted_scale(name, d)
+            if sc == scale_used:
+                r = rad[0].double()
+            else:
+                plants = planted_outliers(c.seed, n_kv, T, d, kb, c.planted_fraction, scale=sc)
+                k_alt = k.clone()
+                kv_i = torch.tensor([p[0] for p in plants], device="cuda")
+                tok_i = torch.tensor([p[2] for p in plants], device="cuda")
+                bits = np.stack([f32_to_bf16_bits(p[3]) for p in plants]).view(np.int16)
+                k_alt[0, kv_i, tok_i] = torch.from_numpy(bits).view(torch.bfloat16).cuda()
+                cen_alt, rad_alt = torch.empty_like(cen), torch.empty_like(rad)
+                ga.ga_block_stats(k_alt, kb, centroid=cen_alt, radius=rad_alt)
+                r = rad_alt[0].double()
+                del k_alt, cen_alt, rad_alt
+            z = (r - r.mean(dim=1, keepdim=True)) / r.std(dim=1, correction=0, keepdim=True)
+            zp = z[planted]
+            readings[label] = {"planted_z_mean": float(zp.mean()), "planted_z_min": float(zp.min()),
+                               "rescued_at_lambda": float((zp >= lam).double().mean())}
+        res["planted_key_scale"] = {"in_use": OUTLIER_SCALES[outlier_scale], "lambda_radius": lam,
+                                    "readings": readings}
+    except Exception as e:  # report, never hide
+        res["planted_key_scale"] = {"error": repr(e)}
     if select_only:
         return res
     # tau for target densities (bisection on the measured density)
@@ -566,7 +604,8 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
     elif args.case == "mla":
         res = part_mla(torch, ga, args.steps, warmup, flush, peaks)
     else:
-        res = part_sparse(torch, ga, args.steps, warmup, flush, peaks, select_only=args.case == "select")
+        res = part_sparse(torch, ga, args.steps, warmup, flush, peaks, select_only=args.case == "select",
+                          outlier_scale=args.outlier_scale)
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": warmup, **res}))
     return 0
 
@@ -597,6 +636,8 @@ def main():
     ap.add_argument("--case", default="all",
                     choices=["all", "prefill", "decode", "chunk", "window", "ring", "diff", "dsa", "mla", "sparse", "select"],
                     help="run one workload alone and print its own JSON line (for profiling)")
+    ap.add_argument("--outlier-scale", default="8sqrtd", choices=sorted(OUTLIER_SCALES),
+                    help="norm of the 128K workload's planted keys: 8*sqrt(d) (default) or the literal 8")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --case prefill/decode/chunk: a smaller batch (profiling captures)")
     args = ap.parse_args()
@@ -737,7 +778,7 @@ def main():
         ps, pw = max(3, min(20, args.steps // 4)), 3
         for name, fn in (("decode_chunk", part_decode_and_chunk), ("window_sink", part_window_sink),
                          ("ring", part_ring), ("diff", part_diff), ("dsa", part_dsa), ("mla", part_mla),
-                         ("sparse_128k", part_sparse)):
+                         ("sparse_128k", functools.partial(part_sparse, outlier_scale=args.outlier_scale))):
             try:
                 parts.update(fn(torch, ga, ps, pw, flush, peaks))
             except Exception as e:  # report, never hide

@@ -290,3 +290,31 @@ def test_group_shared_selection():
     ref = _brute_select(pooled, c, r, T, qb, kb, 0, 0.05, 2.0)
     for h in range(n_kv * g):
         assert np.array_equal(m[0, h], ref[0, h // g])
+
+
+def test_planted_key_scale_reading():
+    """The 128K workload's planted key, two readings of "8x a random unit direction": the literal
+    8 u has norm 8, under an ordinary N(0, I) key's norm of about sqrt(d), so it sits inside its
+    block's radius and the radius branch (z >= 3) rescues none of the planted blocks; the reading
+    taken, 8 sqrt(d) u, lifts every planted block's radius out of the distribution, and the
+    blocks at z >= 3 are then exactly the planted ones (the outliers themselves widen sigma, so
+    their z stays near 4.5 at 5 % of blocks)."""
+    from workloads import planted_outliers
+    n_kv, T, d, kb = 1, 8192, 128, 64
+    base = np.random.default_rng(181).standard_normal((1, n_kv, T, d))
+    rescued = {}
+    for name, scale in (("literal", 8.0), ("taken", None)):
+        k = base.copy()
+        planted = planted_outliers(182, n_kv, T, d, kb, 0.05, scale=scale)
+        for kvh, blk, tok, vec in planted:
+            k[0, kvh, tok] = vec
+        _, radius = block_stats(k, k_block=kb)
+        z = radius_zscores(radius[0, 0], "z")
+        blocks = [blk for _, blk, _, _ in planted]
+        rescued[name] = float(np.mean(z[blocks] >= 3.0))
+        if name == "literal":
+            assert np.max(z[blocks]) < 3.0
+        else:
+            assert np.min(z[blocks]) > 4.0
+            assert set(np.flatnonzero(z >= 3.0).tolist()) == set(blocks)
+    assert rescued == {"literal": 0.0, "taken": 1.0}
