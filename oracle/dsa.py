@@ -57,6 +57,8 @@ def sparse_attend(q, k, v, scores, topk: int, sink=None):
         i = L - T + t                                       # absolute position of row t
         keep = topk_indices(scores[t], np.arange(L) <= i, topk)
         reads[t] = keep.size
+        if keep.size == 0:            # no token to read (an empty cache): the row stays 0, as
+            continue                  # attend leaves a row with no allowed key
         for h in range(H):
             s = k[h // g, keep] @ q[h, t] / math.sqrt(d)
             m = s.max() if sink is None else max(s.max(), float(sink[h]))

@@ -68,3 +68,22 @@ def test_dsa_decode_is_the_last_row():
         ref, _ = sparse_attend(q[b], k[b, :, :L], v[b, :, :L], sc, kk)
         assert np.max(np.abs(out[b] - ref)) <= 1e-14
         assert chosen[b].size == min(kk, L)
+
+
+def test_empty_cache_gives_a_zero_row_like_attend():
+    """A sequence with no cached token reads nothing: its row is 0 with or without a sink, the
+    convention attend follows for a row with no allowed key (checked here against attend with
+    an all-zero block mask); the other sequence is unaffected."""
+    B, H, n_kv, Lm, d, Hi, di, kk = 2, 4, 2, 30, 8, 3, 4, 7
+    q = _rand((B, H, 1, d), 421)
+    k, v = _rand((B, n_kv, Lm, d), 422), _rand((B, n_kv, Lm, d), 423)
+    qi, ki, wi = _rand((B, Hi, di), 424), _rand((B, Lm, di), 425), _rand((B, Hi), 426)
+    sink = np.array([0.5, -1.0, 0.25, 2.0])
+    for sk in (None, sink):
+        out, chosen = dsa_decode(q, k, v, qi, ki, wi, [30, 0], kk, sink=sk)
+        assert chosen[1].size == 0 and np.all(out[1] == 0.0)
+        none, _ = attend(q[1:2], k[1:2], v[1:2], causal=False, sink=sk,
+                         block_mask=np.zeros((1, H, 1, 1), dtype=bool), q_block=1, k_block=Lm)
+        assert np.array_equal(out[1:2], none)
+        ref, _ = dsa_decode(q[:1], k[:1], v[:1], qi[:1], ki[:1], wi[:1], [30], kk, sink=sk)
+        assert np.array_equal(out[:1], ref)
