@@ -112,7 +112,21 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   const int Tk = seq_keys(s.a.k_lens, b, s.a.Tk_max);
   int kbeg, kend;
   decode_chunk_range(s, Tk, c, kbeg, kend);
-  if (kbeg >= kend) return;                       // chunk holds no usable key (uniform)
+  if (kbeg >= kend) {                             // chunk holds no usable key (uniform)
+    // Only an empty sequence (Tk = 0) leaves every chunk without keys.  With several chunks
+    // the combine writes its rows; as the only chunk, this CTA does: no allowed key, so
+    // out = 0 and lse = the sink's logit (or -inf).
+    if (s.n_chunks == 1) {
+      for (int e = threadIdx.x; e < s.rows * D; e += C::THREADS) {
+        const int m = e / D, dim = e % D;
+        const int hh = kvh * s.g + m % s.g;
+        const size_t qrow = ((size_t)b * s.a.n_heads + hh) * s.a.Tq + m / s.g;
+        out[qrow * D + dim] = __float2bfloat16_rn(0.0f);
+        if (lse && dim == 0) lse[qrow] = s.a.sink ? s.a.sink[hh] : -INFINITY;
+      }
+    }
+    return;
+  }
   const int n_tiles = (kend - kbeg + C::TILE - 1) / C::TILE;
   const uint64_t tmo = s.a.timeout_ns;
 

@@ -139,3 +139,23 @@ def test_dsa_full_size_sampled():
         expect, _ = oracle.attend(qr[b:b + 1], f64(kb[b:b + 1, :, chosen]), f64(vb[b:b + 1, :, chosen]),
                                   causal=False)
         assert_close(to_f64(out[b:b + 1]), expect, "bf16", f"dsa full size b={b}")
+
+
+@pytest.mark.parametrize("Lm,topk", [(500, 64), (6000, 5000)])   # one key chunk; ten chunks + combine
+def test_dsa_decode_empty_cache_row_is_zero(Lm, topk):
+    """A sequence with no cached token: the indexer scores -inf, top-k selects nothing, and the
+    gathered decode writes a zero row (the sink carries no value); the other sequence is exact."""
+    B, H, n_kv, d = 2, 8, 2, 128
+    dev, ref = _decode_inputs(B, H, n_kv, Lm, d, 8, 128, seed=551)
+    q, k, v, qi, wi, ki = dev
+    qr, kr, vr, qir, kir, wr = ref
+    lens = [Lm, 0]
+    skr = np.linspace(-1.0, 1.0, H).astype(np.float32)
+    out, idx, n_sel, scores = ga.dsa_decode(q, k, v, qi, wi, ki, topk,
+                                            torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                            sink=torch.from_numpy(skr).cuda())
+    assert ga.ga_read_device_status() == ga.GA_OK
+    assert n_sel.cpu().tolist() == [min(topk, Lm), 0]
+    assert torch.all(out[1] == 0)
+    expect, _ = oracle.dsa_decode(qr, kr, vr, qir, kir, wr, lens, topk, sink=skr, scores=to_f64(scores))
+    assert_close(to_f64(out), expect, "bf16", "dsa empty cache")
