@@ -192,8 +192,10 @@ size_t ga_attend_gather_workspace_size(int batch, int n_heads, int n_kv, int d, 
  * ga_attend_gather -- decode attention of q [batch, n_heads, 1, d] over the cached tokens
  *   idx[b, 0 .. n_sel[b]-1] of k, v [batch, n_kv, Tk_max, d] (bf16): softmax over exactly
  *   those keys (plus the optional sink), for every head of the sequence.  The split-K decode
- *   reads the selected rows straight from the cache; no compact copy is made.  idx entries must lie in [0, Tk_max) (others are clamped into it);
- *   idx 4-byte aligned, n_sel, lse and sink 16-byte aligned.
+ *   reads the selected rows straight from the cache; no compact copy is made.  n_sel[b] = 0
+ *   (an empty cache) gives a zero row, and lse = the sink's logit or -inf.  idx entries must
+ *   lie in [0, Tk_max) (others are clamped into it); idx 4-byte aligned, n_sel, lse and sink
+ *   16-byte aligned.
  *   d: 64, 128 or 256; n_heads / n_kv <= 16; batch * n_kv * Tk_max < 2^31 (GA_ERR_UNSUPPORTED
  *   otherwise).  sink, lse as in ga_attend.
  */

@@ -631,11 +631,11 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
     const dim3 vgrid((unsigned)n_cta);
     const __nv_bfloat16* kp = (const __nv_bfloat16*)k;
     if (k_block <= 64 && (d == 32 || d == 64 || d == 128)) {   // block held in registers: one read
-      switch (d / 8) {
-        case 4: block_stats_reg_kernel<4><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
-        case 8: block_stats_reg_kernel<8><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
-        default: block_stats_reg_kernel<16><<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid, radius); break;
-      }
+      const auto kern = d == 32 ? block_stats_reg_kernel<4>
+                      : d == 64 ? block_stats_reg_kernel<8>
+                                : block_stats_reg_kernel<16>;
+      kern<<<vgrid, 32 * kStatsVecWarps, 0, stream>>>(kp, k_lens, batch, n_kv, Tk_max, k_block, nKb, centroid,
+                                                      radius);
       return launch_status();
     }
     switch (d / 8) {
