@@ -214,7 +214,9 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
  *   q_nope   device bf16 [batch, n_heads, 128];  q_rope: [batch, n_heads, 64].
  *   latent   device bf16 [batch, L_max, 576]: per token c_kv (512) then k_rope (64).
  *   w_uk     device bf16 [n_heads, 512, 128];  w_uv: [n_heads, 512, 128].
- *   lens     device int32 [batch] (clamped to [0, L_max]) or NULL (= L_max).
+ *   lens     device int32 [batch]: tokens cached, the new token's latent included, so
+ *            1..L_max (larger values are clamped to L_max; 0 leaves the row undefined);
+ *            or NULL (= L_max).
  *   out      device bf16 [batch, n_heads, 128].
  *   workspace of ga_mla_decode_workspace_size(batch, n_heads, L_max) bytes, 16-byte aligned.
  *   n_heads <= 16 (GA_ERR_UNSUPPORTED otherwise).  q_lat is rounded to bf16 before the scores.
