@@ -326,3 +326,34 @@ def test_empty_rows_and_block_mask_expansion():
     fine = np.repeat(np.repeat(bm, 4, axis=2), 4, axis=3)
     o3, _ = attend(q, k, v, causal=True, block_mask=fine, q_block=1, k_block=1)
     assert np.array_equal(o3, o)
+
+
+def test_padding_mask_example_is_the_key_length_mask():
+    """"Attention Masking" Example 1: the batch [[1, 2, 3, 0], [4, 5, 0, 0]] (id 0 = padding) has
+    the padding pattern of key lengths 3 and 2, and attention with those lengths equals the guide's
+    form -- -1e9 added to the padded keys' scores before the softmax -- written out with NumPy
+    (e^-1e9 underflows to exactly 0 in float64)."""
+    sec, cur = {}, None
+    for line in open(os.path.join(GOLDEN, "padding_mask_example1.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line.startswith("["):
+            cur = line[1:-1]
+            sec[cur] = []
+        else:
+            sec[cur].append(line)
+    ids = np.array([[int(x) for x in row.split()] for row in sec["input_ids"]])
+    keys = np.array([[c == "1" for c in row] for row in sec["keys"]])
+    assert np.array_equal(ids != 0, keys)
+    lens = keys.sum(axis=1)
+    assert lens.tolist() == [3, 2]
+    B, H, T, d = 2, 4, 4, 8
+    # two query rows (the boundary keeps Tq <= each sequence's key count) over the padded keys
+    q, k, v = _rand((B, H, 2, d), 191), _rand((B, 2, T, d), 192), _rand((B, 2, T, d), 193)
+    ours, _ = attend(q, k, v, k_lens=lens, causal=False)
+    kk, vv = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)             # GQA: head h reads kv h // 2
+    s = q @ np.swapaxes(kk, -1, -2) / math.sqrt(d) + np.where(keys, 0.0, -1e9)[:, None, None, :]
+    p = np.exp(s - s.max(axis=-1, keepdims=True))
+    guide = (p / p.sum(axis=-1, keepdims=True)) @ vv
+    assert np.max(np.abs(ours - guide)) <= 1e-14
