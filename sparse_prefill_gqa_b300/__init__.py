@@ -142,6 +142,23 @@ def _need(t, name, dtype=None, dims=None):
         raise ValueError(f"{name} must have {dims} dimensions")
 
 
+def _need_size(t, name, n):
+    """The kernels index ``t`` up to ``n`` elements: a shorter tensor is refused."""
+    if t.numel() < n:
+        raise ValueError(f"{name} must hold at least {n} elements (it holds {t.numel()})")
+
+
+def _need_out(t, name, dtype, shape):
+    _need(t, name, dtype, len(shape))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}")
+
+
+def _need_ws(t):
+    if t is not None:
+        _need(t, "workspace")
+
+
 def ga_workspace_size(batch, n_heads, n_kv, d, Tq, Tk_max, dtype) -> int:
     return int(lib().ga_workspace_size(batch, n_heads, n_kv, d, Tq, Tk_max, _DTYPES[dtype]))
 
@@ -166,15 +183,20 @@ def ga_attend(q, k, v, out=None, *, k_lens=None, causal=True, window=0, sink=Non
         raise ValueError("k and v must be [batch, n_kv, Tk_max, d] matching q")
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", q.dtype, 4)
+    _need_out(out, "out", q.dtype, q.shape)
     if k_lens is not None:
         _need(k_lens, "k_lens", torch.int32, 1)
+        _need_size(k_lens, "k_lens", B)
     if sink is not None:
         _need(sink, "sink", torch.float32, 1)
+        _need_size(sink, "sink", H)
     if block_mask is not None:
         _need(block_mask, "block_mask", torch.uint8, 4)
+        _need_size(block_mask, "block_mask", B * H * -(-Tq // max(1, q_block)) * -(-Tk_max // max(1, k_block)))
     if lse is not None:
         _need(lse, "lse", torch.float32, 3)
+        _need_size(lse, "lse", B * H * Tq)
+    _need_ws(workspace)
     need = ga_workspace_size(B, H, n_kv, d, Tq, Tk_max, q.dtype) if H % max(n_kv, 1) == 0 else 0
     if need == 2 ** 64 - 1:
         need = 0
@@ -205,13 +227,16 @@ def ga_attend_decode_static(q, k, v, out=None, *, k_lens=None, causal=True, wind
         raise ValueError("k and v must be [batch, n_kv, Tk_max, d] matching q")
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, 4)
+    _need_out(out, "out", torch.bfloat16, q.shape)
     if k_lens is not None:
         _need(k_lens, "k_lens", torch.int32, 1)
+        _need_size(k_lens, "k_lens", B)
     if sink is not None:
         _need(sink, "sink", torch.float32, 1)
+        _need_size(sink, "sink", H)
     if lse is not None:
         _need(lse, "lse", torch.float32, 3)
+        _need_size(lse, "lse", B * H * Tq)
     st = L.ga_attend_decode_static(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tq, Tk_max,
                                    _ptr(k_lens), int(bool(causal)), int(window), _ptr(sink), _ptr(lse),
                                    _stream(stream))
@@ -233,9 +258,11 @@ def ga_attend_diff(q1, k1, q2, k2, v, lam, out=None, *, k_lens=None, causal=True
         raise ValueError("q1, q2 [B, H, Tq, d]; k1, k2, v [B, n_kv, Tk_max, d]")
     if out is None:
         out = torch.empty_like(q1)
-    _need(out, "out", torch.bfloat16, 4)
+    _need_out(out, "out", torch.bfloat16, q1.shape)
     if k_lens is not None:
         _need(k_lens, "k_lens", torch.int32, 1)
+        _need_size(k_lens, "k_lens", B)
+    _need_ws(workspace)
     need = B * H * Tq * d * 4
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q1.device)
@@ -260,9 +287,10 @@ def ga_dsa_indexer(qi, wi, ki, lens=None, scores=None, *, stream=None):
         raise ValueError("qi [B, Hi, di], ki [B, L_max, di], wi [B, Hi]")
     if lens is not None:
         _need(lens, "lens", torch.int32, 1)
+        _need_size(lens, "lens", B)
     if scores is None:
         scores = torch.empty(B, L_max, dtype=torch.float32, device=qi.device)
-    _need(scores, "scores", torch.float32, 2)
+    _need_out(scores, "scores", torch.float32, (B, L_max))
     _check(L.ga_dsa_indexer(_ptr(qi), _ptr(wi), _ptr(ki), _ptr(lens), B, Hi, di, L_max, _ptr(scores),
                             _stream(stream)), "ga_dsa_indexer")
     return scores
@@ -276,10 +304,14 @@ def ga_topk_indices(scores, topk, lens=None, idx=None, n_sel=None, *, stream=Non
     B, L_max = scores.shape
     if lens is not None:
         _need(lens, "lens", torch.int32, 1)
+        _need_size(lens, "lens", B)
     if idx is None:
         idx = torch.empty(B, topk, dtype=torch.int32, device=scores.device)
     if n_sel is None:
         n_sel = torch.empty(B, dtype=torch.int32, device=scores.device)
+    _need_out(idx, "idx", torch.int32, (B, int(topk)))
+    _need(n_sel, "n_sel", torch.int32, 1)
+    _need_size(n_sel, "n_sel", B)
     _check(L.ga_topk_indices(_ptr(scores), _ptr(lens), B, L_max, int(topk), _ptr(idx), _ptr(n_sel),
                              _stream(stream)), "ga_topk_indices")
     return idx, n_sel
@@ -297,12 +329,17 @@ def ga_attend_gather(q, k, v, idx, n_sel, out=None, *, sink=None, lse=None, work
     topk = idx.shape[1]
     if Tq != 1 or v.shape != k.shape or idx.shape[0] != B:
         raise ValueError("q [B, H, 1, d], k, v [B, n_kv, Tk_max, d], idx [B, topk]")
+    _need_size(n_sel, "n_sel", B)
     if out is None:
         out = torch.empty_like(q)
+    _need_out(out, "out", torch.bfloat16, q.shape)
     if sink is not None:
         _need(sink, "sink", torch.float32, 1)
+        _need_size(sink, "sink", H)
     if lse is not None:
         _need(lse, "lse", torch.float32, 3)
+        _need_size(lse, "lse", B * H)
+    _need_ws(workspace)
     need = int(L.ga_attend_gather_workspace_size(B, H, n_kv, d, topk))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -337,8 +374,11 @@ def ga_mla_decode(q_nope, q_rope, latent, w_uk, w_uv, lens=None, out=None, *, wo
         raise ValueError("MLA shapes: q_nope [B,H,128], q_rope [B,H,64], latent [B,L,576], w_uk/w_uv [H,512,128]")
     if lens is not None:
         _need(lens, "lens", torch.int32, 1)
+        _need_size(lens, "lens", B)
     if out is None:
         out = torch.empty(B, H, 128, dtype=torch.bfloat16, device=q_nope.device)
+    _need_out(out, "out", torch.bfloat16, (B, H, 128))
+    _need_ws(workspace)
     need = int(L.ga_mla_decode_workspace_size(B, H, L_max))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q_nope.device)
@@ -381,11 +421,14 @@ def ga_attend_ring(q, k_ring, v_ring, n_seen, out=None, *, sink=None, lse=None, 
         raise ValueError("q [B, n_heads, 1, d], rings [B, n_kv, W, d], n_seen [B]")
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, 4)
+    _need_out(out, "out", torch.bfloat16, q.shape)
     if sink is not None:
         _need(sink, "sink", torch.float32, 1)
+        _need_size(sink, "sink", H)
     if lse is not None:
         _need(lse, "lse", torch.float32, 3)
+        _need_size(lse, "lse", B * H)
+    _need_ws(workspace)
     need = ga_workspace_size(B, H, n_kv, d, 1, W, q.dtype) if H % max(n_kv, 1) == 0 else 0
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -400,6 +443,8 @@ def ga_block_stats(k, k_block=64, *, k_lens=None, centroid=None, radius=None, st
     """Centroid [B, n_kv, nKb, d] and maximum radius [B, n_kv, nKb] of every key block."""
     L = lib()
     _need(k, "k", None, 4)
+    if k.dtype not in _DTYPES:
+        raise ValueError("k must be float32 or bfloat16")
     B, n_kv, Tk_max, d = k.shape
     nKb = -(-Tk_max // k_block)
     if centroid is None:
@@ -407,9 +452,12 @@ def ga_block_stats(k, k_block=64, *, k_lens=None, centroid=None, radius=None, st
     if radius is None:
         radius = torch.empty(B, n_kv, nKb, dtype=torch.float32, device=k.device)
     _need(centroid, "centroid", torch.float32, 4)
+    _need_size(centroid, "centroid", B * n_kv * nKb * d)
     _need(radius, "radius", torch.float32, 3)
+    _need_size(radius, "radius", B * n_kv * nKb)
     if k_lens is not None:
         _need(k_lens, "k_lens", torch.int32, 1)
+        _need_size(k_lens, "k_lens", B)
     st = L.ga_block_stats(_ptr(k), _ptr(k_lens), B, n_kv, d, Tk_max, int(k_block), _ptr(centroid),
                           _ptr(radius), _DTYPES[k.dtype], _stream(stream))
     _check(st, "ga_block_stats")
@@ -427,15 +475,25 @@ def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, c
     group_shared: one selection per kv head from its heads' pooled query rows."""
     L = lib()
     _need(q, "q", None, 4)
+    if q.dtype not in _DTYPES:
+        raise ValueError("q must be float32 or bfloat16")
+    _need(centroid, "centroid", torch.float32, 4)
+    _need(radius, "radius", torch.float32, 3)
     B, H, Tq, d = q.shape
     n_kv = centroid.shape[1] if n_kv is None else n_kv
     nKb_out = centroid.shape[2]
     Tk = nKb_out * k_block if Tk is None else Tk
     nQb = -(-Tq // q_block)
+    _need_size(centroid, "centroid", B * n_kv * nKb_out * d)
+    _need_size(radius, "radius", B * n_kv * nKb_out)
     if block_mask is None:
         block_mask = torch.empty(B, H, nQb, nKb_out, dtype=torch.uint8, device=q.device)
     if n_selected is None:
         n_selected = torch.empty(B, H, nQb, dtype=torch.int32, device=q.device)
+    _need(block_mask, "block_mask", torch.uint8, 4)
+    _need_size(block_mask, "block_mask", B * H * nQb * nKb_out)
+    _need(n_selected, "n_selected", torch.int32, 3)
+    _need_size(n_selected, "n_selected", B * H * nQb)
     rule = {"z": GA_RADIUS_ZSCORE, "mad": GA_RADIUS_MAD}[radius_rule]
     tb = -math.inf if tau_bound is None else float(tau_bound)
     st = L.ga_select_blocks_ex(_ptr(q), _ptr(centroid), _ptr(radius), B, H, n_kv, d, Tq, int(Tk),
