@@ -454,7 +454,9 @@ def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False, outli
     tsel = timed_steps(torch, lambda: select(0.05), steps, warmup, flush)
     sel_bytes = q.numel() * 2 + cen.numel() * 4 + mask.numel()
     res["block_select"] = {"ms": statistics.mean(tsel),
-                           "GB/s": sel_bytes / (statistics.mean(tsel) * 1e-3) / 1e9}
+                           "GB/s": sel_bytes / (statistics.mean(tsel) * 1e-3) / 1e9,
+                           "frac_hbm": sel_bytes / (statistics.mean(tsel) * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "algorithmic_bytes": sel_bytes}
     # Selection variants at tau_mean = 0.02 (about density 0.1): the mean branch alone, with the
     # radius rescue (z-score or median/MAD, lambda from the workload), and with the bound branch
     # as the rescue instead (bound >= best mean score + 3, no radius branch); time, density and
@@ -553,14 +555,18 @@ def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False, outli
 
 
 # ------------------------------------------------------------------------------ CPU oracle
-def cpu_oracle_timed(budget_s):
+def cpu_oracle_timed(budget_s=None, n_pairs=None):
+    """The float64 oracle on 256 sampled query rows of (batch, head) pairs of the dense causal
+    workload, one pair after another, until ``budget_s`` seconds of oracle time or ``n_pairs``
+    pairs.  Returns (TFLOP/s on the sampled rows, cores, sample text, oracle seconds, pairs)."""
     import oracle
     from workloads import get_config, normal_slices, bf16_bits_to_f32, sample_rows
     cores = len(os.sched_getaffinity(0))
     c = get_config(2)
     rows = sample_rows(c.Tq, 256, seed=c.seed)
+    limit = c.batch * c.n_heads if n_pairs is None else min(n_pairs, c.batch * c.n_heads)
     tot_flops, tot_time, heads = 0, 0.0, 0
-    while tot_time < budget_s and heads < c.batch * c.n_heads:
+    while heads < limit and (budget_s is None or tot_time < budget_s):
         b, h = divmod(heads, c.n_heads)
         kvh = h // c.g
         q = bf16_bits_to_f32(normal_slices(c.seed, "q", b, h, c.Tq, c.d))[None, None].astype(np.float64)
@@ -573,7 +579,80 @@ def cpu_oracle_timed(budget_s):
         heads += 1
     sample = (f"{heads} (batch, head) pairs x {len(rows)} sampled query rows of the B2 H32 Hkv8 d128 "
               f"T8192 causal workload through the float64 NumPy oracle (input generation excluded)")
-    return tot_flops / tot_time / 1e12, cores, sample, tot_time
+    return tot_flops / tot_time / 1e12, cores, sample, tot_time, heads
+
+
+def reference_arm(args, warmup, flops_step, workload):
+    """--impl reference: the oracle, as it stands, on the host cores.  A step is a fixed sample
+    (256 rows of each of P (batch, head) pairs), P chosen from one timed pair so that the
+    warm-up and timed steps together take about two minutes; ms_per_step is that step's
+    measured wall time, and the full workload's time is reported apart, as an extrapolation."""
+    per_pair = cpu_oracle_timed(n_pairs=1)[3]
+    n_steps = warmup + args.steps
+    pairs = int(max(1, min(64, 120.0 / max(1, n_steps) / max(per_pair, 1e-3))))
+    vals, walls = [], []
+    cores, sample = 0, ""
+    for i in range(n_steps):
+        t0 = time.perf_counter()
+        v, cores, sample, _, _ = cpu_oracle_timed(n_pairs=pairs)
+        wall = (time.perf_counter() - t0) * 1e3
+        if i >= warmup:
+            vals.append(v)
+            walls.append(wall)
+    val = statistics.mean(vals)
+    ms_step = statistics.mean(walls)
+    sample += f"; one step = these {pairs} pairs, {ms_step / 1e3:.2f} s wall per step (input generation included)"
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded PCG64 N(0,1), cast to bf16 on the host, upcast to f64)",
+            "config": workload,
+            "extrapolated_full_step_ms": {"value": flops_step / (val * 1e12) * 1e3,
+                                          "what": "an extrapolation, not a measurement: the whole B2 H32 "
+                                                  "T8192 step's FLOPs at the sampled rows' rate"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _r(x, n=4):
+    """x rounded to n significant digits (None stays None)."""
+    if x is None or not isinstance(x, (int, float)) or not math.isfinite(x):
+        return x
+    return float(f"{x:.{n}g}")
+
+
+def targets_summary(line, peaks):
+    """The per-workload figures the targets are judged on, in one short object (printed last,
+    so that a reader of the line's tail sees them): TFLOP/s and GB/s with their fractions of
+    the measured burst peaks."""
+    p = line.get("parts", {})
+    bf, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    def g(part, key):
+        d = p.get(part)
+        return d.get(key) if isinstance(d, dict) else None
+    t = {"prefill_TFLOPs": _r(line["roofline"]["achieved"]), "prefill_frac": _r(line["roofline"]["frac"], 3)}
+    for key, part in (("decode", "decode"), ("ring", "ring_decode")):
+        gbs = g(part, "GB/s")
+        t[key + "_GBs"] = _r(gbs)
+        t[key + "_frac"] = _r(gbs / hbm, 3) if gbs else None
+    for key, part in (("chunk", "chunk"), ("window", "window"), ("full", "full_causal"), ("diff", "diff_attention")):
+        tf = g(part, "TFLOP/s")
+        t[key + "_TFLOPs"] = _r(tf)
+        t[key + "_frac"] = _r(tf / bf, 3) if tf else None
+    t["composite_TFLOPs"] = _r(g("composite_5to1", "TFLOP/s"))
+    t["stats_frac"] = _r(g("block_stats", "frac_hbm"), 3)
+    t["select_ms"] = _r(g("block_select", "ms"), 3)
+    t["select_frac"] = _r(g("block_select", "frac_hbm"), 3)
+    sp = p.get("sparse_attention", {})
+    if isinstance(sp, dict) and sp.get("sweep"):
+        t["sparse_r2"] = _r(sp.get("r2"), 3)
+        t["sparse_ratio_0.1"] = _r(sp.get("sparse_over_dense_at_0.1"), 3)
+        t["sparse_TFLOPs_by_density"] = {f"{s['density']:.2f}": _r(s["TFLOP/s"]) for s in sp["sweep"]}
+    t["dsa_ms"] = _r(g("dsa_decode", "ms"), 3)
+    t["gather_frac"] = _r(g("dsa_decode", "gather_decode_frac_hbm"), 3)
+    t["mla_frac"] = _r(g("mla_decode", "frac_hbm"), 3)
+    t["peaks"] = f"measured burst: {hbm:g} GB/s, {bf:g} TFLOP/s bf16"
+    return t
 
 
 # ------------------------------------------------------------------------------ one case
@@ -658,24 +737,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + warmup)))
-        vals = []
-        cores = 0
-        sample = ""
-        for i in range(warmup + args.steps):
-            v, cores, sample, _ = cpu_oracle_timed(budget)
-            if i >= warmup:
-                vals.append(v)
-        val = statistics.mean(vals)
-        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": warmup, "ms_per_step": flops_step / (val * 1e12) * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic (seeded PCG64 N(0,1), cast to bf16 on the host, upcast to f64)",
-                "config": workload,
-                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                                 "sample": sample + f"; about {budget:.0f} s of oracle time per step"},
-                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        print(json.dumps(reference_arm(args, warmup, flops_step, workload)))
         return 0
 
     import torch
@@ -786,9 +848,12 @@ def main():
             torch.cuda.empty_cache()
         line["parts"] = parts
     if not args.no_cpu_baseline:
-        val, cores, sample, _ = cpu_oracle_timed(12.0)
+        val, cores, sample, _, _ = cpu_oracle_timed(12.0, 64)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
+    if "parts" in line:                       # the parts last but one, the short summary last
+        line["parts"] = line.pop("parts")
+        line["targets"] = targets_summary(line, peaks)
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()

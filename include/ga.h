@@ -127,7 +127,8 @@ size_t ga_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk
  *     the array's device address and sets the decode kernels' shared-memory limit.  Make
  *     that first call before any stream capture.
  *   - Every call shares the one array, which keeps the last call's contents.  Nothing in it
- *     needs to start at zero: each call writes every scratch slot before it reads it.
+ *     needs to start at zero: each call writes every scratch slot it reads before reading it
+ *     (a key chunk whose wait ran out writes an empty partial, which the combine skips).
  *   - Calls that overlap on the GPU race on the array: on different streams, or from host
  *     threads with no ordering between them.  Order such calls on one stream or with events.
  *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
@@ -359,9 +360,11 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
                         int group_shared, uint8_t* block_mask, int32_t* n_selected,
                         ga_dtype dtype, ga_stream_t stream);
 
-/* Synchronises `stream`, then returns and clears the sticky device status: GA_OK, or
- * GA_ERR_DEVICE_TIMEOUT when some kernel gave up on a wait since the last read.  Returns
- * GA_ERR_CUDA when the synchronisation itself fails. */
+/* Synchronises `stream`, then returns and clears the sticky device status of the device
+ * current in the calling thread (each device has its own status word; make the device whose
+ * kernels are to be checked current first, and pass a stream of that device): GA_OK, or
+ * GA_ERR_DEVICE_TIMEOUT when some kernel on that device gave up on a wait since the last read.
+ * Returns GA_ERR_CUDA when the synchronisation itself fails. */
 int ga_read_device_status(ga_stream_t stream);
 
 /* Time limit for every device-side wait, in nanoseconds (default 2e9; minimum 1e5).

@@ -121,9 +121,23 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream(stream, device=None):
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _one_device(tensors, stream=None):
+    """The one CUDA device that every given tensor (None entries skipped) and the explicit
+    stream, if any, live on.  The library launches on the device current in the calling
+    thread, with that device's static scratch and stream, so tensors on another device would
+    reach a kernel as foreign pointers: mixed devices are refused here."""
+    devs = {t.device for t in tensors if t is not None}
+    if stream is not None:
+        devs.add(torch.device(stream.device))
+    if len(devs) != 1:
+        raise ValueError("all tensors (and the stream) must be on one CUDA device, got "
+                         + ", ".join(sorted(str(d) for d in devs)))
+    return devs.pop()
 
 
 def _check(status: int, what: str):
@@ -203,10 +217,12 @@ def ga_attend(q, k, v, out=None, *, k_lens=None, causal=True, window=0, sink=Non
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = L.ga_attend(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tq, Tk_max, _ptr(k_lens),
-                     int(bool(causal)), int(window), _ptr(sink), _ptr(block_mask), int(q_block),
-                     int(k_block), _ptr(lse), _DTYPES[q.dtype], _ptr(workspace), ws_bytes,
-                     _stream(stream))
+    dev = _one_device([q, k, v, out, k_lens, sink, block_mask, lse, workspace], stream)
+    with torch.cuda.device(dev):
+        st = L.ga_attend(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tq, Tk_max, _ptr(k_lens),
+                         int(bool(causal)), int(window), _ptr(sink), _ptr(block_mask), int(q_block),
+                         int(k_block), _ptr(lse), _DTYPES[q.dtype], _ptr(workspace), ws_bytes,
+                         _stream(stream, dev))
     _check(st, "ga_attend")
     return out
 
@@ -237,9 +253,11 @@ def ga_attend_decode_static(q, k, v, out=None, *, k_lens=None, causal=True, wind
     if lse is not None:
         _need(lse, "lse", torch.float32, 3)
         _need_size(lse, "lse", B * H * Tq)
-    st = L.ga_attend_decode_static(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tq, Tk_max,
-                                   _ptr(k_lens), int(bool(causal)), int(window), _ptr(sink), _ptr(lse),
-                                   _stream(stream))
+    dev = _one_device([q, k, v, out, k_lens, sink, lse], stream)
+    with torch.cuda.device(dev):
+        st = L.ga_attend_decode_static(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tq, Tk_max,
+                                       _ptr(k_lens), int(bool(causal)), int(window), _ptr(sink), _ptr(lse),
+                                       _stream(stream, dev))
     _check(st, "ga_attend_decode_static")
     return out
 
@@ -267,9 +285,11 @@ def ga_attend_diff(q1, k1, q2, k2, v, lam, out=None, *, k_lens=None, causal=True
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q1.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = L.ga_attend_diff(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), _ptr(out), B, H, n_kv, d, Tq,
-                          Tk_max, _ptr(k_lens), int(bool(causal)), int(window), float(lam), _ptr(workspace),
-                          ws_bytes, _stream(stream))
+    dev = _one_device([q1, k1, q2, k2, v, out, k_lens, workspace], stream)
+    with torch.cuda.device(dev):
+        st = L.ga_attend_diff(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), _ptr(out), B, H, n_kv, d, Tq,
+                              Tk_max, _ptr(k_lens), int(bool(causal)), int(window), float(lam), _ptr(workspace),
+                              ws_bytes, _stream(stream, dev))
     _check(st, "ga_attend_diff")
     return out
 
@@ -291,8 +311,10 @@ def ga_dsa_indexer(qi, wi, ki, lens=None, scores=None, *, stream=None):
     if scores is None:
         scores = torch.empty(B, L_max, dtype=torch.float32, device=qi.device)
     _need_out(scores, "scores", torch.float32, (B, L_max))
-    _check(L.ga_dsa_indexer(_ptr(qi), _ptr(wi), _ptr(ki), _ptr(lens), B, Hi, di, L_max, _ptr(scores),
-                            _stream(stream)), "ga_dsa_indexer")
+    dev = _one_device([qi, wi, ki, lens, scores], stream)
+    with torch.cuda.device(dev):
+        _check(L.ga_dsa_indexer(_ptr(qi), _ptr(wi), _ptr(ki), _ptr(lens), B, Hi, di, L_max, _ptr(scores),
+                                _stream(stream, dev)), "ga_dsa_indexer")
     return scores
 
 
@@ -312,8 +334,10 @@ def ga_topk_indices(scores, topk, lens=None, idx=None, n_sel=None, *, stream=Non
     _need_out(idx, "idx", torch.int32, (B, int(topk)))
     _need(n_sel, "n_sel", torch.int32, 1)
     _need_size(n_sel, "n_sel", B)
-    _check(L.ga_topk_indices(_ptr(scores), _ptr(lens), B, L_max, int(topk), _ptr(idx), _ptr(n_sel),
-                             _stream(stream)), "ga_topk_indices")
+    dev = _one_device([scores, lens, idx, n_sel], stream)
+    with torch.cuda.device(dev):
+        _check(L.ga_topk_indices(_ptr(scores), _ptr(lens), B, L_max, int(topk), _ptr(idx), _ptr(n_sel),
+                                 _stream(stream, dev)), "ga_topk_indices")
     return idx, n_sel
 
 
@@ -344,9 +368,11 @@ def ga_attend_gather(q, k, v, idx, n_sel, out=None, *, sink=None, lse=None, work
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(L.ga_attend_gather(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tk_max, _ptr(idx),
-                              _ptr(n_sel), topk, _ptr(sink), _ptr(lse), _ptr(workspace), ws_bytes,
-                              _stream(stream)), "ga_attend_gather")
+    dev = _one_device([q, k, v, idx, n_sel, out, sink, lse, workspace], stream)
+    with torch.cuda.device(dev):
+        _check(L.ga_attend_gather(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n_kv, d, Tk_max, _ptr(idx),
+                                  _ptr(n_sel), topk, _ptr(sink), _ptr(lse), _ptr(workspace), ws_bytes,
+                                  _stream(stream, dev)), "ga_attend_gather")
     return out
 
 
@@ -383,8 +409,10 @@ def ga_mla_decode(q_nope, q_rope, latent, w_uk, w_uv, lens=None, out=None, *, wo
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q_nope.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(L.ga_mla_decode(_ptr(q_nope), _ptr(q_rope), _ptr(latent), _ptr(w_uk), _ptr(w_uv), _ptr(lens), _ptr(out),
-                           B, H, L_max, _ptr(workspace), ws_bytes, _stream(stream)), "ga_mla_decode")
+    dev = _one_device([q_nope, q_rope, latent, w_uk, w_uv, lens, out, workspace], stream)
+    with torch.cuda.device(dev):
+        _check(L.ga_mla_decode(_ptr(q_nope), _ptr(q_rope), _ptr(latent), _ptr(w_uk), _ptr(w_uv), _ptr(lens), _ptr(out),
+                               B, H, L_max, _ptr(workspace), ws_bytes, _stream(stream, dev)), "ga_mla_decode")
     return out
 
 
@@ -402,8 +430,10 @@ def ga_ring_append(k_ring, v_ring, k_new, v_new, n_seen, *, stream=None):
     if v_ring.shape != k_ring.shape or k_new.shape != (B, n_kv, d) or v_new.shape != k_new.shape \
             or n_seen.shape != (B,):
         raise ValueError("ring shapes: rings [B, n_kv, W, d], new tokens [B, n_kv, d], n_seen [B]")
-    st = L.ga_ring_append(_ptr(k_ring), _ptr(v_ring), _ptr(k_new), _ptr(v_new), _ptr(n_seen),
-                          B, n_kv, d, W, _stream(stream))
+    dev = _one_device([k_ring, v_ring, k_new, v_new, n_seen], stream)
+    with torch.cuda.device(dev):
+        st = L.ga_ring_append(_ptr(k_ring), _ptr(v_ring), _ptr(k_new), _ptr(v_new), _ptr(n_seen),
+                              B, n_kv, d, W, _stream(stream, dev))
     _check(st, "ga_ring_append")
 
 
@@ -433,8 +463,10 @@ def ga_attend_ring(q, k_ring, v_ring, n_seen, out=None, *, sink=None, lse=None, 
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = L.ga_attend_ring(_ptr(q), _ptr(k_ring), _ptr(v_ring), _ptr(out), B, H, n_kv, d, W, _ptr(n_seen),
-                          _ptr(sink), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream))
+    dev = _one_device([q, k_ring, v_ring, out, n_seen, sink, lse, workspace], stream)
+    with torch.cuda.device(dev):
+        st = L.ga_attend_ring(_ptr(q), _ptr(k_ring), _ptr(v_ring), _ptr(out), B, H, n_kv, d, W, _ptr(n_seen),
+                              _ptr(sink), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream, dev))
     _check(st, "ga_attend_ring")
     return out
 
@@ -458,8 +490,10 @@ def ga_block_stats(k, k_block=64, *, k_lens=None, centroid=None, radius=None, st
     if k_lens is not None:
         _need(k_lens, "k_lens", torch.int32, 1)
         _need_size(k_lens, "k_lens", B)
-    st = L.ga_block_stats(_ptr(k), _ptr(k_lens), B, n_kv, d, Tk_max, int(k_block), _ptr(centroid),
-                          _ptr(radius), _DTYPES[k.dtype], _stream(stream))
+    dev = _one_device([k, k_lens, centroid, radius], stream)
+    with torch.cuda.device(dev):
+        st = L.ga_block_stats(_ptr(k), _ptr(k_lens), B, n_kv, d, Tk_max, int(k_block), _ptr(centroid),
+                              _ptr(radius), _DTYPES[k.dtype], _stream(stream, dev))
     _check(st, "ga_block_stats")
     return centroid, radius
 
@@ -496,11 +530,13 @@ def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, c
     _need_size(n_selected, "n_selected", B * H * nQb)
     rule = {"z": GA_RADIUS_ZSCORE, "mad": GA_RADIUS_MAD}[radius_rule]
     tb = -math.inf if tau_bound is None else float(tau_bound)
-    st = L.ga_select_blocks_ex(_ptr(q), _ptr(centroid), _ptr(radius), B, H, n_kv, d, Tq, int(Tk),
-                               nKb_out, int(q_block), int(k_block), int(bool(causal)), int(window),
-                               float(tau_mean), float(lambda_radius), rule, tb, int(bool(group_shared)),
-                               _ptr(block_mask),
-                               _ptr(n_selected), _DTYPES[q.dtype], _stream(stream))
+    dev = _one_device([q, centroid, radius, block_mask, n_selected], stream)
+    with torch.cuda.device(dev):
+        st = L.ga_select_blocks_ex(_ptr(q), _ptr(centroid), _ptr(radius), B, H, n_kv, d, Tq, int(Tk),
+                                   nKb_out, int(q_block), int(k_block), int(bool(causal)), int(window),
+                                   float(tau_mean), float(lambda_radius), rule, tb, int(bool(group_shared)),
+                                   _ptr(block_mask),
+                                   _ptr(n_selected), _DTYPES[q.dtype], _stream(stream, dev))
     _check(st, "ga_select_blocks")
     return block_mask, n_selected
 

@@ -389,10 +389,27 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
   }
   asm volatile("bar.sync 1, 128;" ::: "memory");             // consumer warps only
-  if (aborted) return;
   const bool final_out = s.n_chunks == 1;
   for (int e = threadIdx.x; e < s.rows * D; e += 128) {
     const int m = e / D, dim = e % D;
+    if (aborted) {
+      // A wait ran out (the status word says so): publish an empty chunk -- zero output, or a
+      // partial with max -inf and sum 0 that the combine skips -- never what an earlier call
+      // left in the workspace.
+      const size_t qrow = ((size_t)b * s.a.n_heads + kvh * g + m % g) * s.a.Tq + m / g;
+      if (final_out) {
+        out[qrow * D + dim] = __float2bfloat16_rn(0.0f);
+        if (lse && dim == 0) lse[qrow] = -INFINITY;
+      } else {
+        const size_t slot = qrow * s.n_chunks + c;
+        ws_o[slot * D + dim] = 0.0f;
+        if (dim == 0) {
+          ws_ml[slot * 2 + 0] = -INFINITY;
+          ws_ml[slot * 2 + 1] = 0.0f;
+        }
+      }
+      continue;
+    }
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 4; ++w) M = fmaxf(M, mml[(w * 16 + m) * 2]);

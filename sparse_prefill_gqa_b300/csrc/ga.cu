@@ -125,10 +125,74 @@ static __device__ __align__(256) unsigned char g_decode_static_scratch[GA_DECODE
 
 namespace {
 
+// ---- once per device: kernel attributes and properties -----------------------------------
+// cudaFuncSetAttribute applies to the device current when it is called, so every device a
+// process launches on gets its own set-up, the first time an entry point runs there.  Each
+// kernel family keeps its own status (a family whose register budget does not fit is
+// refused on its own); the record never changes once filled.
+constexpr int kMaxDevices = 128;
+
+struct DeviceKernels {
+  int prefill128, prefill256;   // prefill_wide_kernel at d = 128 / 256 (every epilogue mode)
+  int decode;                   // decode_splitk_kernel, plain and gathered
+  int select;                   // select_blocks_kernel
+  int mla;                      // mla_decode_kernel
+  int n_sm;                     // streaming multiprocessors
+};
+
+std::mutex g_dev_mu;
+bool g_dev_ready[kMaxDevices] = {};
+DeviceKernels g_dev[kMaxDevices];
+
+int first_error(std::initializer_list<int> sts) {
+  for (int s : sts)
+    if (s != GA_OK) return s;
+  return GA_OK;
+}
+
+// The set-up record of the device current in the calling thread (null when that device cannot
+// be queried).
+const DeviceKernels* device_kernels() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!g_dev_ready[dev]) {
+    DeviceKernels& d = g_dev[dev];
+    {
+      using C = WideCfg<128>;
+      constexpr int need = 256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS;
+      d.prefill128 = first_error({set_smem_split(prefill_wide_kernel<128, false>, C::SMEM_BYTES, C::THREADS, need),
+                                  set_smem_split(prefill_wide_kernel<128, true>, C::SMEM_BYTES, C::THREADS, need),
+                                  set_smem_split(prefill_wide_kernel<128, false, 1>, C::SMEM_BYTES, C::THREADS, need),
+                                  set_smem_split(prefill_wide_kernel<128, false, 2>, C::SMEM_BYTES, C::THREADS, need)});
+    }
+    {
+      using C = WideCfg<256>;
+      d.prefill256 = first_error({set_smem(prefill_wide_kernel<256, false>, C::SMEM_BYTES),
+                                  set_smem(prefill_wide_kernel<256, true>, C::SMEM_BYTES),
+                                  set_smem(prefill_wide_kernel<256, false, 1>, C::SMEM_BYTES),
+                                  set_smem(prefill_wide_kernel<256, false, 2>, C::SMEM_BYTES)});
+    }
+    d.decode = first_error({set_smem(decode_splitk_kernel<256, false>, DecodeCfg<256>::SMEM_BYTES),
+                            set_smem(decode_splitk_kernel<128, false>, DecodeCfg<128>::SMEM_BYTES),
+                            set_smem(decode_splitk_kernel<64, false>, DecodeCfg<64>::SMEM_BYTES),
+                            set_smem(decode_splitk_kernel<256, true>, DecodeCfg<256>::GATHER_SMEM_BYTES),
+                            set_smem(decode_splitk_kernel<128, true>, DecodeCfg<128>::GATHER_SMEM_BYTES),
+                            set_smem(decode_splitk_kernel<64, true>, DecodeCfg<64>::GATHER_SMEM_BYTES)});
+    d.select = first_error({set_smem(select_blocks_kernel<__nv_bfloat16>, 220 * 1024),
+                            set_smem(select_blocks_kernel<float>, 220 * 1024)});
+    d.mla = set_smem(mla_decode_kernel, MlaCfg::SMEM_BYTES);
+    int n_sm = 0;
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) n_sm = 148;
+    d.n_sm = n_sm;
+    g_dev_ready[dev] = true;
+  }
+  return &g_dev[dev];
+}
+
 // Device address of g_decode_static_scratch on the current device.  Host code must not use
 // the symbol itself as a pointer (on the host it names a stand-in, not device memory), so
 // the address is looked up once per device, with that device current, and cached.
-constexpr int kMaxDevices = 128;
 std::mutex g_static_mu;
 void* g_static_scratch_addr[kMaxDevices] = {};
 
@@ -139,10 +203,6 @@ int static_scratch_setup(void** addr) {
   if (g_static_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_static_scratch) != cudaSuccess || p == nullptr)
-      return GA_ERR_CUDA;
-    if (set_smem(decode_splitk_kernel<256>, DecodeCfg<256>::SMEM_BYTES) != GA_OK ||
-        set_smem(decode_splitk_kernel<128>, DecodeCfg<128>::SMEM_BYTES) != GA_OK ||
-        set_smem(decode_splitk_kernel<64>, DecodeCfg<64>::SMEM_BYTES) != GA_OK)
       return GA_ERR_CUDA;
     g_static_scratch_addr[dev] = p;
   }
@@ -157,8 +217,9 @@ int launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfl
                     __nv_bfloat16* ob, float* lse, float* ws_o, float* ws_ml, const DecodeShape& ds,
                     cudaStream_t stream) {
   constexpr int smem = GATHER ? DecodeCfg<D>::GATHER_SMEM_BYTES : DecodeCfg<D>::SMEM_BYTES;
-  static int ok = set_smem(decode_splitk_kernel<D, GATHER>, smem);
-  if (ok != GA_OK) return ok;
+  const DeviceKernels* dk = device_kernels();
+  if (!dk) return GA_ERR_CUDA;
+  if (dk->decode != GA_OK) return dk->decode;
   const dim3 grid(ds.n_chunks, ds.a.n_kv, ds.a.batch);
   decode_splitk_kernel<D, GATHER><<<grid, DecodeCfg<D>::THREADS, smem, stream>>>(
       tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
@@ -196,16 +257,12 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, __nv_bfloat16
     return GA_ERR_CUDA;
   const long long n_cta = (long long)((Tq + 127) / 128) * sh.n_heads * sh.batch;
   if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+  const DeviceKernels* dk = device_kernels();
+  if (!dk) return GA_ERR_CUDA;
   if (d == 128) {
     using C = WideCfg<128>;
     static_assert(C::VK == 128, "V map box");
-    constexpr int need = 256 * C::SOFTMAX_REGS + 128 * C::OTHER_REGS;
-    static int ok0 = set_smem_split(prefill_wide_kernel<128, false>, C::SMEM_BYTES, C::THREADS, need);
-    static int ok1 = set_smem_split(prefill_wide_kernel<128, true>, C::SMEM_BYTES, C::THREADS, need);
-    static int ok2 = set_smem_split(prefill_wide_kernel<128, false, 1>, C::SMEM_BYTES, C::THREADS, need);
-    static int ok3 = set_smem_split(prefill_wide_kernel<128, false, 2>, C::SMEM_BYTES, C::THREADS, need);
-    for (int o : {ok0, ok1, ok2, ok3})
-      if (o != GA_OK) return o;
+    if (dk->prefill128 != GA_OK) return dk->prefill128;
     auto kern = epi.mode == 1 ? prefill_wide_kernel<128, false, 1>
               : epi.mode == 2 ? prefill_wide_kernel<128, false, 2>
               : masked        ? prefill_wide_kernel<128, true>
@@ -214,12 +271,7 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, __nv_bfloat16
   } else {
     using C = WideCfg<256>;
     static_assert(C::VK == 64, "V map box");
-    static int ok0 = set_smem(prefill_wide_kernel<256, false>, C::SMEM_BYTES);
-    static int ok1 = set_smem(prefill_wide_kernel<256, true>, C::SMEM_BYTES);
-    static int ok2 = set_smem(prefill_wide_kernel<256, false, 1>, C::SMEM_BYTES);
-    static int ok3 = set_smem(prefill_wide_kernel<256, false, 2>, C::SMEM_BYTES);
-    for (int o : {ok0, ok1, ok2, ok3})
-      if (o != GA_OK) return o;
+    if (dk->prefill256 != GA_OK) return dk->prefill256;
     auto kern = epi.mode == 1 ? prefill_wide_kernel<256, false, 1>
               : epi.mode == 2 ? prefill_wide_kernel<256, false, 2>
               : masked        ? prefill_wide_kernel<256, true>
@@ -573,8 +625,9 @@ int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, co
                                          up(rows * s.n_chunks * C::R * 4));
   CUtensorMap tm;
   if (!make_map_bf16(&tm, latent, C::DK, L_max, batch, C::TILE)) return GA_ERR_CUDA;
-  static int ok = set_smem(mla_decode_kernel, C::SMEM_BYTES);
-  if (ok != GA_OK) return ok;
+  const DeviceKernels* dk = device_kernels();
+  if (!dk) return GA_ERR_CUDA;
+  if (dk->mla != GA_OK) return dk->mla;
   mla_absorb_kernel<<<dim3(n_heads, batch), 256, 0, stream>>>(
       (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_rope, (const __nv_bfloat16*)w_uk, q_abs, n_heads);
   mla_decode_kernel<<<dim3(s.n_chunks, batch), C::THREADS, C::SMEM_BYTES, stream>>>(tm, q_abs, ws_o, ws_ml,
@@ -699,9 +752,9 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
     for (s.sort_len = 1; s.sort_len < nKb; s.sort_len <<= 1) {}
   const size_t smem = select_smem_bytes(d, (int)nKb, s.sort_len);
   if (smem > 220 * 1024) return GA_ERR_UNSUPPORTED;
-  static int ok_bf = set_smem(select_blocks_kernel<__nv_bfloat16>, 220 * 1024);
-  static int ok_f = set_smem(select_blocks_kernel<float>, 220 * 1024);
-  if (ok_bf != GA_OK || ok_f != GA_OK) return GA_ERR_CUDA;
+  const DeviceKernels* dk = device_kernels();
+  if (!dk) return GA_ERR_CUDA;
+  if (dk->select != GA_OK) return dk->select;
   dim3 grid((s.nQb + kSelQT - 1) / kSelQT, group_shared ? n_kv : n_heads, batch);
   if (dtype == GA_BF16)
     select_blocks_kernel<__nv_bfloat16><<<grid, kSelThreads, smem, stream>>>(

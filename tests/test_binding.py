@@ -55,3 +55,22 @@ def test_missing_library_raises(monkeypatch):
     monkeypatch.setattr(ga, "library_path", lambda: "/nonexistent/libga.so")
     with pytest.raises(RuntimeError, match="not built"):
         ga.lib()
+
+
+class _OnDevice:
+    """Stands in for a tensor or stream by its device alone (no GPU is needed to check the rule)."""
+
+    def __init__(self, dev):
+        self.device = torch.device(dev)
+
+
+def test_tensors_on_several_devices_are_refused():
+    """The library launches on the calling thread's current device with that device's stream and
+    static scratch: tensors (or an explicit stream) on another device are refused before any call."""
+    a, b = _OnDevice("cuda:0"), _OnDevice("cuda:1")
+    assert ga._one_device([a, None, a]) == torch.device("cuda:0")
+    assert ga._one_device([b], stream=_OnDevice("cuda:1")) == torch.device("cuda:1")
+    with pytest.raises(ValueError, match="one CUDA device"):
+        ga._one_device([a, b])
+    with pytest.raises(ValueError, match="one CUDA device"):
+        ga._one_device([a, a], stream=_OnDevice("cuda:1"))

@@ -357,3 +357,26 @@ def test_padding_mask_example_is_the_key_length_mask():
     p = np.exp(s - s.max(axis=-1, keepdims=True))
     guide = (p / p.sum(axis=-1, keepdims=True)) @ vv
     assert np.max(np.abs(ours - guide)) <= 1e-14
+
+
+@pytest.mark.parametrize("sink_kind", ["random", "large", "minus_inf"])
+def test_ring_decode_with_sink_equals_window_mask_with_sink(sink_kind):
+    """"Attention in Code" s.2 and s.3 together: a W = 8 ring over 50 tokens with a per-head sink
+    gives, at every step, what the pinned attend gives under the window mask with the same sink
+    (the sink joins the normaliser of every row and carries no value), so a wrong sink term in
+    the ring's own softmax (scaled by 1/sqrt(d), given a value, or taken against the wrong row
+    maximum) shows up here."""
+    H, n_kv, T, d, W = 4, 2, 50, 16, 8
+    q = _rand((H, T, d), 81)
+    k = _rand((n_kv, T, d), 82)
+    v = _rand((n_kv, T, d), 83)
+    sink = {"random": _rand((H,), 84), "large": np.array([6.0, 9.0, 12.0, 15.0]),
+            "minus_inf": np.full(H, -np.inf)}[sink_kind]
+    ring = ring_decode(q, k, v, W, sink=sink)
+    masked, _ = attend(q[None], k[None], v[None], causal=True, window=W, sink=sink)
+    assert np.max(np.abs(ring - masked[0])) <= 1e-13
+    if sink_kind == "minus_inf":
+        assert np.array_equal(ring, ring_decode(q, k, v, W))
+    else:
+        plain = ring_decode(q, k, v, W)
+        assert np.all(np.linalg.norm(ring, axis=-1) < np.linalg.norm(plain, axis=-1))

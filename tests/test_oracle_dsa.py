@@ -87,3 +87,37 @@ def test_empty_cache_gives_a_zero_row_like_attend():
         assert np.array_equal(out[1:2], none)
         ref, _ = dsa_decode(q[:1], k[:1], v[:1], qi[:1], ki[:1], wi[:1], [30], kk, sink=sk)
         assert np.array_equal(out[:1], ref)
+
+
+def test_sparse_attend_with_sink_equals_attend_on_the_chosen_tokens():
+    """"Attention in Code" s.3 and s.5 together: with a sink, top-k sparse attention equals the
+    pinned attend with a key-level mask (q_block = k_block = 1) that admits exactly each row's
+    chosen tokens, the same sink in the normaliser; so the sink branch of sparse_attend is
+    checked against attend's, which the SDPA and closed-form pins fix.  Also for the decode form."""
+    H, n_kv, T, d, Hi, di, kk = 4, 2, 40, 8, 2, 4, 9
+    q, k, v = _rand((H, T, d), 431), _rand((n_kv, T, d), 432), _rand((n_kv, T, d), 433)
+    sc = indexer_scores(_rand((Hi, T, di), 434), _rand((T, di), 435), np.abs(_rand((Hi, T), 436)))
+    for sink in (_rand((H,), 437), np.array([5.0, 8.0, -3.0, 12.0])):
+        out, reads = sparse_attend(q, k, v, sc, kk, sink=sink)
+        mask = np.zeros((1, H, T, T), dtype=bool)
+        for t in range(T):
+            mask[0, :, t, topk_indices(sc[t], np.arange(T) <= t, kk)] = True
+        ref, _ = attend(q[None], k[None], v[None], causal=True, sink=sink, block_mask=mask,
+                        q_block=1, k_block=1)
+        assert np.max(np.abs(out - ref[0])) <= 1e-13
+        assert np.array_equal(reads, mask[0, 0].sum(axis=1))
+    # decode form with a sink: the last row of each sequence
+    B, Lm = 2, 30
+    qd = _rand((B, H, 1, d), 438)
+    kd, vd = _rand((B, n_kv, Lm, d), 439), _rand((B, n_kv, Lm, d), 440)
+    qi, ki, wi = _rand((B, Hi, di), 441), _rand((B, Lm, di), 442), _rand((B, Hi), 443)
+    sink = _rand((H,), 444)
+    lens = [30, 17]
+    out, chosen = dsa_decode(qd, kd, vd, qi, ki, wi, lens, kk, sink=sink)
+    for b in range(B):
+        L = lens[b]
+        m = np.zeros((1, H, 1, L), dtype=bool)
+        m[0, :, 0, chosen[b]] = True
+        ref, _ = attend(qd[b:b + 1], kd[b:b + 1, :, :L], vd[b:b + 1, :, :L], causal=True, sink=sink,
+                        block_mask=m, q_block=1, k_block=1)
+        assert np.max(np.abs(out[b] - ref[0])) <= 1e-13
