@@ -443,10 +443,12 @@ def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False, outli
                           "frac_hbm": stats_bytes / (statistics.mean(ts) * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     mask = torch.empty(B, H, nQb, nKb, dtype=torch.uint8, device="cuda")
     nsel = torch.empty(B, H, nQb, dtype=torch.int32, device="cuda")
+    sel_ws = torch.empty(int(ga.lib().ga_select_workspace_size(B, H, n_kv, d, T, T, qb, kb, 0)),
+                         dtype=torch.uint8, device="cuda")
 
     def select(tau):
         ga.ga_select_blocks(q, cen, rad, Tk=T, q_block=qb, k_block=kb, tau_mean=tau, lambda_radius=lam,
-                            block_mask=mask, n_selected=nsel)
+                            block_mask=mask, n_selected=nsel, workspace=sel_ws)
 
     def density():
         return float(mask.sum()) / allowed_blocks
@@ -473,7 +475,7 @@ def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False, outli
         def run_sel(tau_m):
             ga.ga_select_blocks(q, cen, rad, Tk=T, q_block=qb, k_block=kb, tau_mean=tau_m,
                                 lambda_radius=lm, block_mask=mask, n_selected=nsel,
-                                radius_rule=rule, tau_bound=tb, group_shared=grp)
+                                radius_rule=rule, tau_bound=tb, group_shared=grp, workspace=sel_ws)
         tau_v = 0.02
         if grp:        # the pooled query's scores spread less: match the per-head density instead
             ref_dens = variants["z rescue"]["density"]

@@ -216,8 +216,8 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
  *   latent   device bf16 [batch, L_max, 576]: per token c_kv (512) then k_rope (64).
  *   w_uk     device bf16 [n_heads, 512, 128];  w_uv: [n_heads, 512, 128].
  *   lens     device int32 [batch]: tokens cached, the new token's latent included, so
- *            1..L_max (larger values are clamped to L_max; 0 leaves the row undefined);
- *            or NULL (= L_max).
+ *            1..L_max (larger values are clamped to L_max; 0, an empty cache, gives a zero
+ *            row); or NULL (= L_max).
  *   out      device bf16 [batch, n_heads, 128].
  *   workspace of ga_mla_decode_workspace_size(batch, n_heads, L_max) bytes, 16-byte aligned.
  *   n_heads <= 16 (GA_ERR_UNSUPPORTED otherwise).  q_lat is rounded to bf16 before the scores.
@@ -314,6 +314,10 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
  *              the row length of block_mask, centroid and radius (nKb_out >= ceil(Tk/k_block)).
  *   block_mask device uint8 out [batch, n_heads, ceil(Tq/q_block), nKb_out].
  *   n_selected device int32 out [batch, n_heads, ceil(Tq/q_block)], or NULL.
+ *   workspace  device scratch of ga_select_workspace_size(...) bytes, 256-byte aligned
+ *              (GA_ERR_WORKSPACE otherwise): the mean query row of every query block, its
+ *              norm, the row maxima and the rescue flags, computed once per call and shared
+ *              by every score.  Must not be used by another call in flight.
  *   d: 1..256; q_block: 1..4096; ceil(Tk/k_block) <= 32768.
  */
 int ga_select_blocks(const void* q, const float* centroid, const float* radius,
@@ -321,7 +325,13 @@ int ga_select_blocks(const void* q, const float* centroid, const float* radius,
                      int q_block, int k_block, int causal, int window,
                      float tau_mean, float lambda_radius,
                      uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype,
-                     ga_stream_t stream);
+                     void* workspace, size_t workspace_bytes, ga_stream_t stream);
+
+/* Bytes of workspace ga_select_blocks / ga_select_blocks_ex need (SIZE_MAX for invalid sizes):
+ * batch * P * ceil(Tq/q_block) * (d + 2) floats and batch * n_kv * ceil(Tk/k_block) bytes, each
+ * part rounded to 256 bytes, with P = n_kv when group_shared is 1 and n_heads otherwise. */
+size_t ga_select_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk, int q_block,
+                                int k_block, int group_shared);
 
 /* Radius rules of ga_select_blocks_ex. */
 typedef enum {
@@ -358,7 +368,8 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
                         int q_block, int k_block, int causal, int window,
                         float tau_mean, float lambda_radius, int radius_rule, float tau_bound,
                         int group_shared, uint8_t* block_mask, int32_t* n_selected,
-                        ga_dtype dtype, ga_stream_t stream);
+                        ga_dtype dtype, void* workspace, size_t workspace_bytes,
+                        ga_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the sticky device status of the device
  * current in the calling thread (each device has its own status word; make the device whose
@@ -376,6 +387,14 @@ void ga_set_wait_timeout_ns(uint64_t ns);
  * after `timeout_ns` and records GA_ERR_DEVICE_TIMEOUT, which ga_read_device_status then
  * reports.  Used to test the failure path without faulting or hanging the GPU. */
 int ga_selftest_wait_timeout(uint64_t timeout_ns, ga_stream_t stream);
+
+/* Test only (the failure-path test of the pipeline waits): from the next call on, the
+ * tensor-core prefill's producer in its first CTA skips the load of ring chunk number `chunk`
+ * (counted over that CTA's work, from 0), so every wait on that chunk runs out after the wait
+ * limit and the launch ends with GA_ERR_DEVICE_TIMEOUT in the status word, its other loads and
+ * MMAs drained and its tensor memory freed.  -1 (the default) turns it off again; nothing else
+ * in the library reads it.  Not for concurrent use with other calls. */
+void ga_selftest_drop_prefill_chunk(int chunk);
 
 /* Human-readable name of a ga_status value (a static string). */
 const char* ga_status_string(int status);

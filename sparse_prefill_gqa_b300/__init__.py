@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "GAError", "lib", "library_path", "ga_attend", "ga_workspace_size", "ga_block_stats",
     "ga_select_blocks", "ga_read_device_status", "ga_set_wait_timeout_ns",
-    "ga_selftest_wait_timeout", "ga_status_string", "ga_version", "GA_OK", "GA_ERR_INVALID_ARG",
+    "ga_selftest_wait_timeout", "ga_selftest_drop_prefill_chunk", "ga_status_string", "ga_version", "GA_OK", "GA_ERR_INVALID_ARG",
     "GA_ERR_UNSUPPORTED", "GA_ERR_CUDA", "GA_ERR_DEVICE_TIMEOUT", "GA_ERR_WORKSPACE",
     "GA_ERR_SCRATCH_LIMIT", "GA_DECODE_STATIC_SCRATCH_BYTES", "ga_attend_decode_static",
     "ga_ring_append", "ga_attend_ring", "ga_attend_diff", "ga_dsa_indexer", "ga_topk_indices",
@@ -90,17 +90,21 @@ def lib() -> ctypes.CDLL:
     L.ga_block_stats.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp]
     L.ga_block_stats.restype = i32
     L.ga_select_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                   f32, f32, vp, vp, i32, vp]
+                                   f32, f32, vp, vp, i32, vp, sz, vp]
     L.ga_select_blocks.restype = i32
     L.ga_select_blocks_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                      f32, f32, i32, f32, i32, vp, vp, i32, vp]
+                                      f32, f32, i32, f32, i32, vp, vp, i32, vp, sz, vp]
     L.ga_select_blocks_ex.restype = i32
+    L.ga_select_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32]
+    L.ga_select_workspace_size.restype = sz
     L.ga_read_device_status.argtypes = [vp]
     L.ga_read_device_status.restype = i32
     L.ga_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     L.ga_set_wait_timeout_ns.restype = None
     L.ga_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     L.ga_selftest_wait_timeout.restype = i32
+    L.ga_selftest_drop_prefill_chunk.argtypes = [i32]
+    L.ga_selftest_drop_prefill_chunk.restype = None
     L.ga_status_string.argtypes = [i32]
     L.ga_status_string.restype = ctypes.c_char_p
     L.ga_version.argtypes = []
@@ -501,12 +505,13 @@ def ga_block_stats(k, k_block=64, *, k_lens=None, centroid=None, radius=None, st
 def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, causal=True,
                      window=0, tau_mean=math.inf, lambda_radius=3.0, block_mask=None,
                      n_selected=None, n_kv=None, radius_rule="z", tau_bound=None, group_shared=False,
-                     stream=None):
+                     workspace=None, stream=None):
     """Block mask (uint8 [B, H, nQb, nKb]) and per-row counts (int32 [B, H, nQb]).
 
     radius_rule: "z" (mean and population std) or "mad" (median and 1.4826 * MAD);
     tau_bound: threshold of the Cauchy-Schwarz bound branch, None for no bound branch;
-    group_shared: one selection per kv head from its heads' pooled query rows."""
+    group_shared: one selection per kv head from its heads' pooled query rows;
+    workspace: uint8 scratch of ga_select_workspace_size(...) bytes (allocated here if None)."""
     L = lib()
     _need(q, "q", None, 4)
     if q.dtype not in _DTYPES:
@@ -530,13 +535,22 @@ def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, c
     _need_size(n_selected, "n_selected", B * H * nQb)
     rule = {"z": GA_RADIUS_ZSCORE, "mad": GA_RADIUS_MAD}[radius_rule]
     tb = -math.inf if tau_bound is None else float(tau_bound)
-    dev = _one_device([q, centroid, radius, block_mask, n_selected], stream)
+    _need_ws(workspace)
+    need = int(L.ga_select_workspace_size(B, H, n_kv, d, Tq, int(Tk), int(q_block), int(k_block),
+                                          int(bool(group_shared))))
+    if need == 2 ** 64 - 1:
+        need = 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    dev = _one_device([q, centroid, radius, block_mask, n_selected, workspace], stream)
     with torch.cuda.device(dev):
         st = L.ga_select_blocks_ex(_ptr(q), _ptr(centroid), _ptr(radius), B, H, n_kv, d, Tq, int(Tk),
                                    nKb_out, int(q_block), int(k_block), int(bool(causal)), int(window),
                                    float(tau_mean), float(lambda_radius), rule, tb, int(bool(group_shared)),
                                    _ptr(block_mask),
-                                   _ptr(n_selected), _DTYPES[q.dtype], _stream(stream, dev))
+                                   _ptr(n_selected), _DTYPES[q.dtype], _ptr(workspace), ws_bytes,
+                                   _stream(stream, dev))
     _check(st, "ga_select_blocks")
     return block_mask, n_selected
 
@@ -551,3 +565,9 @@ def ga_set_wait_timeout_ns(ns: int) -> None:
 
 def ga_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
     return int(lib().ga_selftest_wait_timeout(int(timeout_ns), _stream(stream)))
+
+
+def ga_selftest_drop_prefill_chunk(chunk: int) -> None:
+    """Test only: the tensor-core prefill's first CTA skips loading ring chunk ``chunk`` from
+    the next call on, so its pipeline waits run out (-1 turns it off)."""
+    lib().ga_selftest_drop_prefill_chunk(int(chunk))

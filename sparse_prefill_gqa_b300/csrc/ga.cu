@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -19,12 +20,15 @@
 #include "mla.cuh"
 #include "prefill_wide.cuh"
 #include "ring.cuh"
+#include "select.cuh"
 
 namespace ga {
 
 namespace {
 
 uint64_t g_timeout_ns = 2000000000ull;
+int g_test_drop_chunk = -1;    // test only: ring chunk the prefill producer of CTA 0 skips
+std::atomic<unsigned> g_wide_epoch{0};   // launch counter: each prefill launch's item-counter slot
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -179,8 +183,9 @@ const DeviceKernels* device_kernels() {
                             set_smem(decode_splitk_kernel<256, true>, DecodeCfg<256>::GATHER_SMEM_BYTES),
                             set_smem(decode_splitk_kernel<128, true>, DecodeCfg<128>::GATHER_SMEM_BYTES),
                             set_smem(decode_splitk_kernel<64, true>, DecodeCfg<64>::GATHER_SMEM_BYTES)});
-    d.select = first_error({set_smem(select_blocks_kernel<__nv_bfloat16>, 220 * 1024),
-                            set_smem(select_blocks_kernel<float>, 220 * 1024)});
+    d.select = first_error({set_smem(select_rescue_kernel, 16384 * 8),
+                            set_smem(select_score_kernel<void, false>, kScSmem),
+                            set_smem(select_score_kernel<void, true>, kScSmem)});
     d.mla = set_smem(mla_decode_kernel, MlaCfg::SMEM_BYTES);
     int n_sm = 0;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) n_sm = 148;
@@ -255,10 +260,13 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, __nv_bfloat16
       !make_map_bf16(&tk, k, d, Tk_max, kvz, 128) || !make_map_bf16(&tv, v, d, Tk_max, kvz, vk) ||
       !make_map_bf16(&tk64, k, d, Tk_max, kvz, 64) || !make_map_bf16(&tv64, v, d, Tk_max, kvz, 64))
     return GA_ERR_CUDA;
-  const long long n_cta = (long long)((Tq + 127) / 128) * sh.n_heads * sh.batch;
-  if (n_cta > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+  const long long n_items = wide_items(sh);
+  if (n_items > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
   const DeviceKernels* dk = device_kernels();
   if (!dk) return GA_ERR_CUDA;
+  // persistent: one CTA per SM (or per item when there are fewer items)
+  const unsigned n_cta = (unsigned)(n_items < dk->n_sm ? n_items : dk->n_sm);
+  const int epoch = (int)(g_wide_epoch.fetch_add(1u) % (unsigned)kWideEpochs);
   if (d == 128) {
     using C = WideCfg<128>;
     static_assert(C::VK == 128, "V map box");
@@ -267,7 +275,7 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, __nv_bfloat16
               : epi.mode == 2 ? prefill_wide_kernel<128, false, 2>
               : masked        ? prefill_wide_kernel<128, true>
                               : prefill_wide_kernel<128, false>;
-    kern<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh, epi);
+    kern<<<n_cta, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh, epi, epoch, g_test_drop_chunk);
   } else {
     using C = WideCfg<256>;
     static_assert(C::VK == 64, "V map box");
@@ -276,7 +284,7 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, __nv_bfloat16
               : epi.mode == 2 ? prefill_wide_kernel<256, false, 2>
               : masked        ? prefill_wide_kernel<256, true>
                               : prefill_wide_kernel<256, false>;
-    kern<<<dim3((unsigned)n_cta), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh, epi);
+    kern<<<n_cta, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tk64, tv64, ob, lse, sh, epi, epoch, g_test_drop_chunk);
   }
   return launch_status();
 }
@@ -315,6 +323,8 @@ int ga_read_device_status(ga_stream_t stream) {
   if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return GA_ERR_CUDA;
   return v;
 }
+
+void ga_selftest_drop_prefill_chunk(int chunk) { g_test_drop_chunk = chunk < 0 ? -1 : chunk; }
 
 int ga_selftest_wait_timeout(uint64_t timeout_ns, ga_stream_t stream) {
   int* flag = nullptr;
@@ -578,12 +588,12 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
 }
 
 namespace {
-// Token chunk of the MLA decode: about two waves of one CTA per SM over the batch at full
-// length, whole 64-token tiles.
+// Token chunk of the MLA decode: about four CTAs per SM over the batch at full length (two run
+// at a time on each SM), whole 32-token tiles.
 int mla_chunk_len(int batch, int L_max) {
-  long long c = (long long)L_max * batch / (148LL * 2);
+  long long c = (long long)L_max * batch / (148LL * 4);
   c = c < 256 ? 256 : (c > 4096 ? 4096 : c);
-  return (int)((c + 63) / 64 * 64);
+  return (int)((c + MlaCfg::TILE - 1) / MlaCfg::TILE * MlaCfg::TILE);
 }
 }  // namespace
 
@@ -594,7 +604,7 @@ size_t ga_mla_decode_workspace_size(int batch, int n_heads, int L_max) {
   const size_t n_chunks = (L_max + chunk - 1) / chunk;
   const size_t rows = (size_t)batch * n_heads;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  return up(rows * C::DK * 2) + up(rows * C::R * 4) + up(rows * n_chunks * C::R * 4) + up(rows * n_chunks * 2 * 4);
+  return up(rows * C::DK * 2) + up(rows * n_chunks * C::R * 4) + up(rows * n_chunks * 2 * 4);
 }
 
 int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, const void* w_uk,
@@ -604,7 +614,7 @@ int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, co
   cudaStream_t stream = (cudaStream_t)stream_;
   if (!q_nope || !q_rope || !latent || !w_uk || !w_uv || !out) return GA_ERR_INVALID_ARG;
   if (batch < 1 || n_heads < 1 || L_max < 1) return GA_ERR_INVALID_ARG;
-  if (n_heads > 16 || batch > 65535) return GA_ERR_UNSUPPORTED;
+  if (n_heads > 16 || batch > 65535 * C::EX_SEQ) return GA_ERR_UNSUPPORTED;
   for (const void* p : {q_nope, q_rope, latent, w_uk, w_uv, (const void*)out})
     if (!aligned16(p)) return GA_ERR_INVALID_ARG;
   if (lens && (reinterpret_cast<uintptr_t>(lens) & 3)) return GA_ERR_INVALID_ARG;
@@ -615,26 +625,23 @@ int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, co
   s.batch = batch; s.n_heads = n_heads; s.L_max = L_max; s.lens = lens; s.timeout_ns = g_timeout_ns;
   s.chunk_len = mla_chunk_len(batch, L_max);
   s.n_chunks = (L_max + s.chunk_len - 1) / s.chunk_len;
+  if (s.n_chunks > 65535) return GA_ERR_UNSUPPORTED;
   const size_t rows = (size_t)batch * n_heads;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   unsigned char* w = static_cast<unsigned char*>(workspace);
   auto* q_abs = reinterpret_cast<__nv_bfloat16*>(w);
-  auto* o_lat = reinterpret_cast<float*>(w + up(rows * C::DK * 2));
-  auto* ws_o = reinterpret_cast<float*>(w + up(rows * C::DK * 2) + up(rows * C::R * 4));
-  auto* ws_ml = reinterpret_cast<float*>(w + up(rows * C::DK * 2) + up(rows * C::R * 4) +
-                                         up(rows * s.n_chunks * C::R * 4));
+  auto* ws_o = reinterpret_cast<float*>(w + up(rows * C::DK * 2));
+  auto* ws_ml = reinterpret_cast<float*>(w + up(rows * C::DK * 2) + up(rows * s.n_chunks * C::R * 4));
   CUtensorMap tm;
   if (!make_map_bf16(&tm, latent, C::DK, L_max, batch, C::TILE)) return GA_ERR_CUDA;
   const DeviceKernels* dk = device_kernels();
   if (!dk) return GA_ERR_CUDA;
   if (dk->mla != GA_OK) return dk->mla;
-  mla_absorb_kernel<<<dim3(n_heads, batch), 256, 0, stream>>>(
-      (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_rope, (const __nv_bfloat16*)w_uk, q_abs, n_heads);
-  mla_decode_kernel<<<dim3(s.n_chunks, batch), C::THREADS, C::SMEM_BYTES, stream>>>(tm, q_abs, ws_o, ws_ml,
-                                                                                   o_lat, s);
-  if (s.n_chunks > 1) mla_combine_kernel<<<dim3(n_heads, batch), C::R, 0, stream>>>(ws_o, ws_ml, o_lat, s);
-  mla_expand_kernel<<<dim3(n_heads, batch), C::DV, 0, stream>>>(o_lat, (const __nv_bfloat16*)w_uv,
-                                                                 (__nv_bfloat16*)out, n_heads);
+  mla_absorb_kernel<<<dim3(C::R / C::AB_ROWS, n_heads), 256, 0, stream>>>(
+      (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_rope, (const __nv_bfloat16*)w_uk, q_abs, n_heads, batch);
+  mla_decode_kernel<<<dim3(s.n_chunks, batch), C::THREADS, C::SMEM_BYTES, stream>>>(tm, q_abs, ws_o, ws_ml, s);
+  mla_expand_kernel<<<dim3(C::DV / C::EX_DIMS, n_heads, (batch + C::EX_SEQ - 1) / C::EX_SEQ), 256, 0, stream>>>(
+      ws_o, ws_ml, (const __nv_bfloat16*)w_uv, (__nv_bfloat16*)out, s);
   return launch_status();
 }
 
@@ -711,20 +718,49 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
   return launch_status();
 }
 
+namespace {
+// Workspace of the selection: pooled query rows, their norms, the row maxima and the rescue
+// flags, each part 256-byte aligned.
+struct SelectWs {
+  size_t qmean, qnorm, rowmax, rescue, total;
+};
+SelectWs select_ws(int batch, int n_hp, int n_kv, int d, int nQb, int nKb) {
+  SelectWs w;
+  w.qmean = 0;
+  w.qnorm = w.qmean + sel_up256((size_t)batch * n_hp * nQb * d * 4);
+  w.rowmax = w.qnorm + sel_up256((size_t)batch * n_hp * nQb * 4);
+  w.rescue = w.rowmax + sel_up256((size_t)batch * n_hp * nQb * 4);
+  w.total = w.rescue + sel_up256((size_t)batch * n_kv * nKb);
+  return w;
+}
+}  // namespace
+
+size_t ga_select_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk, int q_block,
+                                int k_block, int group_shared) {
+  if (batch < 1 || n_heads < 1 || n_kv < 1 || n_kv > n_heads || n_heads % n_kv != 0 || d < 1 || d > 256 ||
+      Tq < 1 || Tk < Tq || q_block < 1 || k_block < 1 || (group_shared != 0 && group_shared != 1))
+    return SIZE_MAX;
+  const int nQb = (Tq + q_block - 1) / q_block;
+  const int nKb = (int)(((long long)Tk + k_block - 1) / k_block);
+  return select_ws(batch, group_shared ? n_kv : n_heads, n_kv, d, nQb, nKb).total;
+}
+
 int ga_select_blocks(const void* q, const float* centroid, const float* radius, int batch,
                      int n_heads, int n_kv, int d, int Tq, int Tk, int nKb_out, int q_block,
                      int k_block, int causal, int window, float tau_mean, float lambda_radius,
-                     uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype, ga_stream_t stream_) {
+                     uint8_t* block_mask, int32_t* n_selected, ga_dtype dtype, void* workspace,
+                     size_t workspace_bytes, ga_stream_t stream_) {
   return ga_select_blocks_ex(q, centroid, radius, batch, n_heads, n_kv, d, Tq, Tk, nKb_out, q_block,
                              k_block, causal, window, tau_mean, lambda_radius, GA_RADIUS_ZSCORE,
-                             -INFINITY, 0, block_mask, n_selected, dtype, stream_);
+                             -INFINITY, 0, block_mask, n_selected, dtype, workspace, workspace_bytes, stream_);
 }
 
 int ga_select_blocks_ex(const void* q, const float* centroid, const float* radius, int batch,
                         int n_heads, int n_kv, int d, int Tq, int Tk, int nKb_out, int q_block,
                         int k_block, int causal, int window, float tau_mean, float lambda_radius,
                         int radius_rule, float tau_bound, int group_shared, uint8_t* block_mask,
-                        int32_t* n_selected, ga_dtype dtype, ga_stream_t stream_) {
+                        int32_t* n_selected, ga_dtype dtype, void* workspace, size_t workspace_bytes,
+                        ga_stream_t stream_) {
   cudaStream_t stream = (cudaStream_t)stream_;
   if (!q || !centroid || !radius || !block_mask) return GA_ERR_INVALID_ARG;
   if (dtype != GA_F32 && dtype != GA_BF16) return GA_ERR_INVALID_ARG;
@@ -739,29 +775,46 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
   const long long nKb = ((long long)Tk + k_block - 1) / k_block;
   if (nKb_out < nKb) return GA_ERR_INVALID_ARG;
   if (nKb > 32768 || batch > 65535 || n_heads > 65535) return GA_ERR_UNSUPPORTED;
+  if (radius_rule == GA_RADIUS_MAD && nKb > 16384) return GA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(centroid) || !aligned16(radius)) return GA_ERR_INVALID_ARG;
+  if (n_selected && (reinterpret_cast<uintptr_t>(n_selected) & 3)) return GA_ERR_INVALID_ARG;
+  const int n_hp = group_shared ? n_kv : n_heads;
+  const int nQb = (Tq + q_block - 1) / q_block;
+  const SelectWs ws = select_ws(batch, n_hp, n_kv, d, nQb, (int)nKb);
+  if (!workspace || workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return GA_ERR_WORKSPACE;
+  if ((long long)batch * n_hp > 65535 || nQb > 0x7fffffff / 2) return GA_ERR_UNSUPPORTED;
 
   SelectShape s{};
   s.batch = batch; s.n_heads = n_heads; s.n_kv = n_kv; s.d = d; s.Tq = Tq; s.Tk = Tk;
   s.nKb_out = nKb_out; s.q_block = q_block; s.k_block = k_block; s.causal = causal;
-  s.window = window; s.nQb = (Tq + q_block - 1) / q_block; s.nKb = (int)nKb;
+  s.window = window; s.nQb = nQb; s.nKb = (int)nKb;
   s.tau_mean = tau_mean; s.lambda_radius = lambda_radius;
   s.radius_rule = radius_rule; s.tau_bound = tau_bound; s.group_shared = group_shared;
+  s.n_hp = n_hp;
   s.sort_len = 0;
   if (radius_rule == GA_RADIUS_MAD)
     for (s.sort_len = 1; s.sort_len < nKb; s.sort_len <<= 1) {}
-  const size_t smem = select_smem_bytes(d, (int)nKb, s.sort_len);
-  if (smem > 220 * 1024) return GA_ERR_UNSUPPORTED;
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  s.qmean = reinterpret_cast<float*>(w + ws.qmean);
+  s.qnorm = reinterpret_cast<float*>(w + ws.qnorm);
+  s.rowmax = reinterpret_cast<int*>(w + ws.rowmax);
+  s.rescue = w + ws.rescue;
   const DeviceKernels* dk = device_kernels();
   if (!dk) return GA_ERR_CUDA;
   if (dk->select != GA_OK) return dk->select;
-  dim3 grid((s.nQb + kSelQT - 1) / kSelQT, group_shared ? n_kv : n_heads, batch);
+
+  const dim3 pool_grid(nQb, n_hp, batch);
   if (dtype == GA_BF16)
-    select_blocks_kernel<__nv_bfloat16><<<grid, kSelThreads, smem, stream>>>(
-        (const __nv_bfloat16*)q, centroid, radius, block_mask, n_selected, s);
+    select_pool_kernel<__nv_bfloat16><<<pool_grid, kPoolThreads, 0, stream>>>((const __nv_bfloat16*)q, s);
   else
-    select_blocks_kernel<float><<<grid, kSelThreads, smem, stream>>>((const float*)q, centroid, radius,
-                                                                     block_mask, n_selected, s);
+    select_pool_kernel<float><<<pool_grid, kPoolThreads, 0, stream>>>((const float*)q, s);
+  select_rescue_kernel<<<dim3(n_kv, batch), kRescueThreads, (size_t)s.sort_len * 8, stream>>>(radius, s);
+  const dim3 score_grid((nKb_out + kScB - 1) / kScB, (nQb + kScA - 1) / kScA, batch * n_hp);
+  select_score_kernel<void, false><<<score_grid, kScThreads, kScSmem, stream>>>(centroid, radius, block_mask,
+                                                                               n_selected, s);
+  select_score_kernel<void, true><<<score_grid, kScThreads, kScSmem, stream>>>(centroid, radius, block_mask,
+                                                                              n_selected, s);
   return launch_status();
 }
 

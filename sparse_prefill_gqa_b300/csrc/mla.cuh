@@ -9,9 +9,11 @@
 // so every head reads the same 576 numbers per cached token.  Decode: one new token per
 // sequence at position lens[b] - 1, which sees every cached token.
 //
-// Kernels: mla_absorb_kernel (q_lat, then q = [q_lat | q_rope] in bf16), mla_decode_kernel
-// (split over token chunks; the heads are the 16 rows of mma.sync m16n8k16), mla_combine_kernel
-// (log-sum-exp re-association of the chunks), mla_expand_kernel (o_lat w_uv).
+// Kernels: mla_absorb_kernel (q_lat, then q = [q_lat | q_rope] in bf16; one CTA per (head, 64
+// latent rows) for every sequence, so each weight row is read once), mla_decode_kernel (split
+// over token chunks, two CTAs per SM; the heads are the 16 rows of mma.sync m16n8k16) and
+// mla_expand_kernel (the log-sum-exp re-association of the chunks, then o_lat w_uv, per head,
+// 64 output dims and 16 sequences).
 #pragma once
 
 #include "common.cuh"
@@ -22,9 +24,9 @@ struct MlaCfg {
   static constexpr int R = 512, DR = 64, DN = 128, DV = 128;
   static constexpr int DK = R + DR;                     // 576 numbers per cached token
   static constexpr int SLABS = DK / 64;                 // 9 SW128 boxes of 64 columns
-  static constexpr int TILE = 64;                       // tokens per stage
+  static constexpr int TILE = 32;                       // tokens per stage (8 per compute warp)
   static constexpr int STAGES = 2;
-  static constexpr int STAGE_BYTES = TILE * DK * 2;     // 73728
+  static constexpr int STAGE_BYTES = TILE * DK * 2;     // 36864
   static constexpr int QROW = DK * 2 + 16;              // padded row of the query tile (bytes)
   static constexpr int PROW = TILE * 2 + 16;            // padded row of the P tile (bytes)
   static constexpr int OFF_Q = STAGES * STAGE_BYTES;
@@ -33,7 +35,9 @@ struct MlaCfg {
   static constexpr int OFF_BAR = OFF_X + 4 * 16 * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;
   static constexpr int THREADS = 160;
-  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(2 * SMEM_BYTES <= 232448, "shared memory: two CTAs per SM");
+  // absorb: latent rows per CTA, sequences staged at a time; expand: output dims and sequences
+  static constexpr int AB_ROWS = 64, AB_SEQ = 64, EX_DIMS = 64, EX_SEQ = 16;
 };
 
 struct MlaShape {
@@ -42,33 +46,47 @@ struct MlaShape {
   uint64_t timeout_ns;
 };
 
-// grid: (n_heads, batch); block: 256.  q[b, h] = [q_nope w_uk[h]^T (fp32 sums, rounded to bf16) |
-// q_rope].  Warp w computes latent dims w, w + 8, ...: lanes split the 128 nope dims (4 each).
-// One (sequence, head) per CTA: the grid's many warps hide the latency of the weight rows,
-// which L2 serves to every sequence.
+// grid: (R / 64, n_heads); block: 256.  q[b, h] = [q_nope w_uk[h]^T (fp32 sums, rounded to
+// bf16) | q_rope] for latent rows 64 x .. 64 x + 63 of head h and every sequence b: the 64 weight
+// rows (16 KB) are staged once, transposed to [dim][row] so that the threads of a warp read
+// consecutive rows, and the sequences' q_nope rows 64 at a time; thread t computes row t % 64 for
+// the sequences t / 64, t / 64 + 4, ...
 __global__ void __launch_bounds__(256)
 mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16* __restrict__ q_rope,
-                  const __nv_bfloat16* __restrict__ w_uk, __nv_bfloat16* __restrict__ q_abs, int n_heads) {
+                  const __nv_bfloat16* __restrict__ w_uk, __nv_bfloat16* __restrict__ q_abs, int n_heads,
+                  int batch) {
   using C = MlaCfg;
-  const int h = blockIdx.x, b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row = (size_t)b * n_heads + h;
-  float qn[4];
-  {
-    const __nv_bfloat16* src = q_nope + row * C::DN + 4 * lane;
+  __shared__ __nv_bfloat16 w_s[C::DN][C::AB_ROWS + 2];  // [dim][row]
+  __shared__ __nv_bfloat16 q_s[C::AB_SEQ][C::DN];       // [sequence][dim]
+  const int rb = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
+  const int r = t % C::AB_ROWS, bg = t / C::AB_ROWS;
+  const __nv_bfloat16* wsrc = w_uk + ((size_t)h * C::R + (size_t)rb * C::AB_ROWS) * C::DN;
+  for (int e = t; e < C::AB_ROWS * C::DN; e += 256) w_s[e % C::DN][e / C::DN] = wsrc[e];
+  for (int b0 = 0; b0 < batch; b0 += C::AB_SEQ) {
+    const int nb = min(C::AB_SEQ, batch - b0);
+    __syncthreads();
+    for (int e = t; e < nb * C::DN; e += 256)
+      q_s[e / C::DN][e % C::DN] = q_nope[((size_t)(b0 + e / C::DN) * n_heads + h) * C::DN + e % C::DN];
+    __syncthreads();
+    float a[C::AB_SEQ / 4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) qn[e] = __bfloat162float(src[e]);
+    for (int i = 0; i < C::AB_SEQ / 4; ++i) a[i] = 0.0f;
+#pragma unroll 4
+    for (int k = 0; k < C::DN; ++k) {
+      const float wk = __bfloat162float(w_s[k][r]);
+#pragma unroll
+      for (int i = 0; i < C::AB_SEQ / 4; ++i) a[i] = fmaf(wk, __bfloat162float(q_s[bg + 4 * i][k]), a[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < C::AB_SEQ / 4; ++i) {
+      const int b = b0 + bg + 4 * i;
+      if (b < b0 + nb) q_abs[((size_t)b * n_heads + h) * C::DK + rb * C::AB_ROWS + r] = __float2bfloat16_rn(a[i]);
+    }
   }
-  __nv_bfloat16* dst = q_abs + row * C::DK;
-  for (int c = warp; c < C::R; c += 8) {
-    const __nv_bfloat16* w = w_uk + ((size_t)h * C::R + c) * C::DN + 4 * lane;
-    float a = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) a = fmaf(__bfloat162float(w[e]), qn[e], a);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-    if (lane == 0) dst[c] = __float2bfloat16_rn(a);
-  }
-  for (int e = threadIdx.x; e < C::DR; e += 256) dst[C::R + e] = q_rope[row * C::DR + e];
+  if (rb == 0)                                          // the rope part of every sequence's query
+    for (int e = t; e < batch * C::DR; e += 256)
+      q_abs[((size_t)(e / C::DR) * n_heads + h) * C::DK + C::R + e % C::DR] =
+          q_rope[((size_t)(e / C::DR) * n_heads + h) * C::DR + e % C::DR];
 }
 
 struct MlaBars {
@@ -86,15 +104,16 @@ __device__ __forceinline__ bool consumers_all(bool ok) {
   return res != 0;
 }
 
-// grid: (n_chunks, batch); block: 160 -- warps 0-3 compute, warp 4 loads 64-token tiles of the
-// latent cache [batch, L_max, 576] by TMA (9 boxes of 64 columns, 128-byte swizzle).
-// Per tile: warp w scores its 16 tokens for the 16 query rows (the heads; rows >= n_heads are
+// grid: (n_chunks, batch); block: 160 -- warps 0-3 compute, warp 4 loads 32-token tiles of the
+// latent cache [batch, L_max, 576] by TMA (9 boxes of 64 columns, 128-byte swizzle); two CTAs
+// per SM, so that one streams while the other starts or finishes.
+// Per tile: warp w scores its 8 tokens for the 16 query rows (the heads; rows >= n_heads are
 // zero), the warps agree on each row's tile maximum through shared memory, write their
-// probabilities into a shared 16 x 64 P tile, and each accumulates latent dims 128 w .. 128 w +
-// 127 of P c_kv over all 64 tokens.
-__global__ void __launch_bounds__(MlaCfg::THREADS, 1)
+// probabilities into a shared 16 x 32 P tile, and each accumulates latent dims 128 w .. 128 w +
+// 127 of P c_kv over all 32 tokens.
+__global__ void __launch_bounds__(MlaCfg::THREADS, 2)
 mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat16* __restrict__ q_abs,
-                  float* __restrict__ ws_o, float* __restrict__ ws_ml, float* __restrict__ o_lat, MlaShape s) {
+                  float* __restrict__ ws_o, float* __restrict__ ws_ml, MlaShape s) {
   using C = MlaCfg;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -168,31 +187,32 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
     if (!consumers_all(got)) break;
     const uint32_t kb = sbase + st * C::STAGE_BYTES;
     const int t0 = kbeg + it * C::TILE;                // first token of the tile
-    // ---- scores of this warp's 16 tokens ------------------------------------------------
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // ---- scores of this warp's 8 tokens ---------------------------------------------------
+    // One 4-matrix load brings the keys' dims of two 16-dim steps: matrices 0, 1 the low and
+    // high 8 dims of step kk, matrices 2, 3 those of step kk + 1.
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
     {
-      const int keyr = 16 * warp + ((mi >> 1) << 3) + rr;
-#pragma unroll 4
-      for (int kk = 0; kk < C::DK / 16; ++kk) {
-        uint32_t a[4];
-        ldmatrix_x4(qs + (lane & 15) * C::QROW + (kk * 16 + (lane >> 4) * 8) * 2, a[0], a[1], a[2], a[3]);
-        const int dchunk = 2 * kk + (mi & 1);
+      const int keyr = 8 * warp + rr;
+#pragma unroll 2
+      for (int kk = 0; kk < C::DK / 16; kk += 2) {
+        uint32_t a0[4], a1[4];
+        ldmatrix_x4(qs + (lane & 15) * C::QROW + (kk * 16 + (lane >> 4) * 8) * 2, a0[0], a0[1], a0[2], a0[3]);
+        ldmatrix_x4(qs + (lane & 15) * C::QROW + ((kk + 1) * 16 + (lane >> 4) * 8) * 2, a1[0], a1[1], a1[2], a1[3]);
+        const int dchunk = 2 * (kk + (mi >> 1)) + (mi & 1);
         const uint32_t addr = kb + (dchunk >> 3) * (C::TILE * 128) + keyr * 128 + (((dchunk & 7) ^ (keyr & 7)) << 4);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(addr, b0, b1, b2, b3);
-        mma_bf16_16816(sc[0], a, b0, b1);
-        mma_bf16_16816(sc[1], a, b2, b3);
+        mma_bf16_16816(sc, a0, b0, b1);
+        mma_bf16_16816(sc, a1, b2, b3);
       }
     }
     float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = t0 + 16 * warp + 8 * n + 2 * (lane & 3) + (e & 1);
-        sc[n][e] = j < kend ? sc[n][e] * scale_log2 : -INFINITY;
-        mt[e >> 1] = fmaxf(mt[e >> 1], sc[n][e]);
-      }
+    for (int e = 0; e < 4; ++e) {
+      const int j = t0 + 8 * warp + 2 * (lane & 3) + (e & 1);
+      sc[e] = j < kend ? sc[e] * scale_log2 : -INFINITY;
+      mt[e >> 1] = fmaxf(mt[e >> 1], sc[e]);
+    }
 #pragma unroll
     for (int row = 0; row < 2; ++row) {
       mt[row] = fmaxf(mt[row], __shfl_xor_sync(0xffffffffu, mt[row], 1));
@@ -215,15 +235,14 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
       l_part[row] *= alpha[row];
     }
     unsigned char* pb = smem + C::OFF_P;
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
+    {
       float p[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        p[e] = ex2(sc[n][e] - m_use[e >> 1]);
+        p[e] = ex2(sc[e] - m_use[e >> 1]);
         l_part[e >> 1] += p[e];
       }
-      const int col = 16 * warp + 8 * n + 2 * (lane & 3);
+      const int col = 8 * warp + 2 * (lane & 3);
       *reinterpret_cast<uint32_t*>(pb + r_lo * C::PROW + col * 2) = pack_bf16x2(p[0], p[1]);
       *reinterpret_cast<uint32_t*>(pb + r_hi * C::PROW + col * 2) = pack_bf16x2(p[2], p[3]);
     }
@@ -235,7 +254,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");   // the P tile is complete
-    // ---- o += P c_kv over the tile's 64 tokens, latent dims 128 warp .. -------------------
+    // ---- o += P c_kv over the tile's 32 tokens, latent dims 128 warp .. -------------------
     const int lim = kend - t0;                        // first tile row past the end
     const bool tail = lim < C::TILE;
 #pragma unroll
@@ -277,79 +296,93 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
     xs[warp * 16 + r_hi] = l_part[1];
   }
   __syncthreads();
-  if (*abort_flag != 0) return;
+  // a wait that ran out (the status word says so) publishes an empty partial: max -inf and sum
+  // 0, which the re-association skips, never what an earlier call left in the workspace
+  const bool aborted = *abort_flag != 0;
   float lsum[2];
 #pragma unroll
   for (int row = 0; row < 2; ++row) {
     const int r = row ? r_hi : r_lo;
-    lsum[row] = (xs[r] + xs[16 + r]) + (xs[32 + r] + xs[48 + r]);
+    lsum[row] = aborted ? 0.0f : (xs[r] + xs[16 + r]) + (xs[32 + r] + xs[48 + r]);
+    if (aborted) m_run[row] = -INFINITY;
   }
-  const bool final_out = s.n_chunks == 1;
 #pragma unroll
   for (int row = 0; row < 2; ++row) {
     const int h = row ? r_hi : r_lo;
     if (h >= H) continue;
-    const size_t qrow = (size_t)b * H + h;
-    const float inv = lsum[row] > 0.0f ? 1.0f / lsum[row] : 0.0f;
+    const size_t slot = ((size_t)b * H + h) * s.n_chunks + c;
 #pragma unroll
     for (int n = 0; n < 16; ++n) {
       const int dim = 128 * warp + 8 * n + 2 * (lane & 3);
-      const float v0 = o[n][2 * row], v1 = o[n][2 * row + 1];
-      if (final_out) {
-        o_lat[qrow * C::R + dim] = v0 * inv;
-        o_lat[qrow * C::R + dim + 1] = v1 * inv;
-      } else {
-        float* dst = ws_o + (qrow * s.n_chunks + c) * C::R + dim;
-        dst[0] = v0;
-        dst[1] = v1;
+      *reinterpret_cast<float2*>(ws_o + slot * C::R + dim) = make_float2(o[n][2 * row], o[n][2 * row + 1]);
+    }
+    if (warp == 0 && (lane & 3) == 0) {
+      ws_ml[slot * 2 + 0] = m_run[row];
+      ws_ml[slot * 2 + 1] = lsum[row];
+    }
+  }
+}
+
+// grid: (DV / 64, n_heads, ceil(batch / 16)); block: 256.  For 16 sequences of head h: the chunk
+// partials re-associated into the latent output (o_lat = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M)
+// l_c over the chunks holding tokens; one warp per two sequences, the lanes over the latent
+// dims), then out = o_lat w_uv[h] for output dims 64 x .. 64 x + 63 (thread t: dim t % 64 of
+// sequences t / 64 + 4 i; fp32 sums, each weight element read once for the 16 sequences).
+__global__ void __launch_bounds__(256)
+mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
+                  const __nv_bfloat16* __restrict__ w_uv, __nv_bfloat16* __restrict__ out, MlaShape s) {
+  using C = MlaCfg;
+  __shared__ float lat[C::EX_SEQ][C::R];
+  const int xb = blockIdx.x, h = blockIdx.y, b0 = blockIdx.z * C::EX_SEQ;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = min(C::EX_SEQ, s.batch - b0);
+  for (int i = warp; i < C::EX_SEQ; i += 8) {
+    float o[C::R / 32];
+#pragma unroll
+    for (int u = 0; u < C::R / 32; ++u) o[u] = 0.0f;
+    if (i < nb) {
+      const int b = b0 + i;
+      const int L = seq_keys(s.lens, b, s.L_max);
+      const size_t qrow = (size_t)b * s.n_heads + h;
+      const int n_used = min(s.n_chunks, (L + s.chunk_len - 1) / s.chunk_len);
+      float M = -INFINITY;
+      for (int c = lane; c < n_used; c += 32) M = fmaxf(M, ws_ml[(qrow * s.n_chunks + c) * 2]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float Lsum = 0.0f;
+      if (M != -INFINITY) {
+        for (int c = 0; c < n_used; ++c) {
+          const float mc = ws_ml[(qrow * s.n_chunks + c) * 2];
+          if (mc == -INFINITY) continue;
+          const float f = ex2(mc - M);
+          Lsum += f * ws_ml[(qrow * s.n_chunks + c) * 2 + 1];
+          const float* src = ws_o + (qrow * s.n_chunks + c) * C::R + lane;
+#pragma unroll
+          for (int u = 0; u < C::R / 32; ++u) o[u] = fmaf(f, src[32 * u], o[u]);
+        }
       }
+      const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+#pragma unroll
+      for (int u = 0; u < C::R / 32; ++u) o[u] *= inv;
     }
-    if (!final_out && warp == 0 && (lane & 3) == 0) {
-      ws_ml[(qrow * s.n_chunks + c) * 2 + 0] = m_run[row];
-      ws_ml[(qrow * s.n_chunks + c) * 2 + 1] = lsum[row];
-    }
+#pragma unroll
+    for (int u = 0; u < C::R / 32; ++u) lat[i][lane + 32 * u] = o[u];
   }
-}
-
-// grid: (n_heads, batch); block: 512 (one latent dim each).  o_lat = sum_c 2^(m_c - M) o_c /
-// sum_c 2^(m_c - M) l_c over the chunks that hold tokens.
-__global__ void __launch_bounds__(MlaCfg::R)
-mla_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml, float* __restrict__ o_lat,
-                   MlaShape s) {
-  using C = MlaCfg;
-  const int h = blockIdx.x, b = blockIdx.y, dim = threadIdx.x;
-  const int L = seq_keys(s.lens, b, s.L_max);
-  const size_t qrow = (size_t)b * s.n_heads + h;
-  const int n_used = min(s.n_chunks, (L + s.chunk_len - 1) / s.chunk_len);
-  float M = -INFINITY;
-  for (int c = 0; c < n_used; ++c) M = fmaxf(M, ws_ml[(qrow * s.n_chunks + c) * 2]);
-  float Lsum = 0.0f, O = 0.0f;
-  if (M != -INFINITY) {
-    for (int c = 0; c < n_used; ++c) {
-      const float mc = ws_ml[(qrow * s.n_chunks + c) * 2];
-      if (mc == -INFINITY) continue;
-      const float f = ex2(mc - M);
-      Lsum += f * ws_ml[(qrow * s.n_chunks + c) * 2 + 1];
-      O += f * ws_o[(qrow * s.n_chunks + c) * C::R + dim];
-    }
-  }
-  o_lat[qrow * C::R + dim] = Lsum > 0.0f ? O / Lsum : 0.0f;
-}
-
-// grid: (n_heads, batch); block: 128 (one output dim each).  out = o_lat w_uv[h] (fp32 sums).
-__global__ void __launch_bounds__(MlaCfg::DV)
-mla_expand_kernel(const float* __restrict__ o_lat, const __nv_bfloat16* __restrict__ w_uv,
-                  __nv_bfloat16* __restrict__ out, int n_heads) {
-  using C = MlaCfg;
-  __shared__ float lat[C::R];
-  const int h = blockIdx.x, b = blockIdx.y, e = threadIdx.x;
-  const size_t qrow = (size_t)b * n_heads + h;
-  for (int c = e; c < C::R; c += C::DV) lat[c] = o_lat[qrow * C::R + c];
   __syncthreads();
-  const __nv_bfloat16* w = w_uv + (size_t)h * C::R * C::DV + e;
-  float a = 0.0f;
-  for (int c = 0; c < C::R; ++c) a = fmaf(lat[c], __bfloat162float(w[(size_t)c * C::DV]), a);
-  out[qrow * C::DV + e] = __float2bfloat16_rn(a);
+  const int e = threadIdx.x % C::EX_DIMS, rg = threadIdx.x / C::EX_DIMS;
+  const __nv_bfloat16* w = w_uv + (size_t)h * C::R * C::DV + xb * C::EX_DIMS + e;
+  float a[C::EX_SEQ / 4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int c = 0; c < C::R; ++c) {
+    const float wc = __bfloat162float(w[(size_t)c * C::DV]);
+#pragma unroll
+    for (int i = 0; i < C::EX_SEQ / 4; ++i) a[i] = fmaf(lat[rg + 4 * i][c], wc, a[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < C::EX_SEQ / 4; ++i) {
+    const int r = rg + 4 * i;
+    if (r < nb) out[((size_t)(b0 + r) * s.n_heads + h) * C::DV + xb * C::EX_DIMS + e] = __float2bfloat16_rn(a[i]);
+  }
 }
 
 }  // namespace ga

@@ -88,6 +88,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns, abort_flag));
 }
 
+// AND of `ok` over the N threads that meet at named barrier `id` (N a multiple of 32): every
+// participating warp gets the same answer, so a wait that gave up in one warp never leaves
+// another waiting at a barrier the first will not reach.
+template <int ID, int N>
+__device__ __forceinline__ bool named_all(bool ok) {
+  uint32_t res;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(res) : "r"(ok ? 1u : 0u), "n"(ID), "n"(N) : "memory");
+  return res != 0;
+}
+
 // ---------------------------------------------------------------------------------------
 // Register reallocation between warpgroups (all four warps of a warpgroup execute it).
 // The sum over warpgroups of (128 x registers) must stay within what the CTA was launched

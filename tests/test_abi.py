@@ -79,7 +79,16 @@ def test_block_calls_reject_invalid_arguments(L):
     assert L.ga_block_stats(None, None, 1, 1, 128, 64, 64, p, p, 1, None) == ga.GA_ERR_INVALID_ARG
     assert L.ga_block_stats(p, None, 1, 1, 128, 64, 0, p, p, 1, None) == ga.GA_ERR_INVALID_ARG
     assert L.ga_block_stats(p, None, 1, 1, 300, 64, 64, p, p, 1, None) == ga.GA_ERR_INVALID_ARG
-    args = [p, p, p, 1, 8, 2, 128, 256, 256, 4, 128, 64, 1, 0, math.inf, 3.0, p, None, 1, None]
+    ws = L.ga_select_workspace_size(1, 8, 2, 128, 256, 256, 128, 64, 0)
+    assert 0 < ws < 2 ** 64 - 1
+    assert L.ga_select_workspace_size(1, 8, 3, 128, 256, 256, 128, 64, 0) == 2 ** 64 - 1
+    args = [p, p, p, 1, 8, 2, 128, 256, 256, 4, 128, 64, 1, 0, math.inf, 3.0, p, None, 1, p, ws, None]
+    bad = list(args)
+    bad[19] = None                              # no workspace
+    assert L.ga_select_blocks(*bad) == ga.GA_ERR_WORKSPACE
+    bad = list(args)
+    bad[20] = ws - 1                            # workspace too small
+    assert L.ga_select_blocks(*bad) == ga.GA_ERR_WORKSPACE
     bad = list(args)
     bad[5] = 3                                  # n_heads % n_kv != 0
     assert L.ga_select_blocks(*bad) == ga.GA_ERR_INVALID_ARG
@@ -112,7 +121,9 @@ def test_ring_calls_reject_invalid_arguments(L):
 
 def test_select_ex_rejects_invalid_rule_and_nan_bound(L):
     p = ctypes.c_void_p(4096)
-    args = [p, p, p, 1, 8, 2, 128, 256, 256, 4, 128, 64, 1, 0, math.inf, 3.0, 0, -math.inf, 0, p, None, 1, None]
+    ws = L.ga_select_workspace_size(1, 8, 2, 128, 256, 256, 128, 64, 0)
+    args = [p, p, p, 1, 8, 2, 128, 256, 256, 4, 128, 64, 1, 0, math.inf, 3.0, 0, -math.inf, 0, p, None, 1, p, ws,
+            None]
     bad = list(args)
     bad[16] = 2                                 # unknown radius rule
     assert L.ga_select_blocks_ex(*bad) == ga.GA_ERR_INVALID_ARG

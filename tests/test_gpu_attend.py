@@ -214,3 +214,29 @@ def test_failure_path_reports_device_timeout_and_context_survives():
     assert ga.ga_read_device_status() == ga.GA_ERR_DEVICE_TIMEOUT
     assert ga.ga_read_device_status() == ga.GA_OK        # cleared by the read
     check(run_case(1, 2, 1, 64, 64, 128, "bf16", seed=43), "bf16", "after timeout")
+
+
+@pytest.mark.parametrize("d,masked", [(128, False), (256, False), (128, True)])
+def test_prefill_pipeline_wait_runs_out_then_recovers(d, masked):
+    """The waits inside the tensor-core prefill's TMA/MMA pipeline are bounded too: with one K
+    chunk of the first CTA never loaded (a test-only switch) and a 1 ms limit, the launch ends
+    by itself with GA_ERR_DEVICE_TIMEOUT recorded -- its warps leave together, drain their
+    loads and MMAs and free tensor memory -- and the next launches on the same context are
+    exact again."""
+    B, H, n_kv, T = 1, 2, 1, 1024
+    q, _ = host_tensor(45, "q", (B, H, T, d), "bf16")
+    k, _ = host_tensor(45, "k", (B, n_kv, T, d), "bf16")
+    v, _ = host_tensor(45, "v", (B, n_kv, T, d), "bf16")
+    bm = torch.ones(B, H, T // 128, T // 64, dtype=torch.uint8, device="cuda") if masked else None
+    assert ga.ga_read_device_status() == ga.GA_OK
+    ga.ga_set_wait_timeout_ns(1_000_000)
+    ga.ga_selftest_drop_prefill_chunk(3)
+    try:
+        ga.ga_attend(q, k, v, block_mask=bm)
+        assert ga.ga_read_device_status() == ga.GA_ERR_DEVICE_TIMEOUT
+    finally:
+        ga.ga_selftest_drop_prefill_chunk(-1)
+        ga.ga_set_wait_timeout_ns(2_000_000_000)
+    assert ga.ga_read_device_status() == ga.GA_OK
+    check(run_case(1, 4, 2, 300, 300, d, "bf16", seed=46, mask_density=0.6 if masked else None),
+          "bf16", "after a pipeline timeout")

@@ -95,42 +95,123 @@ def test_window_sink_and_full_causal_32k_d256():
     check_rows(out, qb, kb, vb, rows, heads, sink=sink, what="full causal+sink")
 
 
-def test_block_sparse_prefill_128k():
+def test_diff_attention_full_size_sampled():
+    """Differential attention at the size the bench times it (B2 H32 Hkv8 d128 T8192 causal,
+    lambda 0.8, the bench's inputs): 256 sampled rows of four (sequence, head) pairs against
+    the float64 oracle ("Attention Variants", differential attention)."""
+    c = get_config(2)
+    B, H, n_kv, d, T = c.batch, c.n_heads, c.n_kv, c.d, c.Tq
+    shp_q, shp_k = (B, H, T, d), (B, n_kv, T, d)
+    bits = {t: randn_bhtd(c.seed, "diff_" + t, shp_q if t[0] == "q" else shp_k)
+            for t in ("q1", "q2", "k1", "k2", "v")}
+    dev = {t: upload(x) for t, x in bits.items()}
+    out = ga.ga_attend_diff(dev["q1"], dev["k1"], dev["q2"], dev["k2"], dev["v"], 0.8)
+    assert ga.ga_read_device_status() == ga.GA_OK
+    rows = sample_rows(T, 256, seed=c.seed)
+    o = out[:, :, rows].float().cpu().numpy().astype(np.float64)
+    for b, h in ((0, 0), (0, 13), (1, 6), (1, 31)):
+        kvh = h // c.g
+        ref = oracle.diff_attend(f64(bits["q1"][b:b + 1, h:h + 1]), f64(bits["k1"][b:b + 1, kvh:kvh + 1]),
+                                 f64(bits["q2"][b:b + 1, h:h + 1]), f64(bits["k2"][b:b + 1, kvh:kvh + 1]),
+                                 f64(bits["v"][b:b + 1, kvh:kvh + 1]), 0.8, rows=rows)
+        assert_close(o[b, h][None, None], ref, "bf16", f"diff attention b={b} h={h}")
+
+
+@pytest.fixture(scope="module")
+def sparse_128k():
+    """The 128K block-sparse workload (planted outliers), on the device, with the oracle's block
+    statistics of every block."""
     c = get_config(5)
-    B, H, n_kv, d, T, qbk, kbk = c.batch, c.n_heads, c.n_kv, c.d, c.Tq, c.q_block, c.k_block
+    B, H, n_kv, d, T = c.batch, c.n_heads, c.n_kv, c.d, c.Tq
     qb = randn_bhtd(c.seed, "q", (B, H, T, d))
     kb = randn_bhtd(c.seed, "k", (B, n_kv, T, d))
-    planted = planted_outliers(c.seed, n_kv, T, d, kbk, c.planted_fraction)
+    planted = planted_outliers(c.seed, n_kv, T, d, c.k_block, c.planted_fraction)
     for kvh, blk, tok, vec in planted:
         kb[0, kvh, tok] = f32_to_bf16_bits(vec)
     vb = randn_bhtd(c.seed, "v", (B, n_kv, T, d))
     q, k, v = upload(qb), upload(kb), upload(vb)
-    cen, rad = ga.ga_block_stats(k, kbk)
-    mask, nsel = ga.ga_select_blocks(q, cen, rad, Tk=T, q_block=qbk, k_block=kbk, tau_mean=0.03,
+    cen, rad = ga.ga_block_stats(k, c.k_block)
+    cr, rr = oracle.block_stats(f64(kb), None, c.k_block)
+    return dict(c=c, qb=qb, kb=kb, vb=vb, q=q, k=k, v=v, cen=cen, rad=rad, cr=cr, rr=rr, planted=planted)
+
+
+def _near(*margins):
+    """Blocks whose oracle score lies within 1e-6 of one of its thresholds."""
+    out = None
+    for m in margins:
+        x = np.abs(np.nan_to_num(m, nan=np.inf)) < 1e-6
+        out = x if out is None else out | x
+    return out
+
+
+def test_block_sparse_prefill_128k(sparse_128k):
+    s = sparse_128k
+    c = s["c"]
+    T, qbk, kbk = c.Tq, c.q_block, c.k_block
+    cen, rad, cr, rr, planted = s["cen"], s["rad"], s["cr"], s["rr"], s["planted"]
+    mask, nsel = ga.ga_select_blocks(s["q"], cen, rad, Tk=T, q_block=qbk, k_block=kbk, tau_mean=0.03,
                                      lambda_radius=c.extra["lambda_radius"])
-    out = ga.ga_attend(q, k, v, block_mask=mask, q_block=qbk, k_block=kbk)
+    out = ga.ga_attend(s["q"], s["k"], s["v"], block_mask=mask, q_block=qbk, k_block=kbk)
     assert ga.ga_read_device_status() == ga.GA_OK
     # block statistics, every block
-    kr = f64(kb)
-    cr, rr = oracle.block_stats(kr, None, kbk)
     assert np.max(np.abs(cen.cpu().numpy() - cr)) <= 1e-5
     assert np.max(np.abs(rad.cpu().numpy() - rr) / np.maximum(rr, 1.0)) <= 1e-5
-    # selection, every block, two query heads per kv head
+    # selection, every block, four query heads
     gm = mask.cpu().numpy()
-    qr = None
     for h in (0, 3, 12, 31):
         kvh = h // c.g
-        qh = f64(qb[:, h:h + 1])
+        qh = f64(s["qb"][:, h:h + 1])
         mref, nref, mm, zm = oracle.select_blocks(qh, cr[:, kvh:kvh + 1], rr[:, kvh:kvh + 1], Tk=T,
                                                   q_block=qbk, k_block=kbk, tau_mean=0.03,
                                                   lambda_radius=c.extra["lambda_radius"],
                                                   return_margins=True)
         diff = gm[:, h:h + 1] != mref
-        near = (np.abs(np.nan_to_num(mm, nan=np.inf)) < 1e-6) | (np.abs(np.nan_to_num(zm, nan=np.inf)) < 1e-6)
-        assert not (diff & ~near).any(), f"head {h}: {(diff & ~near).sum()} decisions differ"
+        assert not (diff & ~_near(mm, zm)).any(), f"head {h}: {(diff & ~_near(mm, zm)).sum()} decisions differ"
         # every planted block of this kv head is rescued for the last query block
         blocks = [blk for kh, blk, _, _ in planted if kh == kvh]
         assert gm[0, h, -1, blocks].all()
     # sparse attention on sampled rows, with the GPU's own mask
     rows = sample_rows(T, 128, seed=c.seed, extra=[tok + 1 for _, _, tok, _ in planted[:20]])
-    check_rows(out, qb, kb, vb, rows, [(0, 0), (0, 21)], mask=gm, what="sparse 128K")
+    check_rows(out, s["qb"], s["kb"], s["vb"], rows, [(0, 0), (0, 21)], mask=gm, what="sparse 128K")
+
+
+@pytest.mark.parametrize("variant", ["mad", "bound", "group_shared"])
+def test_selection_variants_128k(sparse_128k, variant):
+    """The selection variants at the size the bench times them (the 128K workload, tau_mean 0.02,
+    lambda 3): the robust MAD radius rule, the Cauchy-Schwarz bound branch as the rescue (no
+    radius branch, tau_bound -3), and group-shared selection; every decision of the heads of two
+    kv groups against the float64 oracle, mismatches allowed only within 1e-6 of a threshold
+    ("RBS-Attention review": the two sieves, radius against its own distribution)."""
+    s = sparse_128k
+    c = s["c"]
+    T, qbk, kbk, g = c.Tq, c.q_block, c.k_block, c.g
+    lam = c.extra["lambda_radius"]
+    kw = {"mad": dict(radius_rule="mad", lambda_radius=lam),
+          "bound": dict(tau_bound=-3.0, lambda_radius=math.inf),
+          "group_shared": dict(group_shared=True, lambda_radius=lam)}[variant]
+    tau = 0.01 if variant == "group_shared" else 0.02
+    mask, _ = ga.ga_select_blocks(s["q"], s["cen"], s["rad"], Tk=T, q_block=qbk, k_block=kbk, tau_mean=tau, **kw)
+    assert ga.ga_read_device_status() == ga.GA_OK
+    gm = mask.cpu().numpy()
+    kvhs = (0, 5)
+    heads = [h for kvh in kvhs for h in range(kvh * g, (kvh + 1) * g)] if variant == "group_shared" else [1, 22]
+    okw = {"radius_rule": kw.get("radius_rule", "z"), "tau_bound": kw.get("tau_bound"),
+           "group_shared": kw.get("group_shared", False), "lambda_radius": kw["lambda_radius"]}
+    for kvh in sorted({h // g for h in heads}):
+        hs = [h for h in heads if h // g == kvh]
+        h0 = kvh * g
+        # the oracle gets the whole group's rows when the group is pooled, else one head's
+        qh = f64(s["qb"][:, h0:h0 + g]) if okw["group_shared"] else None
+        for h in hs:
+            q_in = qh if okw["group_shared"] else f64(s["qb"][:, h:h + 1])
+            res = oracle.select_blocks(q_in, s["cr"][:, kvh:kvh + 1], s["rr"][:, kvh:kvh + 1], Tk=T, q_block=qbk,
+                                       k_block=kbk, tau_mean=tau, return_margins=True, **okw)
+            mref = res[0][:, (h - h0):(h - h0) + 1] if okw["group_shared"] else res[0]
+            margins = [m[:, (h - h0):(h - h0) + 1] if okw["group_shared"] else m for m in res[2:]]
+            diff = gm[:, h:h + 1] != mref
+            bad = diff & ~_near(*margins)
+            assert not bad.any(), f"{variant} head {h}: {int(bad.sum())} decisions differ outside the band"
+            if okw["group_shared"]:
+                break                          # every head of the group holds the same mask
+        if okw["group_shared"]:
+            assert all(np.array_equal(gm[:, h], gm[:, h0]) for h in range(h0, h0 + g))

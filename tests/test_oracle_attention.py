@@ -113,10 +113,11 @@ def test_attend_matches_torch_sdpa(n_kv, window, sink):
         ref_lse = torch.logsumexp(torch.cat([s, col], dim=-1), dim=-1)
     else:
         ref = torch.nn.functional.scaled_dot_product_attention(tq, K, V, attn_mask=m)
-        # the normaliser from scipy over numpy scores (torch's CPU logsumexp was seen to differ
-        # by ~7e-10 in about one run in fifteen; the comparison of outputs never did)
+        s = (tq @ K.transpose(-1, -2) / math.sqrt(d)).masked_fill(~m, -math.inf)
+        ref_lse = torch.logsumexp(s, dim=-1)
+        # the normaliser once more from scipy over numpy scores (an independent library)
         sn = np.einsum("bhtd,bhsd->bhts", q, K.numpy()) / math.sqrt(d)
-        ref_lse = torch.from_numpy(logsumexp(np.where(m.numpy(), sn, -np.inf), axis=-1))
+        assert np.max(np.abs(lse - logsumexp(np.where(m.numpy(), sn, -np.inf), axis=-1))) <= 1e-12
     assert np.max(np.abs(o - ref.numpy())) <= 1e-12
     assert np.max(np.abs(lse - ref_lse.numpy())) <= 1e-12
 

@@ -52,3 +52,16 @@ def test_diff_by_hand():
     b = np.exp([0.5 * 1.0, 0.5 * 3.0]); b /= b.sum()
     expect = (a[0] - lam * b[0]) * 10.0 + (a[1] - lam * b[1]) * 20.0
     assert abs(out[0, 0, 1, 0] - expect) < 1e-13
+
+
+def test_diff_rows_subset_is_the_same_rows_of_the_full_result():
+    """Evaluating only some query rows (as the full-size parity tests do) gives exactly those
+    rows of the full computation, with per-sequence lengths and a window."""
+    B, H, n_kv, T, d = 2, 4, 2, 41, 8
+    q1, k1, q2, k2, v = (_rand(s, 240 + i) for i, s in enumerate(
+        [(B, H, T, d), (B, n_kv, T, d), (B, H, T, d), (B, n_kv, T, d), (B, n_kv, T, d)]))
+    rows = np.array([0, 5, 17, 40, 23])
+    for kw in ({}, {"k_lens": [41, 36], "window": 7}):
+        full = diff_attend(q1, k1, q2, k2, v, 0.8, **kw)
+        part = diff_attend(q1, k1, q2, k2, v, 0.8, rows=rows, **kw)
+        assert np.array_equal(part, full[:, :, rows])
