@@ -409,6 +409,41 @@ def planted_scale(name, d):
     return 8.0 * math.sqrt(d) if name == "8sqrtd" else 8.0
 
 
+def part_sparse_once(torch, ga, steps, warmup, flush, peaks, tau=0.01, heads=None):
+    """The 128K block-sparse workload once per step at a fixed mean threshold: block statistics,
+    selection and the sparse attention, each timed on its own (a short case for profiling;
+    ``heads`` keeps the first query heads and their kv heads only)."""
+    from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
+    c = get_config(5)
+    B, H, n_kv, d, T, qb, kb = c.batch, c.n_heads, c.n_kv, c.d, c.Tq, c.q_block, c.k_block
+    if heads:
+        H, n_kv = heads, max(1, heads // c.g)
+    q = device_bf16(torch, c.seed, "q", (B, H, T, d))
+    kbits = randn_bhtd(c.seed, "k", (B, n_kv, T, d), "bf16")
+    for kvh, blk, tok, vec in planted_outliers(c.seed, n_kv, T, d, kb, c.planted_fraction):
+        kbits[0, kvh, tok] = f32_to_bf16_bits(vec)
+    k = torch.from_numpy(kbits.view(np.int16)).view(torch.bfloat16).cuda()
+    del kbits
+    v = device_bf16(torch, c.seed, "v", (B, n_kv, T, d))
+    nQb, nKb = T // qb, T // kb
+    cen = torch.empty(B, n_kv, nKb, d, dtype=torch.float32, device="cuda")
+    rad = torch.empty(B, n_kv, nKb, dtype=torch.float32, device="cuda")
+    mask = torch.empty(B, H, nQb, nKb, dtype=torch.uint8, device="cuda")
+    nsel = torch.empty(B, H, nQb, dtype=torch.int32, device="cuda")
+    ws = torch.empty(int(ga.lib().ga_select_workspace_size(B, H, n_kv, d, T, T, qb, kb, 0)), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(q)
+    ts = timed_steps(torch, lambda: ga.ga_block_stats(k, kb, centroid=cen, radius=rad), steps, warmup, flush)
+    tsel = timed_steps(torch, lambda: ga.ga_select_blocks(q, cen, rad, Tk=T, q_block=qb, k_block=kb, tau_mean=tau,
+                                                          lambda_radius=c.extra["lambda_radius"], block_mask=mask,
+                                                          n_selected=nsel, workspace=ws), steps, warmup, flush)
+    ta = timed_steps(torch, lambda: ga.ga_attend(q, k, v, out, block_mask=mask, q_block=qb, k_block=kb),
+                     steps, warmup, flush)
+    return {"sparse_once": {"heads": H, "tau_mean": tau, "density_blocks": float(mask.sum()) / float(mask.numel()),
+                            "stats_ms": statistics.mean(ts), "select_ms": statistics.mean(tsel),
+                            "attend_ms": statistics.mean(ta)}}
+
+
 def part_sparse(torch, ga, steps, warmup, flush, peaks, select_only=False, outlier_scale="8sqrtd"):
     from workloads import f32_to_bf16_bits, get_config, planted_outliers, randn_bhtd
     c = get_config(5)
@@ -684,6 +719,8 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
         res = part_dsa(torch, ga, args.steps, warmup, flush, peaks)
     elif args.case == "mla":
         res = part_mla(torch, ga, args.steps, warmup, flush, peaks)
+    elif args.case == "sparse_once":
+        res = part_sparse_once(torch, ga, args.steps, warmup, flush, peaks, tau=args.tau, heads=args.heads)
     else:
         res = part_sparse(torch, ga, args.steps, warmup, flush, peaks, select_only=args.case == "select",
                           outlier_scale=args.outlier_scale)
@@ -715,10 +752,15 @@ def main():
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="all",
-                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "diff", "dsa", "mla", "sparse", "select"],
+                    choices=["all", "prefill", "decode", "chunk", "window", "ring", "diff", "dsa", "mla", "sparse", "select",
+                             "sparse_once"],
                     help="run one workload alone and print its own JSON line (for profiling)")
     ap.add_argument("--outlier-scale", default="8sqrtd", choices=sorted(OUTLIER_SCALES),
                     help="norm of the 128K workload's planted keys: 8*sqrt(d) (default) or the literal 8")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="with --case sparse_once: the first query heads only (profiling captures)")
+    ap.add_argument("--tau", type=float, default=0.01,
+                    help="with --case sparse_once: the mean-branch threshold")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --case prefill/decode/chunk: a smaller batch (profiling captures)")
     args = ap.parse_args()

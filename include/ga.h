@@ -316,8 +316,8 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
  *   n_selected device int32 out [batch, n_heads, ceil(Tq/q_block)], or NULL.
  *   workspace  device scratch of ga_select_workspace_size(...) bytes, 256-byte aligned
  *              (GA_ERR_WORKSPACE otherwise): the mean query row of every query block, its
- *              norm, the row maxima and the rescue flags, computed once per call and shared
- *              by every score.  Must not be used by another call in flight.
+ *              norm, the row maxima, the rescue flags and every mean-branch score, each
+ *              computed once per call.  Must not be used by another call in flight.
  *   d: 1..256; q_block: 1..4096; ceil(Tk/k_block) <= 32768.
  */
 int ga_select_blocks(const void* q, const float* centroid, const float* radius,
@@ -328,8 +328,9 @@ int ga_select_blocks(const void* q, const float* centroid, const float* radius,
                      void* workspace, size_t workspace_bytes, ga_stream_t stream);
 
 /* Bytes of workspace ga_select_blocks / ga_select_blocks_ex need (SIZE_MAX for invalid sizes):
- * batch * P * ceil(Tq/q_block) * (d + 2) floats and batch * n_kv * ceil(Tk/k_block) bytes, each
- * part rounded to 256 bytes, with P = n_kv when group_shared is 1 and n_heads otherwise. */
+ * batch * P * ceil(Tq/q_block) * (d + 2 + S) floats and batch * n_kv * ceil(Tk/k_block) bytes,
+ * each part rounded to 256 bytes, with P = n_kv when group_shared is 1 and n_heads otherwise and
+ * S = ceil(Tk/k_block) rounded up to a multiple of 128 (one score per key block). */
 size_t ga_select_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk, int q_block,
                                 int k_block, int group_shared);
 
@@ -389,7 +390,7 @@ void ga_set_wait_timeout_ns(uint64_t ns);
 int ga_selftest_wait_timeout(uint64_t timeout_ns, ga_stream_t stream);
 
 /* Test only (the failure-path test of the pipeline waits): from the next call on, the
- * tensor-core prefill's producer in its first CTA skips the load of ring chunk number `chunk`
+ * tensor-core prefill's producer in every CTA skips the load of ring chunk number `chunk`
  * (counted over that CTA's work, from 0), so every wait on that chunk runs out after the wait
  * limit and the launch ends with GA_ERR_DEVICE_TIMEOUT in the status word, its other loads and
  * MMAs drained and its tensor memory freed.  -1 (the default) turns it off again; nothing else

@@ -47,7 +47,9 @@ class GAError(RuntimeError):
 
 
 def library_path() -> str:
-    return os.path.join(_HERE, "libga.so")
+    """The in-tree libga.so, or the library the GA_LIBRARY environment variable names (another
+    build of the same sources, e.g. one with in-kernel checks)."""
+    return os.environ.get("GA_LIBRARY") or os.path.join(_HERE, "libga.so")
 
 
 def lib() -> ctypes.CDLL:
@@ -568,6 +570,6 @@ def ga_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
 
 
 def ga_selftest_drop_prefill_chunk(chunk: int) -> None:
-    """Test only: the tensor-core prefill's first CTA skips loading ring chunk ``chunk`` from
-    the next call on, so its pipeline waits run out (-1 turns it off)."""
+    """Test only: every CTA of the tensor-core prefill skips loading its ring chunk ``chunk``
+    from the next call on, so its pipeline waits run out (-1 turns it off)."""
     lib().ga_selftest_drop_prefill_chunk(int(chunk))

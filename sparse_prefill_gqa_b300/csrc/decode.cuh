@@ -45,14 +45,15 @@ struct DecodeCfg {
   static constexpr int BODY = OFF_BAR > MERGE_BYTES ? OFF_BAR : MERGE_BYTES;
   static constexpr int SMEM_BYTES = BODY + 256 + 1024;
   static constexpr int THREADS = 160;
-  // gathered form: more stages (each warp keeps GSTAGES - 1 of its tiles in flight), then the
-  // barriers, then the chunk's cache rows (at most kGatherMaxKeys)
-  static constexpr int GSTAGES = D >= 256 ? 3 : (D >= 128 ? 6 : 12);
+  // gathered form: each warp keeps GSTAGES - 1 of its tiles in flight; then the barriers, then
+  // the chunk's cache rows (at most kGatherMaxKeys).  Up to d = 128 two CTAs fit on an SM, so one
+  // streams while the other starts or finishes.
+  static constexpr int GSTAGES = D >= 128 ? 3 : 6;
   static constexpr int GBODY = GSTAGES * STAGE_BYTES > MERGE_BYTES ? GSTAGES * STAGE_BYTES : MERGE_BYTES;
-  static constexpr int GATHER_SMEM_BYTES = GBODY + 256 + 4 * 4096 + 1024;
+  static constexpr int GATHER_SMEM_BYTES = GBODY + 256 + 4 * 1024 + 1024;
 };
 
-constexpr int kGatherMaxKeys = 4096;              // longest key chunk of the gathered form
+constexpr int kGatherMaxKeys = 1024;              // longest key chunk of the gathered form
 
 struct DecodeBars {
   uint64_t full[8], empty[8];
@@ -92,7 +93,7 @@ __device__ __forceinline__ void decode_chunk_range(const DecodeShape& s, int Tk,
 // warp, were measured at about 6 bytes per clock per SM on this workload, half the rate of these
 // copies.)
 template <int D, bool GATHER = false>
-__global__ void __launch_bounds__(160)
+__global__ void __launch_bounds__(160, D >= 256 ? 1 : 2)
 decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out,
                      float* __restrict__ lse, float* __restrict__ ws_o, float* __restrict__ ws_ml,

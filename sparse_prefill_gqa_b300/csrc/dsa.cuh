@@ -116,6 +116,7 @@ dsa_indexer_kernel(const __nv_bfloat16* __restrict__ qi, const float* __restrict
 // ordered compaction that keeps every score above it and, among scores equal to it, the lowest
 // indices -- exactly k indices (all of them when L_b <= k), in increasing order.
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkStageMax = 53248;          // longest row whose keys are staged in shared memory
 
 __device__ __forceinline__ uint32_t order_key(float x) {     // larger float -> larger key
   const uint32_t u = __float_as_uint(x);
@@ -130,10 +131,14 @@ __device__ __forceinline__ uint32_t order_key(float x) {     // larger float -> 
 //   compaction: warp w owns a contiguous segment of the scores; a first sweep counts its keys
 //     above and equal to the k-th, a second writes its selected indices at its offset, which
 //     keeps the indices in increasing order with one barrier in all.
+// STAGED: the row's keys are read from global memory once, into shared memory (L_max <=
+// kTopkStageMax), and every pass and sweep reads them there; otherwise each reads the row again.
+template <bool STAGED>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__ lens, int L_max, int topk,
                    int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
   constexpr int NW = kTopkThreads / 32;
+  extern __shared__ uint32_t skeys[];            // STAGED: the row's order-preserving keys
   __shared__ int hist[256];
   __shared__ int w_gt[NW], w_eq[NW];
   __shared__ uint32_t s_prefix;
@@ -151,6 +156,11 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
     if (threadIdx.x == 0) n_sel[b] = L;
     return;
   }
+  if (STAGED) {
+#pragma unroll 8
+    for (int j = threadIdx.x; j < L; j += kTopkThreads) skeys[j] = order_key(row[j]);
+  }
+  auto key_at = [&](int j) -> uint32_t { return STAGED ? skeys[j] : order_key(row[j]); };
   // ---- radix select of the k-th largest key ------------------------------------------------
   if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
   for (int pass = 0; pass < 4; ++pass) {
@@ -161,7 +171,7 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
     const uint32_t prefix = s_prefix;
     for (int base = 0; base < L; base += kTopkThreads) {       // uniform trip count per warp
       const int j = base + (int)threadIdx.x;
-      const uint32_t key = j < L ? order_key(row[j]) : 0u;
+      const uint32_t key = j < L ? key_at(j) : 0u;
       const bool in = j < L && (key & hi_mask) == prefix;
       const uint32_t act = __ballot_sync(0xffffffffu, in);
       if (in) {
@@ -204,7 +214,7 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
   int n_gt = 0, n_eq = 0;
   for (int base = j0; base < j1; base += 32) {
     const int j = base + lane;
-    const uint32_t key = j < j1 ? order_key(row[j]) : 0u;
+    const uint32_t key = j < j1 ? key_at(j) : 0u;
     n_gt += __popc(__ballot_sync(0xffffffffu, j < j1 && key > kth));
     n_eq += __popc(__ballot_sync(0xffffffffu, j < j1 && key == kth));
   }
@@ -220,7 +230,7 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
   int out_run = gt_before + min(eq_run, quota);
   for (int base = j0; base < j1; base += 32) {
     const int j = base + lane;
-    const uint32_t key = j < j1 ? order_key(row[j]) : 0u;
+    const uint32_t key = j < j1 ? key_at(j) : 0u;
     const bool gt = j < j1 && key > kth, eq = j < j1 && key == kth;
     const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
     const bool sel = gt || (eq && eq_run + __popc(eq_bal & lt_mask) < quota);

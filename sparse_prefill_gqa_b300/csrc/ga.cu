@@ -141,6 +141,7 @@ struct DeviceKernels {
   int decode;                   // decode_splitk_kernel, plain and gathered
   int select;                   // select_blocks_kernel
   int mla;                      // mla_decode_kernel
+  int topk;                     // topk_select_kernel with the row staged in shared memory
   int n_sm;                     // streaming multiprocessors
 };
 
@@ -183,10 +184,9 @@ const DeviceKernels* device_kernels() {
                             set_smem(decode_splitk_kernel<256, true>, DecodeCfg<256>::GATHER_SMEM_BYTES),
                             set_smem(decode_splitk_kernel<128, true>, DecodeCfg<128>::GATHER_SMEM_BYTES),
                             set_smem(decode_splitk_kernel<64, true>, DecodeCfg<64>::GATHER_SMEM_BYTES)});
-    d.select = first_error({set_smem(select_rescue_kernel, 16384 * 8),
-                            set_smem(select_score_kernel<void, false>, kScSmem),
-                            set_smem(select_score_kernel<void, true>, kScSmem)});
+    d.select = first_error({set_smem(select_rescue_kernel, 16384 * 8), set_smem(select_score_kernel, kScSmem)});
     d.mla = set_smem(mla_decode_kernel, MlaCfg::SMEM_BYTES);
+    d.topk = set_smem(topk_select_kernel<true>, kTopkStageMax * 4);
     int n_sm = 0;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) n_sm = 148;
     d.n_sm = n_sm;
@@ -537,13 +537,34 @@ int ga_topk_indices(const float* scores, const int32_t* lens, int batch, int L_m
   if (batch > 0x7fffffff / 2) return GA_ERR_UNSUPPORTED;
   for (const void* p : {(const void*)scores, (const void*)idx, (const void*)n_sel, (const void*)lens})
     if (p && (reinterpret_cast<uintptr_t>(p) & 3)) return GA_ERR_INVALID_ARG;
-  topk_select_kernel<<<batch, kTopkThreads, 0, stream>>>(scores, lens, L_max, topk, idx, n_sel);
+  if (L_max <= kTopkStageMax) {
+    const DeviceKernels* dk = device_kernels();
+    if (!dk) return GA_ERR_CUDA;
+    if (dk->topk != GA_OK) return dk->topk;
+    topk_select_kernel<true><<<batch, kTopkThreads, (size_t)L_max * 4, stream>>>(scores, lens, L_max, topk, idx, n_sel);
+  } else {
+    topk_select_kernel<false><<<batch, kTopkThreads, 0, stream>>>(scores, lens, L_max, topk, idx, n_sel);
+  }
   return launch_status();
 }
 
+namespace {
+// Key chunk of the gathered decode: about four CTAs per SM over the launch, at most
+// kGatherMaxKeys keys, the selected keys split evenly into whole 64-key tiles.
+int gather_chunk_len(int batch, int n_kv, int topk) {
+  long long want = (long long)topk * batch * n_kv / (148LL * 4);
+  want = want < 256 ? 256 : (want > kGatherMaxKeys ? kGatherMaxKeys : want);
+  const long long n = (topk + want - 1) / want;
+  return (int)(((topk + n - 1) / n + 63) / 64 * 64);
+}
+}  // namespace
+
 size_t ga_attend_gather_workspace_size(int batch, int n_heads, int n_kv, int d, int topk) {
   if (batch < 1 || n_heads < 1 || n_kv < 1 || d < 1 || topk < 1 || n_heads % n_kv != 0) return SIZE_MAX;
-  return ga_workspace_size(batch, n_heads, n_kv, d, 1, topk, GA_BF16);   // the decode's partials
+  const int chunk = gather_chunk_len(batch, n_kv, topk);
+  const size_t n_chunks = (topk + chunk - 1) / chunk;
+  if (n_chunks <= 1) return 0;                  // one chunk writes the output itself
+  return (size_t)batch * n_heads * n_chunks * (size_t)(d + 2) * sizeof(float);
 }
 
 int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int batch, int n_heads,
@@ -572,12 +593,11 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
   ds.a = sh;
   ds.g = n_heads / n_kv;
   ds.rows = ds.g;
-  ds.chunk_len = decode_chunk_len(batch, n_kv, topk);
+  ds.chunk_len = gather_chunk_len(batch, n_kv, topk);
   ds.n_chunks = (topk + ds.chunk_len - 1) / ds.chunk_len;
-  if (ds.n_chunks == 1) ds.chunk_len = (topk + 63) / 64 * 64;
   ds.gidx = idx; ds.gidx_stride = topk; ds.cache_T = Tk_max;
   ds.gk = (const __nv_bfloat16*)k; ds.gv = (const __nv_bfloat16*)v;
-  if (ds.chunk_len > kGatherMaxKeys) return GA_ERR_UNSUPPORTED;    // not reached: chunks are <= 4096 keys
+  if (ds.chunk_len > kGatherMaxKeys) return GA_ERR_UNSUPPORTED;    // not reached: chunks are <= 1024 keys
   float* ws_o = need ? static_cast<float*>(workspace) : nullptr;
   float* ws_ml = need ? ws_o + (size_t)batch * n_heads * ds.n_chunks * d : nullptr;
   CUtensorMap tk, tv;                             // not read by the gathered form
@@ -637,7 +657,7 @@ int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, co
   const DeviceKernels* dk = device_kernels();
   if (!dk) return GA_ERR_CUDA;
   if (dk->mla != GA_OK) return dk->mla;
-  mla_absorb_kernel<<<dim3(C::R / C::AB_ROWS, n_heads), 256, 0, stream>>>(
+  mla_absorb_kernel<<<dim3(C::R / C::AB_ROWS, n_heads, (batch + C::AB_SEQ - 1) / C::AB_SEQ), 256, 0, stream>>>(
       (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_rope, (const __nv_bfloat16*)w_uk, q_abs, n_heads, batch);
   mla_decode_kernel<<<dim3(s.n_chunks, batch), C::THREADS, C::SMEM_BYTES, stream>>>(tm, q_abs, ws_o, ws_ml, s);
   mla_expand_kernel<<<dim3(C::DV / C::EX_DIMS, n_heads, (batch + C::EX_SEQ - 1) / C::EX_SEQ), 256, 0, stream>>>(
@@ -719,10 +739,10 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
 }
 
 namespace {
-// Workspace of the selection: pooled query rows, their norms, the row maxima and the rescue
-// flags, each part 256-byte aligned.
+// Workspace of the selection: pooled query rows, their norms, the row maxima, the rescue flags
+// and the mean-branch scores, each part 256-byte aligned.
 struct SelectWs {
-  size_t qmean, qnorm, rowmax, rescue, total;
+  size_t qmean, qnorm, rowmax, rescue, scores, total;
 };
 SelectWs select_ws(int batch, int n_hp, int n_kv, int d, int nQb, int nKb) {
   SelectWs w;
@@ -730,7 +750,8 @@ SelectWs select_ws(int batch, int n_hp, int n_kv, int d, int nQb, int nKb) {
   w.qnorm = w.qmean + sel_up256((size_t)batch * n_hp * nQb * d * 4);
   w.rowmax = w.qnorm + sel_up256((size_t)batch * n_hp * nQb * 4);
   w.rescue = w.rowmax + sel_up256((size_t)batch * n_hp * nQb * 4);
-  w.total = w.rescue + sel_up256((size_t)batch * n_kv * nKb);
+  w.scores = w.rescue + sel_up256((size_t)batch * n_kv * nKb);
+  w.total = w.scores + sel_up256((size_t)batch * n_hp * nQb * sel_score_stride(nKb) * 4);
   return w;
 }
 }  // namespace
@@ -800,21 +821,23 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
   s.qnorm = reinterpret_cast<float*>(w + ws.qnorm);
   s.rowmax = reinterpret_cast<int*>(w + ws.rowmax);
   s.rescue = w + ws.rescue;
+  s.scores = reinterpret_cast<float*>(w + ws.scores);
   const DeviceKernels* dk = device_kernels();
   if (!dk) return GA_ERR_CUDA;
   if (dk->select != GA_OK) return dk->select;
 
-  const dim3 pool_grid(nQb, n_hp, batch);
+  const dim3 pool_grid(nQb + 1, n_hp, batch);          // column nQb: the z-score radius branch
   if (dtype == GA_BF16)
-    select_pool_kernel<__nv_bfloat16><<<pool_grid, kPoolThreads, 0, stream>>>((const __nv_bfloat16*)q, s);
+    select_pool_kernel<__nv_bfloat16><<<pool_grid, kPoolThreads, 0, stream>>>((const __nv_bfloat16*)q, radius, s);
   else
-    select_pool_kernel<float><<<pool_grid, kPoolThreads, 0, stream>>>((const float*)q, s);
-  select_rescue_kernel<<<dim3(n_kv, batch), kRescueThreads, (size_t)s.sort_len * 8, stream>>>(radius, s);
-  const dim3 score_grid((nKb_out + kScB - 1) / kScB, (nQb + kScA - 1) / kScA, batch * n_hp);
-  select_score_kernel<void, false><<<score_grid, kScThreads, kScSmem, stream>>>(centroid, radius, block_mask,
-                                                                               n_selected, s);
-  select_score_kernel<void, true><<<score_grid, kScThreads, kScSmem, stream>>>(centroid, radius, block_mask,
-                                                                              n_selected, s);
+    select_pool_kernel<float><<<pool_grid, kPoolThreads, 0, stream>>>((const float*)q, radius, s);
+  if (radius_rule == GA_RADIUS_MAD)
+    select_rescue_kernel<<<dim3(n_kv, batch), kRescueThreads, (size_t)s.sort_len * 8, stream>>>(radius, s);
+  const dim3 score_grid(((int)nKb + kScB - 1) / kScB, (nQb + kScA - 1) / kScA, batch * n_hp);
+  select_score_kernel<<<score_grid, kScThreads, kScSmem, stream>>>(centroid, s);
+  const long long n_rows = (long long)batch * n_hp * nQb;
+  select_decide_kernel<<<(unsigned)((n_rows + kDecWarps - 1) / kDecWarps), 32 * kDecWarps, 0, stream>>>(
+      radius, block_mask, n_selected, s);
   return launch_status();
 }
 

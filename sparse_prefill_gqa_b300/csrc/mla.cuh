@@ -37,7 +37,7 @@ struct MlaCfg {
   static constexpr int THREADS = 160;
   static_assert(2 * SMEM_BYTES <= 232448, "shared memory: two CTAs per SM");
   // absorb: latent rows per CTA, sequences staged at a time; expand: output dims and sequences
-  static constexpr int AB_ROWS = 64, AB_SEQ = 64, EX_DIMS = 64, EX_SEQ = 16;
+  static constexpr int AB_ROWS = 64, AB_SEQ = 16, EX_DIMS = 64, EX_SEQ = 4;
 };
 
 struct MlaShape {
@@ -46,27 +46,37 @@ struct MlaShape {
   uint64_t timeout_ns;
 };
 
-// grid: (R / 64, n_heads); block: 256.  q[b, h] = [q_nope w_uk[h]^T (fp32 sums, rounded to
-// bf16) | q_rope] for latent rows 64 x .. 64 x + 63 of head h and every sequence b: the 64 weight
-// rows (16 KB) are staged once, transposed to [dim][row] so that the threads of a warp read
-// consecutive rows, and the sequences' q_nope rows 64 at a time; thread t computes row t % 64 for
-// the sequences t / 64, t / 64 + 4, ...
+// grid: (R / 64, n_heads, ceil(batch / 16)); block: 256.  q[b, h] = [q_nope w_uk[h]^T (fp32
+// sums, rounded to bf16) | q_rope] for latent rows 64 x .. 64 x + 63 of head h and 16 sequences:
+// the 64 weight rows (16 KB) are staged transposed to [dim][row], so that the threads of a warp
+// read consecutive rows, with the sequences' q_nope rows; thread t computes row t % 64 for the
+// sequences t / 64, t / 64 + 4, ...
 __global__ void __launch_bounds__(256)
 mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16* __restrict__ q_rope,
                   const __nv_bfloat16* __restrict__ w_uk, __nv_bfloat16* __restrict__ q_abs, int n_heads,
                   int batch) {
   using C = MlaCfg;
   __shared__ __nv_bfloat16 w_s[C::DN][C::AB_ROWS + 2];  // [dim][row]
-  __shared__ __nv_bfloat16 q_s[C::AB_SEQ][C::DN];       // [sequence][dim]
+  __shared__ __align__(16) __nv_bfloat16 q_s[C::AB_SEQ][C::DN];   // [sequence][dim]
   const int rb = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
+  const int b_lo = blockIdx.z * C::AB_SEQ, b_hi = min(batch, b_lo + C::AB_SEQ);
   const int r = t % C::AB_ROWS, bg = t / C::AB_ROWS;
   const __nv_bfloat16* wsrc = w_uk + ((size_t)h * C::R + (size_t)rb * C::AB_ROWS) * C::DN;
-  for (int e = t; e < C::AB_ROWS * C::DN; e += 256) w_s[e % C::DN][e / C::DN] = wsrc[e];
-  for (int b0 = 0; b0 < batch; b0 += C::AB_SEQ) {
-    const int nb = min(C::AB_SEQ, batch - b0);
+  for (int e = t; e < C::AB_ROWS * C::DN / 8; e += 256) {     // 16-byte loads, 8 dims of one row
+    const uint4 v = *reinterpret_cast<const uint4*>(wsrc + 8 * e);
+    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&v);
+    const int row = (8 * e) / C::DN, k0 = (8 * e) % C::DN;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) w_s[k0 + u][row] = x[u];
+  }
+  for (int b0 = b_lo; b0 < b_hi; b0 += C::AB_SEQ) {
+    const int nb = min(C::AB_SEQ, b_hi - b0);
     __syncthreads();
-    for (int e = t; e < nb * C::DN; e += 256)
-      q_s[e / C::DN][e % C::DN] = q_nope[((size_t)(b0 + e / C::DN) * n_heads + h) * C::DN + e % C::DN];
+    for (int e = t; e < nb * C::DN / 8; e += 256) {
+      const int bb = (8 * e) / C::DN, k0 = (8 * e) % C::DN;
+      *reinterpret_cast<uint4*>(&q_s[bb][k0]) =
+          *reinterpret_cast<const uint4*>(q_nope + ((size_t)(b0 + bb) * n_heads + h) * C::DN + k0);
+    }
     __syncthreads();
     float a[C::AB_SEQ / 4];
 #pragma unroll
@@ -83,10 +93,11 @@ mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16*
       if (b < b0 + nb) q_abs[((size_t)b * n_heads + h) * C::DK + rb * C::AB_ROWS + r] = __float2bfloat16_rn(a[i]);
     }
   }
-  if (rb == 0)                                          // the rope part of every sequence's query
-    for (int e = t; e < batch * C::DR; e += 256)
-      q_abs[((size_t)(e / C::DR) * n_heads + h) * C::DK + C::R + e % C::DR] =
-          q_rope[((size_t)(e / C::DR) * n_heads + h) * C::DR + e % C::DR];
+  if (rb == 0)                                          // the rope part of the sequences' queries
+    for (int e = t; e < (b_hi - b_lo) * C::DR; e += 256) {
+      const size_t row = (size_t)(b_lo + e / C::DR) * n_heads + h;
+      q_abs[row * C::DK + C::R + e % C::DR] = q_rope[row * C::DR + e % C::DR];
+    }
 }
 
 struct MlaBars {
@@ -323,20 +334,24 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
   }
 }
 
-// grid: (DV / 64, n_heads, ceil(batch / 16)); block: 256.  For 16 sequences of head h: the chunk
-// partials re-associated into the latent output (o_lat = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M)
-// l_c over the chunks holding tokens; one warp per two sequences, the lanes over the latent
-// dims), then out = o_lat w_uv[h] for output dims 64 x .. 64 x + 63 (thread t: dim t % 64 of
-// sequences t / 64 + 4 i; fp32 sums, each weight element read once for the 16 sequences).
+// grid: (DV / 64, n_heads, ceil(batch / 4)); block: 256.  For 4 sequences of head h: warps 0-3
+// re-associate the chunk partials of one sequence each into the latent output (o_lat = sum_c
+// 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the chunks holding tokens; the lanes over the
+// latent dims, the chunks' loads overlapped), then out = o_lat w_uv[h] for output dims 64 x ..
+// 64 x + 63: thread t takes dim t % 64 over latent dims 128 (t / 64) .. + 127 for the 4
+// sequences (fp32 sums, every weight element read once for all 4), and the four partial sums of
+// each output meet in shared memory.
 __global__ void __launch_bounds__(256)
 mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
                   const __nv_bfloat16* __restrict__ w_uv, __nv_bfloat16* __restrict__ out, MlaShape s) {
   using C = MlaCfg;
   __shared__ float lat[C::EX_SEQ][C::R];
+  __shared__ float part[4][C::EX_SEQ][C::EX_DIMS];
   const int xb = blockIdx.x, h = blockIdx.y, b0 = blockIdx.z * C::EX_SEQ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = min(C::EX_SEQ, s.batch - b0);
-  for (int i = warp; i < C::EX_SEQ; i += 8) {
+  if (warp < C::EX_SEQ) {
+    const int i = warp;
     float o[C::R / 32];
 #pragma unroll
     for (int u = 0; u < C::R / 32; ++u) o[u] = 0.0f;
@@ -345,17 +360,18 @@ mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_m
       const int L = seq_keys(s.lens, b, s.L_max);
       const size_t qrow = (size_t)b * s.n_heads + h;
       const int n_used = min(s.n_chunks, (L + s.chunk_len - 1) / s.chunk_len);
+      const float* ml = ws_ml + qrow * s.n_chunks * 2;
       float M = -INFINITY;
-      for (int c = lane; c < n_used; c += 32) M = fmaxf(M, ws_ml[(qrow * s.n_chunks + c) * 2]);
+      for (int c = lane; c < n_used; c += 32) M = fmaxf(M, ml[2 * c]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
       float Lsum = 0.0f;
       if (M != -INFINITY) {
+#pragma unroll 2
         for (int c = 0; c < n_used; ++c) {
-          const float mc = ws_ml[(qrow * s.n_chunks + c) * 2];
-          if (mc == -INFINITY) continue;
-          const float f = ex2(mc - M);
-          Lsum += f * ws_ml[(qrow * s.n_chunks + c) * 2 + 1];
+          const float mc = ml[2 * c];
+          const float f = mc == -INFINITY ? 0.0f : ex2(mc - M);
+          Lsum = fmaf(f, ml[2 * c + 1], Lsum);
           const float* src = ws_o + (qrow * s.n_chunks + c) * C::R + lane;
 #pragma unroll
           for (int u = 0; u < C::R / 32; ++u) o[u] = fmaf(f, src[32 * u], o[u]);
@@ -369,19 +385,24 @@ mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_m
     for (int u = 0; u < C::R / 32; ++u) lat[i][lane + 32 * u] = o[u];
   }
   __syncthreads();
-  const int e = threadIdx.x % C::EX_DIMS, rg = threadIdx.x / C::EX_DIMS;
-  const __nv_bfloat16* w = w_uv + (size_t)h * C::R * C::DV + xb * C::EX_DIMS + e;
-  float a[C::EX_SEQ / 4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-  for (int c = 0; c < C::R; ++c) {
+  const int e = threadIdx.x % C::EX_DIMS, cp = threadIdx.x / C::EX_DIMS;   // output dim, latent quarter
+  const __nv_bfloat16* w = w_uv + ((size_t)h * C::R + (size_t)cp * (C::R / 4)) * C::DV + xb * C::EX_DIMS + e;
+  float a[C::EX_SEQ] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 16
+  for (int c = 0; c < C::R / 4; ++c) {
     const float wc = __bfloat162float(w[(size_t)c * C::DV]);
 #pragma unroll
-    for (int i = 0; i < C::EX_SEQ / 4; ++i) a[i] = fmaf(lat[rg + 4 * i][c], wc, a[i]);
+    for (int i = 0; i < C::EX_SEQ; ++i) a[i] = fmaf(lat[i][cp * (C::R / 4) + c], wc, a[i]);
   }
 #pragma unroll
-  for (int i = 0; i < C::EX_SEQ / 4; ++i) {
-    const int r = rg + 4 * i;
-    if (r < nb) out[((size_t)(b0 + r) * s.n_heads + h) * C::DV + xb * C::EX_DIMS + e] = __float2bfloat16_rn(a[i]);
+  for (int i = 0; i < C::EX_SEQ; ++i) part[cp][i][e] = a[i];
+  __syncthreads();
+  if (threadIdx.x < C::EX_SEQ * C::EX_DIMS) {
+    const int i = threadIdx.x / C::EX_DIMS, d = threadIdx.x % C::EX_DIMS;
+    if (i < nb) {
+      const float y = (part[0][i][d] + part[1][i][d]) + (part[2][i][d] + part[3][i][d]);
+      out[((size_t)(b0 + i) * s.n_heads + h) * C::DV + xb * C::EX_DIMS + d] = __float2bfloat16_rn(y);
+    }
   }
 }
 

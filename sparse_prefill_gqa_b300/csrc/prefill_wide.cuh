@@ -9,8 +9,8 @@
 // attention is computed only over the blocks the selection keeps).
 //
 // Items are numbered heaviest causal tiles first across every (query head, sequence); a CTA's
-// producer takes the next unclaimed item from a launch-wide counter whenever it is ready for
-// one (so the longest items start first and the CTAs finish together whatever the sequence
+// producer takes the next unclaimed item from a launch-wide counter, one item ahead of the one
+// it loads (so the longest items start first and the CTAs finish together whatever the sequence
 // lengths), and publishes it to the CTA's other roles.  The warps run decoupled across items:
 // while the softmax
 // warpgroups finish one item (the last tiles and the epilogue), the producer already loads the
@@ -30,16 +30,20 @@
 // output accumulator O_w in tensor memory; the epilogue merges the two partial results by the
 // log-sum-exp rule (the same re-association as split-K decode).  The split depends on the item
 // alone, never on which items the CTA ran before, so results do not depend on the scheduling.
+// Tile j of an item uses S buffer j % 2 and accumulates into O_(j%2): buffer, accumulator and
+// warpgroup go together, and each role counts the uses of each buffer (the barrier phases)
+// across the CTA's items.
 //   warps 0-3, 4-7  softmax: thread r of a warpgroup = query row r = TMEM lane r;
 //   warp 8          producer: Q once per item, then K and V through a ring of 32 KB chunks
 //                   (5 slots), K one tile ahead of V; lists the units of block-masked items;
-//   warp 9          S issuer (one lane): S(J) = Q K(J)^T into S buffer J & 1;
-//   warp 10         PV issuer (one lane): O_(j%2) += P(J) V(J), j the tile's index in its item;
+//   warp 9          S issuer (one lane): S(j) = Q K(j)^T into S buffer j % 2;
+//   warp 10         PV issuer (one lane): O_(j%2) += P(j) V(j), j the tile's index in its item;
 //   warp 11         idle (completes the warpgroup whose registers move to the softmax).
-// Tensor memory: O_0 [0,128), O_1 [128,256), S buffers [256,384) and [384,512).  P(J) (bf16) is
-// written over the first 64 columns of S buffer J & 1 and read from there by the PV MMA, in two
-// halves of 64 keys.  S(J+2) overwrites P(J), so the S issuer waits for PV(J) first.  The first
-// PV of an item into an accumulator waits until the previous item's epilogue has read it.
+// Tensor memory: O_0 [0,128), O_1 [128,256), S buffers [256,384) and [384,512).  P (bf16) is
+// written over the first 64 columns of its tile's S buffer and read from there by the PV MMA, in
+// two halves of 64 keys.  The next S into a buffer overwrites that P, so the S issuer waits for
+// its PV first.  The first PV of an item into an accumulator waits until the previous item's
+// epilogue has read it.
 //
 // d = 256 (6 warps): one softmax warpgroup takes every tile, warp 4 is the producer, warp 5
 // alone issues S(J+1) before PV(J) (in-order completion makes S overwrite P only after PV read
@@ -183,9 +187,9 @@ __host__ __device__ inline long long wide_items(const AttnShape& sh) {
 // kernel compiles to contiguous 128-key tiles only.
 // EPI: the epilogue's mode (WideEpi::mode), fixed at compile time so that plain launches carry
 // none of the other modes' code.
-// drop_chunk: test only -- the producer skips the load of ring chunk number drop_chunk (counted
-// over the CTA's sequence) of CTA 0, so the waits on it run out; -1 (always, outside the
-// failure-path test) loads every chunk.
+// drop_chunk: test only -- every CTA's producer skips the load of its ring chunk number
+// drop_chunk (counted over the CTA's sequence), so the waits on it run out; -1 (always, outside
+// the failure-path test) loads every chunk.
 template <int D_, bool UNITS, int EPI = 0>
 __global__ void __launch_bounds__(WideCfg<D_>::THREADS, 1)
 prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -271,10 +275,16 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       int cnt = 0, n_tail = 0, J = 0, qn = 0;          // chunks, tail chunks, tiles, Q loads
       bool ok = true;
+      // Items are claimed one ahead (the heaviest one left each time), so that the next index is
+      // known by the time this item's loads are issued.
+      int w_next = n_items;
+      if (lane == 0) w_next = (int)atomicAdd(&g_wide_next[epoch], 1u);
       for (int k_item = 0;; ++k_item) {
-        // claim the next item (the heaviest one left)
         int w = n_items;
-        if (lane == 0 && ok) w = (int)atomicAdd(&g_wide_next[epoch], 1u);
+        if (lane == 0 && ok) {
+          w = w_next;
+          if (w < n_items) w_next = (int)atomicAdd(&g_wide_next[epoch], 1u);
+        }
         w = __shfl_sync(0xffffffffu, w, 0);
         const bool end = w >= n_items;
         const WideItem it = wide_item<BM, BN>(sh, end ? 0 : w);
@@ -371,7 +381,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
               int slot;
               if (!slot_acquire(slot)) return false;
               unsigned char* dst = sR + slot * C::CHUNK;
-              if (cnt != drop_chunk || blockIdx.x != 0) {
+              if (cnt != drop_chunk) {
                 mbar_arrive_expect_tx(&bars->full[slot], C::CHUNK);
                 for (int s = 0; s < 2; ++s) {
                   if (!UNITS) {
@@ -537,6 +547,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           static_assert(C::KCH == 1 && C::VCH == 1 && C::VK == C::BN, "d = 128 chunk layout");
           const int xi = warp - C::W_S;                    // 0: S issuer, 1: PV issuer
           int pos0 = 0, J = 0, qn = 0;
+          int uses0 = 0, uses1 = 0;                        // S issuer: S per buffer; PV issuer: PV per buffer
           for (int k_item = 0;; ++k_item) {
             int w, n_tiles;
             if (!(ok = item_get(k_item, false, w, n_tiles)) || w < 0) break;
@@ -546,12 +557,14 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (xi == 0) {
               if (!(ok = mbar_wait(&bars->q_full, qn & 1, tmo, abort_flag))) break;
               for (int j = 0; ok && j < n_tiles; ++j) {
-                // S(J) into buffer J & 1, once PV(J-2) has read the P held there.  K(J) is waited
-                // for first: it has usually landed long before, so only the PV wait is exposed.
-                const int Jg = J + j, buf = Jg & 1;
+                // S(j) into buffer j % 2, once the PV of the buffer's previous tile has read the P
+                // held there.  K(j) is waited for first: it has usually landed long before, so
+                // only the PV wait is exposed.
+                const int buf = j & 1, u = buf ? uses1 : uses0;
                 const int pos = kpos(j), slot = pos % C::RING;
                 if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
-                if (Jg >= 2 && !(ok = mbar_wait(&bars->p_free[buf], ((Jg >> 1) - 1) & 1, tmo, abort_flag))) break;
+                if (u >= 1 && !(ok = mbar_wait(&bars->p_free[buf], (u - 1) & 1, tmo, abort_flag))) break;
+                if (buf) ++uses1; else ++uses0;
                 tc_fence_after();
                 const uint32_t d_s = tmem + C::COL_S + buf * BN;
                 const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
@@ -566,21 +579,22 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
               }
               if (ok) umma_commit(&bars->q_free);               // the item's last S read Q
             } else {
-              // O_(j%2) += P(J) V(J), P in the first 64 columns of S buffer J & 1.  The softmax
+              // O_(j%2) += P(j) V(j), P in the first 64 columns of S buffer j % 2.  The softmax
               // publishes P in two halves of 64 keys; the first half's MMAs run while the
               // second half is exponentiated.
               for (int j = 0; ok && j < n_tiles; ++j) {
-                const int Jg = J + j, buf = Jg & 1;
+                const int buf = j & 1, u = buf ? uses1 : uses0;
+                if (buf) ++uses1; else ++uses0;
                 const int pos = vpos(j), slot = pos % C::RING;
                 if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
                 // the item's first PVs overwrite O_0 and O_1: the previous item's epilogue has
                 // read them
                 if (j == 0 && qn > 0 && !(ok = mbar_wait(&bars->o_free, (qn - 1) & 1, tmo, abort_flag))) break;
                 const uint32_t p_col = tmem + C::COL_S + buf * BN;
-                const uint32_t d_o = tmem + C::COL_O + (j & 1) * D;
+                const uint32_t d_o = tmem + C::COL_O + buf * D;
                 const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
                 for (int half = 0; ok && half < 2; ++half) {
-                  if (!(ok = mbar_wait(&bars->p_full[buf][half], (Jg >> 1) & 1, tmo, abort_flag))) break;
+                  if (!(ok = mbar_wait(&bars->p_full[buf][half], u & 1, tmo, abort_flag))) break;
                   tc_fence_after();
 #pragma unroll
                   for (int k4 = 0; k4 < 4; ++k4) {               // 4 steps of 16 keys
@@ -615,6 +629,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const float scale_log2 = kLog2e / sqrtf((float)D);
     float2* xch = reinterpret_cast<float2*>(smem + C::OFF_XCH);
     int J = 0, qn = 0;
+    int own = 0;                                      // d = 128: tiles this warpgroup has taken (uses of S buffer wg)
     for (int k_item = 0;; ++k_item) {
       int w = -1, n_tiles = 0;
       bool ok = item_get(k_item, true, w, n_tiles);
@@ -634,8 +649,11 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       // this warpgroup's tiles of the item: j with j % NWG == wg
       const int j_first = C::DUAL ? wg : 0;
       for (int j = j_first; ok && j < n_tiles; j += C::NWG) {
-        const int Jg = J + j, buf = Jg & 1;
-        if (!(ok = warp_wait(&bars->s_full[buf], (Jg >> 1) & 1, tmo, abort_flag))) break;
+        const int Jg = J + j;
+        const int buf = C::DUAL ? wg : (Jg & 1);
+        const uint32_t s_par = C::DUAL ? (uint32_t)(own & 1) : (uint32_t)((Jg >> 1) & 1);
+        if (C::DUAL) ++own;
+        if (!(ok = warp_wait(&bars->s_full[buf], s_par, tmo, abort_flag))) break;
         tc_fence_after();
         const uint32_t t_s = tmem + C::COL_S + buf * BN + lane_off;
         float sv[BN];
@@ -792,13 +810,13 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const float L = l0 * a0 + l1 * a1;
         const float inv_l = L > 0.0f ? 1.0f / L : 0.0f;
         const float s0 = a0 * inv_l, s1 = a1 * inv_l;
-        const bool has0 = n_tiles >= 1, has1 = n_tiles >= 2;
+        const bool has0 = n_tiles >= 1, has1 = n_tiles >= 2;   // warpgroup w had a tile of the item
         const uint32_t t_o0 = tmem + C::COL_O + lane_off, t_o1 = t_o0 + D;
 #pragma unroll 1
         for (int c = 64 * wg; c < 64 * wg + 64; c += 32) {
           float o0[32], o1[32];
-          if (has0) tmem_ld32(t_o0 + c, o0);
-          if (has1) tmem_ld32(t_o1 + c, o1);
+          tmem_ld32(t_o0 + c, o0);              // both always: a select drops an unused one
+          tmem_ld32(t_o1 + c, o1);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 32; ++u) {

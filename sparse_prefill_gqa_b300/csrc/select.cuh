@@ -14,12 +14,12 @@
 //                             once at the copy rate; each row maximum starts at -inf
 //   2. select_rescue_kernel   per (sequence, kv head): the radius statistics in fp64 and the
 //                             rescue flag of every key block, once
-//   3. select_score_kernel<A> scores of 128 query blocks x 128 key blocks per CTA, fp32 fused
-//                             multiply-adds in dimension order; the row maxima by atomicMax
-//   4. select_score_kernel<B> the same scores, bit for bit (same operations, same order),
-//                             thresholded, OR-ed with rescue, diagonal and bound, written as
-//                             mask rows through shared memory, and the per-row counts
-// The pooled queries, row maxima and rescue flags live in the caller's workspace.
+//   3. select_score_kernel    scores of 128 query blocks x 128 key blocks per CTA, fp32 fused
+//                             multiply-adds in dimension order, stored once; the row maxima by
+//                             atomicMax
+//   4. select_decide_kernel   per row: the stored scores thresholded, OR-ed with rescue, diagonal
+//                             and bound, written as the mask rows, and the per-row counts
+// The pooled queries, row maxima, rescue flags and scores live in the caller's workspace.
 #pragma once
 
 #include "attend_simt.cuh"
@@ -40,6 +40,7 @@ struct SelectShape {
   float* qnorm;                   // workspace [batch, n_hp, nQb]: their Euclidean norms
   int* rowmax;                    // workspace [batch, n_hp, nQb]: row maxima, order-preserving ints
   uint8_t* rescue;                // workspace [batch, n_kv, nKb]: radius-branch flags
+  float* scores;                  // workspace [batch, n_hp, nQb, stride]: the mean-branch scores
 };
 
 // Bytes of each workspace part, 256-byte aligned.
@@ -53,6 +54,30 @@ __device__ __forceinline__ int f2ord(float f) {
 }
 __device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
 
+// Key blocks query block alpha may see, [vlo, vhi): rows at absolute positions i_first .. i_last
+// = Tk - Tq + those rows; with the causal rule the last visible block holds key i_last, with a
+// window the first holds key i_first - W + 1.
+__device__ __forceinline__ void sel_visible(const SelectShape& s, int alpha, int& vlo, int& vhi) {
+  const long long t0 = (long long)alpha * s.q_block;
+  const long long t1 = min((long long)s.Tq, t0 + s.q_block);
+  const long long i_first = (long long)s.Tk - s.Tq + t0, i_last = (long long)s.Tk - s.Tq + t1 - 1;
+  vhi = s.causal ? (int)min((long long)s.nKb, i_last / s.k_block + 1) : s.nKb;
+  vlo = 0;
+  if (s.causal && s.window > 0) {
+    const long long x = i_first - s.window + 1;
+    vlo = x <= 0 ? 0 : (int)(x / s.k_block);
+  }
+}
+
+// Key blocks overlapping the query block's own positions [i_first, i_last]: [dlo, dhi].
+__device__ __forceinline__ void sel_diagonal(const SelectShape& s, int alpha, int& dlo, int& dhi) {
+  const long long t0 = (long long)alpha * s.q_block;
+  const long long t1 = min((long long)s.Tq, t0 + s.q_block);
+  const long long i_first = (long long)s.Tk - s.Tq + t0, i_last = (long long)s.Tk - s.Tq + t1 - 1;
+  dlo = (int)(i_first / s.k_block);
+  dhi = (int)min((long long)s.nKb - 1, i_last / s.k_block);
+}
+
 // ---------------------------------------------------------------------------------------
 // 1. Pooling: one CTA per (query block, pooled head, sequence).  bf16 rows with d = 8 L
 // (L = 1 .. 32): lane l reads 16 bytes (8 dims, 8 (l % L) ..) of rows l / L + k 32 / L, the
@@ -61,12 +86,18 @@ __device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i
 // ---------------------------------------------------------------------------------------
 constexpr int kPoolThreads = 128;
 
+__device__ void rescue_zscore(const float* __restrict__ radius, SelectShape s, int kvh, int b);
+
 template <typename T>
 __global__ void __launch_bounds__(kPoolThreads)
-select_pool_kernel(const T* __restrict__ q, SelectShape s) {
+select_pool_kernel(const T* __restrict__ q, const float* __restrict__ radius, SelectShape s) {
   __shared__ float part[kPoolThreads / 32][kSimtMaxD];
   __shared__ float mean_s[kSimtMaxD];
   const int alpha = blockIdx.x, hp = blockIdx.y, b = blockIdx.z;
+  if (alpha == s.nQb) {         // the extra column: the z-score radius branch, beside the pooling
+    if (s.radius_rule == 0 && hp < s.n_kv) rescue_zscore(radius, s, hp, b);
+    return;
+  }
   const int d = s.d, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = s.n_heads / s.n_kv;
   const int h0 = s.group_shared ? hp * g : hp, n_pool = s.group_shared ? g : 1;
@@ -118,10 +149,10 @@ select_pool_kernel(const T* __restrict__ q, SelectShape s) {
 }
 
 // ---------------------------------------------------------------------------------------
-// 2. Radius branch: one CTA per (kv head, sequence).  z rule: mean and population std of the
-// kv head's radii in fp64 (a fixed reduction tree); MAD rule: median and median absolute
-// deviation by an exact fp64 bitonic sort in shared memory.  rescue = z >= lambda (nothing
-// when the scale is zero).
+// 2. Radius branch: one CTA per (kv head, sequence) -- extra CTAs of the pooling launch for the z
+// rule (mean and population std of the kv head's radii in fp64, a fixed reduction tree), a launch
+// of its own for the MAD rule (median and median absolute deviation by an exact fp64 bitonic sort
+// in shared memory).  rescue = z >= lambda (nothing when the scale is zero).
 // ---------------------------------------------------------------------------------------
 constexpr int kRescueThreads = 512;
 
@@ -144,6 +175,38 @@ __device__ inline double sorted_median(const double* buf, int n) {
   return (n & 1) ? buf[n / 2] : (buf[n / 2 - 1] + buf[n / 2]) * 0.5;
 }
 
+// z rule by the CTA's threads (any multiple of 32 up to 1024): mean and population std of the kv
+// head's radii in fp64 over a fixed reduction tree (strided per-thread sums, then the warps in
+// order), and z >= lambda tested as r - mu >= lambda sigma (no fp64 division, which is slow here).
+__device__ void rescue_zscore(const float* __restrict__ radius, SelectShape s, int kvh, int b) {
+  __shared__ double zred[32];
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31, nw = nt >> 5;
+  const float* rrow = radius + ((size_t)b * s.n_kv + kvh) * s.nKb_out;
+  uint8_t* out = s.rescue + ((size_t)b * s.n_kv + kvh) * s.nKb;
+  auto block_sum = [&](double x) -> double {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    __syncthreads();
+    if (lane == 0) zred[warp] = x;
+    __syncthreads();
+    double tot = 0.0;
+    for (int w = 0; w < nw; ++w) tot += zred[w];
+    return tot;
+  };
+  double acc = 0.0;
+  for (int x = tid; x < s.nKb; x += nt) acc += (double)rrow[x];
+  const double mu = block_sum(acc) / s.nKb;
+  acc = 0.0;
+  for (int x = tid; x < s.nKb; x += nt) {
+    const double e = (double)rrow[x] - mu;
+    acc += e * e;
+  }
+  const double sigma = sqrt(block_sum(acc) / s.nKb);
+  const double bar = (double)s.lambda_radius * sigma;
+  for (int x = tid; x < s.nKb; x += nt) out[x] = (sigma > 0.0 && (double)rrow[x] - mu >= bar) ? 1 : 0;
+}
+
+// The MAD rule (the z rule runs inside the pooling launch).
 __global__ void __launch_bounds__(kRescueThreads)
 select_rescue_kernel(const float* __restrict__ radius, SelectShape s) {
   extern __shared__ double sortbuf[];                // rule 1: sort_len doubles
@@ -163,17 +226,7 @@ select_rescue_kernel(const float* __restrict__ radius, SelectShape s) {
     return tot;
   };
   if (s.radius_rule == 0) {
-    double acc = 0.0;
-    for (int x = tid; x < s.nKb; x += kRescueThreads) acc += (double)rrow[x];
-    const double mu = block_sum(acc) / s.nKb;
-    acc = 0.0;
-    for (int x = tid; x < s.nKb; x += kRescueThreads) {
-      const double e = (double)rrow[x] - mu;
-      acc += e * e;
-    }
-    const double sigma = sqrt(block_sum(acc) / s.nKb);
-    for (int x = tid; x < s.nKb; x += kRescueThreads)
-      out[x] = (sigma > 0.0 && ((double)rrow[x] - mu) / sigma >= (double)s.lambda_radius) ? 1 : 0;
+    rescue_zscore(radius, s, kvh, b);
   } else {
     for (int x = tid; x < s.sort_len; x += kRescueThreads) sortbuf[x] = x < s.nKb ? (double)rrow[x] : INFINITY;
     __syncthreads();
@@ -186,18 +239,22 @@ select_rescue_kernel(const float* __restrict__ radius, SelectShape s) {
     rescue_sort(sortbuf, s.sort_len);
     const double mad = sorted_median(sortbuf, s.nKb);
     const double scale_r = 1.4826 * mad;   // consistency factor of the MAD for normal data
+    const double bar = (double)s.lambda_radius * scale_r;
     for (int x = tid; x < s.nKb; x += kRescueThreads)
-      out[x] = (mad > 0.0 && ((double)rrow[x] - med) / scale_r >= (double)s.lambda_radius) ? 1 : 0;
+      out[x] = (mad > 0.0 && (double)rrow[x] - med >= bar) ? 1 : 0;
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// 3./4. Scores.  One CTA per (128 key blocks, 128 query blocks, pooled head x sequence), 8
-// warps.  Lane l owns query blocks l, l + 32, l + 64, l + 96 of the tile, warp w key blocks
-// 16 w .. 16 w + 15, so each dimension step is four conflict-free loads of query means (one
-// per query block, consecutive across the lanes), four broadcast 16-byte loads of centroids,
-// and 64 fused multiply-adds (32 packed instructions); the query means and centroids are
-// staged 64 dimensions at a time, dimension-major.
+// 3. Scores.  One CTA per (128 key blocks, 128 query blocks, pooled head x sequence), 8 warps,
+// two CTAs per SM.  Lane l owns query blocks l, l + 32, l + 64, l + 96 of the tile, warp w key
+// blocks 16 w .. 16 w + 15, so each dimension step is four conflict-free loads of query means
+// (one per query block, consecutive across the lanes), four broadcast 16-byte loads of centroids,
+// and 64 fused multiply-adds (32 packed instructions); the query means and centroids are staged
+// 64 dimensions at a time, dimension-major.  Every score s = acc / sqrt(d) (fp32) is stored in the
+// workspace through shared memory (whole 512-byte row segments) and the row maxima over the
+// visible key blocks go to the workspace by atomicMax.  Tiles no query block of which sees a key
+// block of the CTA's range store nothing.
 // ---------------------------------------------------------------------------------------
 constexpr int kScThreads = 256;
 constexpr int kScA = 128;            // query blocks per CTA
@@ -205,211 +262,213 @@ constexpr int kScB = 128;            // key blocks per CTA
 constexpr int kScDC = 64;            // dimensions staged at a time
 constexpr int kScQS = kScA + 4;      // row stride (floats) of the staged query means [c][a]
 constexpr int kScCS = kScB + 4;      // row stride (floats) of the staged centroids [c][beta]
-constexpr int kScMS = kScB + 16;     // row stride (bytes) of the staged mask rows [a][beta]
-// shared memory: query means | centroids | mask rows | per-row ranges, maxima, norms, counts
-constexpr int kScSmem = kScDC * (kScQS + kScCS) * 4 + kScA * kScMS + kScA * 4 * 4 + kScA * 4 * 2 +
-                        (kScThreads / 32) * kScA * 4 + kScB;
+constexpr int kScSS = kScB + 4;      // row stride (floats) of the staged scores [a][beta]
+// shared memory: query means | centroids (the scores reuse both) | per-row ranges | warp maxima
+constexpr int kScSmem = kScDC * (kScQS + kScCS) * 4 + kScA * 4 * 4 + (kScThreads / 32) * kScA * 4;
+static_assert(kScA * kScSS <= kScDC * (kScQS + kScCS), "scores fit in the staging area");
 
-template <typename Unused, bool PASS_B>
+// Row stride of the stored scores: the key blocks rounded up to whole CTA ranges.
+__host__ __device__ inline int sel_score_stride(int nKb) { return (nKb + kScB - 1) / kScB * kScB; }
+
 __global__ void __launch_bounds__(kScThreads, 2)
-select_score_kernel(const float* __restrict__ centroid, const float* __restrict__ radius,
-                    uint8_t* __restrict__ block_mask, int32_t* __restrict__ n_selected, SelectShape s) {
+select_score_kernel(const float* __restrict__ centroid, SelectShape s) {
   extern __shared__ __align__(16) unsigned char sc_smem[];
   float* sq = reinterpret_cast<float*>(sc_smem);                       // [DC][QS]
   float* sc = sq + kScDC * kScQS;                                      // [DC][CS]
-  uint8_t* sm = reinterpret_cast<uint8_t*>(sc + kScDC * kScCS);        // [A][MS]
-  int* rng = reinterpret_cast<int*>(sm + kScA * kScMS);                // [A][4]
-  float* rmax = reinterpret_cast<float*>(rng + kScA * 4);              // [A]
-  float* qn = rmax + kScA;                                             // [A]
-  int* wpart = reinterpret_cast<int*>(qn + kScA);                      // [8][A]
-  uint8_t* resc = reinterpret_cast<uint8_t*>(wpart + (kScThreads / 32) * kScA);   // [B]
+  float* ss = sq;                                                      // [A][SS] (after the dot products)
+  int* rng = reinterpret_cast<int*>(sc + kScDC * kScCS);               // [A][2]: visible [vlo, vhi)
+  int* wpart = rng + kScA * 4;                                         // [8][A]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int beta0 = blockIdx.x * kScB, a0 = blockIdx.y * kScA;
   const int b = blockIdx.z / s.n_hp, hp = blockIdx.z % s.n_hp;
   const int g = s.n_heads / s.n_kv;
   const int kvh = s.group_shared ? hp : hp / g;
-  const int h_out0 = s.group_shared ? hp * g : hp, n_out = s.group_shared ? g : 1;
   const int d = s.d;
   const size_t row0 = ((size_t)b * s.n_hp + hp) * s.nQb;             // first pooled row of (b, hp)
 
-  // per query block of the tile: visible key blocks [vlo, vhi), diagonal blocks [dlo, dhi]
   for (int i = tid; i < kScA; i += kScThreads) {
     const int alpha = a0 + i;
-    int vlo = 0, vhi = 0, dlo = 1, dhi = 0;                            // empty by default
-    if (alpha < s.nQb) {
-      const long long t0 = (long long)alpha * s.q_block;
-      const long long t1 = min((long long)s.Tq, t0 + s.q_block);
-      const long long i_first = (long long)s.Tk - s.Tq + t0, i_last = (long long)s.Tk - s.Tq + t1 - 1;
-      vhi = s.causal ? (int)min((long long)s.nKb, i_last / s.k_block + 1) : s.nKb;
-      if (s.causal && s.window > 0) {
-        const long long x = i_first - s.window + 1;                    // first key a row may see
-        vlo = x <= 0 ? 0 : (int)(x / s.k_block);
-      }
-      dlo = (int)(i_first / s.k_block);
-      dhi = (int)min((long long)s.nKb - 1, i_last / s.k_block);
-      if (PASS_B) {
-        rmax[i] = ord2f(s.rowmax[row0 + alpha]);
-        qn[i] = s.qnorm[row0 + alpha];
-      }
-    }
-    rng[4 * i + 0] = vlo; rng[4 * i + 1] = vhi; rng[4 * i + 2] = dlo; rng[4 * i + 3] = dhi;
-    if (!PASS_B && blockIdx.x == 0 && alpha < s.nQb && n_selected)    // pass B adds the counts
-      for (int o = 0; o < n_out; ++o) n_selected[((size_t)b * s.n_heads + h_out0 + o) * s.nQb + alpha] = 0;
+    int vlo = 0, vhi = 0;
+    if (alpha < s.nQb) sel_visible(s, alpha, vlo, vhi);
+    rng[4 * i + 0] = vlo;
+    rng[4 * i + 1] = vhi;
   }
-  if (PASS_B)
-    for (int j = tid; j < kScB; j += kScThreads)
-      resc[j] = beta0 + j < s.nKb ? s.rescue[((size_t)b * s.n_kv + kvh) * s.nKb + beta0 + j] : 0;
   __syncthreads();
   // does any query block of the tile see a key block of this CTA's range?
   bool mine = false;
-  for (int i = lane; i < kScA; i += 32)
-    mine |= max(rng[4 * i], beta0) < min(rng[4 * i + 1], beta0 + kScB);
-  const bool any = __syncthreads_or(mine ? 1 : 0) != 0;
-  const int n_cols = min(kScB, s.nKb_out - beta0);                    // mask columns of the CTA
-  const int n_rows = min(kScA, s.nQb - a0);
-  const bool vec4 = (s.nKb_out % 4) == 0 && (reinterpret_cast<uintptr_t>(block_mask) & 3) == 0;
+  for (int i = lane; i < kScA; i += 32) mine |= max(rng[4 * i], beta0) < min(rng[4 * i + 1], beta0 + kScB);
+  if (__syncthreads_or(mine ? 1 : 0) == 0) return;
 
-  if (any) {
-    float acc[4][16];
+  float acc[4][16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
-    const float* cbase = centroid + ((size_t)b * s.n_kv + kvh) * (size_t)s.nKb_out * d;
-    const float* qbase = s.qmean + row0 * d;
-    for (int c0 = 0; c0 < d; c0 += kScDC) {
-      const int dc = min(kScDC, d - c0);
-      __syncthreads();
-      // stage query means and centroids of dims c0 .. c0 + dc, dimension-major (zeros outside):
-      // 16-byte loads along a row, the block index fastest across threads, so that the
-      // transposed stores of a warp fall in consecutive banks
-      if (d % 4 == 0) {
-        for (int e = tid; e < kScA * (kScDC / 4); e += kScThreads) {
-          const int a = e % kScA, c = 4 * (e / kScA);
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (c < dc && a0 + a < s.nQb) v = *reinterpret_cast<const float4*>(qbase + (size_t)(a0 + a) * d + c0 + c);
-          sq[(c + 0) * kScQS + a] = v.x;
-          sq[(c + 1) * kScQS + a] = v.y;
-          sq[(c + 2) * kScQS + a] = v.z;
-          sq[(c + 3) * kScQS + a] = v.w;
-        }
-        for (int e = tid; e < kScB * (kScDC / 4); e += kScThreads) {
-          const int j = e % kScB, c = 4 * (e / kScB);
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (c < dc && beta0 + j < s.nKb) v = *reinterpret_cast<const float4*>(cbase + (size_t)(beta0 + j) * d + c0 + c);
-          sc[(c + 0) * kScCS + j] = v.x;
-          sc[(c + 1) * kScCS + j] = v.y;
-          sc[(c + 2) * kScCS + j] = v.z;
-          sc[(c + 3) * kScCS + j] = v.w;
-        }
-      } else {
-        for (int e = tid; e < kScA * kScDC; e += kScThreads) {
-          const int a = e % kScA, c = e / kScA;
-          sq[c * kScQS + a] = (c < dc && a0 + a < s.nQb) ? qbase[(size_t)(a0 + a) * d + c0 + c] : 0.0f;
-        }
-        for (int e = tid; e < kScB * kScDC; e += kScThreads) {
-          const int j = e % kScB, c = e / kScB;
-          sc[c * kScCS + j] = (c < dc && beta0 + j < s.nKb) ? cbase[(size_t)(beta0 + j) * d + c0 + c] : 0.0f;
-        }
+    for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
+  const float* cbase = centroid + ((size_t)b * s.n_kv + kvh) * (size_t)s.nKb_out * d;
+  const float* qbase = s.qmean + row0 * d;
+  for (int c0 = 0; c0 < d; c0 += kScDC) {
+    const int dc = min(kScDC, d - c0);
+    __syncthreads();
+    // stage query means and centroids of dims c0 .. c0 + dc, dimension-major (zeros outside):
+    // 16-byte loads along a row, the block index fastest across threads, so that the
+    // transposed stores of a warp fall in consecutive banks
+    if (d % 4 == 0) {
+      for (int e = tid; e < kScA * (kScDC / 4); e += kScThreads) {
+        const int a = e % kScA, c = 4 * (e / kScA);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < dc && a0 + a < s.nQb) v = *reinterpret_cast<const float4*>(qbase + (size_t)(a0 + a) * d + c0 + c);
+        sq[(c + 0) * kScQS + a] = v.x;
+        sq[(c + 1) * kScQS + a] = v.y;
+        sq[(c + 2) * kScQS + a] = v.z;
+        sq[(c + 3) * kScQS + a] = v.w;
       }
-      __syncthreads();
-      const float* qp = sq + lane;
-      const float* cp = sc + 16 * warp;
-#pragma unroll 2
-      for (int c = 0; c < dc; ++c) {       // fused multiply-adds in dimension order, two per op
-        float x[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[i] = qp[c * kScQS + 32 * i];
-        const float4 y0 = *reinterpret_cast<const float4*>(cp + c * kScCS);
-        const float4 y1 = *reinterpret_cast<const float4*>(cp + c * kScCS + 4);
-        const float4 y2 = *reinterpret_cast<const float4*>(cp + c * kScCS + 8);
-        const float4 y3 = *reinterpret_cast<const float4*>(cp + c * kScCS + 12);
-        const float ys[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
-                              y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 16; j += 2)
-            ffma2(acc[i][j], acc[i][j + 1], ys[j], ys[j + 1], x[i], x[i], acc[i][j], acc[i][j + 1]);
-      }
-    }
-    const float scale = 1.0f / sqrtf((float)d);
-    if (!PASS_B) {
-      // row maxima over the visible key blocks: per thread, over the warps, then atomicMax
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int a = lane + 32 * i;
-        const int vlo = rng[4 * a], vhi = rng[4 * a + 1];
-        float m = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int beta = beta0 + 16 * warp + j;
-          if (beta >= vlo && beta < vhi) m = fmaxf(m, __fmul_rn(acc[i][j], scale));
-        }
-        wpart[warp * kScA + a] = f2ord(m);
-      }
-      __syncthreads();
-      for (int a = tid; a < n_rows; a += kScThreads) {
-        int m = wpart[a];
-        for (int w = 1; w < kScThreads / 32; ++w) m = max(m, wpart[w * kScA + a]);
-        if (m > f2ord(-INFINITY)) atomicMax(&s.rowmax[row0 + a0 + a], m);
-      }
-      return;
-    }
-    // pass B: keep = visible && (mean || rescue || diagonal || bound); the bytes of each row go
-    // to shared memory first
-    const bool bound = s.tau_bound != -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int a = lane + 32 * i;
-      const int vlo = rng[4 * a], vhi = rng[4 * a + 1], dlo = rng[4 * a + 2], dhi = rng[4 * a + 3];
-      const float thr = rmax[a] - s.tau_mean, thr_b = rmax[a] - s.tau_bound, qna = qn[a];
-      uint32_t w4[4] = {0u, 0u, 0u, 0u};
-      int kept = 0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int jl = 16 * warp + j, beta = beta0 + jl;
-        const bool vis = beta >= vlo && beta < vhi;
-        const float sc_ = __fmul_rn(acc[i][j], scale);
-        bool keep = vis && (sc_ >= thr || resc[jl] != 0 || (beta >= dlo && beta <= dhi));
-        if (bound && vis && !keep) keep = __fmaf_rn(qna, __fmul_rn(radius[((size_t)b * s.n_kv + kvh) * s.nKb_out + beta], scale), sc_) >= thr_b;
-        w4[j >> 2] |= (keep ? 1u : 0u) << (8 * (j & 3));
-        kept += keep ? 1 : 0;
-      }
-      *reinterpret_cast<uint4*>(sm + a * kScMS + 16 * warp) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      wpart[warp * kScA + a] = kept;
-    }
-  } else if (PASS_B) {
-    for (int e = tid; e < kScA * kScB / 16; e += kScThreads)
-      *reinterpret_cast<uint4*>(sm + (e / (kScB / 16)) * kScMS + 16 * (e % (kScB / 16))) = make_uint4(0u, 0u, 0u, 0u);
-    for (int e = tid; e < (kScThreads / 32) * kScA; e += kScThreads) wpart[e] = 0;
-  } else {
-    return;                                           // pass A: nothing visible here
-  }
-  __syncthreads();
-  // the tile's mask rows, every head written (all g heads of the group when group-shared)
-  for (int o = 0; o < n_out; ++o) {
-    uint8_t* mbase = block_mask + (((size_t)b * s.n_heads + h_out0 + o) * s.nQb + a0) * s.nKb_out + beta0;
-    if (vec4 && n_cols == kScB) {
-      for (int e = tid; e < n_rows * (kScB / 4); e += kScThreads) {
-        const int a = e / (kScB / 4), q4 = e % (kScB / 4);
-        *reinterpret_cast<uint32_t*>(mbase + (size_t)a * s.nKb_out + 4 * q4) =
-            *reinterpret_cast<const uint32_t*>(sm + a * kScMS + 4 * q4);
+      for (int e = tid; e < kScB * (kScDC / 4); e += kScThreads) {
+        const int j = e % kScB, c = 4 * (e / kScB);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < dc && beta0 + j < s.nKb) v = *reinterpret_cast<const float4*>(cbase + (size_t)(beta0 + j) * d + c0 + c);
+        sc[(c + 0) * kScCS + j] = v.x;
+        sc[(c + 1) * kScCS + j] = v.y;
+        sc[(c + 2) * kScCS + j] = v.z;
+        sc[(c + 3) * kScCS + j] = v.w;
       }
     } else {
-      for (int e = tid; e < n_rows * kScB; e += kScThreads) {
-        const int a = e / kScB, j = e % kScB;
-        if (j < n_cols) mbase[(size_t)a * s.nKb_out + j] = sm[a * kScMS + j];
+      for (int e = tid; e < kScA * kScDC; e += kScThreads) {
+        const int a = e % kScA, c = e / kScA;
+        sq[c * kScQS + a] = (c < dc && a0 + a < s.nQb) ? qbase[(size_t)(a0 + a) * d + c0 + c] : 0.0f;
+      }
+      for (int e = tid; e < kScB * kScDC; e += kScThreads) {
+        const int j = e % kScB, c = e / kScB;
+        sc[c * kScCS + j] = (c < dc && beta0 + j < s.nKb) ? cbase[(size_t)(beta0 + j) * d + c0 + c] : 0.0f;
       }
     }
-    if (n_selected)
-      for (int a = tid; a < n_rows; a += kScThreads) {
-        int cnt = 0;
-        for (int w = 0; w < kScThreads / 32; ++w) cnt += wpart[w * kScA + a];
-        if (cnt) atomicAdd(&n_selected[((size_t)b * s.n_heads + h_out0 + o) * s.nQb + a0 + a], cnt);
-      }
+    __syncthreads();
+    const float* qp = sq + lane;
+    const float* cp = sc + 16 * warp;
+#pragma unroll 2
+    for (int c = 0; c < dc; ++c) {       // fused multiply-adds in dimension order, two per op
+      float x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = qp[c * kScQS + 32 * i];
+      const float4 y0 = *reinterpret_cast<const float4*>(cp + c * kScCS);
+      const float4 y1 = *reinterpret_cast<const float4*>(cp + c * kScCS + 4);
+      const float4 y2 = *reinterpret_cast<const float4*>(cp + c * kScCS + 8);
+      const float4 y3 = *reinterpret_cast<const float4*>(cp + c * kScCS + 12);
+      const float ys[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
+                            y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 16; j += 2)
+          ffma2(acc[i][j], acc[i][j + 1], ys[j], ys[j + 1], x[i], x[i], acc[i][j], acc[i][j + 1]);
+    }
   }
+  const float scale = 1.0f / sqrtf((float)d);
+  __syncthreads();                                   // the staging area now holds the scores
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int a = lane + 32 * i;
+    const int vlo = rng[4 * a], vhi = rng[4 * a + 1];
+    float sv[16];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      sv[j] = __fmul_rn(acc[i][j], scale);
+      const int beta = beta0 + 16 * warp + j;
+      if (beta >= vlo && beta < vhi) m = fmaxf(m, sv[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; j += 4)
+      *reinterpret_cast<float4*>(ss + a * kScSS + 16 * warp + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+    wpart[warp * kScA + a] = f2ord(m);
+  }
+  __syncthreads();
+  const int n_rows = min(kScA, s.nQb - a0);
+  const int stride = sel_score_stride(s.nKb);
+  for (int a = tid; a < n_rows; a += kScThreads) {
+    int m = wpart[a];
+    for (int w = 1; w < kScThreads / 32; ++w) m = max(m, wpart[w * kScA + a]);
+    if (m > f2ord(-INFINITY)) atomicMax(&s.rowmax[row0 + a0 + a], m);
+  }
+  float* dst = s.scores + (row0 + a0) * stride + beta0;
+  for (int e = tid; e < n_rows * (kScB / 4); e += kScThreads) {
+    const int a = e / (kScB / 4), q4 = e % (kScB / 4);
+    *reinterpret_cast<float4*>(dst + (size_t)a * stride + 4 * q4) = *reinterpret_cast<const float4*>(ss + a * kScSS + 4 * q4);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// 4. Decisions.  One warp per (query block, pooled head, sequence) row: keep = visible && (s >=
+// max - tau_mean || rescue || diagonal || bound), read from the stored scores and written as
+// the mask row of every head of the row (all g heads of the group when group-shared), with the
+// row's count.  Lane l takes key blocks 4 l + 128 t .. + 3: 16-byte score loads, 4-byte mask
+// stores where the row length allows.
+// ---------------------------------------------------------------------------------------
+constexpr int kDecWarps = 8;
+
+__global__ void __launch_bounds__(32 * kDecWarps)
+select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ block_mask,
+                     int32_t* __restrict__ n_selected, SelectShape s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kDecWarps + warp;    // (b, hp, alpha)
+  if (row >= (long long)s.batch * s.n_hp * s.nQb) return;
+  const int alpha = (int)(row % s.nQb);
+  const int bh = (int)(row / s.nQb), b = bh / s.n_hp, hp = bh % s.n_hp;
+  const int g = s.n_heads / s.n_kv;
+  const int kvh = s.group_shared ? hp : hp / g;
+  const int h_out0 = s.group_shared ? hp * g : hp, n_out = s.group_shared ? g : 1;
+  int vlo, vhi, dlo, dhi;
+  sel_visible(s, alpha, vlo, vhi);
+  sel_diagonal(s, alpha, dlo, dhi);
+  const float rmax = ord2f(s.rowmax[row]);
+  const float thr = rmax - s.tau_mean, thr_b = rmax - s.tau_bound, qn = s.qnorm[row];
+  const bool bound = s.tau_bound != -INFINITY;
+  const float scale = 1.0f / sqrtf((float)s.d);
+  const float* srow = s.scores + (size_t)row * sel_score_stride(s.nKb);
+  const float* rrow = radius + ((size_t)b * s.n_kv + kvh) * s.nKb_out;
+  const uint8_t* resc = s.rescue + ((size_t)b * s.n_kv + kvh) * s.nKb;
+  const bool vec4 = (s.nKb_out % 4) == 0 && (reinterpret_cast<uintptr_t>(block_mask) & 3) == 0;
+  int kept = 0;
+  for (int base = 4 * lane; base < s.nKb_out; base += 4 * 128) {
+    float4 sv[4];                                   // four steps' scores in flight
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int beta0 = base + 128 * u;
+      sv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (beta0 < s.nKb_out && beta0 + 3 >= vlo && beta0 < vhi)    // stored for every visible block
+        sv[u] = *reinterpret_cast<const float4*>(srow + beta0);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+    const int beta0 = base + 128 * u;
+    if (beta0 >= s.nKb_out) break;
+    uint32_t bytes = 0u;
+    const float sa[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int beta = beta0 + jj;
+      const bool vis = beta >= vlo && beta < vhi;
+      bool keep = vis && (sa[jj] >= thr || resc[beta] != 0 || (beta >= dlo && beta <= dhi));
+      if (bound && vis && !keep) keep = __fmaf_rn(qn, __fmul_rn(rrow[beta], scale), sa[jj]) >= thr_b;
+      bytes |= (keep ? 1u : 0u) << (8 * jj);
+      kept += keep ? 1 : 0;
+    }
+    for (int o = 0; o < n_out; ++o) {
+      uint8_t* mrow = block_mask + (((size_t)b * s.n_heads + h_out0 + o) * s.nQb + alpha) * s.nKb_out;
+      if (vec4) {
+        *reinterpret_cast<uint32_t*>(mrow + beta0) = bytes;
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          if (beta0 + jj < s.nKb_out) mrow[beta0 + jj] = (uint8_t)((bytes >> (8 * jj)) & 1u);
+      }
+    }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
+  if (lane == 0 && n_selected)
+    for (int o = 0; o < n_out; ++o) n_selected[((size_t)b * s.n_heads + h_out0 + o) * s.nQb + alpha] = kept;
 }
 
 }  // namespace ga

@@ -200,7 +200,10 @@ def test_topk_sparse_decode_calls_reject_invalid_arguments(L):
     assert gather(lse=ctypes.c_void_p(4100)) == ga.GA_ERR_INVALID_ARG
     assert gather(ws=None) == ga.GA_ERR_WORKSPACE                      # 16 key chunks: partials needed
     assert gather(wsb=16) == ga.GA_ERR_WORKSPACE
-    # the gathered decode needs only the split-K partials over topk keys
+    # the gathered decode needs only the split-K partials over topk keys: one sequence with two
+    # kv heads splits 8192 selected keys into 32 chunks of 256 (about four CTAs per SM over the
+    # launch, at least 256 keys a chunk), one fp32 partial row of d plus (max, sum) per head
     need = L.ga_attend_gather_workspace_size(1, 8, 2, 128, 8192)
-    assert need > 0 and need == L.ga_workspace_size(1, 8, 2, 128, 1, 8192, 1)
+    assert need == 1 * 8 * 32 * (128 + 2) * 4
+    assert L.ga_attend_gather_workspace_size(64, 32, 8, 128, 2048) == 64 * 32 * 2 * (128 + 2) * 4   # 2 x 1024
     assert L.ga_attend_gather_workspace_size(1, 6, 4, 128, 8192) == 2 ** 64 - 1

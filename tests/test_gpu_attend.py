@@ -219,15 +219,15 @@ def test_failure_path_reports_device_timeout_and_context_survives():
 @pytest.mark.parametrize("d,masked", [(128, False), (256, False), (128, True)])
 def test_prefill_pipeline_wait_runs_out_then_recovers(d, masked):
     """The waits inside the tensor-core prefill's TMA/MMA pipeline are bounded too: with one K
-    chunk of the first CTA never loaded (a test-only switch) and a 1 ms limit, the launch ends
-    by itself with GA_ERR_DEVICE_TIMEOUT recorded -- its warps leave together, drain their
-    loads and MMAs and free tensor memory -- and the next launches on the same context are
-    exact again."""
-    B, H, n_kv, T = 1, 2, 1, 1024
-    q, _ = host_tensor(45, "q", (B, H, T, d), "bf16")
-    k, _ = host_tensor(45, "k", (B, n_kv, T, d), "bf16")
-    v, _ = host_tensor(45, "v", (B, n_kv, T, d), "bf16")
-    bm = torch.ones(B, H, T // 128, T // 64, dtype=torch.uint8, device="cuda") if masked else None
+    chunk never loaded (a test-only switch) on a one-CTA launch (one query tile over 1024 keys,
+    8 key tiles) and a 1 ms limit, the launch ends by itself with GA_ERR_DEVICE_TIMEOUT
+    recorded -- its warps leave together, drain their loads and MMAs and free tensor memory --
+    and the next launches on the same context are exact again."""
+    B, H, n_kv, Tq, Tk = 1, 1, 1, 128, 1024
+    q, _ = host_tensor(45, "q", (B, H, Tq, d), "bf16")
+    k, _ = host_tensor(45, "k", (B, n_kv, Tk, d), "bf16")
+    v, _ = host_tensor(45, "v", (B, n_kv, Tk, d), "bf16")
+    bm = torch.ones(B, H, 1, Tk // 64, dtype=torch.uint8, device="cuda") if masked else None
     assert ga.ga_read_device_status() == ga.GA_OK
     ga.ga_set_wait_timeout_ns(1_000_000)
     ga.ga_selftest_drop_prefill_chunk(3)
