@@ -296,23 +296,68 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (masked && n_tiles > 0) {
           // the selected 64-key units in key order, paired into tiles (unit list_a[t] in the
           // first half of tile t, list_b[t] in the second), by the whole warp
-          // (16 mask bytes per lane in flight at a time: one memory round trip per 512 units)
           const int u_lo = it.key_lo / 64, u_hi = (it.key_hi + 63) / 64;
           const uint32_t lt = (1u << lane) - 1u;
           int run = 0;
-          for (int base = u_lo; base < u_hi; base += 32 * 16) {
-            bool sel[16];
+          auto put = [&](int rank, int u) {
+            if (rank < 2 * C::LIST_MAX) (rank & 1 ? list_b : list_a)[rank >> 1] = (uint32_t)u;
+          };
+          if (sh.k_block == 64) {
+            // one mask byte per unit: the row is read as 16-byte words (the aligned words
+            // covering units u_lo ... u_hi - 1; bytes outside that range are ignored), four
+            // words a lane in flight, so a row of 2048 units is a single memory round trip
+            const uintptr_t a0 = reinterpret_cast<uintptr_t>(mrow + u_lo) & ~uintptr_t(15);
+            const int n_words = (int)((reinterpret_cast<uintptr_t>(mrow + u_hi) - a0 + 15) >> 4);
+            const int u_a0 = (int)((intptr_t)a0 - reinterpret_cast<intptr_t>(mrow));   // unit of a0's byte 0
+            for (int w0 = 0; w0 < n_words; w0 += 32 * 4) {
+              uint4 wv[4];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-              const int u = base + 32 * r + lane;
-              sel[r] = u < u_hi && mrow[(64 * u) / sh.k_block] != 0;
+              for (int r = 0; r < 4; ++r) {
+                const int wi = w0 + 32 * r + lane;
+                wv[r] = wi < n_words ? __ldg(reinterpret_cast<const uint4*>(a0) + wi) : make_uint4(0u, 0u, 0u, 0u);
+              }
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const int ub = u_a0 + 16 * (w0 + 32 * r + lane);          // unit of this word's byte 0
+                // bit j: byte j is nonzero (the top bit of each byte of __vcmpne4, gathered to
+                // bits 28..31 by one multiply: the four partial products land on distinct bits)
+                const uint32_t wd[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+                uint32_t bits = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  bits |= (((__vcmpne4(wd[c], 0u) & 0x80808080u) * 0x00204081u) >> 28) << (4 * c);
+                const int cut_lo = min(max(u_lo - ub, 0), 16), cut_hi = min(max(u_hi - ub, 0), 16);
+                bits &= ((1u << cut_hi) - 1u) & ~((1u << cut_lo) - 1u);
+                const int c = __popc(bits);
+                int incl = c;                                  // inclusive prefix over the lanes
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                  const int t = __shfl_up_sync(0xffffffffu, incl, off);
+                  if (lane >= off) incl += t;
+                }
+                int rank = run + incl - c;
+                while (bits) {
+                  put(rank++, ub + __ffs(bits) - 1);
+                  bits &= bits - 1u;
+                }
+                run += __shfl_sync(0xffffffffu, incl, 31);
+              }
             }
+          } else {
+            // several units per mask byte: 16 mask bytes per lane in flight at a time
+            for (int base = u_lo; base < u_hi; base += 32 * 16) {
+              bool sel[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-              const uint32_t bal = __ballot_sync(0xffffffffu, sel[r]);
-              const int rank = run + __popc(bal & lt);
-              if (sel[r] && rank < 2 * C::LIST_MAX) (rank & 1 ? list_b : list_a)[rank >> 1] = (uint32_t)(base + 32 * r + lane);
-              run += __popc(bal);
+              for (int r = 0; r < 16; ++r) {
+                const int u = base + 32 * r + lane;
+                sel[r] = u < u_hi && mrow[(64 * u) / sh.k_block] != 0;
+              }
+#pragma unroll
+              for (int r = 0; r < 16; ++r) {
+                const uint32_t bal = __ballot_sync(0xffffffffu, sel[r]);
+                if (sel[r]) put(run + __popc(bal & lt), base + 32 * r + lane);
+                run += __popc(bal);
+              }
             }
           }
           if (run <= 2 * C::LIST_MAX) {     // else: contiguous tiles, masked per half
@@ -332,6 +377,24 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (end || !ok) break;
+        {
+          // The next item is already claimed: start moving its Q tile and its mask row into L2,
+          // so that its list and its first scores are not held up by memory latency when this
+          // item's loads are done.
+          const int wn = __shfl_sync(0xffffffffu, w_next, 0);
+          if (wn < n_items) {
+            const WideItem nx = wide_item<BM, BN>(sh, wn);
+            if (lane == 0)
+              for (int s = 0; s < D / 64; ++s)
+                tma_prefetch_l2_3d(&tm_q, 64 * s, nx.t0, nx.b * sh.n_heads + nx.h);
+            if (masked && nx.n_dense > 0) {
+              const uint8_t* mr = sh.block_mask + (((size_t)nx.b * sh.n_heads + nx.h) * sh.nQb + nx.t0 / sh.q_block) * sh.nKb;
+              const uintptr_t a0 = reinterpret_cast<uintptr_t>(mr + (64 * (nx.key_lo / 64)) / sh.k_block) & ~uintptr_t(127);
+              const uintptr_t a1 = reinterpret_cast<uintptr_t>(mr + (64 * ((nx.key_hi + 63) / 64) - 1) / sh.k_block);
+              for (uintptr_t a = a0 + 128 * lane; a <= a1; a += 128 * 32) prefetch_l2(reinterpret_cast<const void*>(a));
+            }
+          }
+        }
         if (lane == 0 && ok && n_tiles > 0) {
           // Tile t's units; a lone unit is loaded into both halves, the second masked, so that
           // no half ever holds unloaded data.
@@ -410,17 +473,20 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
               bool tail = false;
               for (int p = 0; p < PARTS; ++p) tail |= 64 * part_unit(p) + 64 > it.Tk;
               uint64_t* bar = tail ? &bars->v_tail : &bars->full[slot];
-              mbar_arrive_expect_tx(bar, C::CHUNK);
-              for (int s = 0; s < D / 64; ++s) {
-                if (!UNITS) {
-                  tma_load_3d(dst + s * C::VK * 128, &tm_v, bar, 64 * s, (it.kt_lo + j) * BN + C::VK * c, kz);
-                } else {
-                  for (int p = 0; p < PARTS; ++p)
-                    tma_load_3d(dst + s * C::VK * 128 + p * 64 * 128, &tm_v64, bar, 64 * s, 64 * part_unit(p), kz);
+              const bool drop = cnt == drop_chunk;
+              if (!drop) {
+                mbar_arrive_expect_tx(bar, C::CHUNK);
+                for (int s = 0; s < D / 64; ++s) {
+                  if (!UNITS) {
+                    tma_load_3d(dst + s * C::VK * 128, &tm_v, bar, 64 * s, (it.kt_lo + j) * BN + C::VK * c, kz);
+                  } else {
+                    for (int p = 0; p < PARTS; ++p)
+                      tma_load_3d(dst + s * C::VK * 128 + p * 64 * 128, &tm_v64, bar, 64 * s, 64 * part_unit(p), kz);
+                  }
                 }
               }
               if (tail) {
-                if (!mbar_wait(&bars->v_tail, n_tail & 1, tmo, abort_flag)) return false;
+                if (drop || !mbar_wait(&bars->v_tail, n_tail & 1, tmo, abort_flag)) return false;
                 ++n_tail;
                 for (int p = 0; p < PARTS; ++p)
                   for (int row = max(0, it.Tk - 64 * part_unit(p)); row < 64; ++row)

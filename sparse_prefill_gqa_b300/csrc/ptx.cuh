@@ -141,6 +141,18 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Starts moving a tile of a tensor into L2 (no shared memory, no completion to wait for): a
+// later tma_load_3d of the same box then finds it there.  Same coordinate rule as the load.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z) : "memory");
+}
+
+// Starts moving the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // ---------------------------------------------------------------------------------------
 // tcgen05: tensor memory, UMMA, commit, TMEM <-> register moves
 // ---------------------------------------------------------------------------------------
