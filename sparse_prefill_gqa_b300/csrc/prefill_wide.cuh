@@ -80,8 +80,9 @@ struct WideCfg {
   static constexpr int IINFO = 4;                       // item ring (block masks)
   static constexpr int OFF_IINFO = OFF_TINFO + TINFO * 16;        // IINFO x int2 (item, tiles)
   static constexpr int LIST_MAX = 2048;                 // block-mask tile list: tiles (2 units each)
-  static constexpr int OFF_LIST = OFF_IINFO + 64;
-  static constexpr int SMEM_BYTES = OFF_LIST + 2 * LIST_MAX * 4 + 1024;
+  static constexpr int OFF_LIST = OFF_IINFO + 64;       // 2 x LIST_MAX 16-bit unit indices
+  static constexpr int OFF_STAGE = (OFF_LIST + 2 * LIST_MAX * 2 + 127) / 128 * 128;   // epilogue: 2 KB a softmax warp
+  static constexpr int SMEM_BYTES = OFF_STAGE + 8 * 2048 + 1024;
   static constexpr int NWG = DUAL ? 2 : 1;              // softmax warpgroups
   static constexpr int SM_THREADS = 128 * NWG;          // softmax threads
   static constexpr int W_PROD = 4 * NWG;                // producer warp
@@ -130,7 +131,7 @@ struct WideEpi {
 };
 
 // A list entry naming no unit: the tile holds one unit, in its first half.
-constexpr uint32_t kUnitNone = 0xFFFFFFFFu;
+constexpr uint16_t kUnitNone = 0xFFFFu;
 
 // Launch-wide item counters.  Launch number e (host side, modulo kWideEpochs) claims items from
 // g_wide_next[e] and counts its finished CTAs in g_wide_done[e]; the last CTA to finish sets
@@ -206,8 +207,8 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   WideBars* bars = reinterpret_cast<WideBars*>(smem + C::OFF_BAR);
   WideTile* tinfo = reinterpret_cast<WideTile*>(smem + C::OFF_TINFO);
   int2* iinfo = reinterpret_cast<int2*>(smem + C::OFF_IINFO);
-  uint32_t* list_a = reinterpret_cast<uint32_t*>(smem + C::OFF_LIST);
-  uint32_t* list_b = list_a + C::LIST_MAX;
+  uint16_t* list_a = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST);
+  uint16_t* list_b = list_a + C::LIST_MAX;
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -293,14 +294,16 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const uint8_t* mrow = masked
             ? sh.block_mask + (((size_t)it.b * sh.n_heads + it.h) * sh.nQb + it.t0 / sh.q_block) * sh.nKb
             : nullptr;
-        if (masked && n_tiles > 0) {
+        // (unit indices are 16-bit: sequences of more than 64 * 65534 keys take the contiguous
+        // tiles, masked per half)
+        if (masked && n_tiles > 0 && (it.key_hi + 63) / 64 < (int)kUnitNone) {
           // the selected 64-key units in key order, paired into tiles (unit list_a[t] in the
           // first half of tile t, list_b[t] in the second), by the whole warp
           const int u_lo = it.key_lo / 64, u_hi = (it.key_hi + 63) / 64;
           const uint32_t lt = (1u << lane) - 1u;
           int run = 0;
           auto put = [&](int rank, int u) {
-            if (rank < 2 * C::LIST_MAX) (rank & 1 ? list_b : list_a)[rank >> 1] = (uint32_t)u;
+            if (rank < 2 * C::LIST_MAX) (rank & 1 ? list_b : list_a)[rank >> 1] = (uint16_t)u;
           };
           if (sh.k_block == 64) {
             // one mask byte per unit: the row is read as 16-byte words (the aligned words
@@ -400,7 +403,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           // no half ever holds unloaded data.
           auto tile_units = [&](int t, int& ua, int& ub, uint32_t& present) {
             if (list) {
-              const uint32_t lb = list_b[t];
+              const uint16_t lb = list_b[t];
               ua = (int)list_a[t];
               ub = lb == kUnitNone ? ua : (int)lb;
               present = lb == kUnitNone ? 1u : 3u;
@@ -529,8 +532,12 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           mbar_wait(&bars->full[k % C::RING], (k / C::RING) & 1, tmo, nullptr);
       }
     } else if (warp == C::W_S || warp == C::W_PV) {
-      // The issuer warps issue MMAs and nothing else.
-      if (lane == 0) {
+      // The issuer warps issue MMAs and nothing else.  Each runs its loop with all 32 lanes
+      // converged (every wait, index and descriptor is the same in every lane) and one elected
+      // lane executes each tcgen05 instruction: issued that way, with the descriptors of a
+      // tile's MMAs a per-chunk base plus constants, one warp keeps pace with the tensor pipe
+      // (64 cycles per 128x128x16 MMA); issued from a lone lane it cannot.
+      {
         constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
         const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -547,7 +554,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const uint32_t d_s = tmem + C::COL_S + (Jg & 1) * BN;
             for (int c = 0; c < C::KCH; ++c) {
               const int slot = cnt % C::RING;
-              if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
+              if (!warp_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
               tc_fence_after();
               const uint64_t bk = dr_k + (uint64_t)((slot * C::CHUNK) >> 4);
 #pragma unroll
@@ -555,12 +562,12 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 const int kk = 8 * c + k8;
                 const uint64_t aq = dq + (uint64_t)(((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4);
                 const uint64_t bo = bk + (uint64_t)(((k8 >> 2) * BN * 128 + (k8 & 3) * 32) >> 4);
-                umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
+                umma_bf16_ss_elect(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
               }
-              umma_commit(&bars->empty[slot]);
+              umma_commit_elect(&bars->empty[slot]);
               ++cnt;
             }
-            umma_commit(&bars->s_full[Jg & 1]);
+            umma_commit_elect(&bars->s_full[Jg & 1]);
             return true;
           };
           // O (+)= P(J) V(J), P in the first 64 columns of S buffer J & 1
@@ -568,44 +575,44 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const uint32_t p_col = tmem + C::COL_S + (Jg & 1) * BN;
             for (int c = 0; c < C::VCH; ++c) {
               const int slot = cnt % C::RING;
-              if (!mbar_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
+              if (!warp_wait(&bars->full[slot], (cnt / C::RING) & 1, tmo, abort_flag)) return false;
               tc_fence_after();
               const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
 #pragma unroll
               for (int k4 = 0; k4 < C::VK / 16; ++k4) {       // steps of 16 keys in this chunk
                 const int kk = (C::VK / 16) * c + k4;
-                umma_bf16_ts(tmem + C::COL_O, p_col + kk * 8, bv + (uint64_t)((k4 * 2048) >> 4), idesc_pv,
+                umma_bf16_ts_elect(tmem + C::COL_O, p_col + kk * 8, bv + (uint64_t)((k4 * 2048) >> 4), idesc_pv,
                              (!first || kk > 0) ? 1u : 0u);
               }
-              umma_commit(&bars->empty[slot]);
+              umma_commit_elect(&bars->empty[slot]);
               ++cnt;
             }
             return true;
           };
           for (;; ++k_item) {
             int w, n_tiles;
-            if (!(ok = item_get(k_item, false, w, n_tiles)) || w < 0) break;
+            if (!(ok = item_get(k_item, true, w, n_tiles)) || w < 0) break;
             if (n_tiles == 0) continue;
-            if (!(ok = mbar_wait(&bars->q_full, qn & 1, tmo, abort_flag))) break;
+            if (!(ok = warp_wait(&bars->q_full, qn & 1, tmo, abort_flag))) break;
             if (!(ok = issue_s(J))) break;
             for (int j = 0; ok && j < n_tiles; ++j) {
               const int Jg = J + j;
               if (j + 1 < n_tiles && !(ok = issue_s(Jg + 1))) break;
-              if (j + 1 == n_tiles) umma_commit(&bars->q_free);   // every S of the item issued
-              if (!(ok = mbar_wait(&bars->p_full[0][0], Jg & 1, tmo, abort_flag))) break;
+              if (j + 1 == n_tiles) umma_commit_elect(&bars->q_free);   // every S of the item issued
+              if (!(ok = warp_wait(&bars->p_full[0][0], Jg & 1, tmo, abort_flag))) break;
               // the item's first PV overwrites O: the previous item's epilogue has read it
-              if (j == 0 && qn > 0 && !(ok = mbar_wait(&bars->o_free, (qn - 1) & 1, tmo, abort_flag))) break;
+              if (j == 0 && qn > 0 && !(ok = warp_wait(&bars->o_free, (qn - 1) & 1, tmo, abort_flag))) break;
               tc_fence_after();
               if (!(ok = issue_pv(Jg, j == 0))) break;
-              umma_commit(&bars->o_done);
-              if (j + 1 == n_tiles) umma_commit(&bars->o_final);
+              umma_commit_elect(&bars->o_done);
+              if (j + 1 == n_tiles) umma_commit_elect(&bars->o_final);
             }
             J += n_tiles;
             ++qn;
           }
           // Drain: every MMA this thread issued has completed before TMEM can be released.
-          umma_commit(&bars->mma_drain[0]);
-          mbar_wait(&bars->mma_drain[0], 0, tmo, nullptr);
+          umma_commit_elect(&bars->mma_drain[0]);
+          warp_wait(&bars->mma_drain[0], 0, tmo, nullptr);
         } else {
           // ------------------------------------------------------------------ MMA issuers (d = 128)
           // Both find their chunks in the ring from the producer's order: per item K(0), then
@@ -616,20 +623,20 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           int uses0 = 0, uses1 = 0;                        // S issuer: S per buffer; PV issuer: PV per buffer
           for (int k_item = 0;; ++k_item) {
             int w, n_tiles;
-            if (!(ok = item_get(k_item, false, w, n_tiles)) || w < 0) break;
+            if (!(ok = item_get(k_item, true, w, n_tiles)) || w < 0) break;
             if (n_tiles == 0) continue;
             auto kpos = [&](int j) { return pos0 + (j == 0 ? 0 : 2 * j - 1); };
             auto vpos = [&](int j) { return pos0 + (j + 1 < n_tiles ? 2 * j + 2 : 2 * j + 1); };
             if (xi == 0) {
-              if (!(ok = mbar_wait(&bars->q_full, qn & 1, tmo, abort_flag))) break;
+              if (!(ok = warp_wait(&bars->q_full, qn & 1, tmo, abort_flag))) break;
               for (int j = 0; ok && j < n_tiles; ++j) {
                 // S(j) into buffer j % 2, once the PV of the buffer's previous tile has read the P
                 // held there.  K(j) is waited for first: it has usually landed long before, so
                 // only the PV wait is exposed.
                 const int buf = j & 1, u = buf ? uses1 : uses0;
                 const int pos = kpos(j), slot = pos % C::RING;
-                if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
-                if (u >= 1 && !(ok = mbar_wait(&bars->p_free[buf], (u - 1) & 1, tmo, abort_flag))) break;
+                if (!(ok = warp_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
+                if (u >= 1 && !(ok = warp_wait(&bars->p_free[buf], (u - 1) & 1, tmo, abort_flag))) break;
                 if (buf) ++uses1; else ++uses0;
                 tc_fence_after();
                 const uint32_t d_s = tmem + C::COL_S + buf * BN;
@@ -638,12 +645,12 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int kk = 0; kk < 8; ++kk) {                 // 8 steps of 16 dims
                   const uint64_t aq = dq + (uint64_t)(((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4);
                   const uint64_t bo = bk + (uint64_t)(((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4);
-                  umma_bf16_ss(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
+                  umma_bf16_ss_elect(d_s, aq, bo, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&bars->empty[slot]);
-                umma_commit(&bars->s_full[buf]);
+                umma_commit_elect(&bars->empty[slot]);
+                umma_commit_elect(&bars->s_full[buf]);
               }
-              if (ok) umma_commit(&bars->q_free);               // the item's last S read Q
+              if (ok) umma_commit_elect(&bars->q_free);               // the item's last S read Q
             } else {
               // O_(j%2) += P(j) V(j), P in the first 64 columns of S buffer j % 2.  The softmax
               // publishes P in two halves of 64 keys; the first half's MMAs run while the
@@ -652,27 +659,27 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 const int buf = j & 1, u = buf ? uses1 : uses0;
                 if (buf) ++uses1; else ++uses0;
                 const int pos = vpos(j), slot = pos % C::RING;
-                if (!(ok = mbar_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
+                if (!(ok = warp_wait(&bars->full[slot], (pos / C::RING) & 1, tmo, abort_flag))) break;
                 // the item's first PVs overwrite O_0 and O_1: the previous item's epilogue has
                 // read them
-                if (j == 0 && qn > 0 && !(ok = mbar_wait(&bars->o_free, (qn - 1) & 1, tmo, abort_flag))) break;
+                if (j == 0 && qn > 0 && !(ok = warp_wait(&bars->o_free, (qn - 1) & 1, tmo, abort_flag))) break;
                 const uint32_t p_col = tmem + C::COL_S + buf * BN;
                 const uint32_t d_o = tmem + C::COL_O + buf * D;
                 const uint64_t bv = dr_v + (uint64_t)((slot * C::CHUNK) >> 4);
                 for (int half = 0; ok && half < 2; ++half) {
-                  if (!(ok = mbar_wait(&bars->p_full[buf][half], u & 1, tmo, abort_flag))) break;
+                  if (!(ok = warp_wait(&bars->p_full[buf][half], u & 1, tmo, abort_flag))) break;
                   tc_fence_after();
 #pragma unroll
                   for (int k4 = 0; k4 < 4; ++k4) {               // 4 steps of 16 keys
                     const int kk = 4 * half + k4;
-                    umma_bf16_ts(d_o, p_col + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                    umma_bf16_ts_elect(d_o, p_col + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), idesc_pv,
                                  (j >= 2 || kk > 0) ? 1u : 0u);
                   }
                 }
                 if (!ok) break;
-                umma_commit(&bars->empty[slot]);
-                umma_commit(&bars->p_free[buf]);
-                if (j + 1 == n_tiles) umma_commit(&bars->o_final);
+                umma_commit_elect(&bars->empty[slot]);
+                umma_commit_elect(&bars->p_free[buf]);
+                if (j + 1 == n_tiles) umma_commit_elect(&bars->o_final);
               }
             }
             pos0 += 2 * n_tiles;
@@ -680,8 +687,8 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             ++qn;
           }
           // Drain: every MMA this thread issued has completed before TMEM can be released.
-          umma_commit(&bars->mma_drain[xi]);
-          mbar_wait(&bars->mma_drain[xi], 0, tmo, nullptr);
+          umma_commit_elect(&bars->mma_drain[xi]);
+          warp_wait(&bars->mma_drain[xi], 0, tmo, nullptr);
         }
       }
       __syncwarp();
@@ -833,7 +840,34 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int t = it.t0 + row;
       const size_t orow_off = (((size_t)it.b * sh.n_heads + it.h) * sh.Tq + t) * D;
       __nv_bfloat16* orow = out + orow_off;
+      // Columns [c, c + 32) of this thread's row, times s0.  Plain bf16 output goes through the
+      // warp's 2 KB staging area: each thread writes its row's 64 bytes there (16-byte pieces,
+      // the piece index XOR (row / 2) % 4 so that no two of eight consecutive rows share banks),
+      // then every store instruction of the warp covers 8 rows x 64 contiguous bytes instead of
+      // 32 rows x 16 bytes.
+      unsigned char* stage = smem + C::OFF_STAGE + (warp & 7) * 2048;
       auto store32 = [&](int c, const float (&o)[32], float s0) {
+        if constexpr (EPI == 0) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(o[2 * e] * s0, o[2 * e + 1] * s0);
+          const int sw = (lane >> 1) & 3;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(stage + lane * 64 + ((u ^ sw) << 4)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int q = 32 * i + lane, r = q >> 2, u = q & 3;      // row r of the warp, piece u
+            const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+            const int tr = 32 * (warp & 3) + r;                       // row of the query tile
+            if (tr < it.rows)
+              *reinterpret_cast<uint4*>(out + (((size_t)it.b * sh.n_heads + it.h) * sh.Tq + it.t0 + tr) * D + c + 8 * u) = v;
+          }
+          __syncwarp();
+          return;
+        }
         if (row < it.rows) {
 #pragma unroll
           for (int u = 0; u < 32; u += 8) {
@@ -884,6 +918,11 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           tmem_ld32(t_o0 + c, o0);              // both always: a select drops an unused one
           tmem_ld32(t_o1 + c, o1);
           tmem_wait_ld();
+          if (c == 64 * wg + 32 && n_tiles > 0) {   // O is read: the next item's PVs may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->o_free);
+          }
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const float x0 = has0 ? o0[u] : 0.0f, x1 = has1 ? o1[u] : 0.0f;
@@ -902,6 +941,11 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (n_tiles > 0) {
             tmem_ld32(t_o + c, o);
             tmem_wait_ld();
+            if (c == D - 32) {                  // O is read: the next item's PVs may overwrite it
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->o_free);
+            }
           } else {
 #pragma unroll
             for (int u = 0; u < 32; ++u) o[u] = 0.0f;
@@ -912,13 +956,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           lse[((size_t)it.b * sh.n_heads + it.h) * sh.Tq + t] =
               l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       }
-      if (n_tiles > 0) {
-        // O is read: the next item's first PVs may overwrite it
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->o_free);
-        ++qn;
-      }
+      if (n_tiles > 0) ++qn;
       J += n_tiles;
     }
     tc_fence_before();
