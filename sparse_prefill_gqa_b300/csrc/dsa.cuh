@@ -116,18 +116,25 @@ dsa_indexer_kernel(const __nv_bfloat16* __restrict__ qi, const float* __restrict
 // ordered compaction that keeps every score above it and, among scores equal to it, the lowest
 // indices -- exactly k indices (all of them when L_b <= k), in increasing order.
 constexpr int kTopkThreads = 1024;
-constexpr int kTopkStageMax = 53248;          // longest row whose keys are staged in shared memory
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkCandMax = 8192;            // keys of the chosen bins kept for the later passes
+constexpr int kTopkFixedSmem = (kTopkWarps * 256 + kTopkCandMax) * 4;   // dynamic, before the row
+constexpr int kTopkStageMax = 40960;          // longest row whose keys are staged in shared memory
 
 __device__ __forceinline__ uint32_t order_key(float x) {     // larger float -> larger key
   const uint32_t u = __float_as_uint(x);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// grid: (batch); block: kTopkThreads (32 warps).
-//   radix select: per 8-bit digit, a histogram of the keys that match the digits chosen so far
-//     (increments aggregated per warp over equal bins: the scores are non-negative, so the top
-//     digit falls into one or two bins), then warp 0 finds the bin that holds the k-th largest
-//     key by a suffix scan, each lane covering 8 bins from the top;
+// grid: (batch); block: kTopkThreads (32 warps); dynamic shared memory kTopkFixedSmem (+ 4 L_max
+// bytes when STAGED).
+//   radix select: per 8-bit digit, a histogram of the keys that match the digits chosen so far,
+//     one private histogram per warp (indexer scores are non-negative and concentrated, so the
+//     top digits fall into one or a few bins: a shared histogram would serialise every warp on
+//     them), counted by plain shared-memory atomics and summed per bin; warp 0 finds the bin that holds the k-th largest key by a suffix
+//     scan, each lane covering 8 bins from the top.  Once the chosen bin holds at most
+//     kTopkCandMax keys they are copied to a candidate list, and the remaining digits histogram
+//     only those;
 //   compaction: warp w owns a contiguous segment of the scores; a first sweep counts its keys
 //     above and equal to the k-th, a second writes its selected indices at its offset, which
 //     keeps the indices in increasing order with one barrier in all.
@@ -137,12 +144,15 @@ template <bool STAGED>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__ lens, int L_max, int topk,
                    int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
-  constexpr int NW = kTopkThreads / 32;
-  extern __shared__ uint32_t skeys[];            // STAGED: the row's order-preserving keys
+  constexpr int NW = kTopkWarps;
+  extern __shared__ uint32_t dyn[];
+  int* whist = reinterpret_cast<int*>(dyn);      // NW x 256 per-warp histograms
+  uint32_t* cand = dyn + NW * 256;               // candidate keys
+  uint32_t* skeys = cand + kTopkCandMax;         // STAGED: the row's order-preserving keys
   __shared__ int hist[256];
   __shared__ int w_gt[NW], w_eq[NW];
   __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
+  __shared__ int s_need, s_ncand;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int b = blockIdx.x;
@@ -157,28 +167,49 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
     return;
   }
   if (STAGED) {
-#pragma unroll 8
-    for (int j = threadIdx.x; j < L; j += kTopkThreads) skeys[j] = order_key(row[j]);
+    // 16-byte loads when the row is 16-byte aligned (all of them in flight: at most 10 a thread)
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    const int n4 = vec ? L / 4 : 0;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n4; i += kTopkThreads) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(row) + i);
+      *reinterpret_cast<uint4*>(skeys + 4 * i) = make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
+    }
+    for (int j = 4 * n4 + threadIdx.x; j < L; j += kTopkThreads) skeys[j] = order_key(row[j]);
   }
   auto key_at = [&](int j) -> uint32_t { return STAGED ? skeys[j] : order_key(row[j]); };
   // ---- radix select of the k-th largest key ------------------------------------------------
-  if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
+  if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; s_ncand = -1; }
+  int* my_hist = whist + warp * 256;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     const uint32_t hi_mask = pass == 0 ? 0u : (0xFFFFFFFFu << (32 - 8 * pass));
-    for (int i = threadIdx.x; i < 256; i += kTopkThreads) hist[i] = 0;
+    for (int i = threadIdx.x; i < NW * 256; i += kTopkThreads) whist[i] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix;
-    for (int base = 0; base < L; base += kTopkThreads) {       // uniform trip count per warp
-      const int j = base + (int)threadIdx.x;
-      const uint32_t key = j < L ? key_at(j) : 0u;
-      const bool in = j < L && (key & hi_mask) == prefix;
-      const uint32_t act = __ballot_sync(0xffffffffu, in);
-      if (in) {
-        const int bin = (key >> shift) & 0xFF;
-        const uint32_t peers = __match_any_sync(act, bin);
-        if ((uint32_t)(__ffs(peers) - 1) == (uint32_t)lane) atomicAdd(&hist[bin], __popc(peers));
+    const int n_cand = s_ncand;                  // -1: no candidate list yet
+    auto count = [&](uint32_t key, bool in) {
+      if (in) atomicAdd(&my_hist[(key >> shift) & 0xFF], 1);
+    };
+    if (n_cand >= 0) {
+      for (int base = 0; base < n_cand; base += kTopkThreads) {
+        const int j = base + (int)threadIdx.x;
+        const uint32_t key = j < n_cand ? cand[j] : 0u;
+        count(key, j < n_cand && (key & hi_mask) == prefix);
       }
+    } else {
+      for (int base = 0; base < L; base += kTopkThreads) {       // uniform trip count per warp
+        const int j = base + (int)threadIdx.x;
+        const uint32_t key = j < L ? key_at(j) : 0u;
+        count(key, j < L && (key & hi_mask) == prefix);
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += kTopkThreads) {
+      int t = 0;
+#pragma unroll 8
+      for (int w = 0; w < NW; ++w) t += whist[w * 256 + i];
+      hist[i] = t;
     }
     __syncthreads();
     if (warp == 0) {
@@ -202,9 +233,27 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
         while (bin > 0 && running + hist[bin] < need) { running += hist[bin]; --bin; }
         s_prefix = prefix | ((uint32_t)bin << shift);
         s_need = need - running;                 // how many of this bin's keys are in the top k
+        hist[0] = hist[bin];                     // keys that share the chosen digits (read below)
       }
     }
     __syncthreads();
+    // the first time the chosen bin is small enough, its keys become the candidate list
+    if (pass < 3 && n_cand < 0 && hist[0] <= kTopkCandMax) {
+      const uint32_t pre = s_prefix, m = 0xFFFFFFFFu << (24 - 8 * pass);
+      if (threadIdx.x == 0) s_ncand = 0;
+      __syncthreads();
+      for (int base = 0; base < L; base += kTopkThreads) {
+        const int j = base + (int)threadIdx.x;
+        const uint32_t key = j < L ? key_at(j) : 0u;
+        const bool in = j < L && (key & m) == pre;
+        const uint32_t bal = __ballot_sync(0xffffffffu, in);
+        int at = 0;
+        if (lane == 0 && bal) at = atomicAdd(&s_ncand, __popc(bal));
+        at = __shfl_sync(0xffffffffu, at, 0);
+        if (in) cand[at + __popc(bal & lt_mask)] = key;
+      }
+      __syncthreads();
+    }
   }
   const uint32_t kth = s_prefix;                 // the k-th largest key
   const int quota = s_need;                      // keys equal to kth that are kept

@@ -141,7 +141,7 @@ struct DeviceKernels {
   int decode;                   // decode_splitk_kernel, plain and gathered
   int select;                   // select_blocks_kernel
   int mla;                      // mla_decode_kernel
-  int topk;                     // topk_select_kernel with the row staged in shared memory
+  int topk, topk_unstaged;      // topk_select_kernel with / without the row staged in shared memory
   int n_sm;                     // streaming multiprocessors
 };
 
@@ -186,7 +186,8 @@ const DeviceKernels* device_kernels() {
                             set_smem(decode_splitk_kernel<64, true>, DecodeCfg<64>::GATHER_SMEM_BYTES)});
     d.select = first_error({set_smem(select_rescue_kernel, 16384 * 8), set_smem(select_score_kernel, kScSmem)});
     d.mla = set_smem(mla_decode_kernel, MlaCfg::SMEM_BYTES);
-    d.topk = set_smem(topk_select_kernel<true>, kTopkStageMax * 4);
+    d.topk = set_smem(topk_select_kernel<true>, kTopkFixedSmem + kTopkStageMax * 4);
+    d.topk_unstaged = set_smem(topk_select_kernel<false>, kTopkFixedSmem);
     int n_sm = 0;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) n_sm = 148;
     d.n_sm = n_sm;
@@ -537,13 +538,15 @@ int ga_topk_indices(const float* scores, const int32_t* lens, int batch, int L_m
   if (batch > 0x7fffffff / 2) return GA_ERR_UNSUPPORTED;
   for (const void* p : {(const void*)scores, (const void*)idx, (const void*)n_sel, (const void*)lens})
     if (p && (reinterpret_cast<uintptr_t>(p) & 3)) return GA_ERR_INVALID_ARG;
+  const DeviceKernels* dk = device_kernels();
+  if (!dk) return GA_ERR_CUDA;
   if (L_max <= kTopkStageMax) {
-    const DeviceKernels* dk = device_kernels();
-    if (!dk) return GA_ERR_CUDA;
     if (dk->topk != GA_OK) return dk->topk;
-    topk_select_kernel<true><<<batch, kTopkThreads, (size_t)L_max * 4, stream>>>(scores, lens, L_max, topk, idx, n_sel);
+    topk_select_kernel<true><<<batch, kTopkThreads, kTopkFixedSmem + (size_t)L_max * 4, stream>>>(
+        scores, lens, L_max, topk, idx, n_sel);
   } else {
-    topk_select_kernel<false><<<batch, kTopkThreads, 0, stream>>>(scores, lens, L_max, topk, idx, n_sel);
+    if (dk->topk_unstaged != GA_OK) return dk->topk_unstaged;
+    topk_select_kernel<false><<<batch, kTopkThreads, kTopkFixedSmem, stream>>>(scores, lens, L_max, topk, idx, n_sel);
   }
   return launch_status();
 }

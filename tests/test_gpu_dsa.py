@@ -42,16 +42,23 @@ def test_indexer_scores(B, Hi, di, L, lens):
         assert np.all(np.isneginf(sc[b, n:]))
 
 
-@pytest.mark.parametrize("B,L,topk,ties", [
-    (3, 5000, 512, False),
-    (2, 3000, 2048, True),       # integer-valued scores: many ties at the boundary
-    (2, 1000, 1500, False),      # topk > L: every token
+@pytest.mark.parametrize("B,L,topk,kind", [
+    (3, 5000, 512, "normal"),
+    (2, 3000, 2048, "ties"),       # integer-valued scores: many ties at the boundary
+    (2, 1000, 1500, "normal"),     # topk > L: every token
+    (2, 32768, 2048, "abs"),       # non-negative, concentrated: the top digits fall in one or two bins
+    (1, 50000, 2048, "abs"),       # a row too long to stage in shared memory
+    (2, 30000, 2048, "binary"),    # two values: the chosen bin never shrinks to a candidate list
 ])
-def test_topk_indices_exact(B, L, topk, ties):
+def test_topk_indices_exact(B, L, topk, kind):
     rng = np.random.default_rng(511)
     s = rng.standard_normal((B, L)).astype(np.float32)
-    if ties:
+    if kind == "ties":
         s = np.floor(s * 3.0).astype(np.float32)
+    elif kind == "abs":
+        s = np.abs(s)
+    elif kind == "binary":
+        s = (s > 0).astype(np.float32)
     lens = [L, L // 2, L - 7][:B]
     scores = torch.from_numpy(s).cuda()
     idx, n_sel = ga.ga_topk_indices(scores, topk, torch.tensor(lens, dtype=torch.int32, device="cuda"))
