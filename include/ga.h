@@ -299,7 +299,10 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
  * kvh = h / (n_heads / n_kv):
  *   visible(beta)  key block beta holds a key some row of the block may use under the
  *                  causal rule and window (all blocks when causal == 0);
- *   s(beta)        = mean_rows(q) . centroid[beta] / sqrt(d)             (fp32)
+ *   s(beta)        = mean_rows(q) . centroid[beta] / sqrt(d)             (fp32 operands; the
+ *                  products on the tensor cores as three TF32 products of the operands'
+ *                  high and low parts, accumulated in fp32: within about 2^-20 of each
+ *                  product, rounding order aside)
  *   mean branch    s(beta) >= max_{visible} s - tau_mean                 (INFINITY = dense)
  *   radius branch  (radius[beta] - mu) / sigma >= lambda_radius, mu and sigma (population)
  *                  over the radii of all ceil(Tk/k_block) blocks of (b, kvh), in fp64;
@@ -315,9 +318,10 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
  *   block_mask device uint8 out [batch, n_heads, ceil(Tq/q_block), nKb_out].
  *   n_selected device int32 out [batch, n_heads, ceil(Tq/q_block)], or NULL.
  *   workspace  device scratch of ga_select_workspace_size(...) bytes, 256-byte aligned
- *              (GA_ERR_WORKSPACE otherwise): the mean query row of every query block, its
- *              norm, the row maxima, the rescue flags and every mean-branch score, each
- *              computed once per call.  Must not be used by another call in flight.
+ *              (GA_ERR_WORKSPACE otherwise): the mean query row of every query block and the
+ *              centroids, each split into high and low parts, the rows' norms, the row maxima,
+ *              the rescue flags and every mean-branch score, each computed once per call.
+ *              Must not be used by another call in flight.
  *   d: 1..256; q_block: 1..4096; ceil(Tk/k_block) <= 32768.
  */
 int ga_select_blocks(const void* q, const float* centroid, const float* radius,
@@ -328,9 +332,11 @@ int ga_select_blocks(const void* q, const float* centroid, const float* radius,
                      void* workspace, size_t workspace_bytes, ga_stream_t stream);
 
 /* Bytes of workspace ga_select_blocks / ga_select_blocks_ex need (SIZE_MAX for invalid sizes):
- * batch * P * ceil(Tq/q_block) * (d + 2 + S) floats and batch * n_kv * ceil(Tk/k_block) bytes,
- * each part rounded to 256 bytes, with P = n_kv when group_shared is 1 and n_heads otherwise and
- * S = ceil(Tk/k_block) rounded up to a multiple of 128 (one score per key block). */
+ * batch * P * ceil(Tq/q_block) * (2 D + 2 + S) floats, batch * n_kv * ceil(Tk/k_block) * 2 D
+ * floats and batch * n_kv * ceil(Tk/k_block) bytes, each of the seven parts rounded to 256
+ * bytes, with P = n_kv when group_shared is 1 and n_heads otherwise, D = d rounded up to a
+ * multiple of 32, and S = ceil(Tk/k_block) rounded up to a multiple of 128 (one score per key
+ * block). */
 size_t ga_select_workspace_size(int batch, int n_heads, int n_kv, int d, int Tq, int Tk, int q_block,
                                 int k_block, int group_shared);
 

@@ -67,6 +67,21 @@ bool make_map_bf16(CUtensorMap* map, const void* base, int cols, long long rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp32 map over a [planes, rows, cols] row-major tensor, boxes of box_rows x 32 columns
+// (128 bytes) with the 128-byte swizzle; out-of-range rows read as zero.
+bool make_map_f32(CUtensorMap* map, const void* base, int cols, long long rows, long long planes,
+                  int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)cols * 4 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename K>
 int set_smem(K kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess
@@ -742,15 +757,21 @@ int ga_block_stats(const void* k, const int32_t* k_lens, int batch, int n_kv, in
 }
 
 namespace {
-// Workspace of the selection: pooled query rows, their norms, the row maxima, the rescue flags
-// and the mean-branch scores, each part 256-byte aligned.
+// Workspace of the selection: pooled query rows and centroids split into high and low parts
+// (rows of d rounded up to 32), the rows' norms, the row maxima, the rescue flags and the
+// mean-branch scores, each part 256-byte aligned.
 struct SelectWs {
-  size_t qmean, qnorm, rowmax, rescue, scores, total;
+  size_t q_hi, q_lo, c_hi, c_lo, qnorm, rowmax, rescue, scores, total;
 };
 SelectWs select_ws(int batch, int n_hp, int n_kv, int d, int nQb, int nKb) {
   SelectWs w;
-  w.qmean = 0;
-  w.qnorm = w.qmean + sel_up256((size_t)batch * n_hp * nQb * d * 4);
+  const int dp = (d + 31) / 32 * 32;
+  const size_t qb = sel_up256((size_t)batch * n_hp * nQb * dp * 4), cb = sel_up256((size_t)batch * n_kv * nKb * dp * 4);
+  w.q_hi = 0;
+  w.q_lo = w.q_hi + qb;
+  w.c_hi = w.q_lo + qb;
+  w.c_lo = w.c_hi + cb;
+  w.qnorm = w.c_lo + cb;
   w.rowmax = w.qnorm + sel_up256((size_t)batch * n_hp * nQb * 4);
   w.rescue = w.rowmax + sel_up256((size_t)batch * n_hp * nQb * 4);
   w.scores = w.rescue + sel_up256((size_t)batch * n_kv * nKb);
@@ -820,7 +841,12 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
   if (radius_rule == GA_RADIUS_MAD)
     for (s.sort_len = 1; s.sort_len < nKb; s.sort_len <<= 1) {}
   unsigned char* w = static_cast<unsigned char*>(workspace);
-  s.qmean = reinterpret_cast<float*>(w + ws.qmean);
+  s.dp = (d + 31) / 32 * 32;
+  s.q_hi = reinterpret_cast<float*>(w + ws.q_hi);
+  s.q_lo = reinterpret_cast<float*>(w + ws.q_lo);
+  s.c_hi = reinterpret_cast<float*>(w + ws.c_hi);
+  s.c_lo = reinterpret_cast<float*>(w + ws.c_lo);
+  s.timeout_ns = g_timeout_ns;
   s.qnorm = reinterpret_cast<float*>(w + ws.qnorm);
   s.rowmax = reinterpret_cast<int*>(w + ws.rowmax);
   s.rescue = w + ws.rescue;
@@ -829,15 +855,26 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
   if (!dk) return GA_ERR_CUDA;
   if (dk->select != GA_OK) return dk->select;
 
-  const dim3 pool_grid(nQb + 1, n_hp, batch);          // column nQb: the z-score radius branch
+  CUtensorMap tm_qh, tm_ql, tm_ch, tm_cl;
+  const long long q_rows = (long long)batch * n_hp * nQb, c_rows = (long long)batch * n_kv * nKb;
+  if (q_rows > 0x7fffffffLL || c_rows > 0x7fffffffLL) return GA_ERR_UNSUPPORTED;
+  if (!make_map_f32(&tm_qh, s.q_hi, s.dp, q_rows, 1, kScA) || !make_map_f32(&tm_ql, s.q_lo, s.dp, q_rows, 1, kScA) ||
+      !make_map_f32(&tm_ch, s.c_hi, s.dp, c_rows, 1, kScB) || !make_map_f32(&tm_cl, s.c_lo, s.dp, c_rows, 1, kScB))
+    return GA_ERR_CUDA;
+  // columns: nQb pooled query blocks, the z-score radius branch, then the centroid splits
+  const int n_ct = (int)((nKb + kScB - 1) / kScB);
+  const dim3 pool_grid(nQb + 1 + n_ct, n_hp, batch);
   if (dtype == GA_BF16)
-    select_pool_kernel<__nv_bfloat16><<<pool_grid, kPoolThreads, 0, stream>>>((const __nv_bfloat16*)q, radius, s);
+    select_pool_kernel<__nv_bfloat16><<<pool_grid, kPoolThreads, 0, stream>>>((const __nv_bfloat16*)q, radius,
+                                                                               centroid, s);
   else
-    select_pool_kernel<float><<<pool_grid, kPoolThreads, 0, stream>>>((const float*)q, radius, s);
+    select_pool_kernel<float><<<pool_grid, kPoolThreads, 0, stream>>>((const float*)q, radius, centroid, s);
   if (radius_rule == GA_RADIUS_MAD)
     select_rescue_kernel<<<dim3(n_kv, batch), kRescueThreads, (size_t)s.sort_len * 8, stream>>>(radius, s);
-  const dim3 score_grid(((int)nKb + kScB - 1) / kScB, (nQb + kScA - 1) / kScA, batch * n_hp);
-  select_score_kernel<<<score_grid, kScThreads, kScSmem, stream>>>(centroid, s);
+  // persistent: one CTA per SM (or per tile when there are fewer tiles)
+  const long long n_tiles = sel_score_tiles(batch, n_hp, nQb, (int)nKb);
+  select_score_kernel<<<(unsigned)(n_tiles < dk->n_sm ? n_tiles : dk->n_sm), kScThreads, kScSmem, stream>>>(
+      tm_qh, tm_ql, tm_ch, tm_cl, s);
   const long long n_rows = (long long)batch * n_hp * nQb;
   select_decide_kernel<<<(unsigned)((n_rows + kDecWarps - 1) / kDecWarps), 32 * kDecWarps, 0, stream>>>(
       radius, block_mask, n_selected, s);

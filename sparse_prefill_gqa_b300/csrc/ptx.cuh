@@ -211,6 +211,24 @@ __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
       :: "r"(smem_u32(bar)) : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::tf32: fp32 operands read as TF32 (the top
+// 19 bits), fp32 accumulator; K = 8 per instruction (32 bytes of a 128-byte row).
+__device__ __forceinline__ void umma_tf32_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Instruction descriptor for kind::tf32, both operands K-major, fp32 accumulator: as for
+// kind::f16 below with A and B format 2 (TF32).
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32 accumulator.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format (1 = bf16),
 // 15 A major (0 = K-major), 16 B major (1 = MN-major), [17,23) N >> 3, [24,29) M >> 4.

@@ -14,9 +14,9 @@
 //                             once at the copy rate; each row maximum starts at -inf
 //   2. select_rescue_kernel   per (sequence, kv head): the radius statistics in fp64 and the
 //                             rescue flag of every key block, once
-//   3. select_score_kernel    scores of 128 query blocks x 128 key blocks per CTA, fp32 fused
-//                             multiply-adds in dimension order, stored once; the row maxima by
-//                             atomicMax
+//   3. select_score_kernel    scores of 128 query blocks x 128 key blocks per CTA on the tensor
+//                             cores (three TF32 products of split operands, fp32 accumulation),
+//                             stored once; the row maxima by atomicMax
 //   4. select_decide_kernel   per row: the stored scores thresholded, OR-ed with rescue, diagonal
 //                             and bound, written as the mask rows, and the per-row counts
 // The pooled queries, row maxima, rescue flags and scores live in the caller's workspace.
@@ -36,7 +36,12 @@ struct SelectShape {
   float tau_bound;                // bound branch threshold; -inf: no bound branch
   int group_shared;               // 1: one selection per kv head from the rows of its g heads
   int n_hp;                       // pooled rows: n_heads, or n_kv when group-shared
-  float* qmean;                   // workspace [batch, n_hp, nQb, d]: mean query rows
+  int dp;                         // d rounded up to 32 (the operand rows' length, zero padded)
+  float* q_hi;                    // workspace [batch, n_hp, nQb, dp]: mean query rows, high part
+  float* q_lo;                    //   and the rest (q_hi + q_lo = the fp32 mean exactly)
+  float* c_hi;                    // workspace [batch, n_kv, nKb, dp]: centroids, split the same way
+  float* c_lo;
+  uint64_t timeout_ns;            // limit of the score kernel's pipeline waits
   float* qnorm;                   // workspace [batch, n_hp, nQb]: their Euclidean norms
   int* rowmax;                    // workspace [batch, n_hp, nQb]: row maxima, order-preserving ints
   uint8_t* rescue;                // workspace [batch, n_kv, nKb]: radius-branch flags
@@ -53,6 +58,13 @@ __device__ __forceinline__ int f2ord(float f) {
   return i >= 0 ? i : i ^ 0x7fffffff;
 }
 __device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
+
+// x = hi + lo exactly: hi keeps the sign, exponent and top 10 mantissa bits (a TF32 value), lo
+// the remaining 13 bits (a TF32 value up to its last bit, which the split leaves below 2^-21 x).
+__device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
+  hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  lo = x - hi;
+}
 
 // Key blocks query block alpha may see, [vlo, vhi): rows at absolute positions i_first .. i_last
 // = Tk - Tq + those rows; with the causal rule the last visible block holds key i_last, with a
@@ -90,12 +102,27 @@ __device__ void rescue_zscore(const float* __restrict__ radius, SelectShape s, i
 
 template <typename T>
 __global__ void __launch_bounds__(kPoolThreads)
-select_pool_kernel(const T* __restrict__ q, const float* __restrict__ radius, SelectShape s) {
+select_pool_kernel(const T* __restrict__ q, const float* __restrict__ radius,
+                   const float* __restrict__ centroid, SelectShape s) {
   __shared__ float part[kPoolThreads / 32][kSimtMaxD];
   __shared__ float mean_s[kSimtMaxD];
   const int alpha = blockIdx.x, hp = blockIdx.y, b = blockIdx.z;
   if (alpha == s.nQb) {         // the extra column: the z-score radius branch, beside the pooling
     if (s.radius_rule == 0 && hp < s.n_kv) rescue_zscore(radius, s, hp, b);
+    return;
+  }
+  if (alpha > s.nQb) {          // further columns: 128 centroids of kv head hp, split for the scores
+    if (hp >= s.n_kv) return;
+    const int beta0 = (alpha - s.nQb - 1) * 128, nb = min(128, s.nKb - beta0);
+    const float* src = centroid + (((size_t)b * s.n_kv + hp) * s.nKb_out + beta0) * s.d;
+    const size_t o = (((size_t)b * s.n_kv + hp) * s.nKb + beta0) * s.dp;
+    for (int e = threadIdx.x; e < nb * s.dp; e += kPoolThreads) {
+      const int r = e / s.dp, c = e % s.dp;
+      float hi, lo;
+      tf32_split(c < s.d ? src[(size_t)r * s.d + c] : 0.0f, hi, lo);
+      s.c_hi[o + e] = hi;
+      s.c_lo[o + e] = lo;
+    }
     return;
   }
   const int d = s.d, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -104,7 +131,6 @@ select_pool_kernel(const T* __restrict__ q, const float* __restrict__ radius, Se
   const int t0 = alpha * s.q_block, t1 = min(s.Tq, t0 + s.q_block);
   const float inv_n = 1.0f / (float)((t1 - t0) * n_pool);
   const size_t row = ((size_t)b * s.n_hp + hp) * s.nQb + alpha;
-  float* dst = s.qmean + row * d;
   if (sizeof(T) == 2 && d % 8 == 0 && 32 % (d / 8) == 0) {
     const int L = d / 8, RP = 32 / L;               // lanes per row, rows per warp step
     const int col = 8 * (lane % L), r0 = lane / L;
@@ -139,7 +165,12 @@ select_pool_kernel(const T* __restrict__ q, const float* __restrict__ radius, Se
     }
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < d; c += kPoolThreads) dst[c] = mean_s[c];
+  for (int c = threadIdx.x; c < s.dp; c += kPoolThreads) {
+    float hi, lo;
+    tf32_split(c < d ? mean_s[c] : 0.0f, hi, lo);
+    s.q_hi[row * s.dp + c] = hi;
+    s.q_lo[row * s.dp + c] = lo;
+  }
   if (threadIdx.x == 0) {
     float n2 = 0.0f;                                  // |q_mean| (bound branch)
     for (int c = 0; c < d; ++c) n2 = fmaf(mean_s[c], mean_s[c], n2);
@@ -246,154 +277,224 @@ select_rescue_kernel(const float* __restrict__ radius, SelectShape s) {
 }
 
 // ---------------------------------------------------------------------------------------
-// 3. Scores.  One CTA per (128 key blocks, 128 query blocks, pooled head x sequence), 8 warps,
-// two CTAs per SM.  Lane l owns query blocks l, l + 32, l + 64, l + 96 of the tile, warp w key
-// blocks 16 w .. 16 w + 15, so each dimension step is four conflict-free loads of query means
-// (one per query block, consecutive across the lanes), four broadcast 16-byte loads of centroids,
-// and 64 fused multiply-adds (32 packed instructions); the query means and centroids are staged
-// 64 dimensions at a time, dimension-major.  Every score s = acc / sqrt(d) (fp32) is stored in the
-// workspace through shared memory (whole 512-byte row segments) and the row maxima over the
-// visible key blocks go to the workspace by atomicMax.  Tiles no query block of which sees a key
-// block of the CTA's range store nothing.
+// 3. Scores.  128 x 128 tiles (128 query blocks x 128 key blocks of one pooled head and
+// sequence) S = Q C^T on the tensor cores, a persistent CTA per SM walking every tile with a
+// visible pair (tiles t = blockIdx.x, + gridDim.x, ... in (head, query tile, key tile) order).
+// fp32 operands are split as x = hi + lo (tf32_split) and every product takes three TF32 MMAs,
+// hi.hi + hi.lo + lo.hi, accumulated in fp32: the dropped lo.lo term and the TF32 reading of lo
+// are below 2^-20 of each product, far inside the decision band, at five times the fp32 fused
+// multiply-add rate.  The operands stream through a ring of two stages of 32 dimensions (four
+// 16 KB TMA boxes: Q hi, Q lo, C hi, C lo; 128-byte swizzle); tile j of the CTA accumulates in
+// tensor-memory buffer j % 2, so the loads and MMAs of the next tile overlap the epilogue of
+// this one.
+//   warp 0   TMA producer;
+//   warp 1   MMA issuer (the whole warp, one elected lane issuing);
+//   warps 2-5  epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31, i.e. its query
+//            blocks' rows of S, scales them by 1/sqrt(d), takes each row's maximum over the
+//            visible key blocks (atomicMax into the workspace), stages the rows in shared
+//            memory and stores them as whole 512-byte row segments.
 // ---------------------------------------------------------------------------------------
-constexpr int kScThreads = 256;
-constexpr int kScA = 128;            // query blocks per CTA
-constexpr int kScB = 128;            // key blocks per CTA
-constexpr int kScDC = 64;            // dimensions staged at a time
-constexpr int kScQS = kScA + 4;      // row stride (floats) of the staged query means [c][a]
-constexpr int kScCS = kScB + 4;      // row stride (floats) of the staged centroids [c][beta]
+constexpr int kScThreads = 192;
+constexpr int kScA = 128;            // query blocks per tile (MMA M)
+constexpr int kScB = 128;            // key blocks per tile (MMA N)
+constexpr int kScKC = 32;            // dimensions per stage: one 128-byte fp32 row
+constexpr int kScBox = 128 * 128;    // bytes of one 128-row x 32-dim box
+constexpr int kScStageBytes = 4 * kScBox;
 constexpr int kScSS = kScB + 4;      // row stride (floats) of the staged scores [a][beta]
-// shared memory: query means | centroids (the scores reuse both) | per-row ranges | warp maxima
-constexpr int kScSmem = kScDC * (kScQS + kScCS) * 4 + kScA * 4 * 4 + (kScThreads / 32) * kScA * 4;
-static_assert(kScA * kScSS <= kScDC * (kScQS + kScCS), "scores fit in the staging area");
+constexpr int kScOffSS = 2 * kScStageBytes;
+constexpr int kScOffBar = kScOffSS + kScA * kScSS * 4;
+constexpr int kScSmem = kScOffBar + 128 + 1024;
 
-// Row stride of the stored scores: the key blocks rounded up to whole CTA ranges.
+struct ScoreBars {
+  uint64_t full[2], empty[2], acc_full[2], acc_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(ScoreBars) <= 128, "score barriers");
+
+// Row stride of the stored scores: the key blocks rounded up to whole tiles.
 __host__ __device__ inline int sel_score_stride(int nKb) { return (nKb + kScB - 1) / kScB * kScB; }
 
-__global__ void __launch_bounds__(kScThreads, 2)
-select_score_kernel(const float* __restrict__ centroid, SelectShape s) {
-  extern __shared__ __align__(16) unsigned char sc_smem[];
-  float* sq = reinterpret_cast<float*>(sc_smem);                       // [DC][QS]
-  float* sc = sq + kScDC * kScQS;                                      // [DC][CS]
-  float* ss = sq;                                                      // [A][SS] (after the dot products)
-  int* rng = reinterpret_cast<int*>(sc + kScDC * kScCS);               // [A][2]: visible [vlo, vhi)
-  int* wpart = rng + kScA * 4;                                         // [8][A]
+// Tiles of a launch (every pooled head and sequence) and whether tile t holds a visible pair:
+// the rows' visible ranges are intervals moving right with the row, and consecutive rows'
+// intervals touch, so their union is [vlo(first row), vhi(last row)).
+__host__ __device__ inline long long sel_score_tiles(int batch, int n_hp, int nQb, int nKb) {
+  return (long long)batch * n_hp * ((nQb + kScA - 1) / kScA) * ((nKb + kScB - 1) / kScB);
+}
+__device__ __forceinline__ bool sel_tile(const SelectShape& s, long long t, int& x, int& y, int& bh) {
+  const int nx = (s.nKb + kScB - 1) / kScB, ny = (s.nQb + kScA - 1) / kScA;
+  x = (int)(t % nx);
+  y = (int)((t / nx) % ny);
+  bh = (int)(t / ((long long)nx * ny));
+  int vlo0, vhi0, vlo1, vhi1;
+  sel_visible(s, y * kScA, vlo0, vhi0);
+  sel_visible(s, min(s.nQb, (y + 1) * kScA) - 1, vlo1, vhi1);
+  return vlo0 < (x + 1) * kScB && vhi1 > x * kScB;
+}
 
+// tm_qh, tm_ql: [1, batch * n_hp * nQb, dp] fp32; tm_ch, tm_cl: [1, batch * n_kv * nKb, dp] fp32;
+// boxes of 32 x 128 with the 128-byte swizzle.  Rows past a head's last block belong to the next
+// head (or read as zero past the end): their scores are never visible, stored past the row's
+// blocks or kept.
+__global__ void __launch_bounds__(kScThreads, 1)
+select_score_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_constant__ CUtensorMap tm_ql,
+                    const __grid_constant__ CUtensorMap tm_ch, const __grid_constant__ CUtensorMap tm_cl,
+                    SelectShape s) {
+  extern __shared__ unsigned char sc_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sc_raw) + 1023) & ~uintptr_t(1023));
+  float* ss = reinterpret_cast<float*>(smem + kScOffSS);              // [A][SS]
+  ScoreBars* bars = reinterpret_cast<ScoreBars*>(smem + kScOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int beta0 = blockIdx.x * kScB, a0 = blockIdx.y * kScA;
-  const int b = blockIdx.z / s.n_hp, hp = blockIdx.z % s.n_hp;
   const int g = s.n_heads / s.n_kv;
-  const int kvh = s.group_shared ? hp : hp / g;
-  const int d = s.d;
-  const size_t row0 = ((size_t)b * s.n_hp + hp) * s.nQb;             // first pooled row of (b, hp)
+  const uint64_t tmo = s.timeout_ns;
+  const long long n_tiles = sel_score_tiles(s.batch, s.n_hp, s.nQb, s.nKb);
+  const int n_ch = s.dp / kScKC;
 
-  for (int i = tid; i < kScA; i += kScThreads) {
-    const int alpha = a0 + i;
-    int vlo = 0, vhi = 0;
-    if (alpha < s.nQb) sel_visible(s, alpha, vlo, vhi);
-    rng[4 * i + 0] = vlo;
-    rng[4 * i + 1] = vhi;
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+      mbar_init(&bars->acc_full[i], 1);
+      mbar_init(&bars->acc_empty[i], 4);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
   }
+  if (warp == 1) tmem_alloc(&bars->tmem_base, 256);
+  tc_fence_before();
   __syncthreads();
-  // does any query block of the tile see a key block of this CTA's range?
-  bool mine = false;
-  for (int i = lane; i < kScA; i += 32) mine |= max(rng[4 * i], beta0) < min(rng[4 * i + 1], beta0 + kScB);
-  if (__syncthreads_or(mine ? 1 : 0) == 0) return;
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
 
-  float acc[4][16];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
-  const float* cbase = centroid + ((size_t)b * s.n_kv + kvh) * (size_t)s.nKb_out * d;
-  const float* qbase = s.qmean + row0 * d;
-  for (int c0 = 0; c0 < d; c0 += kScDC) {
-    const int dc = min(kScDC, d - c0);
-    __syncthreads();
-    // stage query means and centroids of dims c0 .. c0 + dc, dimension-major (zeros outside):
-    // 16-byte loads along a row, the block index fastest across threads, so that the
-    // transposed stores of a warp fall in consecutive banks
-    if (d % 4 == 0) {
-      for (int e = tid; e < kScA * (kScDC / 4); e += kScThreads) {
-        const int a = e % kScA, c = 4 * (e / kScA);
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < dc && a0 + a < s.nQb) v = *reinterpret_cast<const float4*>(qbase + (size_t)(a0 + a) * d + c0 + c);
-        sq[(c + 0) * kScQS + a] = v.x;
-        sq[(c + 1) * kScQS + a] = v.y;
-        sq[(c + 2) * kScQS + a] = v.z;
-        sq[(c + 3) * kScQS + a] = v.w;
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_qh);
+      tma_prefetch_desc(&tm_ql);
+      tma_prefetch_desc(&tm_ch);
+      tma_prefetch_desc(&tm_cl);
+      int q = 0;                                       // chunks issued over the CTA's tiles
+      bool ok = true;
+      for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        int x, y, bh;
+        if (!sel_tile(s, t, x, y, bh)) continue;
+        const int b = bh / s.n_hp, hp = bh % s.n_hp, kvh = s.group_shared ? hp : hp / g;
+        const int qrow = bh * s.nQb + y * kScA, crow = (b * s.n_kv + kvh) * s.nKb + x * kScB;
+        for (int k = 0; k < n_ch; ++k, ++q) {
+          const int st = q & 1;
+          if (q >= 2 && !(ok = mbar_wait(&bars->empty[st], ((q >> 1) - 1) & 1, tmo, abort_flag))) break;
+          unsigned char* dst = smem + st * kScStageBytes;
+          mbar_arrive_expect_tx(&bars->full[st], kScStageBytes);
+          tma_load_3d(dst + 0 * kScBox, &tm_qh, &bars->full[st], kScKC * k, qrow, 0);
+          tma_load_3d(dst + 1 * kScBox, &tm_ql, &bars->full[st], kScKC * k, qrow, 0);
+          tma_load_3d(dst + 2 * kScBox, &tm_ch, &bars->full[st], kScKC * k, crow, 0);
+          tma_load_3d(dst + 3 * kScBox, &tm_cl, &bars->full[st], kScKC * k, crow, 0);
+        }
       }
-      for (int e = tid; e < kScB * (kScDC / 4); e += kScThreads) {
-        const int j = e % kScB, c = 4 * (e / kScB);
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < dc && beta0 + j < s.nKb) v = *reinterpret_cast<const float4*>(cbase + (size_t)(beta0 + j) * d + c0 + c);
-        sc[(c + 0) * kScCS + j] = v.x;
-        sc[(c + 1) * kScCS + j] = v.y;
-        sc[(c + 2) * kScCS + j] = v.z;
-        sc[(c + 3) * kScCS + j] = v.w;
-      }
-    } else {
-      for (int e = tid; e < kScA * kScDC; e += kScThreads) {
-        const int a = e % kScA, c = e / kScA;
-        sq[c * kScQS + a] = (c < dc && a0 + a < s.nQb) ? qbase[(size_t)(a0 + a) * d + c0 + c] : 0.0f;
-      }
-      for (int e = tid; e < kScB * kScDC; e += kScThreads) {
-        const int j = e % kScB, c = e / kScB;
-        sc[c * kScCS + j] = (c < dc && beta0 + j < s.nKb) ? cbase[(size_t)(beta0 + j) * d + c0 + c] : 0.0f;
-      }
+      // every load issued has landed before the CTA may exit
+      for (int k = max(0, q - 2); k < q; ++k) mbar_wait(&bars->full[k & 1], (k >> 1) & 1, tmo, nullptr);
     }
-    __syncthreads();
-    const float* qp = sq + lane;
-    const float* cp = sc + 16 * warp;
-#pragma unroll 2
-    for (int c = 0; c < dc; ++c) {       // fused multiply-adds in dimension order, two per op
-      float x[4];
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_tf32_f32(kScA, kScB);
+    bool ok = true;
+    int q = 0, j = 0;                                  // chunks consumed, tiles done
+    for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      int x, y, bh;
+      if (!sel_tile(s, t, x, y, bh)) continue;
+      const int acc = j & 1;
+      // the epilogue has read this buffer's previous tile
+      if (j >= 2 && !(ok = warp_wait(&bars->acc_empty[acc], ((j >> 1) - 1) & 1, tmo, abort_flag))) break;
+      tc_fence_after();
+      const uint32_t d = tmem + 128 * acc;
+      for (int k = 0; k < n_ch; ++k, ++q) {
+        const int st = q & 1;
+        if (!(ok = warp_wait(&bars->full[st], (q >> 1) & 1, tmo, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t base = smem_u32(smem + st * kScStageBytes);
+        const uint64_t dqh = sdesc_sw128(base + 0 * kScBox, 16, 1024), dql = sdesc_sw128(base + 1 * kScBox, 16, 1024);
+        const uint64_t dch = sdesc_sw128(base + 2 * kScBox, 16, 1024), dcl = sdesc_sw128(base + 3 * kScBox, 16, 1024);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = qp[c * kScQS + 32 * i];
-      const float4 y0 = *reinterpret_cast<const float4*>(cp + c * kScCS);
-      const float4 y1 = *reinterpret_cast<const float4*>(cp + c * kScCS + 4);
-      const float4 y2 = *reinterpret_cast<const float4*>(cp + c * kScCS + 8);
-      const float4 y3 = *reinterpret_cast<const float4*>(cp + c * kScCS + 12);
-      const float ys[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
-                            y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
+        for (int kk = 0; kk < kScKC / 8; ++kk) {       // 4 steps of 8 dimensions (32 bytes)
+          const uint64_t o = (uint64_t)((kk * 32) >> 4);
+          umma_tf32_ss_elect(d, dqh + o, dch + o, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+          umma_tf32_ss_elect(d, dqh + o, dcl + o, idesc, 1u);
+          umma_tf32_ss_elect(d, dql + o, dch + o, idesc, 1u);
+        }
+        umma_commit_elect(&bars->empty[st]);
+      }
+      if (!ok) break;
+      umma_commit_elect(&bars->acc_full[acc]);
+      ++j;
+    }
+    // every MMA issued has completed before tensor memory is released
+    umma_commit_elect(&bars->drain);
+    warp_wait(&bars->drain, 0, tmo, nullptr);
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int a = 32 * (warp & 3) + lane;                // query block of the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const float scale = 1.0f / sqrtf((float)s.d);
+    const int stride = sel_score_stride(s.nKb);
+    const int et = tid - 64;                              // 0 .. 127 over the epilogue warps
+    int j = 0;
+    for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      int x, y, bh;
+      if (!sel_tile(s, t, x, y, bh)) continue;
+      const int acc = j & 1;
+      const bool ok = warp_wait(&bars->acc_full[acc], (j >> 1) & 1, tmo, abort_flag);
+      // every epilogue warp takes the same branch
+      uint32_t all;
+      asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                   "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                   : "=r"(all) : "r"(ok && *abort_flag == 0 ? 1u : 0u) : "memory");
+      if (!all) break;
+      tc_fence_after();
+      const int a0 = y * kScA, beta0 = x * kScB;
+      const int alpha = a0 + a;
+      int vlo = 0, vhi = 0;
+      if (alpha < s.nQb) sel_visible(s, alpha, vlo, vhi);
+      float m = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < kScB; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + 128 * acc + lane_off + c, v);
+        tmem_wait_ld();
+        if (c == kScB - 32) {                            // the accumulator is read: release it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+        }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+        for (int jj = 0; jj < 32; ++jj) {
+          v[jj] = __fmul_rn(v[jj], scale);
+          const int beta = beta0 + c + jj;
+          if (beta >= vlo && beta < vhi) m = fmaxf(m, v[jj]);
+        }
 #pragma unroll
-        for (int j = 0; j < 16; j += 2)
-          ffma2(acc[i][j], acc[i][j + 1], ys[j], ys[j + 1], x[i], x[i], acc[i][j], acc[i][j + 1]);
+        for (int jj = 0; jj < 32; jj += 4)
+          *reinterpret_cast<float4*>(ss + a * kScSS + c + jj) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+      }
+      const int n_rows = min(kScA, s.nQb - a0);
+      const size_t row0 = (size_t)bh * s.nQb;
+      if (a < n_rows && m > -INFINITY) atomicMax(&s.rowmax[row0 + a0 + a], f2ord(m));
+      asm volatile("bar.sync 1, 128;" ::: "memory");       // the tile's rows are staged
+      float* dst = s.scores + (row0 + a0) * stride + beta0;
+      for (int e = et; e < n_rows * (kScB / 4); e += 128) {
+        const int r = e / (kScB / 4), q4 = e % (kScB / 4);
+        *reinterpret_cast<float4*>(dst + (size_t)r * stride + 4 * q4) = *reinterpret_cast<const float4*>(ss + r * kScSS + 4 * q4);
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");       // staged rows read: the next tile may write
+      ++j;
     }
   }
-  const float scale = 1.0f / sqrtf((float)d);
-  __syncthreads();                                   // the staging area now holds the scores
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int a = lane + 32 * i;
-    const int vlo = rng[4 * a], vhi = rng[4 * a + 1];
-    float sv[16];
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      sv[j] = __fmul_rn(acc[i][j], scale);
-      const int beta = beta0 + 16 * warp + j;
-      if (beta >= vlo && beta < vhi) m = fmaxf(m, sv[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 16; j += 4)
-      *reinterpret_cast<float4*>(ss + a * kScSS + 16 * warp + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
-    wpart[warp * kScA + a] = f2ord(m);
-  }
+  tc_fence_before();
   __syncthreads();
-  const int n_rows = min(kScA, s.nQb - a0);
-  const int stride = sel_score_stride(s.nKb);
-  for (int a = tid; a < n_rows; a += kScThreads) {
-    int m = wpart[a];
-    for (int w = 1; w < kScThreads / 32; ++w) m = max(m, wpart[w * kScA + a]);
-    if (m > f2ord(-INFINITY)) atomicMax(&s.rowmax[row0 + a0 + a], m);
-  }
-  float* dst = s.scores + (row0 + a0) * stride + beta0;
-  for (int e = tid; e < n_rows * (kScB / 4); e += kScThreads) {
-    const int a = e / (kScB / 4), q4 = e % (kScB / 4);
-    *reinterpret_cast<float4*>(dst + (size_t)a * stride + 4 * q4) = *reinterpret_cast<const float4*>(ss + a * kScSS + 4 * q4);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -428,41 +529,81 @@ select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ blo
   const float* rrow = radius + ((size_t)b * s.n_kv + kvh) * s.nKb_out;
   const uint8_t* resc = s.rescue + ((size_t)b * s.n_kv + kvh) * s.nKb;
   const bool vec4 = (s.nKb_out % 4) == 0 && (reinterpret_cast<uintptr_t>(block_mask) & 3) == 0;
+  // the rescue flags (and radii, for the bound branch) of a lane's four key blocks come with
+  // its scores, as whole words, when the rows are word (16-byte) aligned
+  const bool rvec = (s.nKb % 4) == 0 && (reinterpret_cast<uintptr_t>(resc) & 3) == 0;
+  const bool bvec = bound && (s.nKb_out % 4) == 0 && (reinterpret_cast<uintptr_t>(rrow) & 15) == 0;
+  uint8_t* mrow0 = block_mask + (((size_t)b * s.n_heads + h_out0) * s.nQb + alpha) * s.nKb_out;
+  const size_t mhead = (size_t)s.nQb * s.nKb_out;       // next head's row
   int kept = 0;
   for (int base = 4 * lane; base < s.nKb_out; base += 4 * 128) {
-    float4 sv[4];                                   // four steps' scores in flight
+    float4 sv[4], rv[4];                            // four steps' scores (radii) in flight
+    uint32_t fl[4];                                 // and rescue flags
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int beta0 = base + 128 * u;
-      sv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (beta0 < s.nKb_out && beta0 + 3 >= vlo && beta0 < vhi)    // stored for every visible block
+      sv[u] = rv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      fl[u] = 0u;
+      if (beta0 < s.nKb_out && beta0 + 3 >= vlo && beta0 < vhi) {   // stored for every visible block
         sv[u] = *reinterpret_cast<const float4*>(srow + beta0);
+        if (rvec) fl[u] = __ldg(reinterpret_cast<const uint32_t*>(resc + beta0));
+        if (bvec) rv[u] = __ldg(reinterpret_cast<const float4*>(rrow + beta0));
+      }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-    const int beta0 = base + 128 * u;
-    if (beta0 >= s.nKb_out) break;
-    uint32_t bytes = 0u;
-    const float sa[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+      const int beta0 = base + 128 * u;
+      if (beta0 >= s.nKb_out) break;
+      // keep bytes (0 or 1 each) of key blocks beta0 .. beta0 + 3; groups wholly outside the
+      // visible range keep nothing, wholly inside it and off the diagonal need no per-block
+      // range tests, and the rescue flags are already bytes of 0 and 1
+      uint32_t bytes = 0u;
+      if (beta0 + 3 >= vlo && beta0 < vhi) {
+        const float sa[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+        uint32_t mean = 0u;
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int beta = beta0 + jj;
-      const bool vis = beta >= vlo && beta < vhi;
-      bool keep = vis && (sa[jj] >= thr || resc[beta] != 0 || (beta >= dlo && beta <= dhi));
-      if (bound && vis && !keep) keep = __fmaf_rn(qn, __fmul_rn(rrow[beta], scale), sa[jj]) >= thr_b;
-      bytes |= (keep ? 1u : 0u) << (8 * jj);
-      kept += keep ? 1 : 0;
-    }
-    for (int o = 0; o < n_out; ++o) {
-      uint8_t* mrow = block_mask + (((size_t)b * s.n_heads + h_out0 + o) * s.nQb + alpha) * s.nKb_out;
-      if (vec4) {
-        *reinterpret_cast<uint32_t*>(mrow + beta0) = bytes;
-      } else {
+        for (int jj = 0; jj < 4; ++jj) mean |= (sa[jj] >= thr ? 1u : 0u) << (8 * jj);
+        uint32_t resc4 = fl[u];
+        if (!rvec) {
+          resc4 = 0u;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          if (beta0 + jj < s.nKb_out) mrow[beta0 + jj] = (uint8_t)((bytes >> (8 * jj)) & 1u);
+          for (int jj = 0; jj < 4; ++jj)
+            if (beta0 + jj < s.nKb) resc4 |= (resc[beta0 + jj] != 0 ? 1u : 0u) << (8 * jj);
+        }
+        bytes = mean | resc4;
+        const bool interior = beta0 >= vlo && beta0 + 3 < vhi && (beta0 + 3 < dlo || beta0 > dhi);
+        if (!interior) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int beta = beta0 + jj;
+            const uint32_t bit = 1u << (8 * jj);
+            if (beta >= dlo && beta <= dhi) bytes |= bit;
+            if (beta < vlo || beta >= vhi) bytes &= ~bit;
+          }
+        }
+        if (bound) {
+          const float ra[4] = {rv[u].x, rv[u].y, rv[u].z, rv[u].w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int beta = beta0 + jj;
+            const uint32_t bit = 1u << (8 * jj);
+            if (!(bytes & bit) && beta >= vlo && beta < vhi &&
+                __fmaf_rn(qn, __fmul_rn(bvec ? ra[jj] : rrow[beta], scale), sa[jj]) >= thr_b)
+              bytes |= bit;
+          }
+        }
       }
-    }
+      kept += __popc(bytes);
+      for (int o = 0; o < n_out; ++o) {
+        uint8_t* mrow = mrow0 + o * mhead;
+        if (vec4) {
+          *reinterpret_cast<uint32_t*>(mrow + beta0) = bytes;
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            if (beta0 + jj < s.nKb_out) mrow[beta0 + jj] = (uint8_t)((bytes >> (8 * jj)) & 1u);
+        }
+      }
     }
   }
 #pragma unroll

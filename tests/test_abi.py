@@ -103,6 +103,25 @@ def test_block_calls_reject_invalid_arguments(L):
     assert L.ga_select_blocks(*bad) == ga.GA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("B,H,n_kv,d,Tq,Tk,qb,kb,gs", [
+    (1, 8, 2, 128, 256, 256, 128, 64, 0),
+    (2, 32, 8, 128, 131072, 131072, 128, 64, 0),
+    (1, 4, 1, 40, 1000, 3000, 64, 16, 1),
+    (3, 6, 3, 256, 77, 5000, 200, 128, 0),
+])
+def test_select_workspace_size_matches_the_stated_formula(L, B, H, n_kv, d, Tq, Tk, qb, kb, gs):
+    """The header states the selection workspace as seven 256-byte-rounded parts; the library's
+    figure is exactly that."""
+    up = lambda x: (x + 255) // 256 * 256
+    nQb, nKb = -(-Tq // qb), -(-Tk // kb)
+    P = n_kv if gs else H
+    D = -(-d // 32) * 32
+    S = -(-nKb // 128) * 128
+    want = (2 * up(B * P * nQb * D * 4) + 2 * up(B * n_kv * nKb * D * 4) + 2 * up(B * P * nQb * 4)
+            + up(B * n_kv * nKb) + up(B * P * nQb * S * 4))
+    assert L.ga_select_workspace_size(B, H, n_kv, d, Tq, Tk, qb, kb, gs) == want
+
+
 def test_ring_calls_reject_invalid_arguments(L):
     p = ctypes.c_void_p(4096)
     odd = ctypes.c_void_p(4098)                 # not 4-byte aligned
