@@ -322,14 +322,14 @@ def part_diff(torch, ga, steps, warmup, flush, peaks):
                                "launches_per_step": 2}}
 
 
-def part_dsa(torch, ga, steps, warmup, flush, peaks):
+def part_dsa(torch, ga, steps, warmup, flush, peaks, batch=None):
     """Token top-k sparse decode on the KV-cache decode workload (B64 H32 Hkv8 d128, lengths
     U[16384, 32768]): an indexer of 8 heads x 128 dims scores every cached token, the top
     k = 2048 are kept, and attention reads only those.  Stages timed one by one and together;
     the dense decode of the same cache is timed beside it."""
     from workloads import get_config, uniform_lengths
     c = get_config(3)
-    B, H, n_kv, d, Tk = c.batch, c.n_heads, c.n_kv, c.d, c.Tk
+    B, H, n_kv, d, Tk = batch or c.batch, c.n_heads, c.n_kv, c.d, c.Tk
     Hi, di, topk = 8, 128, 2048
     lens = uniform_lengths(c.seed, B, *c.k_len_range)
     k = device_bf16(torch, c.seed, "k", (B, n_kv, Tk, d), lengths=lens)
@@ -365,7 +365,7 @@ def part_dsa(torch, ga, steps, warmup, flush, peaks):
                                                                       workspace=dws), steps, warmup, flush))
     idx_bytes = int(lens.sum()) * di * 2
     sel_kv = B * n_kv * topk * d * 2 * 2                # selected K and V rows, read once
-    return {"dsa_decode": {"workload": "bf16 top-k sparse decode B64 H32 Hkv8 d128, lengths U[16384, 32768], "
+    return {"dsa_decode": {"workload": f"bf16 top-k sparse decode B{B} H32 Hkv8 d128, lengths U[16384, 32768], "
                                        "indexer 8 x 128, k 2048",
                            "ms": t_all, "indexer_ms": t_idx, "indexer_GB/s": idx_bytes / (t_idx * 1e-3) / 1e9,
                            "indexer_frac_hbm": idx_bytes / (t_idx * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -716,7 +716,7 @@ def run_case(torch, ga, args, warmup, flush, peaks, c):
     elif args.case == "diff":
         res = part_diff(torch, ga, args.steps, warmup, flush, peaks)
     elif args.case == "dsa":
-        res = part_dsa(torch, ga, args.steps, warmup, flush, peaks)
+        res = part_dsa(torch, ga, args.steps, warmup, flush, peaks, batch=args.batch)
     elif args.case == "mla":
         res = part_mla(torch, ga, args.steps, warmup, flush, peaks)
     elif args.case == "sparse_once":
