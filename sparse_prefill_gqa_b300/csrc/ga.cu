@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <utility>
 #include <atomic>
 #include <mutex>
 
@@ -80,6 +81,25 @@ bool make_map_f32(CUtensorMap* map, const void* base, int cols, long long rows, 
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic stream
+// serialization: it may start while the previous kernel on the stream finishes, and waits for it
+// (griddep_wait) only where it reads that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 template <typename K>
@@ -675,11 +695,17 @@ int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, co
   const DeviceKernels* dk = device_kernels();
   if (!dk) return GA_ERR_CUDA;
   if (dk->mla != GA_OK) return dk->mla;
-  mla_absorb_kernel<<<dim3(C::R / C::AB_ROWS, n_heads, (batch + C::AB_SEQ - 1) / C::AB_SEQ), 256, 0, stream>>>(
+  mla_absorb_kernel<<<dim3(C::R / C::AB_ROWS, n_heads, (batch + C::AB_SEQ - 1) / C::AB_SEQ), 128, 0, stream>>>(
       (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_rope, (const __nv_bfloat16*)w_uk, q_abs, n_heads, batch);
-  mla_decode_kernel<<<dim3(s.n_chunks, batch), C::THREADS, C::SMEM_BYTES, stream>>>(tm, q_abs, ws_o, ws_ml, s);
-  mla_expand_kernel<<<dim3(C::DV / C::EX_DIMS, n_heads, (batch + C::EX_SEQ - 1) / C::EX_SEQ), 256, 0, stream>>>(
-      ws_o, ws_ml, (const __nv_bfloat16*)w_uv, (__nv_bfloat16*)out, s);
+  // the decode streams its first latent tiles while the absorption finishes, the expansion
+  // warms its weights while the decode finishes
+  if (launch_pdl(mla_decode_kernel, dim3(s.n_chunks, batch), dim3(C::THREADS), C::SMEM_BYTES, stream, tm,
+                 (const __nv_bfloat16*)q_abs, ws_o, ws_ml, s) != cudaSuccess)
+    return GA_ERR_CUDA;
+  if (launch_pdl(mla_expand_kernel, dim3(C::DV / C::EX_DIMS, n_heads, (batch + C::EX_SEQ - 1) / C::EX_SEQ), dim3(256),
+                 0, stream, (const float*)ws_o, (const float*)ws_ml, (const __nv_bfloat16*)w_uv,
+                 (__nv_bfloat16*)out, s) != cudaSuccess)
+    return GA_ERR_CUDA;
   return launch_status();
 }
 

@@ -29,8 +29,10 @@ struct MlaCfg {
   static constexpr int STAGE_BYTES = TILE * DK * 2;     // 36864
   static constexpr int QROW = DK * 2 + 16;              // padded row of the query tile (bytes)
   static constexpr int PROW = TILE * 2 + 16;            // padded row of the P tile (bytes)
-  static constexpr int OFF_Q = STAGES * STAGE_BYTES;
+  static constexpr int OFF_Q = STAGES * STAGE_BYTES;    // the query tile, then the score partials
+  static constexpr int SXROW = 40;                      // floats per head row of a partial-score tile
   static constexpr int OFF_P = OFF_Q + 16 * QROW;
+  static_assert(4 * 16 * SXROW * 4 <= 16 * QROW, "partial scores fit where the query tile was");
   static constexpr int OFF_X = OFF_P + 16 * PROW;       // [4][16] float exchange
   static constexpr int OFF_BAR = OFF_X + 4 * 16 * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;
@@ -46,56 +48,60 @@ struct MlaShape {
   uint64_t timeout_ns;
 };
 
-// grid: (R / 64, n_heads, ceil(batch / 16)); block: 256.  q[b, h] = [q_nope w_uk[h]^T (fp32
-// sums, rounded to bf16) | q_rope] for latent rows 64 x .. 64 x + 63 of head h and 16 sequences:
-// the 64 weight rows (16 KB) are staged transposed to [dim][row], so that the threads of a warp
-// read consecutive rows, with the sequences' q_nope rows; thread t computes row t % 64 for the
-// sequences t / 64, t / 64 + 4, ...
-__global__ void __launch_bounds__(256)
+// grid: (R / 64, n_heads, ceil(batch / 16)); block: 128.  q[b, h] = [q_nope w_uk[h]^T (fp32
+// sums, rounded to bf16) | q_rope] for latent rows 64 x .. 64 x + 63 of head h and 16 sequences,
+// on the tensor cores: mma.sync m16n8k16 with the 16 sequences as M, the latent rows as N and
+// the 128 nope dims as K; warp w takes latent rows 16 w .. 16 w + 15.  The 64 weight rows (16 KB)
+// and the 16 query rows are staged in shared memory with 272-byte rows (conflict-free 8-row
+// matrix loads); every weight row is read from global memory once per 16 sequences.
+__global__ void __launch_bounds__(128)
 mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16* __restrict__ q_rope,
                   const __nv_bfloat16* __restrict__ w_uk, __nv_bfloat16* __restrict__ q_abs, int n_heads,
                   int batch) {
   using C = MlaCfg;
-  __shared__ __nv_bfloat16 w_s[C::DN][C::AB_ROWS + 2];  // [dim][row]
-  __shared__ __align__(16) __nv_bfloat16 q_s[C::AB_SEQ][C::DN];   // [sequence][dim]
-  const int rb = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
-  const int b_lo = blockIdx.z * C::AB_SEQ, b_hi = min(batch, b_lo + C::AB_SEQ);
-  const int r = t % C::AB_ROWS, bg = t / C::AB_ROWS;
+  constexpr int RS = C::DN * 2 + 16;                    // staged row stride (bytes)
+  __shared__ __align__(16) unsigned char w_s[C::AB_ROWS * RS];
+  __shared__ __align__(16) unsigned char q_s[C::AB_SEQ * RS];
+  const int rb = blockIdx.x, h = blockIdx.y, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int b0 = blockIdx.z * C::AB_SEQ, nb = min(C::AB_SEQ, batch - b0);
+  griddep_launch_dependents();                          // the decode may start streaming the cache
   const __nv_bfloat16* wsrc = w_uk + ((size_t)h * C::R + (size_t)rb * C::AB_ROWS) * C::DN;
-  for (int e = t; e < C::AB_ROWS * C::DN / 8; e += 256) {     // 16-byte loads, 8 dims of one row
-    const uint4 v = *reinterpret_cast<const uint4*>(wsrc + 8 * e);
-    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&v);
-    const int row = (8 * e) / C::DN, k0 = (8 * e) % C::DN;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) w_s[k0 + u][row] = x[u];
+  for (int e = t; e < C::AB_ROWS * C::DN / 8; e += 128) {    // 16-byte pieces, 16 per row
+    const int row = e / (C::DN / 8), c = e % (C::DN / 8);
+    *reinterpret_cast<uint4*>(w_s + row * RS + 16 * c) = *reinterpret_cast<const uint4*>(wsrc + 8 * e);
   }
-  for (int b0 = b_lo; b0 < b_hi; b0 += C::AB_SEQ) {
-    const int nb = min(C::AB_SEQ, b_hi - b0);
-    __syncthreads();
-    for (int e = t; e < nb * C::DN / 8; e += 256) {
-      const int bb = (8 * e) / C::DN, k0 = (8 * e) % C::DN;
-      *reinterpret_cast<uint4*>(&q_s[bb][k0]) =
-          *reinterpret_cast<const uint4*>(q_nope + ((size_t)(b0 + bb) * n_heads + h) * C::DN + k0);
-    }
-    __syncthreads();
-    float a[C::AB_SEQ / 4];
+  for (int e = t; e < C::AB_SEQ * C::DN / 8; e += 128) {
+    const int bb = e / (C::DN / 8), c = e % (C::DN / 8);
+    *reinterpret_cast<uint4*>(q_s + bb * RS + 16 * c) =
+        bb < nb ? *reinterpret_cast<const uint4*>(q_nope + ((size_t)(b0 + bb) * n_heads + h) * C::DN + 8 * c)
+                : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  const uint32_t qs = smem_u32(q_s), ws = smem_u32(w_s);
+  const int mi = lane >> 3, rr = lane & 7;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int i = 0; i < C::AB_SEQ / 4; ++i) a[i] = 0.0f;
-#pragma unroll 4
-    for (int k = 0; k < C::DN; ++k) {
-      const float wk = __bfloat162float(w_s[k][r]);
+  for (int kk = 0; kk < C::DN / 16; ++kk) {
+    uint32_t a[4];
+    ldmatrix_x4(qs + (lane & 15) * RS + (kk * 16 + (lane >> 4) * 8) * 2, a[0], a[1], a[2], a[3]);
+    // matrices: (latent rows 16 w .. + 7, low 8 dims), (same rows, high 8), then rows + 8
+    uint32_t b0_, b1_, b2_, b3_;
+    ldmatrix_x4(ws + (16 * warp + ((mi >> 1) << 3) + rr) * RS + (kk * 16 + (mi & 1) * 8) * 2, b0_, b1_, b2_, b3_);
+    mma_bf16_16816(acc[0], a, b0_, b1_);
+    mma_bf16_16816(acc[1], a, b2_, b3_);
+  }
+  const int s_lo = lane >> 2, s_hi = s_lo + 8;          // sequences of the accumulator rows
 #pragma unroll
-      for (int i = 0; i < C::AB_SEQ / 4; ++i) a[i] = fmaf(wk, __bfloat162float(q_s[bg + 4 * i][k]), a[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < C::AB_SEQ / 4; ++i) {
-      const int b = b0 + bg + 4 * i;
-      if (b < b0 + nb) q_abs[((size_t)b * n_heads + h) * C::DK + rb * C::AB_ROWS + r] = __float2bfloat16_rn(a[i]);
-    }
+  for (int n = 0; n < 2; ++n) {
+    const int r = rb * C::AB_ROWS + 16 * warp + 8 * n + 2 * (lane & 3);   // latent rows r, r + 1
+    if (s_lo < nb)
+      *reinterpret_cast<uint32_t*>(q_abs + ((size_t)(b0 + s_lo) * n_heads + h) * C::DK + r) = pack_bf16x2(acc[n][0], acc[n][1]);
+    if (s_hi < nb)
+      *reinterpret_cast<uint32_t*>(q_abs + ((size_t)(b0 + s_hi) * n_heads + h) * C::DK + r) = pack_bf16x2(acc[n][2], acc[n][3]);
   }
   if (rb == 0)                                          // the rope part of the sequences' queries
-    for (int e = t; e < (b_hi - b_lo) * C::DR; e += 256) {
-      const size_t row = (size_t)(b_lo + e / C::DR) * n_heads + h;
+    for (int e = t; e < nb * C::DR; e += 128) {
+      const size_t row = (size_t)(b0 + e / C::DR) * n_heads + h;
       q_abs[row * C::DK + C::R + e % C::DR] = q_rope[row * C::DR + e % C::DR];
     }
 }
@@ -148,7 +154,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
     fence_barrier_init();
     fence_proxy_async_smem();
   }
+  griddep_launch_dependents();                       // the expansion may start its set-up
   if (warp < 4) {                                    // query tile, zero rows past the heads
+    griddep_wait();                                  // written by the absorption kernel
     for (int e = threadIdx.x; e < 16 * (C::DK / 8); e += 128) {
       const int r = e / (C::DK / 8), ch = e % (C::DK / 8);
       const uint4 v = r < H ? *reinterpret_cast<const uint4*>(q_abs + ((size_t)b * H + r) * C::DK + 8 * ch)
@@ -190,7 +198,19 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
   const uint32_t sbase = smem_u32(smem);
   const uint32_t qs = sbase + C::OFF_Q, ps = sbase + C::OFF_P;
   float* xs = reinterpret_cast<float*>(smem + C::OFF_X);             // [4][16]
+  float* sx = reinterpret_cast<float*>(smem + C::OFF_Q);             // [4 warps][16][SXROW]
   const int mi = lane >> 3, rr = lane & 7;
+  // Scores split over the dimensions: warp w takes the 16-dim steps 9 w .. 9 w + 8 for all 32
+  // tokens of a tile, with its 9 query fragments held in registers for the whole chunk (the
+  // query tile is read from shared memory once); the four partial tiles meet in shared memory
+  // (where the query tile was), each warp summing its own 8 tokens' columns.
+  constexpr int KW = C::DK / 16 / 4;                 // 16-dim steps per warp
+  uint32_t qa[KW][4];
+#pragma unroll
+  for (int i = 0; i < KW; ++i)
+    ldmatrix_x4(qs + (lane & 15) * C::QROW + ((KW * warp + i) * 16 + (lane >> 4) * 8) * 2, qa[i][0], qa[i][1],
+                qa[i][2], qa[i][3]);
+  asm volatile("bar.sync 1, 128;" ::: "memory");     // every warp has its fragments: the tile is free
 
   for (int it = 0; it < n_tiles; ++it) {
     const int st = it % C::STAGES;
@@ -198,24 +218,47 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
     if (!consumers_all(got)) break;
     const uint32_t kb = sbase + st * C::STAGE_BYTES;
     const int t0 = kbeg + it * C::TILE;                // first token of the tile
-    // ---- scores of this warp's 8 tokens ---------------------------------------------------
-    // One 4-matrix load brings the keys' dims of two 16-dim steps: matrices 0, 1 the low and
-    // high 8 dims of step kk, matrices 2, 3 those of step kk + 1.
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- partial scores over this warp's 144 dims, all 32 tokens ------------------------------
     {
-      const int keyr = 8 * warp + rr;
-#pragma unroll 2
-      for (int kk = 0; kk < C::DK / 16; kk += 2) {
-        uint32_t a0[4], a1[4];
-        ldmatrix_x4(qs + (lane & 15) * C::QROW + (kk * 16 + (lane >> 4) * 8) * 2, a0[0], a0[1], a0[2], a0[3]);
-        ldmatrix_x4(qs + (lane & 15) * C::QROW + ((kk + 1) * 16 + (lane >> 4) * 8) * 2, a1[0], a1[1], a1[2], a1[3]);
-        const int dchunk = 2 * (kk + (mi >> 1)) + (mi & 1);
-        const uint32_t addr = kb + (dchunk >> 3) * (C::TILE * 128) + keyr * 128 + (((dchunk & 7) ^ (keyr & 7)) << 4);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(addr, b0, b1, b2, b3);
-        mma_bf16_16816(sc, a0, b0, b1);
-        mma_bf16_16816(sc, a1, b2, b3);
+      float sacc[4][4];
+#pragma unroll
+      for (int nb = 0; nb < 4; ++nb) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.0f;
+#pragma unroll
+      for (int nb = 0; nb < 4; ++nb) {
+        const int keyr = 8 * nb + rr;                 // token row this lane addresses
+#pragma unroll
+        for (int i = 0; i < KW; i += 2) {
+          // one 4-matrix load: matrices 0, 1 the low and high 8 dims of step i, 2, 3 those of
+          // step i + 1 (the last, odd step loads its own dims twice)
+          const int kk = KW * warp + i + ((mi >> 1) && i + 1 < KW ? 1 : 0);
+          const int dchunk = 2 * kk + (mi & 1);
+          const uint32_t addr = kb + (dchunk >> 3) * (C::TILE * 128) + keyr * 128 + (((dchunk & 7) ^ (keyr & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(addr, b0, b1, b2, b3);
+          mma_bf16_16816(sacc[nb], qa[i], b0, b1);
+          if (i + 1 < KW) mma_bf16_16816(sacc[nb], qa[i + 1], b2, b3);
+        }
       }
+      float* mine = sx + warp * 16 * C::SXROW;
+#pragma unroll
+      for (int nb = 0; nb < 4; ++nb) {
+        const int col = 8 * nb + 2 * (lane & 3);
+        *reinterpret_cast<float2*>(mine + r_lo * C::SXROW + col) = make_float2(sacc[nb][0], sacc[nb][1]);
+        *reinterpret_cast<float2*>(mine + r_hi * C::SXROW + col) = make_float2(sacc[nb][2], sacc[nb][3]);
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // the partial tiles are complete
+    float sc[4];
+    {
+      const int col = 8 * warp + 2 * (lane & 3);       // this warp's tokens
+      float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float2 x = *reinterpret_cast<const float2*>(sx + (w * 16 + r_lo) * C::SXROW + col);
+        const float2 y = *reinterpret_cast<const float2*>(sx + (w * 16 + r_hi) * C::SXROW + col);
+        lo.x += x.x; lo.y += x.y; hi.x += y.x; hi.y += y.y;
+      }
+      sc[0] = lo.x; sc[1] = lo.y; sc[2] = hi.x; sc[3] = hi.y;
     }
     float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -334,10 +377,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
   }
 }
 
-// grid: (DV / 64, n_heads, ceil(batch / 4)); block: 256.  For 4 sequences of head h: warps 0-3
-// re-associate the chunk partials of one sequence each into the latent output (o_lat = sum_c
-// 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the chunks holding tokens; the lanes over the
-// latent dims, the chunks' loads overlapped), then out = o_lat w_uv[h] for output dims 64 x ..
+// grid: (DV / 64, n_heads, ceil(batch / 4)); block: 256.  For 4 sequences of head h: warps w and
+// w + 4 re-associate the chunk partials of sequence w into half of its latent output each (o_lat =
+// sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the chunks holding tokens; the lanes over the
+// latent dims, four chunks' loads in flight), then out = o_lat w_uv[h] for output dims 64 x ..
 // 64 x + 63: thread t takes dim t % 64 over latent dims 128 (t / 64) .. + 127 for the 4
 // sequences (fp32 sums, every weight element read once for all 4), and the four partial sums of
 // each output meet in shared memory.
@@ -350,11 +393,19 @@ mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_m
   const int xb = blockIdx.x, h = blockIdx.y, b0 = blockIdx.z * C::EX_SEQ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = min(C::EX_SEQ, s.batch - b0);
-  if (warp < C::EX_SEQ) {
-    const int i = warp;
-    float o[C::R / 32];
+  {
+    // this CTA's weight columns into L2 while the decode finishes, then its partials
+    const __nv_bfloat16* wcol = w_uv + (size_t)h * C::R * C::DV + xb * C::EX_DIMS;
+    for (int r = threadIdx.x; r < C::R; r += 256) prefetch_l2(wcol + (size_t)r * C::DV);
+    griddep_wait();
+  }
+  {
+    // warp w: sequence w % 4, latent dims 256 (w / 4) .. + 255 (lane + 32 u)
+    const int i = warp % C::EX_SEQ, half = warp / C::EX_SEQ;
+    constexpr int U = C::R / 2 / 32;
+    float o[U];
 #pragma unroll
-    for (int u = 0; u < C::R / 32; ++u) o[u] = 0.0f;
+    for (int u = 0; u < U; ++u) o[u] = 0.0f;
     if (i < nb) {
       const int b = b0 + i;
       const int L = seq_keys(s.lens, b, s.L_max);
@@ -367,22 +418,26 @@ mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_m
       for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
       float Lsum = 0.0f;
       if (M != -INFINITY) {
-#pragma unroll 2
+        // the chunks' loads do not depend on their factors: four chunks in flight
+#pragma unroll 4
         for (int c = 0; c < n_used; ++c) {
-          const float mc = ml[2 * c];
-          const float f = mc == -INFINITY ? 0.0f : ex2(mc - M);
-          Lsum = fmaf(f, ml[2 * c + 1], Lsum);
-          const float* src = ws_o + (qrow * s.n_chunks + c) * C::R + lane;
+          const float2 mlc = *reinterpret_cast<const float2*>(ml + 2 * c);
+          const float* src = ws_o + (qrow * s.n_chunks + c) * C::R + C::R / 2 * half + lane;
+          float v[U];
 #pragma unroll
-          for (int u = 0; u < C::R / 32; ++u) o[u] = fmaf(f, src[32 * u], o[u]);
+          for (int u = 0; u < U; ++u) v[u] = src[32 * u];
+          const float f = mlc.x == -INFINITY ? 0.0f : ex2(mlc.x - M);
+          Lsum = fmaf(f, mlc.y, Lsum);
+#pragma unroll
+          for (int u = 0; u < U; ++u) o[u] = fmaf(f, v[u], o[u]);
         }
       }
       const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
 #pragma unroll
-      for (int u = 0; u < C::R / 32; ++u) o[u] *= inv;
+      for (int u = 0; u < U; ++u) o[u] *= inv;
     }
 #pragma unroll
-    for (int u = 0; u < C::R / 32; ++u) lat[i][lane + 32 * u] = o[u];
+    for (int u = 0; u < U; ++u) lat[i][C::R / 2 * half + lane + 32 * u] = o[u];
   }
   __syncthreads();
   const int e = threadIdx.x % C::EX_DIMS, cp = threadIdx.x / C::EX_DIMS;   // output dim, latent quarter

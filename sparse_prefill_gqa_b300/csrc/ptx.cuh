@@ -101,6 +101,19 @@ __device__ __forceinline__ bool named_all(bool ok) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization may
+// start while the previous kernel on the stream still runs; griddep_wait() blocks until that
+// kernel has completed and its memory operations are visible, so a kernel calls it before its
+// first read of what the previous one wrote (and before its first write of anything the previous
+// one reads).  griddep_launch_dependents() lets the next such kernel start launching.  Both are
+// no-ops when the kernel was launched the ordinary way.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------
 // Register reallocation between warpgroups (all four warps of a warpgroup execute it).
 // The sum over warpgroups of (128 x registers) must stay within what the CTA was launched
 // with, or an increase waits forever: callers check that sum against the kernel's
