@@ -385,6 +385,17 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
  * Returns GA_ERR_CUDA when the synchronisation itself fails. */
 int ga_read_device_status(ga_stream_t stream);
 
+/* The debug build (the same sources compiled with GA_DEBUG defined: libga_debug.so) checks, in
+ * the kernels, the offsets of its output stores against the outputs' extents and the coordinates
+ * of its TMA copies, skips an access that fails and records the device's first failure in a
+ * sticky word.  Synchronises `stream`, then stores and clears that word in *first: 0 when no
+ * check failed, else (site << 48) | offset (sites: 1 TMA coordinate or destination, 2 prefill
+ * output, 3 prefill lse, 4 decode partials, 5 decode output, 6 top-k indices, 7 selection
+ * scores, 8 block mask, 9 MLA q_lat, 10 MLA partials, 11 MLA output).  Returns GA_OK, or
+ * GA_ERR_UNSUPPORTED from the ordinary build (no checks compiled), GA_ERR_CUDA on a failed
+ * synchronisation. */
+int ga_debug_violation(uint64_t* first, ga_stream_t stream);
+
 /* Time limit for every device-side wait, in nanoseconds (default 2e9; minimum 1e5).
  * Applies to launches made after the call. */
 void ga_set_wait_timeout_ns(uint64_t ns);

@@ -101,6 +101,8 @@ def lib() -> ctypes.CDLL:
     L.ga_select_workspace_size.restype = sz
     L.ga_read_device_status.argtypes = [vp]
     L.ga_read_device_status.restype = i32
+    L.ga_debug_violation.argtypes = [ctypes.POINTER(ctypes.c_uint64), vp]
+    L.ga_debug_violation.restype = i32
     L.ga_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     L.ga_set_wait_timeout_ns.restype = None
     L.ga_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
@@ -559,6 +561,18 @@ def ga_select_blocks(q, centroid, radius, *, Tk=None, q_block=128, k_block=64, c
 
 def ga_read_device_status(stream=None) -> int:
     return int(lib().ga_read_device_status(_stream(stream)))
+
+
+def ga_debug_violation(stream=None):
+    """The debug build's first failed in-kernel bounds check since the last read (0: none), read
+    and cleared; None from the ordinary build, which compiles no checks."""
+    v = ctypes.c_uint64(0)
+    st = int(lib().ga_debug_violation(ctypes.byref(v), _stream(stream)))
+    if st == GA_ERR_UNSUPPORTED:
+        return None
+    if st != GA_OK:
+        raise GAError(st, "ga_debug_violation")
+    return int(v.value)
 
 
 def ga_set_wait_timeout_ns(ns: int) -> None:

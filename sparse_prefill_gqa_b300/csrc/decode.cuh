@@ -122,8 +122,8 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const int m = e / D, dim = e % D;
         const int hh = kvh * s.g + m % s.g;
         const size_t qrow = ((size_t)b * s.a.n_heads + hh) * s.a.Tq + m / s.g;
-        out[qrow * D + dim] = __float2bfloat16_rn(0.0f);
-        if (lse && dim == 0) lse[qrow] = s.a.sink ? s.a.sink[hh] : -INFINITY;
+        if (GA_BOUNDS(qrow < (size_t)s.a.batch * s.a.n_heads * s.a.Tq && dim < D, 5, qrow)) out[qrow * D + dim] = __float2bfloat16_rn(0.0f);
+        if (lse && dim == 0 && GA_BOUNDS(qrow < (size_t)s.a.batch * s.a.n_heads * s.a.Tq, 5, qrow)) lse[qrow] = s.a.sink ? s.a.sink[hh] : -INFINITY;
       }
     }
     return;
@@ -399,12 +399,12 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       // left in the workspace.
       const size_t qrow = ((size_t)b * s.a.n_heads + kvh * g + m % g) * s.a.Tq + m / g;
       if (final_out) {
-        out[qrow * D + dim] = __float2bfloat16_rn(0.0f);
-        if (lse && dim == 0) lse[qrow] = -INFINITY;
+        if (GA_BOUNDS(qrow < (size_t)s.a.batch * s.a.n_heads * s.a.Tq && dim < D, 5, qrow)) out[qrow * D + dim] = __float2bfloat16_rn(0.0f);
+        if (lse && dim == 0 && GA_BOUNDS(qrow < (size_t)s.a.batch * s.a.n_heads * s.a.Tq, 5, qrow)) lse[qrow] = -INFINITY;
       } else {
         const size_t slot = qrow * s.n_chunks + c;
-        ws_o[slot * D + dim] = 0.0f;
-        if (dim == 0) {
+        if (GA_BOUNDS(slot < (size_t)s.a.batch * s.a.n_heads * s.a.Tq * s.n_chunks && dim < D, 4, slot)) ws_o[slot * D + dim] = 0.0f;
+        if (dim == 0 && GA_BOUNDS(slot < (size_t)s.a.batch * s.a.n_heads * s.a.Tq * s.n_chunks, 4, slot)) {
           ws_ml[slot * 2 + 0] = -INFINITY;
           ws_ml[slot * 2 + 1] = 0.0f;
         }
@@ -433,12 +433,12 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         O = M == -INFINITY ? 0.0f : O * ex2(M - Mn);
         Mf = Mn;
       }
-      out[qrow * D + dim] = __float2bfloat16_rn(Lf > 0.0f ? O / Lf : 0.0f);
-      if (lse && dim == 0) lse[qrow] = Lf > 0.0f ? (Mf + log2f(Lf)) * 0.6931471805599453f : -INFINITY;
+      if (GA_BOUNDS(qrow < (size_t)s.a.batch * s.a.n_heads * s.a.Tq && dim < D, 5, qrow)) out[qrow * D + dim] = __float2bfloat16_rn(Lf > 0.0f ? O / Lf : 0.0f);
+      if (lse && dim == 0 && GA_BOUNDS(qrow < (size_t)s.a.batch * s.a.n_heads * s.a.Tq, 5, qrow)) lse[qrow] = Lf > 0.0f ? (Mf + log2f(Lf)) * 0.6931471805599453f : -INFINITY;
     } else {
       const size_t slot = qrow * s.n_chunks + c;
-      ws_o[slot * D + dim] = O;
-      if (dim == 0) {
+      if (GA_BOUNDS(slot < (size_t)s.a.batch * s.a.n_heads * s.a.Tq * s.n_chunks && dim < D, 4, slot)) ws_o[slot * D + dim] = O;
+      if (dim == 0 && GA_BOUNDS(slot < (size_t)s.a.batch * s.a.n_heads * s.a.Tq * s.n_chunks, 4, slot)) {
         ws_ml[slot * 2 + 0] = M;
         ws_ml[slot * 2 + 1] = L;
       }
@@ -479,8 +479,8 @@ decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ 
     }
     if (s.a.sink) L += ex2(s.a.sink[hh] * kLog2e - Mf);
   }
-  out[qrow * D + dim] = __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
-  if (lse && dim == 0) lse[qrow] = L > 0.0f ? (Mf + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  if (GA_BOUNDS(qrow < (size_t)s.a.batch * s.a.n_heads * s.a.Tq && dim < D, 5, qrow)) out[qrow * D + dim] = __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
+  if (lse && dim == 0 && GA_BOUNDS(qrow < (size_t)s.a.batch * s.a.n_heads * s.a.Tq, 5, qrow)) lse[qrow] = L > 0.0f ? (Mf + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 }  // namespace ga

@@ -284,7 +284,8 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
     const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
     const bool sel = gt || (eq && eq_run + __popc(eq_bal & lt_mask) < quota);
     const uint32_t sel_bal = __ballot_sync(0xffffffffu, sel);
-    if (sel) out[out_run + __popc(sel_bal & lt_mask)] = j;
+    if (sel && GA_BOUNDS(out_run + __popc(sel_bal & lt_mask) < topk, 6, out_run + __popc(sel_bal & lt_mask)))
+      out[out_run + __popc(sel_bal & lt_mask)] = j;
     eq_run += __popc(eq_bal);
     out_run += __popc(sel_bal);
   }

@@ -362,6 +362,22 @@ int ga_read_device_status(ga_stream_t stream) {
 
 void ga_selftest_drop_prefill_chunk(int chunk) { g_test_drop_chunk = chunk < 0 ? -1 : chunk; }
 
+int ga_debug_violation(uint64_t* first, ga_stream_t stream) {
+#ifdef GA_DEBUG
+  if (!first) return GA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GA_ERR_CUDA;
+  unsigned long long v = 0ull, zero = 0ull;
+  if (cudaMemcpyFromSymbol(&v, g_debug_violation, sizeof(v)) != cudaSuccess) return GA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_debug_violation, &zero, sizeof(zero)) != cudaSuccess) return GA_ERR_CUDA;
+  *first = v;
+  return GA_OK;
+#else
+  (void)first;
+  (void)stream;
+  return GA_ERR_UNSUPPORTED;
+#endif
+}
+
 int ga_selftest_wait_timeout(uint64_t timeout_ns, ga_stream_t stream) {
   int* flag = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&flag), g_never_set_flag) != cudaSuccess)

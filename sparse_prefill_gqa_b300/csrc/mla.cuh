@@ -94,10 +94,12 @@ mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16*
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
     const int r = rb * C::AB_ROWS + 16 * warp + 8 * n + 2 * (lane & 3);   // latent rows r, r + 1
-    if (s_lo < nb)
-      *reinterpret_cast<uint32_t*>(q_abs + ((size_t)(b0 + s_lo) * n_heads + h) * C::DK + r) = pack_bf16x2(acc[n][0], acc[n][1]);
-    if (s_hi < nb)
-      *reinterpret_cast<uint32_t*>(q_abs + ((size_t)(b0 + s_hi) * n_heads + h) * C::DK + r) = pack_bf16x2(acc[n][2], acc[n][3]);
+    const size_t lim = (size_t)batch * n_heads * C::DK;
+    const size_t o_lo = ((size_t)(b0 + s_lo) * n_heads + h) * C::DK + r, o_hi = ((size_t)(b0 + s_hi) * n_heads + h) * C::DK + r;
+    if (s_lo < nb && GA_BOUNDS(o_lo + 2 <= lim && r + 2 <= C::R, 9, o_lo))
+      *reinterpret_cast<uint32_t*>(q_abs + o_lo) = pack_bf16x2(acc[n][0], acc[n][1]);
+    if (s_hi < nb && GA_BOUNDS(o_hi + 2 <= lim && r + 2 <= C::R, 9, o_hi))
+      *reinterpret_cast<uint32_t*>(q_abs + o_hi) = pack_bf16x2(acc[n][2], acc[n][3]);
   }
   if (rb == 0)                                          // the rope part of the sequences' queries
     for (int e = t; e < nb * C::DR; e += 128) {
@@ -368,7 +370,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
 #pragma unroll
     for (int n = 0; n < 16; ++n) {
       const int dim = 128 * warp + 8 * n + 2 * (lane & 3);
-      *reinterpret_cast<float2*>(ws_o + slot * C::R + dim) = make_float2(o[n][2 * row], o[n][2 * row + 1]);
+      if (GA_BOUNDS(slot < (size_t)s.batch * H * s.n_chunks && dim + 2 <= C::R, 10, slot))
+        *reinterpret_cast<float2*>(ws_o + slot * C::R + dim) = make_float2(o[n][2 * row], o[n][2 * row + 1]);
     }
     if (warp == 0 && (lane & 3) == 0) {
       ws_ml[slot * 2 + 0] = m_run[row];
@@ -456,7 +459,8 @@ mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_m
     const int i = threadIdx.x / C::EX_DIMS, d = threadIdx.x % C::EX_DIMS;
     if (i < nb) {
       const float y = (part[0][i][d] + part[1][i][d]) + (part[2][i][d] + part[3][i][d]);
-      out[((size_t)(b0 + i) * s.n_heads + h) * C::DV + xb * C::EX_DIMS + d] = __float2bfloat16_rn(y);
+      const size_t off = ((size_t)(b0 + i) * s.n_heads + h) * C::DV + xb * C::EX_DIMS + d;
+      if (GA_BOUNDS(off < (size_t)s.batch * s.n_heads * C::DV, 11, off)) out[off] = __float2bfloat16_rn(y);
     }
   }
 }

@@ -862,8 +862,9 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const int q = 32 * i + lane, r = q >> 2, u = q & 3;      // row r of the warp, piece u
             const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
             const int tr = 32 * (warp & 3) + r;                       // row of the query tile
-            if (tr < it.rows)
-              *reinterpret_cast<uint4*>(out + (((size_t)it.b * sh.n_heads + it.h) * sh.Tq + it.t0 + tr) * D + c + 8 * u) = v;
+            const size_t off = (((size_t)it.b * sh.n_heads + it.h) * sh.Tq + it.t0 + tr) * D + c + 8 * u;
+            if (tr < it.rows && GA_BOUNDS(off + 8 <= (size_t)sh.batch * sh.n_heads * sh.Tq * D, 2, off))
+              *reinterpret_cast<uint4*>(out + off) = v;
           }
           __syncwarp();
           return;
@@ -892,7 +893,8 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             pk.y = pack_bf16x2(x[2], x[3]);
             pk.z = pack_bf16x2(x[4], x[5]);
             pk.w = pack_bf16x2(x[6], x[7]);
-            *reinterpret_cast<uint4*>(orow + c + u) = pk;
+            if (GA_BOUNDS(orow_off + c + u + 8 <= (size_t)sh.batch * sh.n_heads * sh.Tq * D, 2, orow_off + c + u))
+              *reinterpret_cast<uint4*>(orow + c + u) = pk;
           }
         }
       };
@@ -930,7 +932,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           }
           store32(c, o0, 1.0f);
         }
-        if (lse && wg == 0 && row < it.rows)
+        if (lse && wg == 0 && row < it.rows && GA_BOUNDS(((size_t)it.b * sh.n_heads + it.h) * sh.Tq + t < (size_t)sh.batch * sh.n_heads * sh.Tq, 3, t))
           lse[((size_t)it.b * sh.n_heads + it.h) * sh.Tq + t] =
               L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
       } else {
@@ -952,7 +954,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           }
           store32(c, o, inv_l);
         }
-        if (lse && row < it.rows)
+        if (lse && row < it.rows && GA_BOUNDS(((size_t)it.b * sh.n_heads + it.h) * sh.Tq + t < (size_t)sh.batch * sh.n_heads * sh.Tq, 3, t))
           lse[((size_t)it.b * sh.n_heads + it.h) * sh.Tq + t] =
               l_run > 0.0f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
       }

@@ -21,6 +21,21 @@ __device__ __forceinline__ void record_status(int code) {
   atomicCAS(&g_device_status, 0, code);
 }
 
+// In-kernel bounds checks of the debug build (compiled with -DGA_DEBUG).  GA_BOUNDS(ok, site, at)
+// is `ok` there -- the guarded access runs only when it holds -- and a failing check records the
+// first violation of the device in a sticky word: site number << 48 | the offending offset (low 48
+// bits).  In the ordinary build it is `true` and costs nothing.
+__device__ unsigned long long g_debug_violation = 0ull;
+#ifdef GA_DEBUG
+__device__ __forceinline__ bool debug_in_bounds(bool ok, unsigned site, unsigned long long at) {
+  if (!ok) atomicCAS(&g_debug_violation, 0ull, ((unsigned long long)site << 48) | (at & 0xFFFFFFFFFFFFull));
+  return ok;
+}
+#define GA_BOUNDS(ok, site, at) ::ga::debug_in_bounds((ok), (site), (unsigned long long)(at))
+#else
+#define GA_BOUNDS(ok, site, at) true
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -146,6 +161,9 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 // The innermost coordinate x must be a multiple of 8 elements for 16-bit data (16 bytes).
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y, int z) {
+  // every map of the library has 16-bit or 32-bit elements: x a multiple of 4 is the least the
+  // 16-byte rule needs (site 1)
+  if (!GA_BOUNDS((x & 3) == 0 && (smem_u32(smem_dst) & 127) == 0, 1, x)) return;
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];"

@@ -484,7 +484,9 @@ select_score_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_cons
       float* dst = s.scores + (row0 + a0) * stride + beta0;
       for (int e = et; e < n_rows * (kScB / 4); e += 128) {
         const int r = e / (kScB / 4), q4 = e % (kScB / 4);
-        *reinterpret_cast<float4*>(dst + (size_t)r * stride + 4 * q4) = *reinterpret_cast<const float4*>(ss + r * kScSS + 4 * q4);
+        const size_t off = (row0 + a0 + r) * stride + beta0 + 4 * q4;
+        if (GA_BOUNDS(off + 4 <= (size_t)s.batch * s.n_hp * s.nQb * stride, 7, off))
+          *reinterpret_cast<float4*>(dst + (size_t)r * stride + 4 * q4) = *reinterpret_cast<const float4*>(ss + r * kScSS + 4 * q4);
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");       // staged rows read: the next tile may write
       ++j;
@@ -596,6 +598,8 @@ select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ blo
       kept += __popc(bytes);
       for (int o = 0; o < n_out; ++o) {
         uint8_t* mrow = mrow0 + o * mhead;
+        const size_t moff = (size_t)(mrow - block_mask) + beta0;
+        if (!GA_BOUNDS(moff < (size_t)s.batch * s.n_heads * s.nQb * s.nKb_out, 8, moff)) continue;
         if (vec4) {
           *reinterpret_cast<uint32_t*>(mrow + beta0) = bytes;
         } else {

@@ -37,6 +37,16 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), n
 
 
+def test_debug_build_exports_the_same_symbols_and_only_it_reports_checks(L):
+    """libga_debug.so (GA_DEBUG: in-kernel bounds checks) is the same ABI; the ordinary build
+    answers ga_debug_violation with GA_ERR_UNSUPPORTED before any CUDA call."""
+    dbg = ctypes.CDLL(build.build(debug=True))
+    for n in sorted(_declared()):
+        assert hasattr(dbg, n), n
+    v = ctypes.c_uint64(7)
+    assert L.ga_debug_violation(ctypes.byref(v), None) == ga.GA_ERR_UNSUPPORTED
+
+
 def test_status_strings_and_version(L):
     assert ga.ga_status_string(0) == "GA_OK"
     for s in (-1, -2, -3, -4, -5):
