@@ -110,6 +110,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  griddep_launch_dependents();                    // the combine may start its launch
   const int Tk = seq_keys(s.a.k_lens, b, s.a.Tk_max);
   int kbeg, kend;
   decode_chunk_range(s, Tk, c, kbeg, kend);
@@ -447,12 +448,15 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 }
 
 // Combine the chunk partials of one (b, h, query row).  grid: (Tq, n_heads, batch), D threads.
+// Launched as a programmatic dependent of the decode kernel: its CTAs may become resident while
+// the decode's last CTAs run, and read nothing before the decode grid has completed.
 template <int D>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse, DecodeShape s) {
   const int tq = blockIdx.x, hh = blockIdx.y, b = blockIdx.z;
   const int dim = threadIdx.x;
+  griddep_wait();                                 // the partials of the decode kernel
   const int Tk = seq_keys(s.a.k_lens, b, s.a.Tk_max);
   const size_t qrow = ((size_t)b * s.a.n_heads + hh) * s.a.Tq + tq;
   float M = -INFINITY;

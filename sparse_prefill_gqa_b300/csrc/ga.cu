@@ -266,7 +266,9 @@ int launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfl
       tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
   const int st = launch_status();
   if (st != GA_OK || ds.n_chunks == 1) return st;
-  decode_combine_kernel<D><<<dim3(ds.a.Tq, ds.a.n_heads, ds.a.batch), D, 0, stream>>>(ws_o, ws_ml, ob, lse, ds);
+  if (launch_pdl(decode_combine_kernel<D>, dim3(ds.a.Tq, ds.a.n_heads, ds.a.batch), dim3(D), 0, stream, ws_o,
+                 ws_ml, ob, lse, ds) != cudaSuccess)
+    return GA_ERR_CUDA;
   return launch_status();
 }
 
