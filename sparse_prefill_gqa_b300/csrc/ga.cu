@@ -664,23 +664,38 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
 }
 
 namespace {
-// Token chunk of the MLA decode: about four CTAs per SM over the batch at full length (two run
-// at a time on each SM), whole 32-token tiles.
-int mla_chunk_len(int batch, int L_max) {
-  long long c = (long long)L_max * batch / (148LL * 4);
-  c = c < 256 ? 256 : (c > 4096 ? 4096 : c);
-  return (int)((c + MlaCfg::TILE - 1) / MlaCfg::TILE * MlaCfg::TILE);
+// CTAs of the MLA decode: two per SM.  The workspace is sized for kMlaMaxCta, so that it does
+// not depend on the device it is used on.
+constexpr int kMlaMaxCta = 2 * 192;
+
+struct MlaWorkspace {
+  __nv_bfloat16* q_abs;  // [batch, n_heads, 576]
+  float* ws_o;           // [n_ids, n_heads, 512]
+  float* ws_ml;          // [n_ids, n_heads, 2]
+  int2* seg;             // [batch]
+};
+
+// Workspace layout (each part rounded up to 256 bytes); n_ids = kMlaMaxCta + batch - 1.
+size_t mla_layout(int batch, int n_heads, void* base, MlaWorkspace* w) {
+  using C = MlaCfg;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = (size_t)batch * n_heads, ids = (size_t)kMlaMaxCta + batch - 1;
+  const size_t o_q = 0, o_o = o_q + up(rows * C::DK * 2), o_ml = o_o + up(ids * n_heads * C::R * 4),
+               o_seg = o_ml + up(ids * n_heads * 2 * 4), total = o_seg + up((size_t)batch * 8);
+  if (w) {
+    unsigned char* p = static_cast<unsigned char*>(base);
+    w->q_abs = reinterpret_cast<__nv_bfloat16*>(p + o_q);
+    w->ws_o = reinterpret_cast<float*>(p + o_o);
+    w->ws_ml = reinterpret_cast<float*>(p + o_ml);
+    w->seg = reinterpret_cast<int2*>(p + o_seg);
+  }
+  return total;
 }
 }  // namespace
 
 size_t ga_mla_decode_workspace_size(int batch, int n_heads, int L_max) {
   if (batch < 1 || n_heads < 1 || n_heads > 16 || L_max < 1) return SIZE_MAX;
-  using C = MlaCfg;
-  const int chunk = mla_chunk_len(batch, L_max);
-  const size_t n_chunks = (L_max + chunk - 1) / chunk;
-  const size_t rows = (size_t)batch * n_heads;
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  return up(rows * C::DK * 2) + up(rows * n_chunks * C::R * 4) + up(rows * n_chunks * 2 * 4);
+  return mla_layout(batch, n_heads, nullptr, nullptr);
 }
 
 int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, const void* w_uk,
@@ -697,31 +712,28 @@ int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, co
   const size_t need = ga_mla_decode_workspace_size(batch, n_heads, L_max);
   if (need == SIZE_MAX) return GA_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GA_ERR_WORKSPACE;
-  MlaShape s{};
-  s.batch = batch; s.n_heads = n_heads; s.L_max = L_max; s.lens = lens; s.timeout_ns = g_timeout_ns;
-  s.chunk_len = mla_chunk_len(batch, L_max);
-  s.n_chunks = (L_max + s.chunk_len - 1) / s.chunk_len;
-  if (s.n_chunks > 65535) return GA_ERR_UNSUPPORTED;
-  const size_t rows = (size_t)batch * n_heads;
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  unsigned char* w = static_cast<unsigned char*>(workspace);
-  auto* q_abs = reinterpret_cast<__nv_bfloat16*>(w);
-  auto* ws_o = reinterpret_cast<float*>(w + up(rows * C::DK * 2));
-  auto* ws_ml = reinterpret_cast<float*>(w + up(rows * C::DK * 2) + up(rows * s.n_chunks * C::R * 4));
+  MlaWorkspace w;
+  mla_layout(batch, n_heads, workspace, &w);
   CUtensorMap tm;
   if (!make_map_bf16(&tm, latent, C::DK, L_max, batch, C::TILE)) return GA_ERR_CUDA;
   const DeviceKernels* dk = device_kernels();
   if (!dk) return GA_ERR_CUDA;
   if (dk->mla != GA_OK) return dk->mla;
+  MlaShape s{};
+  s.batch = batch; s.n_heads = n_heads; s.L_max = L_max; s.lens = lens; s.timeout_ns = g_timeout_ns;
+  s.n_cta = 2 * dk->n_sm < kMlaMaxCta ? 2 * dk->n_sm : kMlaMaxCta;
+  s.n_ids = s.n_cta + batch - 1;
+  s.seg = w.seg;
   mla_absorb_kernel<<<dim3(C::R / C::AB_ROWS, n_heads, (batch + C::AB_SEQ - 1) / C::AB_SEQ), 128, 0, stream>>>(
-      (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_rope, (const __nv_bfloat16*)w_uk, q_abs, n_heads, batch);
+      (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_rope, (const __nv_bfloat16*)w_uk, w.q_abs, n_heads,
+      batch);
   // the decode streams its first latent tiles while the absorption finishes, the expansion
   // warms its weights while the decode finishes
-  if (launch_pdl(mla_decode_kernel, dim3(s.n_chunks, batch), dim3(C::THREADS), C::SMEM_BYTES, stream, tm,
-                 (const __nv_bfloat16*)q_abs, ws_o, ws_ml, s) != cudaSuccess)
+  if (launch_pdl(mla_decode_kernel, dim3(s.n_cta), dim3(C::THREADS), C::SMEM_BYTES, stream, tm,
+                 (const __nv_bfloat16*)w.q_abs, w.ws_o, w.ws_ml, s) != cudaSuccess)
     return GA_ERR_CUDA;
   if (launch_pdl(mla_expand_kernel, dim3(C::DV / C::EX_DIMS, n_heads, (batch + C::EX_SEQ - 1) / C::EX_SEQ), dim3(256),
-                 0, stream, (const float*)ws_o, (const float*)ws_ml, (const __nv_bfloat16*)w_uv,
+                 0, stream, (const float*)w.ws_o, (const float*)w.ws_ml, (const __nv_bfloat16*)w_uv,
                  (__nv_bfloat16*)out, s) != cudaSuccess)
     return GA_ERR_CUDA;
   return launch_status();

@@ -10,10 +10,10 @@
 // sequence at position lens[b] - 1, which sees every cached token.
 //
 // Kernels: mla_absorb_kernel (q_lat, then q = [q_lat | q_rope] in bf16; one CTA per (head, 64
-// latent rows) for every sequence, so each weight row is read once), mla_decode_kernel (split
-// over token chunks, two CTAs per SM; the heads are the 16 rows of mma.sync m16n8k16) and
-// mla_expand_kernel (the log-sum-exp re-association of the chunks, then o_lat w_uv, per head,
-// 64 output dims and 16 sequences).
+// latent rows) for every sequence, so each weight row is read once), mla_decode_kernel (two
+// CTAs per SM, each taking an equal contiguous share of all sequences' 32-token tiles; the heads
+// are the 16 rows of mma.sync m16n8k16) and mla_expand_kernel (the log-sum-exp re-association of
+// a sequence's partials, then o_lat w_uv, per head, 64 output dims and 4 sequences).
 #pragma once
 
 #include "common.cuh"
@@ -35,7 +35,8 @@ struct MlaCfg {
   static_assert(4 * 16 * SXROW * 4 <= 16 * QROW, "partial scores fit where the query tile was");
   static constexpr int OFF_X = OFF_P + 16 * PROW;       // [4][16] float exchange
   static constexpr int OFF_BAR = OFF_X + 4 * 16 * 4;
-  static constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;
+  static constexpr int BAR_BYTES = 128;
+  static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
   static constexpr int THREADS = 160;
   static_assert(2 * SMEM_BYTES <= 232448, "shared memory: two CTAs per SM");
   // absorb: latent rows per CTA, sequences staged at a time; expand: output dims and sequences
@@ -43,8 +44,11 @@ struct MlaCfg {
 };
 
 struct MlaShape {
-  int batch, n_heads, L_max, chunk_len, n_chunks;
+  int batch, n_heads, L_max;
+  int n_cta;            // CTAs of the decode launch, each taking an equal share of all tiles
+  int n_ids;            // partial slots per head: n_cta + batch - 1
   const int32_t* lens;
+  int2* seg;            // per sequence: its first partial slot and slot count (decode -> expansion)
   uint64_t timeout_ns;
 };
 
@@ -111,7 +115,15 @@ mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16*
 struct MlaBars {
   uint64_t full[2], empty[2];
   int abort_flag;
+  int b0, j0;                                        // this CTA's first sequence, its first tile there
+  long long wsum[MlaCfg::THREADS / 32];              // per-warp tile totals of the partition scan
 };
+static_assert(sizeof(MlaBars) <= MlaCfg::BAR_BYTES, "barrier block");
+
+// 32-token tiles of sequence b.
+__device__ __forceinline__ int mla_tiles(const MlaShape& s, int b) {
+  return (seq_keys(s.lens, b, s.L_max) + MlaCfg::TILE - 1) / MlaCfg::TILE;
+}
 
 // AND of `ok` over the 128 consumer threads (named barrier 1): every consumer warp takes the
 // same branch, so a wait that gave up in one warp can never leave another at a barrier.
@@ -123,9 +135,16 @@ __device__ __forceinline__ bool consumers_all(bool ok) {
   return res != 0;
 }
 
-// grid: (n_chunks, batch); block: 160 -- warps 0-3 compute, warp 4 loads 32-token tiles of the
-// latent cache [batch, L_max, 576] by TMA (9 boxes of 64 columns, 128-byte swizzle); two CTAs
-// per SM, so that one streams while the other starts or finishes.
+// grid: n_cta (two per SM); block: 160 -- warps 0-3 compute, warp 4 loads 32-token tiles of the
+// latent cache [batch, L_max, 576] by TMA (9 boxes of 64 columns, 128-byte swizzle).
+// Partition: the tiles of all sequences, in order, are cut into n_cta equal contiguous shares
+// (per = ceil(total / n_cta)); CTA c takes tiles c per .. c per + per - 1.  Every CTA streams
+// the same amount, so no SM is left with one CTA while others still hold two.  A share covers
+// the end of one sequence, maybe whole short ones, and the start of another: one segment per
+// (CTA, sequence) pair, each publishing its partial (o, m, l) to slot c + b.  Along the tile
+// order both c and b never decrease, so c + b is distinct for distinct segments and stays below
+// n_cta + batch - 1.  The CTA holding a sequence's first tile records the sequence's first slot
+// and slot count for the expansion.
 // Per tile: warp w scores its 8 tokens for the 16 query rows (the heads; rows >= n_heads are
 // zero), the warps agree on each row's tile maximum through shared memory, write their
 // probabilities into a shared 16 x 32 P tile, and each accumulates latent dims 128 w .. 128 w +
@@ -140,13 +159,22 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
   MlaBars* bars = reinterpret_cast<MlaBars*>(smem + C::OFF_BAR);
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x, b = blockIdx.y, H = s.n_heads;
-  const int L = seq_keys(s.lens, b, s.L_max);
-  const int kbeg = c * s.chunk_len, kend = min((c + 1) * s.chunk_len, L);
-  if (kbeg >= kend) return;                          // chunk holds no token (uniform)
-  const int n_tiles = (kend - kbeg + C::TILE - 1) / C::TILE;
+  const int c = blockIdx.x, H = s.n_heads;
   const uint64_t tmo = s.timeout_ns;
+  griddep_launch_dependents();                       // the expansion may start its set-up
 
+  // ---- this CTA's share: a block-wide scan of the sequences' tile counts ---------------------
+  const int per_t = (s.batch + C::THREADS - 1) / C::THREADS;
+  const int blo = min(s.batch, (int)threadIdx.x * per_t), bhi = min(s.batch, blo + per_t);
+  long long mine = 0;
+  for (int b = blo; b < bhi; ++b) mine += mla_tiles(s, b);
+  long long incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) bars->wsum[warp] = incl;
   if (threadIdx.x == 0) {
     for (int st = 0; st < C::STAGES; ++st) {
       mbar_init(&bars->full[st], 1);
@@ -156,234 +184,278 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  griddep_launch_dependents();                       // the expansion may start its set-up
-  if (warp < 4) {                                    // query tile, zero rows past the heads
-    griddep_wait();                                  // written by the absorption kernel
+  __syncthreads();
+  long long before = incl - mine, total = 0;
+#pragma unroll
+  for (int w = 0; w < C::THREADS / 32; ++w) {
+    const long long x = bars->wsum[w];
+    if (w < warp) before += x;
+    total += x;
+  }
+  const long long per = (total + s.n_cta - 1) / s.n_cta;
+  const long long start = (long long)c * per, end = min(start + per, total);
+  if (start < end && before <= start && start < before + mine) {
+    long long p = before;
+    int b = blo;
+    while (p + mla_tiles(s, b) <= start) p += mla_tiles(s, b++);   // the sequence holding tile `start`
+    bars->b0 = b;
+    bars->j0 = (int)(start - p);
+  }
+  __syncthreads();
+  if (start >= end) return;                          // no tile for this CTA (uniform)
+  const int b_first = bars->b0, j_first = bars->j0;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_lat);
+      int it = 0, issued = 0;
+      bool ok = true;
+      long long pos = start;
+      for (int b = b_first, j = j_first; ok && pos < end && b < s.batch; ++b, j = 0) {
+        const int take = (int)min((long long)(mla_tiles(s, b) - j), end - pos);
+        for (int u = 0; u < take; ++u, ++it) {
+          const int st = it % C::STAGES, use = it / C::STAGES;
+          if (it >= C::STAGES && !mbar_wait(&bars->empty[st], (use + 1) & 1, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          unsigned char* dst = smem + st * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&bars->full[st], C::STAGE_BYTES);
+          ++issued;
+          const int key0 = (j + u) * C::TILE;
+          for (int sl = 0; sl < C::SLABS; ++sl)
+            tma_load_3d(dst + sl * C::TILE * 128, &tm_lat, &bars->full[st], 64 * sl, key0, b);
+        }
+        pos += take;
+      }
+      for (int k = max(0, issued - C::STAGES); k < issued; ++k)
+        mbar_wait(&bars->full[k % C::STAGES], (k / C::STAGES) & 1, tmo, nullptr);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------------- consumer warps
+  griddep_wait();                                    // q_lat is written by the absorption kernel
+  const int r_lo = lane >> 2, r_hi = r_lo + 8;
+  const float scale_log2 = kLog2e / sqrtf((float)(C::DN + C::DR));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t qs = sbase + C::OFF_Q, ps = sbase + C::OFF_P;
+  float* xs = reinterpret_cast<float*>(smem + C::OFF_X);             // [4][16]
+  float* sx = reinterpret_cast<float*>(smem + C::OFF_Q);             // [4 warps][16][SXROW]
+  const int mi = lane >> 3, rr = lane & 7;
+  constexpr int KW = C::DK / 16 / 4;                 // 16-dim steps per warp
+  int it = 0;                                        // tiles of the ring consumed so far
+  bool dead = false;                                 // a wait gave up (uniform over the warps)
+  long long pos = start;
+  for (int b = b_first, j = j_first; pos < end && b < s.batch; ++b, j = 0) {
+    const int nt = mla_tiles(s, b);
+    const int take = (int)min((long long)(nt - j), end - pos);
+    if (take <= 0) continue;                         // an empty sequence inside the share
+    const int L = seq_keys(s.lens, b, s.L_max);
+    const int kbeg = j * C::TILE, kend = min((j + take) * C::TILE, L);
+    // query tile of sequence b, zero rows past the heads (the region is free: every warp has
+    // passed the previous segment's last barrier)
     for (int e = threadIdx.x; e < 16 * (C::DK / 8); e += 128) {
       const int r = e / (C::DK / 8), ch = e % (C::DK / 8);
       const uint4 v = r < H ? *reinterpret_cast<const uint4*>(q_abs + ((size_t)b * H + r) * C::DK + 8 * ch)
                             : make_uint4(0u, 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(smem + C::OFF_Q + r * C::QROW + ch * 16) = v;
     }
-  }
-  __syncthreads();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    // Scores split over the dimensions: warp w takes the 16-dim steps 9 w .. 9 w + 8 for all 32
+    // tokens of a tile, with its 9 query fragments held in registers for the whole segment (the
+    // query tile is read from shared memory once); the four partial tiles meet in shared memory
+    // (where the query tile was), each warp summing its own 8 tokens' columns.
+    uint32_t qa[KW][4];
+#pragma unroll
+    for (int i = 0; i < KW; ++i)
+      ldmatrix_x4(qs + (lane & 15) * C::QROW + ((KW * warp + i) * 16 + (lane >> 4) * 8) * 2, qa[i][0], qa[i][1],
+                  qa[i][2], qa[i][3]);
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // every warp has its fragments: the tile is free
+    float o[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.0f, 0.0f};
 
-  if (warp == 4) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_lat);
-      int issued = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int st = it % C::STAGES, use = it / C::STAGES;
-        if (it >= C::STAGES && !mbar_wait(&bars->empty[st], (use + 1) & 1, tmo, abort_flag)) break;
-        unsigned char* dst = smem + st * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&bars->full[st], C::STAGE_BYTES);
-        ++issued;
-        const int key0 = kbeg + it * C::TILE;
-        for (int sl = 0; sl < C::SLABS; ++sl)
-          tma_load_3d(dst + sl * C::TILE * 128, &tm_lat, &bars->full[st], 64 * sl, key0, b);
-      }
-      for (int k = max(0, issued - C::STAGES); k < issued; ++k)
-        mbar_wait(&bars->full[k % C::STAGES], (k / C::STAGES) & 1, tmo, nullptr);
-    }
-    __syncthreads();                                 // matches the consumers' one block barrier
-    return;
-  }
-
-  // ---------------------------------------------------------------------- consumer warps
-  const int r_lo = lane >> 2, r_hi = r_lo + 8;
-  const float scale_log2 = kLog2e / sqrtf((float)(C::DN + C::DR));
-  float o[16][4];
+    for (int u = 0; u < take; ++u, ++it) {
+      const int st = it % C::STAGES;
+      if (!dead) dead = !consumers_all(warp_wait(&bars->full[st], (it / C::STAGES) & 1, tmo, abort_flag));
+      if (dead) continue;
+      const uint32_t kb = sbase + st * C::STAGE_BYTES;
+      const int t0 = kbeg + u * C::TILE;               // first token of the tile
+      // ---- partial scores over this warp's 144 dims, all 32 tokens ----------------------------
+      {
+        float sacc[4][4];
 #pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.0f, 0.0f};
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t qs = sbase + C::OFF_Q, ps = sbase + C::OFF_P;
-  float* xs = reinterpret_cast<float*>(smem + C::OFF_X);             // [4][16]
-  float* sx = reinterpret_cast<float*>(smem + C::OFF_Q);             // [4 warps][16][SXROW]
-  const int mi = lane >> 3, rr = lane & 7;
-  // Scores split over the dimensions: warp w takes the 16-dim steps 9 w .. 9 w + 8 for all 32
-  // tokens of a tile, with its 9 query fragments held in registers for the whole chunk (the
-  // query tile is read from shared memory once); the four partial tiles meet in shared memory
-  // (where the query tile was), each warp summing its own 8 tokens' columns.
-  constexpr int KW = C::DK / 16 / 4;                 // 16-dim steps per warp
-  uint32_t qa[KW][4];
+        for (int nb = 0; nb < 4; ++nb) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.0f;
 #pragma unroll
-  for (int i = 0; i < KW; ++i)
-    ldmatrix_x4(qs + (lane & 15) * C::QROW + ((KW * warp + i) * 16 + (lane >> 4) * 8) * 2, qa[i][0], qa[i][1],
-                qa[i][2], qa[i][3]);
-  asm volatile("bar.sync 1, 128;" ::: "memory");     // every warp has its fragments: the tile is free
-
-  for (int it = 0; it < n_tiles; ++it) {
-    const int st = it % C::STAGES;
-    const bool got = warp_wait(&bars->full[st], (it / C::STAGES) & 1, tmo, abort_flag);
-    if (!consumers_all(got)) break;
-    const uint32_t kb = sbase + st * C::STAGE_BYTES;
-    const int t0 = kbeg + it * C::TILE;                // first token of the tile
-    // ---- partial scores over this warp's 144 dims, all 32 tokens ------------------------------
-    {
-      float sacc[4][4];
+        for (int nb = 0; nb < 4; ++nb) {
+          const int keyr = 8 * nb + rr;               // token row this lane addresses
 #pragma unroll
-      for (int nb = 0; nb < 4; ++nb) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.0f;
+          for (int i = 0; i < KW; i += 2) {
+            // one 4-matrix load: matrices 0, 1 the low and high 8 dims of step i, 2, 3 those of
+            // step i + 1 (the last, odd step loads its own dims twice)
+            const int kk = KW * warp + i + ((mi >> 1) && i + 1 < KW ? 1 : 0);
+            const int dchunk = 2 * kk + (mi & 1);
+            const uint32_t addr = kb + (dchunk >> 3) * (C::TILE * 128) + keyr * 128 + (((dchunk & 7) ^ (keyr & 7)) << 4);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(addr, b0, b1, b2, b3);
+            mma_bf16_16816(sacc[nb], qa[i], b0, b1);
+            if (i + 1 < KW) mma_bf16_16816(sacc[nb], qa[i + 1], b2, b3);
+          }
+        }
+        float* mine_sx = sx + warp * 16 * C::SXROW;
 #pragma unroll
-      for (int nb = 0; nb < 4; ++nb) {
-        const int keyr = 8 * nb + rr;                 // token row this lane addresses
-#pragma unroll
-        for (int i = 0; i < KW; i += 2) {
-          // one 4-matrix load: matrices 0, 1 the low and high 8 dims of step i, 2, 3 those of
-          // step i + 1 (the last, odd step loads its own dims twice)
-          const int kk = KW * warp + i + ((mi >> 1) && i + 1 < KW ? 1 : 0);
-          const int dchunk = 2 * kk + (mi & 1);
-          const uint32_t addr = kb + (dchunk >> 3) * (C::TILE * 128) + keyr * 128 + (((dchunk & 7) ^ (keyr & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(addr, b0, b1, b2, b3);
-          mma_bf16_16816(sacc[nb], qa[i], b0, b1);
-          if (i + 1 < KW) mma_bf16_16816(sacc[nb], qa[i + 1], b2, b3);
+        for (int nb = 0; nb < 4; ++nb) {
+          const int col = 8 * nb + 2 * (lane & 3);
+          *reinterpret_cast<float2*>(mine_sx + r_lo * C::SXROW + col) = make_float2(sacc[nb][0], sacc[nb][1]);
+          *reinterpret_cast<float2*>(mine_sx + r_hi * C::SXROW + col) = make_float2(sacc[nb][2], sacc[nb][3]);
         }
       }
-      float* mine = sx + warp * 16 * C::SXROW;
+      asm volatile("bar.sync 1, 128;" ::: "memory"); // the partial tiles are complete
+      float sc[4];
+      {
+        const int col = 8 * warp + 2 * (lane & 3);     // this warp's tokens
+        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int nb = 0; nb < 4; ++nb) {
-        const int col = 8 * nb + 2 * (lane & 3);
-        *reinterpret_cast<float2*>(mine + r_lo * C::SXROW + col) = make_float2(sacc[nb][0], sacc[nb][1]);
-        *reinterpret_cast<float2*>(mine + r_hi * C::SXROW + col) = make_float2(sacc[nb][2], sacc[nb][3]);
+        for (int w = 0; w < 4; ++w) {
+          const float2 x = *reinterpret_cast<const float2*>(sx + (w * 16 + r_lo) * C::SXROW + col);
+          const float2 y = *reinterpret_cast<const float2*>(sx + (w * 16 + r_hi) * C::SXROW + col);
+          lo.x += x.x; lo.y += x.y; hi.x += y.x; hi.y += y.y;
+        }
+        sc[0] = lo.x; sc[1] = lo.y; sc[2] = hi.x; sc[3] = hi.y;
       }
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");   // the partial tiles are complete
-    float sc[4];
-    {
-      const int col = 8 * warp + 2 * (lane & 3);       // this warp's tokens
-      float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+      float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float2 x = *reinterpret_cast<const float2*>(sx + (w * 16 + r_lo) * C::SXROW + col);
-        const float2 y = *reinterpret_cast<const float2*>(sx + (w * 16 + r_hi) * C::SXROW + col);
-        lo.x += x.x; lo.y += x.y; hi.x += y.x; hi.y += y.y;
+      for (int e = 0; e < 4; ++e) {
+        const int jj = t0 + 8 * warp + 2 * (lane & 3) + (e & 1);
+        sc[e] = jj < kend ? sc[e] * scale_log2 : -INFINITY;
+        mt[e >> 1] = fmaxf(mt[e >> 1], sc[e]);
       }
-      sc[0] = lo.x; sc[1] = lo.y; sc[2] = hi.x; sc[3] = hi.y;
-    }
-    float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = t0 + 8 * warp + 2 * (lane & 3) + (e & 1);
-      sc[e] = j < kend ? sc[e] * scale_log2 : -INFINITY;
-      mt[e >> 1] = fmaxf(mt[e >> 1], sc[e]);
+      for (int row = 0; row < 2; ++row) {
+        mt[row] = fmaxf(mt[row], __shfl_xor_sync(0xffffffffu, mt[row], 1));
+        mt[row] = fmaxf(mt[row], __shfl_xor_sync(0xffffffffu, mt[row], 2));
+      }
+      if ((lane & 3) == 0) {
+        xs[warp * 16 + r_lo] = mt[0];
+        xs[warp * 16 + r_hi] = mt[1];
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      float alpha[2], m_use[2];
+#pragma unroll
+      for (int row = 0; row < 2; ++row) {
+        const int r = row ? r_hi : r_lo;
+        const float tmax = fmaxf(fmaxf(xs[r], xs[16 + r]), fmaxf(xs[32 + r], xs[48 + r]));
+        const float m_new = fmaxf(m_run[row], tmax);
+        alpha[row] = m_new == -INFINITY ? 1.0f : ex2(m_run[row] - m_new);
+        m_run[row] = m_new;
+        m_use[row] = m_new == -INFINITY ? 0.0f : m_new;
+        l_part[row] *= alpha[row];
+      }
+      unsigned char* pb = smem + C::OFF_P;
+      {
+        float pr[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          pr[e] = ex2(sc[e] - m_use[e >> 1]);
+          l_part[e >> 1] += pr[e];
+        }
+        const int col = 8 * warp + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(pb + r_lo * C::PROW + col * 2) = pack_bf16x2(pr[0], pr[1]);
+        *reinterpret_cast<uint32_t*>(pb + r_hi * C::PROW + col * 2) = pack_bf16x2(pr[2], pr[3]);
+      }
+      if (alpha[0] != 1.0f || alpha[1] != 1.0f) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          o[n][0] *= alpha[0]; o[n][1] *= alpha[0];
+          o[n][2] *= alpha[1]; o[n][3] *= alpha[1];
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory"); // the P tile is complete
+      // ---- o += P c_kv over the tile's 32 tokens, latent dims 128 warp .. -----------------
+      const int lim = kend - t0;                      // first tile row past the end
+      const bool tail = lim < C::TILE;
+#pragma unroll
+      for (int kk = 0; kk < C::TILE / 16; ++kk) {
+        uint32_t pa[4];
+        ldmatrix_x4(ps + (lane & 15) * C::PROW + (kk * 16 + (lane >> 4) * 8) * 2, pa[0], pa[1], pa[2], pa[3]);
+        const int key = 16 * kk + ((mi & 1) << 3) + rr;
+        const int kb0 = 16 * kk + 2 * (lane & 3);
+#pragma unroll
+        for (int n = 0; n < 16; n += 2) {
+          const int dchunk = 16 * warp + n + (mi >> 1);
+          const uint32_t addr = kb + (dchunk >> 3) * (C::TILE * 128) + key * 128 + (((dchunk & 7) ^ (key & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+          if (tail) {                                 // latent rows past the end may hold anything
+            auto clip = [&](uint32_t x, int r0) -> uint32_t {
+              const uint32_t lo16 = (r0 < lim) ? (x & 0xFFFFu) : 0u;
+              const uint32_t hi16 = (r0 + 1 < lim) ? (x & 0xFFFF0000u) : 0u;
+              return lo16 | hi16;
+            };
+            b0 = clip(b0, kb0); b1 = clip(b1, kb0 + 8);
+            b2 = clip(b2, kb0); b3 = clip(b3, kb0 + 8);
+          }
+          mma_bf16_16816(o[n], pa, b0, b1);
+          mma_bf16_16816(o[n + 1], pa, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->empty[st]);
     }
+    // ---- row sums over the 4 warps' tokens, then this segment's partial -------------------
 #pragma unroll
     for (int row = 0; row < 2; ++row) {
-      mt[row] = fmaxf(mt[row], __shfl_xor_sync(0xffffffffu, mt[row], 1));
-      mt[row] = fmaxf(mt[row], __shfl_xor_sync(0xffffffffu, mt[row], 2));
+      l_part[row] += __shfl_xor_sync(0xffffffffu, l_part[row], 1);
+      l_part[row] += __shfl_xor_sync(0xffffffffu, l_part[row], 2);
     }
     if ((lane & 3) == 0) {
-      xs[warp * 16 + r_lo] = mt[0];
-      xs[warp * 16 + r_hi] = mt[1];
+      xs[warp * 16 + r_lo] = l_part[0];
+      xs[warp * 16 + r_hi] = l_part[1];
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    float alpha[2], m_use[2];
+    // a wait that ran out publishes an empty partial: max -inf and sum 0, which the
+    // re-association skips, never what an earlier call left in the workspace
+    float lsum[2];
 #pragma unroll
     for (int row = 0; row < 2; ++row) {
       const int r = row ? r_hi : r_lo;
-      const float tmax = fmaxf(fmaxf(xs[r], xs[16 + r]), fmaxf(xs[32 + r], xs[48 + r]));
-      const float m_new = fmaxf(m_run[row], tmax);
-      alpha[row] = m_new == -INFINITY ? 1.0f : ex2(m_run[row] - m_new);
-      m_run[row] = m_new;
-      m_use[row] = m_new == -INFINITY ? 0.0f : m_new;
-      l_part[row] *= alpha[row];
+      lsum[row] = dead ? 0.0f : (xs[r] + xs[16 + r]) + (xs[32 + r] + xs[48 + r]);
+      if (dead) m_run[row] = -INFINITY;
     }
-    unsigned char* pb = smem + C::OFF_P;
-    {
-      float p[4];
+    const int id = c + b;                            // this segment's partial slot
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        p[e] = ex2(sc[e] - m_use[e >> 1]);
-        l_part[e >> 1] += p[e];
-      }
-      const int col = 8 * warp + 2 * (lane & 3);
-      *reinterpret_cast<uint32_t*>(pb + r_lo * C::PROW + col * 2) = pack_bf16x2(p[0], p[1]);
-      *reinterpret_cast<uint32_t*>(pb + r_hi * C::PROW + col * 2) = pack_bf16x2(p[2], p[3]);
-    }
-    if (alpha[0] != 1.0f || alpha[1] != 1.0f) {
+    for (int row = 0; row < 2; ++row) {
+      const int h = row ? r_hi : r_lo;
+      if (h >= H) continue;
+      const size_t slot = (size_t)id * H + h;
 #pragma unroll
       for (int n = 0; n < 16; ++n) {
-        o[n][0] *= alpha[0]; o[n][1] *= alpha[0];
-        o[n][2] *= alpha[1]; o[n][3] *= alpha[1];
+        const int dim = 128 * warp + 8 * n + 2 * (lane & 3);
+        if (GA_BOUNDS(slot < (size_t)s.n_ids * H && dim + 2 <= C::R, 10, slot))
+          *reinterpret_cast<float2*>(ws_o + slot * C::R + dim) =
+              dead ? make_float2(0.0f, 0.0f) : make_float2(o[n][2 * row], o[n][2 * row + 1]);
+      }
+      if (warp == 0 && (lane & 3) == 0 && GA_BOUNDS(slot < (size_t)s.n_ids * H, 10, slot)) {
+        ws_ml[slot * 2 + 0] = m_run[row];
+        ws_ml[slot * 2 + 1] = lsum[row];
       }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");   // the P tile is complete
-    // ---- o += P c_kv over the tile's 32 tokens, latent dims 128 warp .. -------------------
-    const int lim = kend - t0;                        // first tile row past the end
-    const bool tail = lim < C::TILE;
-#pragma unroll
-    for (int kk = 0; kk < C::TILE / 16; ++kk) {
-      uint32_t pa[4];
-      ldmatrix_x4(ps + (lane & 15) * C::PROW + (kk * 16 + (lane >> 4) * 8) * 2, pa[0], pa[1], pa[2], pa[3]);
-      const int key = 16 * kk + ((mi & 1) << 3) + rr;
-      const int kb0 = 16 * kk + 2 * (lane & 3);
-#pragma unroll
-      for (int n = 0; n < 16; n += 2) {
-        const int dchunk = 16 * warp + n + (mi >> 1);
-        const uint32_t addr = kb + (dchunk >> 3) * (C::TILE * 128) + key * 128 + (((dchunk & 7) ^ (key & 7)) << 4);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-        if (tail) {                                   // latent rows past the end may hold anything
-          auto clip = [&](uint32_t x, int r0) -> uint32_t {
-            const uint32_t lo16 = (r0 < lim) ? (x & 0xFFFFu) : 0u;
-            const uint32_t hi16 = (r0 + 1 < lim) ? (x & 0xFFFF0000u) : 0u;
-            return lo16 | hi16;
-          };
-          b0 = clip(b0, kb0); b1 = clip(b1, kb0 + 8);
-          b2 = clip(b2, kb0); b3 = clip(b3, kb0 + 8);
-        }
-        mma_bf16_16816(o[n], pa, b0, b1);
-        mma_bf16_16816(o[n + 1], pa, b2, b3);
-      }
+    if (j == 0 && threadIdx.x == 0 && GA_BOUNDS(b < s.batch, 12, b)) {
+      // the sequence starts in this share: its slots are c + b .. c_last + b
+      const long long c_last = (pos + nt - 1) / per;
+      s.seg[b] = make_int2(id, (int)(c_last - c + 1));
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->empty[st]);
-  }
-  // ---- row sums over the 4 warps' tokens, then this chunk's result ----------------------
-#pragma unroll
-  for (int row = 0; row < 2; ++row) {
-    l_part[row] += __shfl_xor_sync(0xffffffffu, l_part[row], 1);
-    l_part[row] += __shfl_xor_sync(0xffffffffu, l_part[row], 2);
-  }
-  if ((lane & 3) == 0) {
-    xs[warp * 16 + r_lo] = l_part[0];
-    xs[warp * 16 + r_hi] = l_part[1];
-  }
-  __syncthreads();
-  // a wait that ran out (the status word says so) publishes an empty partial: max -inf and sum
-  // 0, which the re-association skips, never what an earlier call left in the workspace
-  const bool aborted = *abort_flag != 0;
-  float lsum[2];
-#pragma unroll
-  for (int row = 0; row < 2; ++row) {
-    const int r = row ? r_hi : r_lo;
-    lsum[row] = aborted ? 0.0f : (xs[r] + xs[16 + r]) + (xs[32 + r] + xs[48 + r]);
-    if (aborted) m_run[row] = -INFINITY;
-  }
-#pragma unroll
-  for (int row = 0; row < 2; ++row) {
-    const int h = row ? r_hi : r_lo;
-    if (h >= H) continue;
-    const size_t slot = ((size_t)b * H + h) * s.n_chunks + c;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int dim = 128 * warp + 8 * n + 2 * (lane & 3);
-      if (GA_BOUNDS(slot < (size_t)s.batch * H * s.n_chunks && dim + 2 <= C::R, 10, slot))
-        *reinterpret_cast<float2*>(ws_o + slot * C::R + dim) = make_float2(o[n][2 * row], o[n][2 * row + 1]);
-    }
-    if (warp == 0 && (lane & 3) == 0) {
-      ws_ml[slot * 2 + 0] = m_run[row];
-      ws_ml[slot * 2 + 1] = lsum[row];
-    }
+    pos += take;
   }
 }
 
 // grid: (DV / 64, n_heads, ceil(batch / 4)); block: 256.  For 4 sequences of head h: warps w and
-// w + 4 re-associate the chunk partials of sequence w into half of its latent output each (o_lat =
-// sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the chunks holding tokens; the lanes over the
-// latent dims, four chunks' loads in flight), then out = o_lat w_uv[h] for output dims 64 x ..
+// w + 4 re-associate the partials of sequence w into half of its latent output each (o_lat =
+// sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the decode's segments of the sequence; the
+// lanes over the latent dims, four partials' loads in flight), then out = o_lat w_uv[h] for output dims 64 x ..
 // 64 x + 63: thread t takes dim t % 64 over latent dims 128 (t / 64) .. + 127 for the 4
 // sequences (fp32 sums, every weight element read once for all 4), and the four partial sums of
 // each output meet in shared memory.
@@ -412,20 +484,22 @@ mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_m
     if (i < nb) {
       const int b = b0 + i;
       const int L = seq_keys(s.lens, b, s.L_max);
-      const size_t qrow = (size_t)b * s.n_heads + h;
-      const int n_used = min(s.n_chunks, (L + s.chunk_len - 1) / s.chunk_len);
-      const float* ml = ws_ml + qrow * s.n_chunks * 2;
+      // an empty sequence has no partial (and no record): zero row
+      const int2 rec = L > 0 ? s.seg[b] : make_int2(0, 0);
+      const int n_used = rec.x >= 0 && rec.y > 0 && rec.x + rec.y <= s.n_ids ? rec.y : 0;
+      const float* ml = ws_ml + ((size_t)rec.x * s.n_heads + h) * 2;
       float M = -INFINITY;
-      for (int c = lane; c < n_used; c += 32) M = fmaxf(M, ml[2 * c]);
+      for (int c = lane; c < n_used; c += 32) M = fmaxf(M, ml[(size_t)c * s.n_heads * 2]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
       float Lsum = 0.0f;
       if (M != -INFINITY) {
-        // the chunks' loads do not depend on their factors: four chunks in flight
+        // the partials' loads do not depend on their factors: four in flight
 #pragma unroll 4
         for (int c = 0; c < n_used; ++c) {
-          const float2 mlc = *reinterpret_cast<const float2*>(ml + 2 * c);
-          const float* src = ws_o + (qrow * s.n_chunks + c) * C::R + C::R / 2 * half + lane;
+          const size_t slot = ((size_t)rec.x + c) * s.n_heads + h;
+          const float2 mlc = *reinterpret_cast<const float2*>(ws_ml + slot * 2);
+          const float* src = ws_o + slot * C::R + C::R / 2 * half + lane;
           float v[U];
 #pragma unroll
           for (int u = 0; u < U; ++u) v[u] = src[32 * u];

@@ -1,7 +1,7 @@
 """GPU parity of MLA decode in the absorbed form ("Attention in Code", section 4) against the
 float64 oracle: DeepSeek-V2-Lite's sizes (latent 512, rope 64, head dims 128), ragged cache
-lengths, several token chunks, poisoned cache rows past each length, and the bench's full-size
-workload on sampled sequences."""
+lengths split over the decode CTAs' shares (an empty one among them), poisoned cache rows past
+each length, and the bench's full-size workload on sampled sequences."""
 import numpy as np
 import pytest
 import torch
@@ -33,9 +33,15 @@ def _oracle(qnr, qpr, latr, wuk, wuv, b, n):
     return mla_absorbed(qnr[b][:, None], qpr[b][:, None], latr[b, :n, :512], latr[b, :n, 512:], wuk, wuv)[:, 0]
 
 
+_SHORT = [int(x) for x in np.random.default_rng(704).integers(0, 201, size=200)]
+
+
 @pytest.mark.parametrize("B,H,L_max,lens,poison", [
     (3, 16, 700, [700, 333, 1], False),
-    (2, 8, 3000, [3000, 1717], True),        # several chunks; rows past each length hold NaN
+    (2, 8, 3000, [3000, 1717], True),        # a sequence over many CTAs; rows past each length hold NaN
+    # shares that end inside one sequence, hold short ones whole, and skip an empty one
+    (8, 16, 8192, [8192, 32, 5, 0, 64, 8192, 1, 700], True),
+    (200, 4, 200, _SHORT, True),             # several short sequences in each CTA's share
 ])
 def test_mla_decode_matches_oracle(B, H, L_max, lens, poison):
     qn, qnr, qp, qpr, lat, latr = _inputs(B, H, L_max, seed=701 + H)
@@ -47,6 +53,9 @@ def test_mla_decode_matches_oracle(B, H, L_max, lens, poison):
     assert ga.ga_read_device_status() == ga.GA_OK
     got = to_f64(out)
     for b, n in enumerate(lens):
+        if n == 0:                           # an empty cache gives a zero row
+            assert np.all(got[b] == 0.0), f"mla b={b} empty"
+            continue
         assert_close(got[b], _oracle(qnr, qpr, latr, wuk, wuv, b, n), "bf16", f"mla b={b} n={n}")
 
 
