@@ -221,6 +221,7 @@ const DeviceKernels* device_kernels() {
                             set_smem(decode_splitk_kernel<64, true>, DecodeCfg<64>::GATHER_SMEM_BYTES)});
     d.select = first_error({set_smem(select_rescue_kernel, 16384 * 8), set_smem(select_score_kernel, kScSmem)});
     d.mla = set_smem(mla_decode_kernel, MlaCfg::SMEM_BYTES);
+    if (d.mla == GA_OK) d.mla = set_smem(mla_expand_kernel, MlaCfg::EX_SMEM);
     d.topk = set_smem(topk_select_kernel<true>, kTopkFixedSmem + kTopkStageMax * 4);
     d.topk_unstaged = set_smem(topk_select_kernel<false>, kTopkFixedSmem);
     int n_sm = 0;
@@ -733,7 +734,7 @@ int ga_mla_decode(const void* q_nope, const void* q_rope, const void* latent, co
                  (const __nv_bfloat16*)w.q_abs, w.ws_o, w.ws_ml, s) != cudaSuccess)
     return GA_ERR_CUDA;
   if (launch_pdl(mla_expand_kernel, dim3(C::DV / C::EX_DIMS, n_heads, (batch + C::EX_SEQ - 1) / C::EX_SEQ), dim3(256),
-                 0, stream, (const float*)w.ws_o, (const float*)w.ws_ml, (const __nv_bfloat16*)w_uv,
+                 C::EX_SMEM, stream, (const float*)w.ws_o, (const float*)w.ws_ml, (const __nv_bfloat16*)w_uv,
                  (__nv_bfloat16*)out, s) != cudaSuccess)
     return GA_ERR_CUDA;
   return launch_status();

@@ -13,7 +13,7 @@
 // latent rows) for every sequence, so each weight row is read once), mla_decode_kernel (two
 // CTAs per SM, each taking an equal contiguous share of all sequences' 32-token tiles; the heads
 // are the 16 rows of mma.sync m16n8k16) and mla_expand_kernel (the log-sum-exp re-association of
-// a sequence's partials, then o_lat w_uv, per head, 64 output dims and 4 sequences).
+// a sequence's partials, then o_lat w_uv, per head, 64 output dims and 8 sequences).
 #pragma once
 
 #include "common.cuh"
@@ -40,7 +40,10 @@ struct MlaCfg {
   static constexpr int THREADS = 160;
   static_assert(2 * SMEM_BYTES <= 232448, "shared memory: two CTAs per SM");
   // absorb: latent rows per CTA, sequences staged at a time; expand: output dims and sequences
-  static constexpr int AB_ROWS = 64, AB_SEQ = 16, EX_DIMS = 64, EX_SEQ = 4;
+  static constexpr int AB_ROWS = 64, AB_SEQ = 16, EX_DIMS = 64, EX_SEQ = 8;
+  static constexpr int EX_SMEM = R * EX_DIMS * 2 + EX_SEQ * R * 4;   // weight slice, latent tile
+  static_assert((256 / EX_DIMS) * EX_SEQ * EX_DIMS * 4 <= EX_SEQ * R * 4, "partial sums fit in the latent tile");
+  static_assert(EX_SEQ % 8 == 0 && 256 % EX_DIMS == 0, "whole sequences per warp, whole latent parts");
 };
 
 struct MlaShape {
@@ -80,6 +83,14 @@ mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16*
         bb < nb ? *reinterpret_cast<const uint4*>(q_nope + ((size_t)(b0 + bb) * n_heads + h) * C::DN + 8 * c)
                 : make_uint4(0u, 0u, 0u, 0u);
   }
+  if (rb == 0)                                          // the rope part of the sequences' queries
+    for (int e = t; e < nb * (C::DR / 8); e += 128) {  // 16-byte pieces, 8 per row
+      const size_t row = (size_t)(b0 + e / (C::DR / 8)) * n_heads + h;
+      const int c = e % (C::DR / 8);
+      if (GA_BOUNDS(row < (size_t)batch * n_heads, 9, row))
+        *reinterpret_cast<uint4*>(q_abs + row * C::DK + C::R + 8 * c) =
+            *reinterpret_cast<const uint4*>(q_rope + row * C::DR + 8 * c);
+    }
   __syncthreads();
   const uint32_t qs = smem_u32(q_s), ws = smem_u32(w_s);
   const int mi = lane >> 3, rr = lane & 7;
@@ -98,18 +109,13 @@ mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16*
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
     const int r = rb * C::AB_ROWS + 16 * warp + 8 * n + 2 * (lane & 3);   // latent rows r, r + 1
-    const size_t lim = (size_t)batch * n_heads * C::DK;
+    [[maybe_unused]] const size_t lim = (size_t)batch * n_heads * C::DK;
     const size_t o_lo = ((size_t)(b0 + s_lo) * n_heads + h) * C::DK + r, o_hi = ((size_t)(b0 + s_hi) * n_heads + h) * C::DK + r;
     if (s_lo < nb && GA_BOUNDS(o_lo + 2 <= lim && r + 2 <= C::R, 9, o_lo))
       *reinterpret_cast<uint32_t*>(q_abs + o_lo) = pack_bf16x2(acc[n][0], acc[n][1]);
     if (s_hi < nb && GA_BOUNDS(o_hi + 2 <= lim && r + 2 <= C::R, 9, o_hi))
       *reinterpret_cast<uint32_t*>(q_abs + o_hi) = pack_bf16x2(acc[n][2], acc[n][3]);
   }
-  if (rb == 0)                                          // the rope part of the sequences' queries
-    for (int e = t; e < nb * C::DR; e += 128) {
-      const size_t row = (size_t)(b0 + e / C::DR) * n_heads + h;
-      q_abs[row * C::DK + C::R + e % C::DR] = q_rope[row * C::DR + e % C::DR];
-    }
 }
 
 struct MlaBars {
@@ -452,87 +458,117 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
   }
 }
 
-// grid: (DV / 64, n_heads, ceil(batch / 4)); block: 256.  For 4 sequences of head h: warps w and
-// w + 4 re-associate the partials of sequence w into half of its latent output each (o_lat =
-// sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the decode's segments of the sequence; the
-// lanes over the latent dims, four partials' loads in flight), then out = o_lat w_uv[h] for output dims 64 x ..
-// 64 x + 63: thread t takes dim t % 64 over latent dims 128 (t / 64) .. + 127 for the 4
-// sequences (fp32 sums, every weight element read once for all 4), and the four partial sums of
-// each output meet in shared memory.
+// grid: (DV / 64, n_heads, ceil(batch / 8)); block: 256; dynamic shared memory EX_SMEM (80 KB).
+// Head h, output dims 64 x .. 64 x + 63, 8 sequences:
+//  1. the weight slice w_uv[h][:, 64 x ..] (512 x 64 bf16, 64 KB) is copied into shared memory
+//     with 16-byte asynchronous copies before the wait on the decode (it does not depend on it);
+//  2. warp w re-associates the partials of sequence w (o_lat = sum_c 2^(m_c - M) o_c / sum_c
+//     2^(m_c - M) l_c over the decode's segments of the sequence; lane l holds latent dims 4 l ..
+//     4 l + 3 of every 128) into a shared [8][512] fp32 tile;
+//  3. out = o_lat w_uv[h]: thread t takes output dim t % 64 over latent rows 128 (t / 64) .. + 127
+//     for the 8 sequences (fp32 sums), and the 4 partial sums of each output meet in shared
+//     memory.
 __global__ void __launch_bounds__(256)
 mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
                   const __nv_bfloat16* __restrict__ w_uv, __nv_bfloat16* __restrict__ out, MlaShape s) {
   using C = MlaCfg;
-  __shared__ float lat[C::EX_SEQ][C::R];
-  __shared__ float part[4][C::EX_SEQ][C::EX_DIMS];
+  extern __shared__ __align__(16) unsigned char ex_smem[];
+  __nv_bfloat16* wsm = reinterpret_cast<__nv_bfloat16*>(ex_smem);            // [R][EX_DIMS]
+  float* lat = reinterpret_cast<float*>(ex_smem + C::R * C::EX_DIMS * 2);      // [EX_SEQ][R]
+  float* part = lat;                          // [8][EX_SEQ][EX_DIMS], once the products are done
   const int xb = blockIdx.x, h = blockIdx.y, b0 = blockIdx.z * C::EX_SEQ;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int nb = min(C::EX_SEQ, s.batch - b0);
   {
-    // this CTA's weight columns into L2 while the decode finishes, then its partials
-    const __nv_bfloat16* wcol = w_uv + (size_t)h * C::R * C::DV + xb * C::EX_DIMS;
-    for (int r = threadIdx.x; r < C::R; r += 256) prefetch_l2(wcol + (size_t)r * C::DV);
-    griddep_wait();
+    constexpr int PR = C::EX_DIMS / 8;                                       // 16-byte pieces per row
+    const __nv_bfloat16* wsrc = w_uv + (size_t)h * C::R * C::DV + xb * C::EX_DIMS;
+    const uint32_t wdst = smem_u32(wsm);
+    for (int e = t; e < C::R * PR; e += 256) {
+      const int r = e / PR, pc = e % PR;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                   :: "r"(wdst + (uint32_t)(r * C::EX_DIMS + 8 * pc) * 2), "l"(wsrc + (size_t)r * C::DV + 8 * pc)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  {
-    // warp w: sequence w % 4, latent dims 256 (w / 4) .. + 255 (lane + 32 u)
-    const int i = warp % C::EX_SEQ, half = warp / C::EX_SEQ;
-    constexpr int U = C::R / 2 / 32;
-    float o[U];
+  griddep_wait();                                    // the partials of the decode kernel
+  constexpr int SPW = C::EX_SEQ / 8;                 // sequences per warp
+  int rx[SPW], nu[SPW];
+  float M[SPW];
 #pragma unroll
-    for (int u = 0; u < U; ++u) o[u] = 0.0f;
-    if (i < nb) {
-      const int b = b0 + i;
-      const int L = seq_keys(s.lens, b, s.L_max);
-      // an empty sequence has no partial (and no record): zero row
-      const int2 rec = L > 0 ? s.seg[b] : make_int2(0, 0);
-      const int n_used = rec.x >= 0 && rec.y > 0 && rec.x + rec.y <= s.n_ids ? rec.y : 0;
-      const float* ml = ws_ml + ((size_t)rec.x * s.n_heads + h) * 2;
-      float M = -INFINITY;
-      for (int c = lane; c < n_used; c += 32) M = fmaxf(M, ml[(size_t)c * s.n_heads * 2]);
+  for (int k = 0; k < SPW; ++k) {
+    const int i = SPW * warp + k, b = b0 + i;
+    // an empty sequence has no partial (and no record): zero row
+    const int2 rec = i < nb && seq_keys(s.lens, b, s.L_max) > 0 ? s.seg[b] : make_int2(0, 0);
+    rx[k] = rec.x;
+    nu[k] = rec.x >= 0 && rec.y > 0 && rec.x + rec.y <= s.n_ids ? rec.y : 0;
+    M[k] = -INFINITY;
+    for (int c = lane; c < nu[k]; c += 32) M[k] = fmaxf(M[k], ws_ml[(((size_t)rx[k] + c) * s.n_heads + h) * 2]);
+  }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      float Lsum = 0.0f;
-      if (M != -INFINITY) {
-        // the partials' loads do not depend on their factors: four in flight
-#pragma unroll 4
-        for (int c = 0; c < n_used; ++c) {
-          const size_t slot = ((size_t)rec.x + c) * s.n_heads + h;
-          const float2 mlc = *reinterpret_cast<const float2*>(ws_ml + slot * 2);
-          const float* src = ws_o + slot * C::R + C::R / 2 * half + lane;
-          float v[U];
+  for (int k = 0; k < SPW; ++k) {
 #pragma unroll
-          for (int u = 0; u < U; ++u) v[u] = src[32 * u];
-          const float f = mlc.x == -INFINITY ? 0.0f : ex2(mlc.x - M);
-          Lsum = fmaf(f, mlc.y, Lsum);
+    for (int off = 16; off > 0; off >>= 1) M[k] = fmaxf(M[k], __shfl_xor_sync(0xffffffffu, M[k], off));
+    float4 o[C::R / 128];
 #pragma unroll
-          for (int u = 0; u < U; ++u) o[u] = fmaf(f, v[u], o[u]);
+    for (int u = 0; u < C::R / 128; ++u) o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Lsum = 0.0f;
+    if (M[k] != -INFINITY) {
+      // the partials' loads do not depend on their factors: two in flight
+#pragma unroll 2
+      for (int c = 0; c < nu[k]; ++c) {
+        const size_t slot = ((size_t)rx[k] + c) * s.n_heads + h;
+        const float2 mlc = *reinterpret_cast<const float2*>(ws_ml + slot * 2);
+        const float* src = ws_o + slot * C::R + 4 * lane;
+        float4 v[C::R / 128];
+#pragma unroll
+        for (int u = 0; u < C::R / 128; ++u) v[u] = *reinterpret_cast<const float4*>(src + 128 * u);
+        const float f = mlc.x == -INFINITY ? 0.0f : ex2(mlc.x - M[k]);
+        Lsum = fmaf(f, mlc.y, Lsum);
+#pragma unroll
+        for (int u = 0; u < C::R / 128; ++u) {
+          o[u].x = fmaf(f, v[u].x, o[u].x); o[u].y = fmaf(f, v[u].y, o[u].y);
+          o[u].z = fmaf(f, v[u].z, o[u].z); o[u].w = fmaf(f, v[u].w, o[u].w);
         }
       }
-      const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-#pragma unroll
-      for (int u = 0; u < U; ++u) o[u] *= inv;
     }
+    const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
 #pragma unroll
-    for (int u = 0; u < U; ++u) lat[i][C::R / 2 * half + lane + 32 * u] = o[u];
+    for (int u = 0; u < C::R / 128; ++u)
+      *reinterpret_cast<float4*>(lat + (SPW * warp + k) * C::R + 128 * u + 4 * lane) =
+          make_float4(o[u].x * inv, o[u].y * inv, o[u].z * inv, o[u].w * inv);
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  const int e = threadIdx.x % C::EX_DIMS, cp = threadIdx.x / C::EX_DIMS;   // output dim, latent quarter
-  const __nv_bfloat16* w = w_uv + ((size_t)h * C::R + (size_t)cp * (C::R / 4)) * C::DV + xb * C::EX_DIMS + e;
-  float a[C::EX_SEQ] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 16
-  for (int c = 0; c < C::R / 4; ++c) {
-    const float wc = __bfloat162float(w[(size_t)c * C::DV]);
+  constexpr int KP = 256 / C::EX_DIMS, KR = C::R / KP;   // latent parts, rows per part
+  const int e = t % C::EX_DIMS, k8 = t / C::EX_DIMS;  // output dim, latent rows KR k8 .. + KR - 1
+  float a[C::EX_SEQ];
 #pragma unroll
-    for (int i = 0; i < C::EX_SEQ; ++i) a[i] = fmaf(lat[i][cp * (C::R / 4) + c], wc, a[i]);
+  for (int i = 0; i < C::EX_SEQ; ++i) a[i] = 0.0f;
+#pragma unroll 2
+  for (int c = KR * k8; c < KR * k8 + KR; c += 4) {
+    float wc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) wc[q] = __bfloat162float(wsm[(c + q) * C::EX_DIMS + e]);
+#pragma unroll
+    for (int i = 0; i < C::EX_SEQ; ++i) {
+      const float4 x = *reinterpret_cast<const float4*>(lat + i * C::R + c);   // same address in the warp
+      a[i] = fmaf(x.x, wc[0], a[i]);
+      a[i] = fmaf(x.y, wc[1], a[i]);
+      a[i] = fmaf(x.z, wc[2], a[i]);
+      a[i] = fmaf(x.w, wc[3], a[i]);
+    }
   }
+  __syncthreads();                                   // every read of the latent tile is done
 #pragma unroll
-  for (int i = 0; i < C::EX_SEQ; ++i) part[cp][i][e] = a[i];
+  for (int i = 0; i < C::EX_SEQ; ++i) part[(k8 * C::EX_SEQ + i) * C::EX_DIMS + e] = a[i];
   __syncthreads();
-  if (threadIdx.x < C::EX_SEQ * C::EX_DIMS) {
-    const int i = threadIdx.x / C::EX_DIMS, d = threadIdx.x % C::EX_DIMS;
+  for (int q = t; q < C::EX_SEQ * C::EX_DIMS; q += 256) {
+    const int i = q / C::EX_DIMS, d = q % C::EX_DIMS;
     if (i < nb) {
-      const float y = (part[0][i][d] + part[1][i][d]) + (part[2][i][d] + part[3][i][d]);
+      float y = 0.0f;
+#pragma unroll
+      for (int k = 0; k < KP; ++k) y += part[(k * C::EX_SEQ + i) * C::EX_DIMS + d];
       const size_t off = ((size_t)(b0 + i) * s.n_heads + h) * C::DV + xb * C::EX_DIMS + d;
       if (GA_BOUNDS(off < (size_t)s.batch * s.n_heads * C::DV, 11, off)) out[off] = __float2bfloat16_rn(y);
     }

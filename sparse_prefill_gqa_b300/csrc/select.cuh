@@ -241,21 +241,10 @@ __device__ void rescue_zscore(const float* __restrict__ radius, SelectShape s, i
 __global__ void __launch_bounds__(kRescueThreads)
 select_rescue_kernel(const float* __restrict__ radius, SelectShape s) {
   extern __shared__ double sortbuf[];                // rule 1: sort_len doubles
-  __shared__ double red[kRescueThreads / 32];
   const int kvh = blockIdx.x, b = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const float* rrow = radius + ((size_t)b * s.n_kv + kvh) * s.nKb_out;
   uint8_t* out = s.rescue + ((size_t)b * s.n_kv + kvh) * s.nKb;
-  auto block_sum = [&](double x) -> double {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = x;
-    __syncthreads();
-    double tot = 0.0;
-    for (int w = 0; w < kRescueThreads / 32; ++w) tot += red[w];
-    return tot;
-  };
   if (s.radius_rule == 0) {
     rescue_zscore(radius, s, kvh, b);
   } else {
@@ -484,7 +473,7 @@ select_score_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_cons
       float* dst = s.scores + (row0 + a0) * stride + beta0;
       for (int e = et; e < n_rows * (kScB / 4); e += 128) {
         const int r = e / (kScB / 4), q4 = e % (kScB / 4);
-        const size_t off = (row0 + a0 + r) * stride + beta0 + 4 * q4;
+        [[maybe_unused]] const size_t off = (row0 + a0 + r) * stride + beta0 + 4 * q4;
         if (GA_BOUNDS(off + 4 <= (size_t)s.batch * s.n_hp * s.nQb * stride, 7, off))
           *reinterpret_cast<float4*>(dst + (size_t)r * stride + 4 * q4) = *reinterpret_cast<const float4*>(ss + r * kScSS + 4 * q4);
       }
@@ -598,7 +587,7 @@ select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ blo
       kept += __popc(bytes);
       for (int o = 0; o < n_out; ++o) {
         uint8_t* mrow = mrow0 + o * mhead;
-        const size_t moff = (size_t)(mrow - block_mask) + beta0;
+        [[maybe_unused]] const size_t moff = (size_t)(mrow - block_mask) + beta0;
         if (!GA_BOUNDS(moff < (size_t)s.batch * s.n_heads * s.nQb * s.nKb_out, 8, moff)) continue;
         if (vec4) {
           *reinterpret_cast<uint32_t*>(mrow + beta0) = bytes;
