@@ -25,25 +25,31 @@ struct MlaCfg {
   static constexpr int DK = R + DR;                     // 576 numbers per cached token
   static constexpr int SLABS = DK / 64;                 // 9 SW128 boxes of 64 columns
   static constexpr int TILE = 32;                       // tokens per stage (8 per compute warp)
+  // The partition weighs each sequence as its tiles + SEQ_COST: starting a sequence inside a
+  // share (publishing the previous partial, the next query tile, restarting the pipeline)
+  // measured about as long as two tiles.
+  static constexpr int SEQ_COST = 2;
   static constexpr int STAGES = 2;
   static constexpr int STAGE_BYTES = TILE * DK * 2;     // 36864
   static constexpr int QROW = DK * 2 + 16;              // padded row of the query tile (bytes)
   static constexpr int PROW = TILE * 2 + 16;            // padded row of the P tile (bytes)
-  static constexpr int OFF_Q = STAGES * STAGE_BYTES;    // the query tile, then the score partials
+  static constexpr int OFF_SX = STAGES * STAGE_BYTES;   // [4 warps][16][SXROW] partial scores
   static constexpr int SXROW = 40;                      // floats per head row of a partial-score tile
-  static constexpr int OFF_P = OFF_Q + 16 * QROW;
-  static_assert(4 * 16 * SXROW * 4 <= 16 * QROW, "partial scores fit where the query tile was");
+  static constexpr int OFF_P = OFF_SX + 4 * 16 * SXROW * 4;
   static constexpr int OFF_X = OFF_P + 16 * PROW;       // [4][16] float exchange
   static constexpr int OFF_BAR = OFF_X + 4 * 16 * 4;
   static constexpr int BAR_BYTES = 128;
-  static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
+  static constexpr int OFF_Q = OFF_BAR + BAR_BYTES;     // the next segment's query tile
+  static constexpr int SMEM_BYTES = OFF_Q + 16 * QROW + 1024;
   static constexpr int THREADS = 160;
   static_assert(2 * SMEM_BYTES <= 232448, "shared memory: two CTAs per SM");
   // absorb: latent rows per CTA, sequences staged at a time; expand: output dims and sequences
   static constexpr int AB_ROWS = 64, AB_SEQ = 16, EX_DIMS = 64, EX_SEQ = 8;
-  static constexpr int EX_SMEM = R * EX_DIMS * 2 + EX_SEQ * R * 4;   // weight slice, latent tile
-  static_assert((256 / EX_DIMS) * EX_SEQ * EX_DIMS * 4 <= EX_SEQ * R * 4, "partial sums fit in the latent tile");
-  static_assert(EX_SEQ % 8 == 0 && 256 % EX_DIMS == 0, "whole sequences per warp, whole latent parts");
+  static constexpr int EX_WROW = EX_DIMS * 2 + 16;     // padded weight row (bytes): conflict-free matrix loads
+  static constexpr int EX_LROW = R + 8;                 // padded latent row (floats)
+  static constexpr int EX_SMEM = R * EX_WROW + EX_SEQ * EX_LROW * 4;   // weight slice, latent tile
+  static_assert(8 * EX_SEQ * EX_DIMS * 4 <= EX_SEQ * EX_LROW * 4, "partial sums fit in the latent tile");
+  static_assert(EX_SEQ == 8 && EX_DIMS % 16 == 0, "one sequence per warp, pairs of 8-dim output tiles");
 };
 
 struct MlaShape {
@@ -121,7 +127,8 @@ mla_absorb_kernel(const __nv_bfloat16* __restrict__ q_nope, const __nv_bfloat16*
 struct MlaBars {
   uint64_t full[2], empty[2];
   int abort_flag;
-  int b0, j0;                                        // this CTA's first sequence, its first tile there
+  int b0;                                            // this CTA's first sequence
+  long long p0;                                      // its first position in the weighted order
   long long wsum[MlaCfg::THREADS / 32];              // per-warp tile totals of the partition scan
 };
 static_assert(sizeof(MlaBars) <= MlaCfg::BAR_BYTES, "barrier block");
@@ -129,6 +136,11 @@ static_assert(sizeof(MlaBars) <= MlaCfg::BAR_BYTES, "barrier block");
 // 32-token tiles of sequence b.
 __device__ __forceinline__ int mla_tiles(const MlaShape& s, int b) {
   return (seq_keys(s.lens, b, s.L_max) + MlaCfg::TILE - 1) / MlaCfg::TILE;
+}
+
+// Cached tokens of sequence b, 0 past the batch.
+__device__ __forceinline__ int mla_keys(const MlaShape& s, int b) {
+  return b < s.batch ? seq_keys(s.lens, b, s.L_max) : 0;
 }
 
 // AND of `ok` over the 128 consumer threads (named barrier 1): every consumer warp takes the
@@ -143,14 +155,15 @@ __device__ __forceinline__ bool consumers_all(bool ok) {
 
 // grid: n_cta (two per SM); block: 160 -- warps 0-3 compute, warp 4 loads 32-token tiles of the
 // latent cache [batch, L_max, 576] by TMA (9 boxes of 64 columns, 128-byte swizzle).
-// Partition: the tiles of all sequences, in order, are cut into n_cta equal contiguous shares
-// (per = ceil(total / n_cta)); CTA c takes tiles c per .. c per + per - 1.  Every CTA streams
-// the same amount, so no SM is left with one CTA while others still hold two.  A share covers
-// the end of one sequence, maybe whole short ones, and the start of another: one segment per
-// (CTA, sequence) pair, each publishing its partial (o, m, l) to slot c + b.  Along the tile
-// order both c and b never decrease, so c + b is distinct for distinct segments and stays below
-// n_cta + batch - 1.  The CTA holding a sequence's first tile records the sequence's first slot
-// and slot count for the expansion.
+// Partition: the sequences, in order, occupy consecutive positions, SEQ_COST for starting the
+// sequence and then one per tile (an empty sequence none); the positions are cut into n_cta
+// equal contiguous shares (per = ceil(total / n_cta)), and CTA c takes the tiles at positions
+// c per .. c per + per - 1.  Every CTA has the same amount of work, so no SM is left with one
+// CTA while others still hold two.  A share covers the end of one sequence, maybe whole short
+// ones, and the start of another: one segment per (CTA, sequence) pair holding tiles, each
+// publishing its partial (o, m, l) to slot c + b.  Along the order both c and b never decrease,
+// so c + b is distinct for distinct segments and stays below n_cta + batch - 1.  The CTA holding
+// a sequence's first tile records the sequence's first slot and slot count for the expansion.
 // Per tile: warp w scores its 8 tokens for the 16 query rows (the heads; rows >= n_heads are
 // zero), the warps agree on each row's tile maximum through shared memory, write their
 // probabilities into a shared 16 x 32 P tile, and each accumulates latent dims 128 w .. 128 w +
@@ -172,8 +185,12 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
   // ---- this CTA's share: a block-wide scan of the sequences' tile counts ---------------------
   const int per_t = (s.batch + C::THREADS - 1) / C::THREADS;
   const int blo = min(s.batch, (int)threadIdx.x * per_t), bhi = min(s.batch, blo + per_t);
+  auto weight = [&](int b) -> long long {
+    const int nt = mla_tiles(s, b);
+    return nt > 0 ? nt + C::SEQ_COST : 0;
+  };
   long long mine = 0;
-  for (int b = blo; b < bhi; ++b) mine += mla_tiles(s, b);
+  for (int b = blo; b < bhi; ++b) mine += weight(b);
   long long incl = mine;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -203,13 +220,14 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
   if (start < end && before <= start && start < before + mine) {
     long long p = before;
     int b = blo;
-    while (p + mla_tiles(s, b) <= start) p += mla_tiles(s, b++);   // the sequence holding tile `start`
+    while (p + weight(b) <= start) p += weight(b++);   // the sequence holding position `start`
     bars->b0 = b;
-    bars->j0 = (int)(start - p);
+    bars->p0 = p;
   }
   __syncthreads();
-  if (start >= end) return;                          // no tile for this CTA (uniform)
-  const int b_first = bars->b0, j_first = bars->j0;
+  if (start >= end) return;                          // nothing for this CTA (uniform)
+  const int b_first = bars->b0;
+  const long long p_first = bars->p0;
 
   if (warp == 4) {
     // ------------------------------------------------------------------ TMA producer
@@ -217,9 +235,17 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
       tma_prefetch_desc(&tm_lat);
       int it = 0, issued = 0;
       bool ok = true;
-      long long pos = start;
-      for (int b = b_first, j = j_first; ok && pos < end && b < s.batch; ++b, j = 0) {
-        const int take = (int)min((long long)(mla_tiles(s, b) - j), end - pos);
+      long long p = p_first;
+      // the next sequence's length is read one sequence ahead, so that a segment boundary does
+      // not wait on a load
+      int L_cur = mla_keys(s, b_first), L_nxt = mla_keys(s, b_first + 1);
+      for (int b = b_first; ok && p < end && b < s.batch; ++b, L_cur = L_nxt, L_nxt = mla_keys(s, b + 1)) {
+        const int nt = (L_cur + C::TILE - 1) / C::TILE;
+        if (nt == 0) continue;
+        const long long r0 = p + C::SEQ_COST;        // position of tile 0 of sequence b
+        const long long lo = max(start, r0), hi = min(end, r0 + nt);
+        p = r0 + nt;
+        const int j = (int)(lo - r0), take = (int)max(0LL, hi - lo);
         for (int u = 0; u < take; ++u, ++it) {
           const int st = it % C::STAGES, use = it / C::STAGES;
           if (it >= C::STAGES && !mbar_wait(&bars->empty[st], (use + 1) & 1, tmo, abort_flag)) {
@@ -233,7 +259,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
           for (int sl = 0; sl < C::SLABS; ++sl)
             tma_load_3d(dst + sl * C::TILE * 128, &tm_lat, &bars->full[st], 64 * sl, key0, b);
         }
-        pos += take;
       }
       for (int k = max(0, issued - C::STAGES); k < issued; ++k)
         mbar_wait(&bars->full[k % C::STAGES], (k / C::STAGES) & 1, tmo, nullptr);
@@ -242,43 +267,61 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
   }
 
   // ---------------------------------------------------------------------- consumer warps
-  griddep_wait();                                    // q_lat is written by the absorption kernel
   const int r_lo = lane >> 2, r_hi = r_lo + 8;
   const float scale_log2 = kLog2e / sqrtf((float)(C::DN + C::DR));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t qs = sbase + C::OFF_Q, ps = sbase + C::OFF_P;
   float* xs = reinterpret_cast<float*>(smem + C::OFF_X);             // [4][16]
-  float* sx = reinterpret_cast<float*>(smem + C::OFF_Q);             // [4 warps][16][SXROW]
+  float* sx = reinterpret_cast<float*>(smem + C::OFF_SX);            // [4 warps][16][SXROW]
   const int mi = lane >> 3, rr = lane & 7;
   constexpr int KW = C::DK / 16 / 4;                 // 16-dim steps per warp
+  constexpr int QPR = C::DK / 8;                     // 16-byte pieces of a query row
+  // The query tile of a segment's sequence is copied into shared memory while the previous
+  // segment runs (16-byte asynchronous copies, one group); rows past the heads stay zero.
+  auto fetch_q = [&](int b) {
+    for (int e = threadIdx.x; e < H * QPR; e += 128) {
+      const int r = e / QPR, ch = e % QPR;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                   :: "r"(qs + (uint32_t)(r * C::QROW + ch * 16)), "l"(q_abs + ((size_t)b * H + r) * C::DK + 8 * ch)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  for (int e = H * QPR + threadIdx.x; e < 16 * QPR; e += 128)
+    *reinterpret_cast<uint4*>(smem + C::OFF_Q + (e / QPR) * C::QROW + (e % QPR) * 16) = make_uint4(0u, 0u, 0u, 0u);
+  griddep_wait();                                    // q_lat is written by the absorption kernel
+  fetch_q(b_first);
   int it = 0;                                        // tiles of the ring consumed so far
   bool dead = false;                                 // a wait gave up (uniform over the warps)
-  long long pos = start;
-  for (int b = b_first, j = j_first; pos < end && b < s.batch; ++b, j = 0) {
-    const int nt = mla_tiles(s, b);
-    const int take = (int)min((long long)(nt - j), end - pos);
-    if (take <= 0) continue;                         // an empty sequence inside the share
-    const int L = seq_keys(s.lens, b, s.L_max);
+  long long p = p_first;
+  int L = mla_keys(s, b_first), L_nxt = mla_keys(s, b_first + 1);   // read ahead, as in the producer
+  for (int b = b_first; p < end && b < s.batch; ++b, L = L_nxt, L_nxt = mla_keys(s, b + 1)) {
+    const int nt = (L + C::TILE - 1) / C::TILE;
+    if (nt == 0) continue;                           // an empty sequence inside the share
+    const long long r0 = p + C::SEQ_COST;            // position of tile 0 of sequence b
+    const long long lo = max(start, r0), hi = min(end, r0 + nt);
+    p = r0 + nt;
+    if (hi <= lo) continue;                          // the share ends before the sequence's tiles
+    const int j = (int)(lo - r0), take = (int)(hi - lo);
     const int kbeg = j * C::TILE, kend = min((j + take) * C::TILE, L);
-    // query tile of sequence b, zero rows past the heads (the region is free: every warp has
-    // passed the previous segment's last barrier)
-    for (int e = threadIdx.x; e < 16 * (C::DK / 8); e += 128) {
-      const int r = e / (C::DK / 8), ch = e % (C::DK / 8);
-      const uint4 v = r < H ? *reinterpret_cast<const uint4*>(q_abs + ((size_t)b * H + r) * C::DK + 8 * ch)
-                            : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(smem + C::OFF_Q + r * C::QROW + ch * 16) = v;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // sequence b's query tile has landed
     // Scores split over the dimensions: warp w takes the 16-dim steps 9 w .. 9 w + 8 for all 32
     // tokens of a tile, with its 9 query fragments held in registers for the whole segment (the
-    // query tile is read from shared memory once); the four partial tiles meet in shared memory
-    // (where the query tile was), each warp summing its own 8 tokens' columns.
+    // query tile is read from shared memory once); the four partial tiles meet in shared
+    // memory, each warp summing its own 8 tokens' columns.
     uint32_t qa[KW][4];
 #pragma unroll
     for (int i = 0; i < KW; ++i)
       ldmatrix_x4(qs + (lane & 15) * C::QROW + ((KW * warp + i) * 16 + (lane >> 4) * 8) * 2, qa[i][0], qa[i][1],
                   qa[i][2], qa[i][3]);
     asm volatile("bar.sync 1, 128;" ::: "memory");   // every warp has its fragments: the tile is free
+    if (p + C::SEQ_COST < end) {                     // a next segment: the next sequence holding tiles
+      int bn = b + 1;
+      if (L_nxt == 0)
+        while (bn < s.batch - 1 && mla_tiles(s, bn) == 0) ++bn;
+      fetch_q(bn);
+    }
     float o[16][4];
 #pragma unroll
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
@@ -450,125 +493,150 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __nv_bfloat1
       }
     }
     if (j == 0 && threadIdx.x == 0 && GA_BOUNDS(b < s.batch, 12, b)) {
-      // the sequence starts in this share: its slots are c + b .. c_last + b
-      const long long c_last = (pos + nt - 1) / per;
+      // the sequence's first tile is in this share: its slots are c + b .. c_last + b
+      const long long c_last = (r0 + nt - 1) / per;
       s.seg[b] = make_int2(id, (int)(c_last - c + 1));
     }
-    pos += take;
   }
+  // a share that holds only the start cost of a sequence never waited for its query tile
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// grid: (DV / 64, n_heads, ceil(batch / 8)); block: 256; dynamic shared memory EX_SMEM (80 KB).
+// grid: (DV / 64, n_heads, ceil(batch / 8)); block: 256; dynamic shared memory EX_SMEM (88 KB).
 // Head h, output dims 64 x .. 64 x + 63, 8 sequences:
-//  1. the weight slice w_uv[h][:, 64 x ..] (512 x 64 bf16, 64 KB) is copied into shared memory
-//     with 16-byte asynchronous copies before the wait on the decode (it does not depend on it);
+//  1. the weight slice w_uv[h][:, 64 x ..] (512 x 64 bf16) is copied into shared memory (144-byte
+//     rows) with 16-byte asynchronous copies before the wait on the decode (it does not depend on
+//     it);
 //  2. warp w re-associates the partials of sequence w (o_lat = sum_c 2^(m_c - M) o_c / sum_c
 //     2^(m_c - M) l_c over the decode's segments of the sequence; lane l holds latent dims 4 l ..
-//     4 l + 3 of every 128) into a shared [8][512] fp32 tile;
-//  3. out = o_lat w_uv[h]: thread t takes output dim t % 64 over latent rows 128 (t / 64) .. + 127
-//     for the 8 sequences (fp32 sums), and the 4 partial sums of each output meet in shared
-//     memory.
+//     4 l + 3 of every 128; the first two partials are loaded together with their (m, l)) into a
+//     shared [8][512] fp32 tile;
+//  3. out = o_lat w_uv[h] on the tensor cores, mma.sync m16n8k16: each fp32 o_lat value x is split
+//     into bf16 hi = rn(x) and lo = rn(x - hi), rows 0-7 of A holding the 8 sequences' hi parts and
+//     rows 8-15 their lo parts, so rows g and g + 8 of the product add up to o_lat w_uv with an
+//     error of about 2^-16 relative to x (fp32 sums).  Warp w takes latent rows 64 w .. 64 w + 63
+//     for all 64 output dims; the 8 warps' sums meet in shared memory.
 __global__ void __launch_bounds__(256)
 mla_expand_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
                   const __nv_bfloat16* __restrict__ w_uv, __nv_bfloat16* __restrict__ out, MlaShape s) {
   using C = MlaCfg;
   extern __shared__ __align__(16) unsigned char ex_smem[];
-  __nv_bfloat16* wsm = reinterpret_cast<__nv_bfloat16*>(ex_smem);            // [R][EX_DIMS]
-  float* lat = reinterpret_cast<float*>(ex_smem + C::R * C::EX_DIMS * 2);      // [EX_SEQ][R]
-  float* part = lat;                          // [8][EX_SEQ][EX_DIMS], once the products are done
+  float* lat = reinterpret_cast<float*>(ex_smem + C::R * C::EX_WROW);         // [EX_SEQ][EX_LROW]
+  float* part = lat;                          // [8 warps][EX_SEQ][EX_DIMS], once the products are done
   const int xb = blockIdx.x, h = blockIdx.y, b0 = blockIdx.z * C::EX_SEQ;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int nb = min(C::EX_SEQ, s.batch - b0);
+  const uint32_t wsm = smem_u32(ex_smem);
   {
     constexpr int PR = C::EX_DIMS / 8;                                       // 16-byte pieces per row
     const __nv_bfloat16* wsrc = w_uv + (size_t)h * C::R * C::DV + xb * C::EX_DIMS;
-    const uint32_t wdst = smem_u32(wsm);
     for (int e = t; e < C::R * PR; e += 256) {
       const int r = e / PR, pc = e % PR;
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                   :: "r"(wdst + (uint32_t)(r * C::EX_DIMS + 8 * pc) * 2), "l"(wsrc + (size_t)r * C::DV + 8 * pc)
+                   :: "r"(wsm + (uint32_t)(r * C::EX_WROW + 16 * pc)), "l"(wsrc + (size_t)r * C::DV + 8 * pc)
                    : "memory");
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
   griddep_wait();                                    // the partials of the decode kernel
-  constexpr int SPW = C::EX_SEQ / 8;                 // sequences per warp
-  int rx[SPW], nu[SPW];
-  float M[SPW];
-#pragma unroll
-  for (int k = 0; k < SPW; ++k) {
-    const int i = SPW * warp + k, b = b0 + i;
+  {
+    constexpr int U = C::R / 128;
+    const int i = warp, b = b0 + i;
     // an empty sequence has no partial (and no record): zero row
     const int2 rec = i < nb && seq_keys(s.lens, b, s.L_max) > 0 ? s.seg[b] : make_int2(0, 0);
-    rx[k] = rec.x;
-    nu[k] = rec.x >= 0 && rec.y > 0 && rec.x + rec.y <= s.n_ids ? rec.y : 0;
-    M[k] = -INFINITY;
-    for (int c = lane; c < nu[k]; c += 32) M[k] = fmaxf(M[k], ws_ml[(((size_t)rx[k] + c) * s.n_heads + h) * 2]);
-  }
+    const int n_used = rec.x >= 0 && rec.y > 0 && rec.x + rec.y <= s.n_ids ? rec.y : 0;
+    auto slot_of = [&](int c) { return ((size_t)rec.x + c) * s.n_heads + h; };
+    float2 ml[2] = {make_float2(-INFINITY, 0.0f), make_float2(-INFINITY, 0.0f)};
+    float4 v[2][U];
 #pragma unroll
-  for (int k = 0; k < SPW; ++k) {
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M[k] = fmaxf(M[k], __shfl_xor_sync(0xffffffffu, M[k], off));
-    float4 o[C::R / 128];
+      for (int u = 0; u < U; ++u) v[c][u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int u = 0; u < C::R / 128; ++u) o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < 2; ++c)
+      if (c < n_used) {
+        ml[c] = *reinterpret_cast<const float2*>(ws_ml + slot_of(c) * 2);
+        const float* src = ws_o + slot_of(c) * C::R + 4 * lane;
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[c][u] = *reinterpret_cast<const float4*>(src + 128 * u);
+      }
+    float M = fmaxf(ml[0].x, ml[1].x);
+    if (n_used > 2) {                                // a sequence over more than two shares
+      float Mx = -INFINITY;
+      for (int c = 2 + lane; c < n_used; c += 32) Mx = fmaxf(Mx, ws_ml[slot_of(c) * 2]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+      M = fmaxf(M, Mx);
+    }
+    float4 o[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     float Lsum = 0.0f;
-    if (M[k] != -INFINITY) {
-      // the partials' loads do not depend on their factors: two in flight
-#pragma unroll 2
-      for (int c = 0; c < nu[k]; ++c) {
-        const size_t slot = ((size_t)rx[k] + c) * s.n_heads + h;
-        const float2 mlc = *reinterpret_cast<const float2*>(ws_ml + slot * 2);
-        const float* src = ws_o + slot * C::R + 4 * lane;
-        float4 v[C::R / 128];
-#pragma unroll
-        for (int u = 0; u < C::R / 128; ++u) v[u] = *reinterpret_cast<const float4*>(src + 128 * u);
-        const float f = mlc.x == -INFINITY ? 0.0f : ex2(mlc.x - M[k]);
+    if (M != -INFINITY) {
+      auto add = [&](float2 mlc, const float4 (&vc)[U]) {
+        const float f = mlc.x == -INFINITY ? 0.0f : ex2(mlc.x - M);
         Lsum = fmaf(f, mlc.y, Lsum);
 #pragma unroll
-        for (int u = 0; u < C::R / 128; ++u) {
-          o[u].x = fmaf(f, v[u].x, o[u].x); o[u].y = fmaf(f, v[u].y, o[u].y);
-          o[u].z = fmaf(f, v[u].z, o[u].z); o[u].w = fmaf(f, v[u].w, o[u].w);
+        for (int u = 0; u < U; ++u) {
+          o[u].x = fmaf(f, vc[u].x, o[u].x); o[u].y = fmaf(f, vc[u].y, o[u].y);
+          o[u].z = fmaf(f, vc[u].z, o[u].z); o[u].w = fmaf(f, vc[u].w, o[u].w);
         }
+      };
+      add(ml[0], v[0]);
+      add(ml[1], v[1]);                              // zero weight when absent (m = -inf)
+      for (int c = 2; c < n_used; ++c) {
+        const float2 mlc = *reinterpret_cast<const float2*>(ws_ml + slot_of(c) * 2);
+        float4 vc[U];
+        const float* src = ws_o + slot_of(c) * C::R + 4 * lane;
+#pragma unroll
+        for (int u = 0; u < U; ++u) vc[u] = *reinterpret_cast<const float4*>(src + 128 * u);
+        add(mlc, vc);
       }
     }
     const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
 #pragma unroll
-    for (int u = 0; u < C::R / 128; ++u)
-      *reinterpret_cast<float4*>(lat + (SPW * warp + k) * C::R + 128 * u + 4 * lane) =
+    for (int u = 0; u < U; ++u)
+      *reinterpret_cast<float4*>(lat + i * C::EX_LROW + 128 * u + 4 * lane) =
           make_float4(o[u].x * inv, o[u].y * inv, o[u].z * inv, o[u].w * inv);
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  constexpr int KP = 256 / C::EX_DIMS, KR = C::R / KP;   // latent parts, rows per part
-  const int e = t % C::EX_DIMS, k8 = t / C::EX_DIMS;  // output dim, latent rows KR k8 .. + KR - 1
-  float a[C::EX_SEQ];
+  const int g = lane >> 2, tq = lane & 3, mi = lane >> 3, rr = lane & 7;
+  float acc[C::EX_DIMS / 8][4];
 #pragma unroll
-  for (int i = 0; i < C::EX_SEQ; ++i) a[i] = 0.0f;
-#pragma unroll 2
-  for (int c = KR * k8; c < KR * k8 + KR; c += 4) {
-    float wc[4];
+  for (int n = 0; n < C::EX_DIMS / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) wc[q] = __bfloat162float(wsm[(c + q) * C::EX_DIMS + e]);
+  for (int ks = 0; ks < C::R / 16 / 8; ++ks) {
+    const int k0 = (C::R / 8) * warp + 16 * ks;
+    const float2 x01 = *reinterpret_cast<const float2*>(lat + g * C::EX_LROW + k0 + 2 * tq);
+    const float2 x23 = *reinterpret_cast<const float2*>(lat + g * C::EX_LROW + k0 + 2 * tq + 8);
+    auto lo_of = [](float x) { return x - __bfloat162float(__float2bfloat16_rn(x)); };
+    uint32_t a[4];
+    a[0] = pack_bf16x2(x01.x, x01.y);                 // row g: hi parts
+    a[1] = pack_bf16x2(lo_of(x01.x), lo_of(x01.y));   // row g + 8: lo parts
+    a[2] = pack_bf16x2(x23.x, x23.y);
+    a[3] = pack_bf16x2(lo_of(x23.x), lo_of(x23.y));
 #pragma unroll
-    for (int i = 0; i < C::EX_SEQ; ++i) {
-      const float4 x = *reinterpret_cast<const float4*>(lat + i * C::R + c);   // same address in the warp
-      a[i] = fmaf(x.x, wc[0], a[i]);
-      a[i] = fmaf(x.y, wc[1], a[i]);
-      a[i] = fmaf(x.z, wc[2], a[i]);
-      a[i] = fmaf(x.w, wc[3], a[i]);
+    for (int n = 0; n < C::EX_DIMS / 8; n += 2) {
+      const int krow = k0 + ((mi & 1) << 3) + rr, chunk = n + (mi >> 1);
+      uint32_t b0_, b1_, b2_, b3_;
+      ldmatrix_x4_trans(wsm + (uint32_t)(krow * C::EX_WROW + chunk * 16), b0_, b1_, b2_, b3_);
+      mma_bf16_16816(acc[n], a, b0_, b1_);
+      mma_bf16_16816(acc[n + 1], a, b2_, b3_);
     }
   }
   __syncthreads();                                   // every read of the latent tile is done
 #pragma unroll
-  for (int i = 0; i < C::EX_SEQ; ++i) part[(k8 * C::EX_SEQ + i) * C::EX_DIMS + e] = a[i];
+  for (int n = 0; n < C::EX_DIMS / 8; ++n)
+    *reinterpret_cast<float2*>(part + (warp * C::EX_SEQ + g) * C::EX_DIMS + 8 * n + 2 * tq) =
+        make_float2(acc[n][0] + acc[n][2], acc[n][1] + acc[n][3]);
   __syncthreads();
   for (int q = t; q < C::EX_SEQ * C::EX_DIMS; q += 256) {
     const int i = q / C::EX_DIMS, d = q % C::EX_DIMS;
     if (i < nb) {
       float y = 0.0f;
 #pragma unroll
-      for (int k = 0; k < KP; ++k) y += part[(k * C::EX_SEQ + i) * C::EX_DIMS + d];
+      for (int w = 0; w < 8; ++w) y += part[(w * C::EX_SEQ + i) * C::EX_DIMS + d];
       const size_t off = ((size_t)(b0 + i) * s.n_heads + h) * C::DV + xb * C::EX_DIMS + d;
       if (GA_BOUNDS(off < (size_t)s.batch * s.n_heads * C::DV, 11, off)) out[off] = __float2bfloat16_rn(y);
     }
