@@ -178,6 +178,7 @@ struct DeviceKernels {
   int mla;                      // mla_decode_kernel
   int topk, topk_unstaged;      // topk_select_kernel with / without the row staged in shared memory
   int n_sm;                     // streaming multiprocessors
+  long long l2_bytes;           // L2 cache size
 };
 
 std::mutex g_dev_mu;
@@ -227,6 +228,9 @@ const DeviceKernels* device_kernels() {
     int n_sm = 0;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) n_sm = 148;
     d.n_sm = n_sm;
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 < 1) l2 = 126 << 20;
+    d.l2_bytes = l2;
     g_dev_ready[dev] = true;
   }
   return &g_dev[dev];
@@ -289,7 +293,8 @@ int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const __n
 // The tensor-core prefill (bf16, d = 128 or 256): tensor maps, then prefill_wide_kernel with or
 // without block-mask unit lists.  The caller has validated the shape.
 int launch_prefill_tc(const void* q, const void* k, const void* v, __nv_bfloat16* ob, float* lse,
-                      const AttnShape& sh, bool masked, WideEpi epi, cudaStream_t stream) {
+                      const AttnShape& sh_in, bool masked, WideEpi epi, cudaStream_t stream) {
+  AttnShape sh = sh_in;
   const int d = sh.d, Tq = sh.Tq, Tk_max = sh.Tk_max;
   // 64-column SW128 boxes: Q 128 rows; K 128 keys and 64 keys; V 16384/d keys and 64 keys
   const long long kvz = (long long)sh.batch * sh.n_kv;
@@ -305,6 +310,22 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, __nv_bfloat16
   if (!dk) return GA_ERR_CUDA;
   // persistent: one CTA per SM (or per item when there are fewer items)
   const unsigned n_cta = (unsigned)(n_items < dk->n_sm ? n_items : dk->n_sm);
+  // Item order: when the keys and values of the launch do not fit in L2 and every query tile
+  // reads all of its sequence's keys (no window), neighbouring query tiles of a kv head are
+  // claimed together (blocks of 4), so that their reads of the same keys meet in L2; otherwise
+  // the plain order, whose concurrent items already share their keys in L2.
+  const double kv_bytes = 4.0 * sh.batch * sh.n_kv * (double)Tk_max * d;
+  const int QB = (sh.window == 0 && kv_bytes > (double)dk->l2_bytes &&
+                  4LL * sh.n_heads * sh.batch <= 0x7fffffffLL) ? 4 : 1;
+  const int n_qt = (Tq + 127) / 128, g = sh.n_heads / sh.n_kv;
+  sh.item_qt_block = QB;
+  sh.fd_hb.init((uint32_t)(sh.n_heads * sh.batch));
+  sh.fd_h.init((uint32_t)sh.n_heads);
+  sh.fd_g.init((uint32_t)g);
+  sh.fd_nkv.init((uint32_t)sh.n_kv);
+  sh.fd_pb.init((uint32_t)(QB * sh.n_heads * sh.batch));
+  sh.fd_cg.init((uint32_t)(QB * g));
+  sh.fd_cgl.init((uint32_t)((n_qt - QB * ((n_qt - 1) / QB)) * g));   // query tiles of the last block x g
   const int epoch = (int)(g_wide_epoch.fetch_add(1u) % (unsigned)kWideEpochs);
   if (d == 128) {
     using C = WideCfg<128>;

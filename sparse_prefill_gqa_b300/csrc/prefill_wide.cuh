@@ -8,7 +8,8 @@
 // restricted to the selected key blocks when a block mask is given ("RBS-Attention review":
 // attention is computed only over the blocks the selection keeps).
 //
-// Items are numbered heaviest causal tiles first across every (query head, sequence); a CTA's
+// Items are numbered heaviest causal tiles first, in blocks of query tiles whose items that
+// share a kv head are numbered together (wide_item); a CTA's
 // producer takes the next unclaimed item from a launch-wide counter, one item ahead of the one
 // it loads (so the longest items start first and the CTAs finish together whatever the sequence
 // lengths), and publishes it to the CTA's other roles.  The warps run decoupled across items:
@@ -150,18 +151,48 @@ struct WideItem {
   int kt_lo, n_dense;          // first 128-key tile and the number of contiguous tiles
 };
 
-// Item w of the launch: heaviest causal tiles (the last query tiles) first, then by head and
-// sequence.
-template <int BM, int BN>
+// Item w of the launch.  The query tiles are taken in blocks of QB = sh.item_qt_block from the
+// last (the heaviest causal tiles) to the first; within a block, sequence by sequence and kv head
+// by kv head, and for each kv head its block's query tiles (last first) times its query heads.
+// So the items that read the same keys and values (one kv head's query heads and, for QB > 1,
+// neighbouring query tiles) are claimed together and stream them through L2 at about the same
+// time, while the heaviest tiles still start first.  QB = 1 is the plain order: query tile, then
+// sequence, then head.
+// Every role of the CTA decodes each item it takes, on the path between two items; FAST (the
+// d = 256 kernel, whose items are short under a window) turns the divisions by launch constants
+// into multiply-shifts (FastDiv).  The d = 128 kernel keeps hardware divisions in the plain
+// order: measured, the multiply-shift form made its main loop 2 % slower.
+template <int BM, int BN, bool FAST>
 __device__ __forceinline__ WideItem wide_item(const AttnShape& sh, int w) {
   WideItem it;
   const int n_qt = (sh.Tq + BM - 1) / BM;
-  const int hb = sh.n_heads * sh.batch;
-  const int qr = w / hb, rem = w % hb;
-  it.h = rem % sh.n_heads;
-  it.b = rem / sh.n_heads;
-  const int qt = n_qt - 1 - qr;
-  it.kvh = it.h / (sh.n_heads / sh.n_kv);
+  const int g = sh.n_heads / sh.n_kv, QB = sh.item_qt_block;
+  int qt;
+  if (QB == 1 && FAST) {
+    const int qr = sh.fd_hb.div(w), rem = w - qr * (sh.n_heads * sh.batch);
+    it.b = sh.fd_h.div(rem);
+    it.h = rem - it.b * sh.n_heads;
+    it.kvh = sh.fd_g.div(it.h);
+    qt = n_qt - 1 - qr;
+  } else if (QB == 1) {
+    const int hb = sh.n_heads * sh.batch;
+    const int qr = w / hb, rem = w - qr * hb;
+    it.b = rem / sh.n_heads;
+    it.h = rem - it.b * sh.n_heads;
+    it.kvh = it.h / g;
+    qt = n_qt - 1 - qr;
+  } else {
+    const int per_block = QB * sh.n_heads * sh.batch;           // items of a full block
+    const int k = FAST ? sh.fd_pb.div(w) : w / per_block, rem = w - k * per_block;
+    const int cnt = min(QB, n_qt - QB * k);                     // query tiles in block k
+    const int grp = FAST ? (cnt == QB ? sh.fd_cg : sh.fd_cgl).div(rem) : rem / (cnt * g);
+    const int r2 = rem - grp * (cnt * g);
+    it.b = FAST ? sh.fd_nkv.div(grp) : grp / sh.n_kv;
+    it.kvh = grp - it.b * sh.n_kv;
+    const int qi = FAST ? sh.fd_g.div(r2) : r2 / g;
+    it.h = it.kvh * g + (r2 - qi * g);
+    qt = n_qt - 1 - (QB * k + qi);
+  }
   it.Tk = seq_keys(sh.k_lens, it.b, sh.Tk_max);
   it.t0 = qt * BM;
   it.rows = min(BM, sh.Tq - it.t0);
@@ -288,7 +319,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         w = __shfl_sync(0xffffffffu, w, 0);
         const bool end = w >= n_items;
-        const WideItem it = wide_item<BM, BN>(sh, end ? 0 : w);
+        const WideItem it = wide_item<BM, BN, D == 256>(sh, end ? 0 : w);
         int n_tiles = end ? 0 : it.n_dense;
         bool list = false;
         const uint8_t* mrow = masked
@@ -386,7 +417,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           // item's loads are done.
           const int wn = __shfl_sync(0xffffffffu, w_next, 0);
           if (wn < n_items) {
-            const WideItem nx = wide_item<BM, BN>(sh, wn);
+            const WideItem nx = wide_item<BM, BN, D == 256>(sh, wn);
             if (lane == 0)
               for (int s = 0; s < D / 64; ++s)
                 tma_prefetch_l2_3d(&tm_q, 64 * s, nx.t0, nx.b * sh.n_heads + nx.h);
@@ -709,7 +740,7 @@ prefill_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       // every softmax warp takes the same branch: the next item, or out (the end, or a wait
       // that gave up somewhere)
       if (!named_all<1, C::SM_THREADS>(ok && w >= 0 && *abort_flag == 0)) break;
-      const WideItem it = wide_item<BM, BN>(sh, w);
+      const WideItem it = wide_item<BM, BN, D == 256>(sh, w);
       const long long i = it.i_first + row;           // absolute position of this row
       const int lo = sh.window > 0 ? (int)max(0LL, i - sh.window + 1) : 0;
       const int hi = sh.causal ? (int)max(0LL, min((long long)it.Tk, i + 1)) : it.Tk;
