@@ -38,7 +38,7 @@ struct DecodeCfg {
   static constexpr int TILE = 64;                       // keys per stage
   static constexpr int SLABS = D / 64;
   static constexpr int TILE_BYTES = TILE * D * 2;       // one K or V tile
-  static constexpr int STAGES = D >= 256 ? 2 : (D >= 128 ? 4 : 8);
+  static constexpr int STAGES = D >= 256 ? 3 : (D >= 128 ? 4 : 8);
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
   static constexpr int MERGE_BYTES = 4 * 16 * D * 4 + 4 * 16 * 2 * 4;  // per-warp O, m, l
