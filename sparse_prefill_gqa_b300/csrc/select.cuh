@@ -498,7 +498,7 @@ select_score_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_cons
 // ---------------------------------------------------------------------------------------
 constexpr int kDecWarps = 8;
 
-__global__ void __launch_bounds__(32 * kDecWarps)
+__global__ void __launch_bounds__(32 * kDecWarps, 3)
 select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ block_mask,
                      int32_t* __restrict__ n_selected, SelectShape s) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -526,8 +526,25 @@ select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ blo
   const bool bvec = bound && (s.nKb_out % 4) == 0 && (reinterpret_cast<uintptr_t>(rrow) & 15) == 0;
   uint8_t* mrow0 = block_mask + (((size_t)b * s.n_heads + h_out0) * s.nQb + alpha) * s.nKb_out;
   const size_t mhead = (size_t)s.nQb * s.nKb_out;       // next head's row
+  // The row's invisible ends (before vlo, from vhi on: about half of a causal row) keep nothing:
+  // when the rows are 16-byte aligned they are written as 16-byte words of zeros, and only the
+  // 16-block-aligned span [gbeg, gend) around the visible blocks goes through the tests below.
+  int gbeg = 0, gend = s.nKb_out;
+  if ((s.nKb_out % 16) == 0 && (reinterpret_cast<uintptr_t>(mrow0) & 15) == 0) {
+    gbeg = vlo / 16 * 16;
+    gend = min(s.nKb_out, (vhi + 15) / 16 * 16);
+    for (int o = 0; o < n_out; ++o) {
+      uint8_t* mrow = mrow0 + o * mhead;
+      for (int z = 16 * lane; z < s.nKb_out; z += 16 * 32) {
+        if (z >= gbeg && z < gend) continue;
+        [[maybe_unused]] const size_t zoff = (size_t)(mrow - block_mask) + z;
+        if (GA_BOUNDS(zoff + 16 <= (size_t)s.batch * s.n_heads * s.nQb * s.nKb_out, 8, zoff))
+          *reinterpret_cast<uint4*>(mrow + z) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
   int kept = 0;
-  for (int base = 4 * lane; base < s.nKb_out; base += 4 * 128) {
+  for (int base = gbeg + 4 * lane; base < gend; base += 4 * 128) {
     float4 sv[4], rv[4];                            // four steps' scores (radii) in flight
     uint32_t fl[4];                                 // and rescue flags
 #pragma unroll
@@ -535,7 +552,7 @@ select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ blo
       const int beta0 = base + 128 * u;
       sv[u] = rv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       fl[u] = 0u;
-      if (beta0 < s.nKb_out && beta0 + 3 >= vlo && beta0 < vhi) {   // stored for every visible block
+      if (beta0 < gend && beta0 + 3 >= vlo && beta0 < vhi) {        // stored for every visible block
         sv[u] = *reinterpret_cast<const float4*>(srow + beta0);
         if (rvec) fl[u] = __ldg(reinterpret_cast<const uint32_t*>(resc + beta0));
         if (bvec) rv[u] = __ldg(reinterpret_cast<const float4*>(rrow + beta0));
@@ -544,7 +561,7 @@ select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ blo
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int beta0 = base + 128 * u;
-      if (beta0 >= s.nKb_out) break;
+      if (beta0 >= gend) break;
       // keep bytes (0 or 1 each) of key blocks beta0 .. beta0 + 3; groups wholly outside the
       // visible range keep nothing, wholly inside it and off the diagonal need no per-block
       // range tests, and the rescue flags are already bytes of 0 and 1
