@@ -219,7 +219,12 @@ int ga_attend_gather(const void* q, const void* k, const void* v, void* out, int
  *            1..L_max (larger values are clamped to L_max; 0, an empty cache, gives a zero
  *            row); or NULL (= L_max).
  *   out      device bf16 [batch, n_heads, 128].
- *   workspace of ga_mla_decode_workspace_size(batch, n_heads, L_max) bytes, 16-byte aligned.
+ *   workspace of ga_mla_decode_workspace_size(batch, n_heads, L_max) bytes, 16-byte aligned:
+ *            four parts, each rounded up to 256 bytes -- q_lat bf16 [batch, n_heads, 576], the
+ *            decode's partial latents fp32 [n_ids, n_heads, 512] and their (max, sum) fp32
+ *            [n_ids, n_heads, 2] with n_ids = 384 + batch - 1 (one slot per (CTA, sequence)
+ *            segment of up to 384 decode CTAs), and per sequence its first slot and slot count,
+ *            int32 [batch, 2].  The size does not depend on L_max.
  *   n_heads <= 16 (GA_ERR_UNSUPPORTED otherwise).  q_lat is rounded to bf16 before the scores.
  */
 size_t ga_mla_decode_workspace_size(int batch, int n_heads, int L_max);

@@ -132,6 +132,16 @@ def test_select_workspace_size_matches_the_stated_formula(L, B, H, n_kv, d, Tq, 
     assert L.ga_select_workspace_size(B, H, n_kv, d, Tq, Tk, qb, kb, gs) == want
 
 
+@pytest.mark.parametrize("B,H,L_max", [(1, 1, 1), (64, 16, 8192), (3, 16, 700), (200, 4, 200), (1000, 7, 65536)])
+def test_mla_workspace_size_matches_the_stated_formula(L, B, H, L_max):
+    """The header states the MLA workspace as four 256-byte-rounded parts over n_ids = 384 +
+    batch - 1 partial slots; the library's figure is exactly that."""
+    up = lambda x: (x + 255) // 256 * 256
+    n_ids = 384 + B - 1
+    want = up(B * H * 576 * 2) + up(n_ids * H * 512 * 4) + up(n_ids * H * 2 * 4) + up(B * 8)
+    assert L.ga_mla_decode_workspace_size(B, H, L_max) == want
+
+
 def test_ring_calls_reject_invalid_arguments(L):
     p = ctypes.c_void_p(4096)
     odd = ctypes.c_void_p(4098)                 # not 4-byte aligned
