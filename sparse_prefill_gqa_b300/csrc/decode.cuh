@@ -110,6 +110,9 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  // The gathered form is launched as a programmatic dependent of the top-k select (its index
+  // lists): nothing is read before that kernel has completed.  Otherwise a no-op.
+  griddep_wait();
   griddep_launch_dependents();                    // the combine may start its launch
   const int Tk = seq_keys(s.a.k_lens, b, s.a.Tk_max);
   int kbeg, kend;

@@ -44,6 +44,7 @@ dsa_indexer_kernel(const __nv_bfloat16* __restrict__ qi, const float* __restrict
   static_assert(HI >= 1 && HI <= DI / 8 && (HI & (HI - 1)) == 0, "indexer heads: power of two <= DI/8");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, b = blockIdx.y;
   const int g = lane >> 2, c = lane & 3;
+  griddep_launch_dependents();                 // the top-k select may start its launch
   const int L = seq_keys(lens, b, L_max);
   uint4 qf[NB][NU];
   float w[NB][2];
@@ -156,6 +157,9 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int b = blockIdx.x;
+  // Launched as a programmatic dependent of the indexer: nothing is read before it has completed.
+  griddep_wait();
+  griddep_launch_dependents();                   // the gathered decode may start its launch
   const int L = seq_keys(lens, b, L_max);
   const float* row = scores + (size_t)b * L_max;
   int32_t* out = idx + (size_t)b * topk;

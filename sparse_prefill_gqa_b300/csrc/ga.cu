@@ -267,8 +267,15 @@ int launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfl
   if (!dk) return GA_ERR_CUDA;
   if (dk->decode != GA_OK) return dk->decode;
   const dim3 grid(ds.n_chunks, ds.a.n_kv, ds.a.batch);
-  decode_splitk_kernel<D, GATHER><<<grid, DecodeCfg<D>::THREADS, smem, stream>>>(
-      tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
+  if (GATHER) {
+    // a programmatic dependent of the previous kernel (the top-k select's index lists)
+    if (launch_pdl(decode_splitk_kernel<D, GATHER>, grid, dim3(DecodeCfg<D>::THREADS), smem, stream, tk, tv, qb, ob,
+                   lse, ws_o, ws_ml, ds) != cudaSuccess)
+      return GA_ERR_CUDA;
+  } else {
+    decode_splitk_kernel<D, GATHER><<<grid, DecodeCfg<D>::THREADS, smem, stream>>>(
+        tk, tv, qb, ob, lse, ws_o, ws_ml, ds);
+  }
   const int st = launch_status();
   if (st != GA_OK || ds.n_chunks == 1) return st;
   if (launch_pdl(decode_combine_kernel<D>, dim3(ds.a.Tq, ds.a.n_heads, ds.a.batch), dim3(D), 0, stream, ws_o,
@@ -617,11 +624,16 @@ int ga_topk_indices(const float* scores, const int32_t* lens, int batch, int L_m
   if (!dk) return GA_ERR_CUDA;
   if (L_max <= kTopkStageMax) {
     if (dk->topk != GA_OK) return dk->topk;
-    topk_select_kernel<true><<<batch, kTopkThreads, kTopkFixedSmem + (size_t)L_max * 4, stream>>>(
-        scores, lens, L_max, topk, idx, n_sel);
+    // a programmatic dependent of the previous kernel (the indexer): its CTAs start launching
+    // while the indexer's last ones run, and wait for it before reading the scores
+    if (launch_pdl(topk_select_kernel<true>, dim3(batch), dim3(kTopkThreads), kTopkFixedSmem + (size_t)L_max * 4,
+                   stream, scores, lens, L_max, topk, idx, n_sel) != cudaSuccess)
+      return GA_ERR_CUDA;
   } else {
     if (dk->topk_unstaged != GA_OK) return dk->topk_unstaged;
-    topk_select_kernel<false><<<batch, kTopkThreads, kTopkFixedSmem, stream>>>(scores, lens, L_max, topk, idx, n_sel);
+    if (launch_pdl(topk_select_kernel<false>, dim3(batch), dim3(kTopkThreads), kTopkFixedSmem, stream, scores,
+                   lens, L_max, topk, idx, n_sel) != cudaSuccess)
+      return GA_ERR_CUDA;
   }
   return launch_status();
 }
