@@ -959,15 +959,21 @@ int ga_select_blocks_ex(const void* q, const float* centroid, const float* radiu
                                                                                centroid, s);
   else
     select_pool_kernel<float><<<pool_grid, kPoolThreads, 0, stream>>>((const float*)q, radius, centroid, s);
-  if (radius_rule == GA_RADIUS_MAD)
-    select_rescue_kernel<<<dim3(n_kv, batch), kRescueThreads, (size_t)s.sort_len * 8, stream>>>(radius, s);
+  // the later launches are programmatic dependents of the one before: each starts launching (and
+  // the score kernel its set-up) while its predecessor finishes, and waits on it before reading
+  if (radius_rule == GA_RADIUS_MAD &&
+      launch_pdl(select_rescue_kernel, dim3(n_kv, batch), dim3(kRescueThreads), (size_t)s.sort_len * 8, stream, radius,
+                 s) != cudaSuccess)
+    return GA_ERR_CUDA;
   // persistent: one CTA per SM (or per tile when there are fewer tiles)
   const long long n_tiles = sel_score_tiles(batch, n_hp, nQb, (int)nKb);
-  select_score_kernel<<<(unsigned)(n_tiles < dk->n_sm ? n_tiles : dk->n_sm), kScThreads, kScSmem, stream>>>(
-      tm_qh, tm_ql, tm_ch, tm_cl, s);
+  if (launch_pdl(select_score_kernel, dim3((unsigned)(n_tiles < dk->n_sm ? n_tiles : dk->n_sm)), dim3(kScThreads),
+                 kScSmem, stream, tm_qh, tm_ql, tm_ch, tm_cl, s) != cudaSuccess)
+    return GA_ERR_CUDA;
   const long long n_rows = (long long)batch * n_hp * nQb;
-  select_decide_kernel<<<(unsigned)((n_rows + kDecWarps - 1) / kDecWarps), 32 * kDecWarps, 0, stream>>>(
-      radius, block_mask, n_selected, s);
+  if (launch_pdl(select_decide_kernel, dim3((unsigned)((n_rows + kDecWarps - 1) / kDecWarps)), dim3(32 * kDecWarps), 0,
+                 stream, radius, block_mask, n_selected, s) != cudaSuccess)
+    return GA_ERR_CUDA;
   return launch_status();
 }
 

@@ -107,6 +107,7 @@ select_pool_kernel(const T* __restrict__ q, const float* __restrict__ radius,
   __shared__ float part[kPoolThreads / 32][kSimtMaxD];
   __shared__ float mean_s[kSimtMaxD];
   const int alpha = blockIdx.x, hp = blockIdx.y, b = blockIdx.z;
+  griddep_launch_dependents();  // the next launch of the selection may start its set-up
   if (alpha == s.nQb) {         // the extra column: the z-score radius branch, beside the pooling
     if (s.radius_rule == 0 && hp < s.n_kv) rescue_zscore(radius, s, hp, b);
     return;
@@ -243,6 +244,8 @@ select_rescue_kernel(const float* __restrict__ radius, SelectShape s) {
   extern __shared__ double sortbuf[];                // rule 1: sort_len doubles
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x;
+  griddep_wait();               // launched as a programmatic dependent of the pooling
+  griddep_launch_dependents();
   const float* rrow = radius + ((size_t)b * s.n_kv + kvh) * s.nKb_out;
   uint8_t* out = s.rescue + ((size_t)b * s.n_kv + kvh) * s.nKb;
   if (s.radius_rule == 0) {
@@ -356,6 +359,10 @@ select_score_kernel(const __grid_constant__ CUtensorMap tm_qh, const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Launched as a programmatic dependent of the pooling (or the MAD rescue): the set-up above ran
+  // while it finished; its pooled rows, centroids and row maxima are read only from here on.
+  griddep_wait();
+  griddep_launch_dependents();  // the decisions may start their launch
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -502,6 +509,7 @@ __global__ void __launch_bounds__(32 * kDecWarps, 3)
 select_decide_kernel(const float* __restrict__ radius, uint8_t* __restrict__ block_mask,
                      int32_t* __restrict__ n_selected, SelectShape s) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();               // launched as a programmatic dependent of the score kernel
   const long long row = (long long)blockIdx.x * kDecWarps + warp;    // (b, hp, alpha)
   if (row >= (long long)s.batch * s.n_hp * s.nQb) return;
   const int alpha = (int)(row % s.nQb);
