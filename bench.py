@@ -8,7 +8,9 @@ Main line: bf16 dense causal GQA prefill, B2 H32 Hkv8 d128 Tq=Tk=8192, TFLOP/s c
 the algorithmic causal FLOPs (4 d per allowed (query, key) pair: QK^T and PV, 2 FLOP per
 multiply-add), with q/k/v resident in HBM.  A step is one ga_attend over that batch; L2 is
 flushed (a 256 MiB write, then a 256 MiB read of another buffer so that none of the written lines
-is still dirty in L2) before every timed step, outside the timed events.
+is still dirty in L2) before every timed step, outside the timed events.  "e2e" is the same call
+from pinned host buffers with every step's copies in and out timed, pipelined over steps on three
+streams (see e2e_times).
 
 "parts" (N = 1, rank 0 only) measures the other workloads of the path with the same timing
 rules: KV-cache decode (GB/s of K/V read), the Tq=512 chunk at absolute positions, window
@@ -93,6 +95,64 @@ def traffic_record(kernel, workload):
             if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == src:
                 return int(m.group(3))
     return None
+
+
+def e2e_times(torch, ga, q, k, v, out, steps):
+    """Per-step time (ms) of the main-line call end to end from pinned host buffers: (1) serial,
+    each step's copy in, call and copy out on one stream; (2) pipelined, the copies of the next and
+    previous steps overlapping the call on their own streams (two device buffer sets).  Both time
+    every step's full host-to-device and device-to-host traffic."""
+    qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    bufs = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out))
+            for _ in range(2)]
+
+    def serial_step():
+        qd, kd, vd, od = bufs[0]
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        ga.ga_attend(qd, kd, vd, od)
+        oh.copy_(od, non_blocking=True)
+
+    serial = statistics.mean(timed_steps(torch, serial_step, steps, 2))
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def pipelined(n):
+        ev_cmp, ev_out = [], []
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(s_in)
+        s_cmp.wait_event(start)
+        s_out.wait_event(start)
+        for i in range(n):
+            qd, kd, vd, od = bufs[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_cmp[i - 2])      # the call two steps back has read this set
+                qd.copy_(qh, non_blocking=True)
+                kd.copy_(kh, non_blocking=True)
+                vd.copy_(vh, non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(e_in)
+                if i >= 2:
+                    s_cmp.wait_event(ev_out[i - 2])     # this set's previous output is copied out
+                ga.ga_attend(qd, kd, vd, od)
+                ev_cmp.append(torch.cuda.Event())
+                ev_cmp[-1].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[-1])
+                oh.copy_(od, non_blocking=True)
+                ev_out.append(torch.cuda.Event())
+                ev_out[-1].record(s_out)
+        end.record(s_out)                                # after the last copy out, itself after all
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / n
+
+    pipelined(2)                                         # warm-up
+    return serial, pipelined(steps)
 
 
 class ClockSampler:
@@ -845,23 +905,10 @@ def main():
     value = job_tflops(world, flops_step, args.steps, total_ms)
     kern_tflops = flops_step / (statistics.mean(times) * 1e-3) / 1e12
 
-    # end to end: pinned host buffers, copies inside the timed region
-    qh = q.cpu().pin_memory()
-    kh = k.cpu().pin_memory()
-    vh = v.cpu().pin_memory()
-    oh = torch.empty_like(qh).pin_memory()
-    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-
-    def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        ga.ga_attend(qd, kd, vd, out)
-        oh.copy_(out, non_blocking=True)
-
+    # end to end: pinned host buffers, every step's copies inside the timed region
     e2e_steps = max(3, min(args.steps, 10))
-    te = timed_steps(torch, e2e_step, e2e_steps, 2)
-    e2e_val = flops_step / (statistics.mean(te) * 1e-3) / 1e12
+    e2e_serial_ms, e2e_ms = e2e_times(torch, ga, q, k, v, out, e2e_steps)
+    e2e_val = flops_step / (e2e_ms * 1e-3) / 1e12
 
     if rank != 0:
         if dist:
@@ -882,7 +929,12 @@ def main():
             "clocks": clk.summary(),
             "e2e": {"value": e2e_val, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
-                    "d2h_bytes_per_step": out.numel() * 2}}
+                    "d2h_bytes_per_step": out.numel() * 2,
+                    "ms_per_step": e2e_ms,
+                    "how": "pipelined over steps: step i+1's inputs copied in, step i computed and step "
+                           "i-1's output copied out on three streams, two device buffer sets; every "
+                           "step's copies inside the timed region",
+                    "serial_value": flops_step / (e2e_serial_ms * 1e-3) / 1e12}}
 
     if not args.no_parts and world == 1:
         parts = {}
