@@ -906,9 +906,14 @@ def main():
     kern_tflops = flops_step / (statistics.mean(times) * 1e-3) / 1e12
 
     # end to end: pinned host buffers, every step's copies inside the timed region
+    # (whole job: every rank's replica, the slowest rank's time, as for the main value)
     e2e_steps = max(3, min(args.steps, 10))
+    if dist:
+        dist.barrier()
     e2e_serial_ms, e2e_ms = e2e_times(torch, ga, q, k, v, out, e2e_steps)
-    e2e_val = flops_step / (e2e_ms * 1e-3) / 1e12
+    e2e_serial_ms = max_over_ranks(torch, dist, e2e_serial_ms, "cuda")
+    e2e_ms = max_over_ranks(torch, dist, e2e_ms, "cuda")
+    e2e_val = job_tflops(world, flops_step, 1, e2e_ms)
 
     if rank != 0:
         if dist:
@@ -934,7 +939,7 @@ def main():
                     "how": "pipelined over steps: step i+1's inputs copied in, step i computed and step "
                            "i-1's output copied out on three streams, two device buffer sets; every "
                            "step's copies inside the timed region",
-                    "serial_value": flops_step / (e2e_serial_ms * 1e-3) / 1e12}}
+                    "serial_value": job_tflops(world, flops_step, 1, e2e_serial_ms)}}
 
     if not args.no_parts and world == 1:
         parts = {}
