@@ -42,6 +42,8 @@ _SHORT = [int(x) for x in np.random.default_rng(704).integers(0, 201, size=200)]
     # shares that end inside one sequence, hold short ones whole, and skip an empty one
     (8, 16, 8192, [8192, 32, 5, 0, 64, 8192, 1, 700], True),
     (200, 4, 200, _SHORT, True),             # several short sequences in each CTA's share
+    (5, 1, 5000, [0, 4999, 1, 2500, 0], True),   # one head; empty sequences at both ends
+    (4, 5, 2048, [33, 2048, 31, 1000], False),   # an odd head count (rows 5..15 of the MMA padded)
 ])
 def test_mla_decode_matches_oracle(B, H, L_max, lens, poison):
     qn, qnr, qp, qpr, lat, latr = _inputs(B, H, L_max, seed=701 + H)
