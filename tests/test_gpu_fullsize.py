@@ -79,22 +79,28 @@ def test_decode_and_chunk_32k():
     check_rows(out, qb, kb, vb, rows, heads, lens=lens, what="chunk")
 
 
-@pytest.mark.parametrize("H,n_kv,Tq,d", [(8, 4, 640, 128), (4, 2, 384, 256)])
-def test_item_order_for_kv_beyond_l2(H, n_kv, Tq, d):
-    """A chunk of Tq rows at the end of a 96K-token cache whose K/V (201 MB) exceed L2: the
-    prefill then numbers its items in blocks of four query tiles grouped by kv head.  Tq = 640 is
-    one full block and a last block of one tile (d = 128); Tq = 384 a single block of three
-    (d = 256, whose item decode divides by multiply-shifts).  Every query tile of every head is
-    checked on sampled rows, so an item the order skipped or repeated shows."""
-    B, Tk, seed = 1, 98304, 1101
-    lens = np.array([Tk - 5], dtype=np.int32)          # absolute positions Tk_b - Tq + t
+@pytest.mark.parametrize("B,H,n_kv,Tq,d,Tk,lens", [
+    (1, 8, 4, 640, 128, 98304, [98299]),
+    (1, 4, 2, 384, 256, 98304, [98299]),
+    (3, 4, 2, 384, 128, 65536, [65536, 40000, 500]),
+])
+def test_item_order_for_kv_beyond_l2(B, H, n_kv, Tq, d, Tk, lens):
+    """A chunk of Tq rows at the end of caches whose K/V (201 MB) exceed L2: the prefill then
+    numbers its items in blocks of four query tiles grouped by kv head.  Tq = 640 is one full
+    block and a last block of one tile (d = 128); Tq = 384 a single block of three (d = 256,
+    whose item decode divides by multiply-shifts; and d = 128 over three sequences of different
+    lengths).  Every query tile of every head is checked on sampled rows, so an item the order
+    skipped or repeated shows."""
+    seed = 1101
+    lens = np.array(lens, dtype=np.int32)              # absolute positions Tk_b - Tq + t
     qb = randn_bhtd(seed, "q", (B, H, Tq, d))
     kb = randn_bhtd(seed, "k", (B, n_kv, Tk, d), lengths=lens)
     vb = randn_bhtd(seed, "v", (B, n_kv, Tk, d), lengths=lens)
     out = ga.ga_attend(upload(qb), upload(kb), upload(vb), k_lens=torch.from_numpy(lens).cuda())
     assert ga.ga_read_device_status() == ga.GA_OK
     rows = sample_rows(Tq, 48, seed=seed, q_block=128)
-    check_rows(out, qb, kb, vb, rows, [(0, h) for h in range(H)], lens=lens, what=f"order d={d}")
+    check_rows(out, qb, kb, vb, rows, [(b, h) for b in range(B) for h in range(H)], lens=lens,
+               what=f"order d={d}")
 
 
 def test_window_sink_and_full_causal_32k_d256():
