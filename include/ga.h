@@ -396,7 +396,8 @@ int ga_read_device_status(ga_stream_t stream);
  * sticky word.  Synchronises `stream`, then stores and clears that word in *first: 0 when no
  * check failed, else (site << 48) | offset (sites: 1 TMA coordinate or destination, 2 prefill
  * output, 3 prefill lse, 4 decode partials, 5 decode output, 6 top-k indices, 7 selection
- * scores, 8 block mask, 9 MLA q_lat, 10 MLA partials, 11 MLA output).  Returns GA_OK, or
+ * scores, 8 block mask, 9 MLA q_lat, 10 MLA partials, 11 MLA output, 12 MLA per-sequence slot
+ * records).  Returns GA_OK, or
  * GA_ERR_UNSUPPORTED from the ordinary build (no checks compiled), GA_ERR_CUDA on a failed
  * synchronisation. */
 int ga_debug_violation(uint64_t* first, ga_stream_t stream);
